@@ -1,0 +1,403 @@
+"""fp64 CPU oracle for the Ulysses sequence-parallel attention hot path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports, calls or links
+this module: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` (``cpu_baseline`` and ``--impl reference``) use it.  It
+shares no code, header, table or helper with the CUDA library; its inputs come
+from the seeded generators in ``usp_workloads`` (which hold no arithmetic of
+the method) or from the tests themselves.
+
+Everything here is the plain definition, written out in float64 with numpy:
+
+* ``relayout_fwd`` / ``relayout_bwd``: the two all-to-all exchanges of the
+  attention wrapper, ``_gather_seq_scatter_heads`` (queries, keys and values go
+  from "my sequence chunk, all heads" to "whole sequence, my heads") and
+  ``_gather_heads_scatter_seq`` (the output goes back).  The backward of each
+  is the other one ("swap scatter and gather").  huggingface/accelerate PR
+  #4209, the comment on the four ``_SeqAllToAll.apply`` call sites.
+* ``cu_seqlens_from_position_ids``: document boundaries of the *gathered*
+  sequence, recomputed from the gathered position_ids instead of the
+  collator's per-shard ``cu_seq_lens_q/k``/``max_length_q/k`` (PR #4209, the
+  comment on stale kwargs: 41.8% of logits mismatched when the per-shard ones
+  were used; and the comment moving the position_ids gather into the forward
+  pre-hook, one gather per forward shared by every layer).
+* ``attention_fwd`` / ``attention_bwd``: varlen softmax attention over the
+  gathered sequence of one rank's heads: documents never see each other,
+  causal, optional sliding window, GQA (ArcticTraining PR #45, "gqa works"),
+  and one sink logit per head sliced to the rank's heads (PR #4209, the
+  gpt-oss finding about ``s_aux``).  The gradients are the textbook ones of
+  that function.
+* ``ulysses_fwd`` / ``ulysses_bwd``: the whole emulated P-rank path, and
+  ``unsharded_fwd`` / ``unsharded_bwd``: the same attention run on the
+  unsharded tensors, the pages' correctness reference ("tested against an
+  unsharded forward/backward", PR #4209; the yunchang script compares against
+  ``flash_attn_func`` on the full tensors).
+
+Readings where the pages are silent (each is listed in the design notes):
+the softmax scale defaults to 1/sqrt(D) (``flash_attn_func`` is called with no
+scale in the yunchang script); a sink is an extra logit with no value, not
+multiplied by the scale, and the log-sum-exp includes it; window_left=w lets
+query i see keys j with i-j <= w (w=127 for "sliding window 128"); a document
+starts at every row start and wherever position_ids is 0; LSE is the natural
+log; heads go to ranks in contiguous blocks; sequence chunks are contiguous in
+rank order.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, library special cases, finite differences, semantic
+encodings); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+from typing import Optional, Tuple
+
+import numpy as np
+
+__all__ = [
+    "OracleError",
+    "relayout_fwd", "relayout_bwd",
+    "cu_seqlens_from_position_ids", "gather_position_ids",
+    "attention_fwd", "attention_bwd",
+    "ulysses_fwd", "ulysses_bwd", "unsharded_fwd", "unsharded_bwd",
+    "visible_pairs",
+]
+
+
+class OracleError(ValueError):
+    """Raised for inputs the method refuses (indivisible heads, bad positions)."""
+
+
+# ---------------------------------------------------------------------------
+# all-to-all exchanges (accelerate PR #4209, _gather_seq_scatter_heads /
+# _gather_heads_scatter_seq)
+# ---------------------------------------------------------------------------
+
+def _check_divisible(S: int, H: int, P: int) -> None:
+    # The torch backend refuses an sp_size that does not divide the heads
+    # (accelerate PR #4209, "What does this PR do?", the list under "How").
+    if P <= 0 or H % P != 0:
+        raise OracleError(f"sp size {P} does not divide {H} heads")
+    if S % P != 0:
+        raise OracleError(f"sp size {P} does not divide sequence length {S}")
+
+
+def relayout_fwd(x_seq: np.ndarray, P: int) -> np.ndarray:
+    """Gather the sequence, scatter the heads.
+
+    ``x_seq`` is ``[P][B][S/P][H][D]``: rank r' holds positions
+    ``[r'*S/P, (r'+1)*S/P)`` of every row, all heads.  The result is
+    ``[P][B][S][H/P][D]``: rank r holds every position, heads
+    ``[r*H/P, (r+1)*H/P)``.  Element for element::
+
+        out[r][b][r'*S/P + s'][j][d] = x_seq[r'][b][s'][r*H/P + j][d]
+
+    Written as a reshape that names the two rank axes and a transpose that
+    swaps them, which is that formula.
+    """
+    Px, B, Sl, H, D = x_seq.shape
+    if Px != P:
+        raise OracleError("leading axis must be the rank axis")
+    _check_divisible(Sl * P, H, P)
+    Hp = H // P
+    y = x_seq.reshape(P, B, Sl, P, Hp, D)       # [r'][b][s'][r][j][d]
+    y = y.transpose(3, 1, 0, 2, 4, 5)           # [r][b][r'][s'][j][d]
+    return np.ascontiguousarray(y).reshape(P, B, P * Sl, Hp, D)
+
+
+def relayout_bwd(x_head: np.ndarray, P: int) -> np.ndarray:
+    """Gather the heads, scatter the sequence: the inverse exchange.
+
+    ``x_head`` is ``[P][B][S][H/P][D]``; the result is ``[P][B][S/P][H][D]``::
+
+        out[r'][b][s'][r*H/P + j][d] = x_head[r][b][r'*S/P + s'][j][d]
+    """
+    Px, B, S, Hp, D = x_head.shape
+    if Px != P:
+        raise OracleError("leading axis must be the rank axis")
+    _check_divisible(S, Hp * P, P)
+    Sl = S // P
+    y = x_head.reshape(P, B, P, Sl, Hp, D)      # [r][b][r'][s'][j][d]
+    y = y.transpose(2, 1, 3, 0, 4, 5)           # [r'][b][s'][r][j][d]
+    return np.ascontiguousarray(y).reshape(P, B, Sl, P * Hp, D)
+
+
+# ---------------------------------------------------------------------------
+# position_ids gather and document boundaries (accelerate PR #4209)
+# ---------------------------------------------------------------------------
+
+def gather_position_ids(pos_shards: np.ndarray) -> np.ndarray:
+    """[P][B][S/P] shards -> [B][S]: the all-gather done once per forward."""
+    P, B, Sl = pos_shards.shape
+    out = np.empty((B, P * Sl), dtype=np.int64)
+    for r in range(P):
+        out[:, r * Sl:(r + 1) * Sl] = pos_shards[r]
+    return out
+
+
+def cu_seqlens_from_position_ids(pos_shards: np.ndarray) -> Tuple[np.ndarray, int, int]:
+    """Document boundaries of the gathered sequence, one sequential pass.
+
+    A document starts at every row start and wherever the gathered position is
+    0 (position_ids count 0, 1, 2, ... inside each packed document).  Returns
+    ``(cu_seqlens, n_docs, max_len)`` with ``cu_seqlens`` int32 of length
+    ``n_docs + 1``, ``cu_seqlens[0] = 0``, ``cu_seqlens[n_docs] = B*S`` and
+    ``max_len`` the longest document.  Negative positions are refused.
+    """
+    pos = gather_position_ids(np.asarray(pos_shards))
+    B, S = pos.shape
+    flat = pos.reshape(-1)
+    starts = []
+    for i in range(flat.shape[0]):
+        p = int(flat[i])
+        if p < 0:
+            raise OracleError(f"negative position id {p} at gathered index {i}")
+        if i % S == 0 or p == 0:
+            starts.append(i)
+    cu = starts + [B * S]
+    max_len = 0
+    for a, b in zip(cu[:-1], cu[1:]):
+        max_len = max(max_len, b - a)
+    return np.asarray(cu, dtype=np.int32), len(starts), max_len
+
+
+# ---------------------------------------------------------------------------
+# varlen attention over one rank's heads
+# ---------------------------------------------------------------------------
+
+def _visible(i0: int, i1: int, a: int, b: int, causal: bool, window_left: int) -> np.ndarray:
+    """Boolean [i1-i0][b-a]: may query i (global index) see key j of doc [a, b)?"""
+    i = np.arange(i0, i1)[:, None]
+    j = np.arange(a, b)[None, :]
+    vis = np.ones((i1 - i0, b - a), dtype=bool)
+    if causal:
+        vis &= j <= i
+    if window_left >= 0:
+        vis &= (i - j) <= window_left
+        if not causal:
+            vis &= (j - i) <= window_left
+    return vis
+
+
+def _doc_row_blocks(a: int, b: int, block: int):
+    for i0 in range(a, b, block):
+        yield i0, min(b, i0 + block)
+
+
+def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, cu_seqlens: np.ndarray,
+                  causal: bool = True, window_left: int = -1, scale: Optional[float] = None,
+                  sinks: Optional[np.ndarray] = None, row_block: int = 512,
+                  heads: Optional[list] = None):
+    """Softmax attention of one rank over its gathered sequence.
+
+    ``q`` [T][hq][D], ``k``/``v`` [T][hk][D] (T = B*S tokens, every document a
+    contiguous range ``[cu[n], cu[n+1])``), ``sinks`` [hq] or None.  Query
+    head h reads key/value head ``h // (hq/hk)``.  For query i of document
+    [a, b) the visible keys are j in [a, b) with j <= i (causal) and
+    i - j <= window_left (window).  With s_ij = scale * q_i . k_j and t the
+    head's sink logit (if any)::
+
+        LSE_i = log( sum_j exp(s_ij) + exp(t) )
+        O_i   = sum_j exp(s_ij - LSE_i) v_j
+
+    Returns ``O`` [T][hq][D] and ``LSE`` [hq][T] in float64.  ``heads``
+    restricts the work to those query heads (other outputs stay NaN).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    T, hq, D = q.shape
+    hk = k.shape[1]
+    if hq % hk != 0:
+        raise OracleError("query heads must be a multiple of key/value heads")
+    G = hq // hk
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    cu = [int(x) for x in cu_seqlens]
+    O = np.full((T, hq, D), np.nan)
+    LSE = np.full((hq, T), np.nan)
+    for h in (range(hq) if heads is None else heads):
+        kh = h // G
+        t = None if sinks is None else float(sinks[h])
+        for a, b in zip(cu[:-1], cu[1:]):
+            K = k[a:b, kh]
+            V = v[a:b, kh]
+            for i0, i1 in _doc_row_blocks(a, b, row_block):
+                s = scale * (q[i0:i1, h] @ K.T)
+                s = np.where(_visible(i0, i1, a, b, causal, window_left), s, -np.inf)
+                m = s.max(axis=1)
+                if t is not None:
+                    m = np.maximum(m, t)
+                e = np.exp(s - m[:, None])
+                z = e.sum(axis=1)
+                if t is not None:
+                    z = z + np.exp(t - m)
+                LSE[h, i0:i1] = m + np.log(z)
+                O[i0:i1, h] = (e / z[:, None]) @ V
+    return O, LSE
+
+
+def attention_bwd(q, k, v, o, lse, do, cu_seqlens, causal: bool = True, window_left: int = -1,
+                  scale: Optional[float] = None, sinks: Optional[np.ndarray] = None,
+                  row_block: int = 512):
+    """Gradients of ``attention_fwd`` for the loss sum(O * dO).
+
+    With P_ij = exp(s_ij - LSE_i) (zero where key j is hidden from i) and
+    D_i = sum_d dO_id O_id::
+
+        dV_j  = sum_i P_ij dO_i
+        dP_ij = dO_i . v_j
+        dS_ij = P_ij (dP_ij - D_i)
+        dQ_i  = scale sum_j dS_ij k_j
+        dK_j  = scale sum_i dS_ij q_i
+        dt    = -sum_i exp(t - LSE_i) D_i          (sink logit of the head)
+
+    Key/value gradients of a GQA group sum over its query heads.  Returns
+    ``dq, dk, dv, dsinks`` (dsinks None without sinks), float64.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    o = np.asarray(o, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    T, hq, D = q.shape
+    hk = k.shape[1]
+    G = hq // hk
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    cu = [int(x) for x in cu_seqlens]
+    Dvec = np.sum(do * o, axis=2)                  # [T][hq]
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    dsinks = None if sinks is None else np.zeros(hq)
+    for h in range(hq):
+        kh = h // G
+        for a, b in zip(cu[:-1], cu[1:]):
+            K = k[a:b, kh]
+            V = v[a:b, kh]
+            for i0, i1 in _doc_row_blocks(a, b, row_block):
+                s = scale * (q[i0:i1, h] @ K.T)
+                vis = _visible(i0, i1, a, b, causal, window_left)
+                Pm = np.where(vis, np.exp(s - lse[h, i0:i1][:, None]), 0.0)
+                dv[a:b, kh] += Pm.T @ do[i0:i1, h]
+                dP = do[i0:i1, h] @ V.T
+                dS = Pm * (dP - Dvec[i0:i1, h][:, None])
+                dq[i0:i1, h] += scale * (dS @ K)
+                dk[a:b, kh] += scale * (dS.T @ q[i0:i1, h])
+                if dsinks is not None:
+                    dsinks[h] += -np.sum(np.exp(float(sinks[h]) - lse[h, i0:i1]) * Dvec[i0:i1, h])
+    return dq, dk, dv, dsinks
+
+
+def visible_pairs(cu_seqlens, causal: bool = True, window_left: int = -1) -> int:
+    """Number of (query, key) pairs the mask keeps, summed over documents."""
+    total = 0
+    cu = [int(x) for x in cu_seqlens]
+    for a, b in zip(cu[:-1], cu[1:]):
+        L = b - a
+        for i in range(L):
+            lo = 0
+            hi = i if causal else L - 1
+            if window_left >= 0:
+                lo = max(0, i - window_left)
+                if not causal:
+                    hi = min(L - 1, i + window_left)
+            total += hi - lo + 1
+    return total
+
+
+# ---------------------------------------------------------------------------
+# the emulated P-rank path and the unsharded reference
+# ---------------------------------------------------------------------------
+
+def _rank_sinks(sinks, r, hq):
+    # Sinks are one logit per head; after the exchange rank r holds heads
+    # [r*hq, (r+1)*hq), so it uses that slice (accelerate PR #4209, gpt-oss).
+    return None if sinks is None else np.asarray(sinks, dtype=np.float64)[r * hq:(r + 1) * hq]
+
+
+def ulysses_fwd(q_seq, k_seq, v_seq, pos_shards, causal=True, window_left=-1, scale=None,
+                sinks=None):
+    """Whole forward of P emulated ranks.
+
+    Inputs are in sequence-shard layout ``[P][B][S/P][H][D]`` (float64 or
+    anything numpy can widen).  Returns a dict with the head-layout tensors,
+    ``cu_seqlens``, per-rank ``o_head``/``lse`` and the output back in
+    sequence-shard layout ``o_seq``.
+    """
+    P, B, Sl, Hq, D = q_seq.shape
+    S = P * Sl
+    qh = relayout_fwd(np.asarray(q_seq, np.float64), P)
+    kh = relayout_fwd(np.asarray(k_seq, np.float64), P)
+    vh = relayout_fwd(np.asarray(v_seq, np.float64), P)
+    cu, n, max_len = cu_seqlens_from_position_ids(pos_shards)
+    hq, hk = Hq // P, kh.shape[3]
+    o_head = np.empty((P, B, S, hq, D))
+    lse = np.empty((P, B, hq, S))
+    for r in range(P):
+        O, L = attention_fwd(qh[r].reshape(B * S, hq, D), kh[r].reshape(B * S, hk, D),
+                             vh[r].reshape(B * S, hk, D), cu, causal, window_left, scale,
+                             _rank_sinks(sinks, r, hq))
+        o_head[r] = O.reshape(B, S, hq, D)
+        lse[r] = L.reshape(hq, B, S).transpose(1, 0, 2)
+    return dict(q_head=qh, k_head=kh, v_head=vh, cu_seqlens=cu, n_docs=n, max_len=max_len,
+                o_head=o_head, lse=lse, o_seq=relayout_bwd(o_head, P))
+
+
+def ulysses_bwd(fwd: dict, do_seq, causal=True, window_left=-1, scale=None, sinks=None):
+    """Whole backward of P emulated ranks: dO goes seq->head, the attention
+    gradients run per rank, and dQ/dK/dV go head->seq (the exchanges swapped)."""
+    P = do_seq.shape[0]
+    doh = relayout_fwd(np.asarray(do_seq, np.float64), P)
+    _, B, S, hq, D = doh.shape
+    hk = fwd["k_head"].shape[3]
+    dqh = np.empty_like(fwd["q_head"])
+    dkh = np.empty_like(fwd["k_head"])
+    dvh = np.empty_like(fwd["v_head"])
+    dsinks = None if sinks is None else np.zeros(hq * P)
+    for r in range(P):
+        lse_r = fwd["lse"][r].transpose(1, 0, 2).reshape(hq, B * S)
+        dq, dk, dv, ds = attention_bwd(
+            fwd["q_head"][r].reshape(B * S, hq, D), fwd["k_head"][r].reshape(B * S, hk, D),
+            fwd["v_head"][r].reshape(B * S, hk, D), fwd["o_head"][r].reshape(B * S, hq, D),
+            lse_r, doh[r].reshape(B * S, hq, D), fwd["cu_seqlens"], causal, window_left,
+            scale, _rank_sinks(sinks, r, hq))
+        dqh[r] = dq.reshape(B, S, hq, D)
+        dkh[r] = dk.reshape(B, S, hk, D)
+        dvh[r] = dv.reshape(B, S, hk, D)
+        if ds is not None:
+            dsinks[r * hq:(r + 1) * hq] = ds
+    return dict(do_head=doh, dq_head=dqh, dk_head=dkh, dv_head=dvh, dsinks=dsinks,
+                dq_seq=relayout_bwd(dqh, P), dk_seq=relayout_bwd(dkh, P),
+                dv_seq=relayout_bwd(dvh, P))
+
+
+def _unshard(x_seq):
+    P, B, Sl = x_seq.shape[:3]
+    return np.moveaxis(np.asarray(x_seq, np.float64), 0, 1).reshape((B, P * Sl) + x_seq.shape[3:])
+
+
+def unsharded_fwd(q_seq, k_seq, v_seq, pos_shards, causal=True, window_left=-1, scale=None,
+                  sinks=None):
+    """Attention on the unsharded [B*S][H][D] tensors with all heads at once."""
+    q = _unshard(q_seq)
+    B, S, Hq, D = q.shape
+    k = _unshard(k_seq)
+    v = _unshard(v_seq)
+    cu, _, _ = cu_seqlens_from_position_ids(pos_shards)
+    O, L = attention_fwd(q.reshape(B * S, Hq, D), k.reshape(B * S, -1, D), v.reshape(B * S, -1, D),
+                         cu, causal, window_left, scale, sinks)
+    return O.reshape(B, S, Hq, D), L
+
+
+def unsharded_bwd(q_seq, k_seq, v_seq, do_seq, pos_shards, causal=True, window_left=-1,
+                  scale=None, sinks=None):
+    q = _unshard(q_seq)
+    B, S, Hq, D = q.shape
+    k = _unshard(k_seq).reshape(B * S, -1, D)
+    v = _unshard(v_seq).reshape(B * S, -1, D)
+    do = _unshard(do_seq).reshape(B * S, Hq, D)
+    q = q.reshape(B * S, Hq, D)
+    cu, _, _ = cu_seqlens_from_position_ids(pos_shards)
+    O, L = attention_fwd(q, k, v, cu, causal, window_left, scale, sinks)
+    dq, dk, dv, ds = attention_bwd(q, k, v, O, L, do, cu, causal, window_left, scale, sinks)
+    return (dq.reshape(B, S, Hq, D), dk.reshape(B, S, -1, D), dv.reshape(B, S, -1, D), ds)
