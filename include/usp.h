@@ -1,0 +1,198 @@
+/*
+ * usp.h — C ABI of the GB300 Ulysses sequence-parallel attention hot path.
+ *
+ * The library emulates P sequence-parallel ranks inside one GPU's memory.  The
+ * calls follow the attention wrapper of huggingface/accelerate PR #4209
+ * ("Add an FSDP2-native Ulysses sequence parallelism backend"):
+ *
+ *   1. usp_relayout_fwd   q, k, v: "gather sequence, scatter heads"
+ *                         (_gather_seq_scatter_heads, the all-to-all comment)
+ *   2. usp_cu_seqlens_from_position_ids
+ *                         document boundaries rebuilt from the *gathered*
+ *                         position_ids, never the collator's per-shard
+ *                         cu_seq_lens_q/k (the stale-kwargs comment: 41.8% of
+ *                         logits mismatched with the per-shard ones)
+ *   3. usp_attn_fwd       varlen causal GQA attention over the gathered
+ *                         sequence, optional sliding window, one sink logit per
+ *                         head sliced to the rank's heads (the gpt-oss finding)
+ *   4. usp_relayout_bwd   the output: "gather heads, scatter sequence"
+ *                         (_gather_heads_scatter_seq)
+ *   backward: usp_relayout_fwd(dO), usp_attn_bwd, usp_relayout_bwd(dQ, dK, dV):
+ *   the exchanges swap scatter and gather (same comment).
+ *
+ * Conventions shared by every call
+ *   - Every pointer is a DEVICE pointer owned by the caller.  The library never
+ *     allocates or frees device memory; scratch space is passed in as a
+ *     workspace whose size a *_workspace_bytes query returns.
+ *   - Every call only enqueues work on `stream` and returns without
+ *     synchronising.  Results are valid once the stream reaches that point.
+ *   - The return value reports host-side argument checks and launch errors.
+ *     Data errors found on the device (stale or malformed cu_seqlens, negative
+ *     position ids) are written to *dev_status (device int32, may be NULL)
+ *     as a usp_status code; a call never clears *dev_status, so zero it
+ *     before the first call and read it after synchronising.
+ *   - Pointers passed to the relayout and attention calls must be 16-byte
+ *     aligned (USP_ERR_ALIGNMENT otherwise).
+ *   - Layout names:  seq-layout  [P][B][S/P][H][D]  rank r holds positions
+ *                                 [r*S/P, (r+1)*S/P) of every row, all heads;
+ *                    head-layout [P][B][S][H/P][D]  rank r holds every position,
+ *                                 heads [r*H/P, (r+1)*H/P).
+ *     Sequence chunks are contiguous in rank order, heads go to ranks in
+ *     contiguous blocks, so rank r's query heads r*hq..r*hq+hq-1 read its own
+ *     key/value heads under GQA.
+ *   - The library is thread-safe per stream and keeps no state beyond a
+ *     per-device cache of the SM count.
+ */
+#ifndef USP_H_
+#define USP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st* usp_stream_t;
+
+typedef enum {
+  USP_OK = 0,
+  USP_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, bad flag */
+  USP_ERR_INDIVISIBLE = 2,   /* P does not divide S, Hq or Hkv, or Hkv does not divide Hq
+                                (accelerate PR #4209: "sp_size not dividing the heads" is refused) */
+  USP_ERR_UNSUPPORTED = 3,   /* head dim, element size or size outside what the kernels take */
+  USP_ERR_ALIGNMENT = 4,     /* pointer or contiguous run not a multiple of 16 bytes */
+  USP_ERR_BAD_SEQLENS = 5,   /* device: cu_seqlens[0] != 0, not increasing, or cu_seqlens[n] != B*S
+                                (e.g. a shard's stale per-shard boundaries) */
+  USP_ERR_BAD_POSITIONS = 6, /* device: a negative position id */
+  USP_ERR_TIMEOUT = 7,       /* device: a bounded wait inside a kernel gave up */
+  USP_ERR_CUDA = 8,          /* a CUDA runtime/driver call or launch failed */
+  USP_ERR_WORKSPACE = 9      /* workspace pointer null/misaligned or smaller than required */
+} usp_status;
+
+/* Static, human-readable name of a status code.  Never NULL. */
+const char* usp_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int usp_version(void);
+
+/* ------------------------------------------------------------------------
+ * Relayout (the all-to-all of each rank, emulated as one permutation of the
+ * P ranks' buffers).  accelerate PR #4209, the comment on the four
+ * _SeqAllToAll.apply call sites: queries/keys/values go from the local
+ * sequence chunk with all heads to the whole sequence with H/P heads, and the
+ * output comes back as [batch, seq, heads/sp_size, head_dim] per rank.
+ *
+ *   usp_relayout_fwd:  x_head[r][b][r'*S/P + s'][j][d] = x_seq[r'][b][s'][r*H/P + j][d]
+ *   usp_relayout_bwd:  x_seq[r'][b][s'][r*H/P + j][d]  = x_head[r][b][r'*S/P + s'][j][d]
+ *
+ * x_seq:  [P][B][S/P][H][D] elements of elem_bytes bytes (input of fwd, output of bwd)
+ * x_head: [P][B][S][H/P][D]                          (output of fwd, input of bwd)
+ * The two buffers must not overlap.  Each contiguous run, (H/P)*D*elem_bytes
+ * bytes, must be a multiple of 16 (USP_ERR_ALIGNMENT otherwise).
+ * Errors: USP_ERR_INVALID_ARG (null pointer, size <= 0, elem_bytes not 1/2/4/8),
+ *         USP_ERR_INDIVISIBLE (H % P or S % P), USP_ERR_ALIGNMENT, USP_ERR_CUDA.
+ * The result is a bit-exact copy of every element.
+ * ---------------------------------------------------------------------- */
+int usp_relayout_fwd(const void* x_seq, void* x_head, int B, int S, int H, int D, int P,
+                     int elem_bytes, usp_stream_t stream);
+int usp_relayout_bwd(const void* x_head, void* x_seq, int B, int S, int H, int D, int P,
+                     int elem_bytes, usp_stream_t stream);
+
+/* Same permutation for three tensors in one launch: q (Hq heads) and k, v
+ * (Hkv heads), all with head dim D.  Equivalent to three usp_relayout_fwd
+ * calls; meant for the q/k/v exchange of one attention layer. */
+int usp_relayout_fwd_qkv(const void* q_seq, const void* k_seq, const void* v_seq,
+                         void* q_head, void* k_head, void* v_head,
+                         int B, int S, int Hq, int Hkv, int D, int P, int elem_bytes,
+                         usp_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Document boundaries from the gathered position_ids.  accelerate PR #4209:
+ * position_ids are all-gathered once per forward in the model's pre-hook and
+ * every layer reads them; the per-shard cu_seq_lens_q/k and max_length_q/k a
+ * padding-free collator computed are dropped and rebuilt from the gathered
+ * positions.
+ *
+ * pos:         int32 [P][B][S/P], each rank's shard.  The gathered sequence is
+ *              gathered[b][r*S/P + s'] = pos[r][b][s'] (for B == 1 the buffer
+ *              already *is* the gathered [S], byte for byte).
+ * cu_seqlens:  int32, capacity B*S + 1 (output).  A document starts at every
+ *              row start b*S and wherever the gathered position is 0.
+ *              cu_seqlens[0] = 0, cu_seqlens[n_docs] = B*S, strictly increasing.
+ * n_docs:      int32 device scalar (output): number of documents.
+ * max_len:     int32 device scalar (output): longest document.
+ * ws:          device workspace of at least usp_cu_seqlens_workspace_bytes(B, S)
+ *              bytes, 16-byte aligned; its contents on entry do not matter.
+ * dev_status:  device int32 (nullable): USP_ERR_BAD_POSITIONS if any position is
+ *              negative (the outputs are then unspecified).
+ * Output is bit-exact (integers).  Errors: USP_ERR_INVALID_ARG, USP_ERR_INDIVISIBLE
+ * (S % P), USP_ERR_UNSUPPORTED (B*S >= 2^31 - 1), USP_ERR_WORKSPACE, USP_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+size_t usp_cu_seqlens_workspace_bytes(int B, int S);
+int usp_cu_seqlens_from_position_ids(const int32_t* pos, int B, int S, int P,
+                                     int32_t* cu_seqlens, int32_t* n_docs, int32_t* max_len,
+                                     void* ws, size_t ws_bytes, int32_t* dev_status,
+                                     usp_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Attention over the gathered sequence, all P emulated ranks in one launch.
+ *
+ * For rank r, local query head j (global head r*hq + j, hq = Hq/P), its key/
+ * value head j / (Hq/Hkv), token t of document [a, b): visible keys u are
+ * a <= u <= t (causal; without causal a <= u < b) and t - u <= window_left
+ * when window_left >= 0.  With s = softmax_scale * q_t . k_u and the sink
+ * logit z = sinks[r*hq + j] (not scaled; absent when sinks == NULL):
+ *     LSE_t = ln( sum_u exp(s_tu) + exp(z) )
+ *     O_t   = sum_u exp(s_tu - LSE_t) v_u
+ * (softmax over the keys plus one value-less sink logit; accelerate PR #4209
+ * gpt-oss finding: "attention sinks are one logit per head, so slice s_aux to
+ * the heads each rank holds").
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int B, S, Hq, Hkv, D, P;   /* global sizes; D must be 64 or 128 */
+  int causal;                /* 1: causal mask inside each document; 0: full document */
+  int window_left;           /* -1: none; else t - u <= window_left ("window 128" = 127) */
+  float softmax_scale;       /* 0: 1/sqrt(D) */
+  const int32_t* cu_seqlens; /* device int32 [n_docs+1], from usp_cu_seqlens_from_position_ids */
+  const int32_t* n_docs;     /* device int32 scalar */
+  const float* sinks;        /* device fp32 [Hq] (global heads), or NULL */
+} usp_attn_params;
+
+/* q:   bf16 head-layout [P][B][S][Hq/P][D];  k, v: bf16 [P][B][S][Hkv/P][D]
+ * o:   bf16 head-layout like q (output)
+ * lse: fp32 [P][B][Hq/P][S] natural-log LSE (output; includes the sink)
+ * dev_status: nullable device int32; USP_ERR_BAD_SEQLENS when cu_seqlens does
+ *   not start at 0, is not strictly increasing, or does not end at B*S (the
+ *   outputs are then left unwritten).
+ * Errors: USP_ERR_INVALID_ARG, USP_ERR_INDIVISIBLE, USP_ERR_UNSUPPORTED (D not
+ * 64/128, window_left < -1, B*S too large), USP_ERR_ALIGNMENT, USP_ERR_CUDA. */
+int usp_attn_fwd(const usp_attn_params* params, const void* q, const void* k, const void* v,
+                 void* o, float* lse, int32_t* dev_status, usp_stream_t stream);
+
+/* Bytes of workspace usp_attn_bwd needs: the fp32 row statistic
+ * D_t = sum_d dO_td O_td for every query row and head, 256-byte aligned. */
+size_t usp_attn_bwd_workspace_bytes(const usp_attn_params* params);
+
+/* Gradients of usp_attn_fwd for the loss sum(O * dO):
+ *   P_tu = exp(s_tu - LSE_t), dS_tu = P_tu (dO_t . v_u - D_t)
+ *   dQ_t = scale sum_u dS_tu k_u,   dK_u = scale sum_t dS_tu q_t,
+ *   dV_u = sum_t P_tu dO_t,         dsink = -sum_t exp(z - LSE_t) D_t
+ * (key/value gradients sum over the query heads of their GQA group).
+ * q, k, v, o, lse: the forward's inputs and outputs; dO: bf16 like o.
+ * dq, dk, dv: bf16 outputs shaped like q, k, v.  dsinks: fp32 [Hq] output or
+ * NULL (ignored when params->sinks is NULL).  ws: at least
+ * usp_attn_bwd_workspace_bytes(params) bytes, 256-byte aligned.
+ * The result is deterministic: no floating-point atomics.
+ * Errors: as usp_attn_fwd, plus USP_ERR_WORKSPACE. */
+int usp_attn_bwd(const usp_attn_params* params, const void* q, const void* k, const void* v,
+                 const void* o, const float* lse, const void* dO,
+                 void* dq, void* dk, void* dv, float* dsinks,
+                 void* ws, size_t ws_bytes, int32_t* dev_status, usp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* USP_H_ */

@@ -56,7 +56,7 @@ __all__ = [
     "OracleError",
     "relayout_fwd", "relayout_bwd",
     "cu_seqlens_from_position_ids", "gather_position_ids",
-    "attention_fwd", "attention_bwd",
+    "attention_fwd", "attention_fwd_rows", "attention_bwd",
     "ulysses_fwd", "ulysses_bwd", "unsharded_fwd", "unsharded_bwd",
     "visible_pairs",
 ]
@@ -163,11 +163,16 @@ def cu_seqlens_from_position_ids(pos_shards: np.ndarray) -> Tuple[np.ndarray, in
 # varlen attention over one rank's heads
 # ---------------------------------------------------------------------------
 
-def _visible(i0: int, i1: int, a: int, b: int, causal: bool, window_left: int) -> np.ndarray:
-    """Boolean [i1-i0][b-a]: may query i (global index) see key j of doc [a, b)?"""
+def _visible(i0: int, i1: int, ka: int, kb: int, causal: bool, window_left: int,
+             a: Optional[int] = None, b: Optional[int] = None) -> np.ndarray:
+    """Boolean [i1-i0][kb-ka]: may query i (global index) see key j in [ka, kb)?
+
+    Queries and keys belong to the document [a, b) (default: [ka, kb))."""
+    a = ka if a is None else a
+    b = kb if b is None else b
     i = np.arange(i0, i1)[:, None]
-    j = np.arange(a, b)[None, :]
-    vis = np.ones((i1 - i0, b - a), dtype=bool)
+    j = np.arange(ka, kb)[None, :]
+    vis = (j >= a) & (j < b) & np.ones((i1 - i0, kb - ka), dtype=bool)
     if causal:
         vis &= j <= i
     if window_left >= 0:
@@ -175,6 +180,18 @@ def _visible(i0: int, i1: int, a: int, b: int, causal: bool, window_left: int) -
         if not causal:
             vis &= (j - i) <= window_left
     return vis
+
+
+def _block_key_span(i0: int, i1: int, a: int, b: int, causal: bool, window_left: int):
+    """Keys of document [a, b) that at least one query in [i0, i1) may see."""
+    ka, kb = a, b
+    if causal:
+        kb = i1
+    if window_left >= 0:
+        ka = max(a, i0 - window_left)
+        if not causal:
+            kb = min(b, i1 + window_left)
+    return ka, kb
 
 
 def _doc_row_blocks(a: int, b: int, block: int):
@@ -218,11 +235,13 @@ def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, cu_seqlens: np.nd
         kh = h // G
         t = None if sinks is None else float(sinks[h])
         for a, b in zip(cu[:-1], cu[1:]):
-            K = k[a:b, kh]
-            V = v[a:b, kh]
             for i0, i1 in _doc_row_blocks(a, b, row_block):
+                # keys outside [ka, kb) are hidden from every row of the block
+                ka, kb = _block_key_span(i0, i1, a, b, causal, window_left)
+                K = k[ka:kb, kh]
+                V = v[ka:kb, kh]
                 s = scale * (q[i0:i1, h] @ K.T)
-                s = np.where(_visible(i0, i1, a, b, causal, window_left), s, -np.inf)
+                s = np.where(_visible(i0, i1, ka, kb, causal, window_left, a, b), s, -np.inf)
                 m = s.max(axis=1)
                 if t is not None:
                     m = np.maximum(m, t)
@@ -232,6 +251,37 @@ def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, cu_seqlens: np.nd
                     z = z + np.exp(t - m)
                 LSE[h, i0:i1] = m + np.log(z)
                 O[i0:i1, h] = (e / z[:, None]) @ V
+    return O, LSE
+
+
+def attention_fwd_rows(q, k, v, cu_seqlens, rows, head: int, causal: bool = True,
+                       window_left: int = -1, scale: Optional[float] = None,
+                       sink: Optional[float] = None):
+    """``attention_fwd`` for the listed query rows of one query head only.
+
+    Same definition, evaluated row by row, so that single rows of a very long
+    document can be checked without computing the whole head.  Returns
+    ``O`` [len(rows)][D] and ``LSE`` [len(rows)].
+    """
+    T, hq, D = q.shape
+    G = hq // k.shape[1]
+    kh = head // G
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    O = np.empty((len(rows), D))
+    LSE = np.empty(len(rows))
+    for n, i in enumerate(rows):
+        d = int(np.searchsorted(cu, i, side="right")) - 1
+        a, b = int(cu[d]), int(cu[d + 1])
+        ka, kb = _block_key_span(i, i + 1, a, b, causal, window_left)
+        s = scale * (np.asarray(k[ka:kb, kh], np.float64) @ np.asarray(q[i, head], np.float64))
+        s = np.where(_visible(i, i + 1, ka, kb, causal, window_left, a, b)[0], s, -np.inf)
+        m = s.max() if sink is None else max(s.max(), sink)
+        e = np.exp(s - m)
+        z = e.sum() + (0.0 if sink is None else np.exp(sink - m))
+        LSE[n] = m + np.log(z)
+        O[n] = (e / z) @ np.asarray(v[ka:kb, kh], np.float64)
     return O, LSE
 
 
@@ -272,17 +322,18 @@ def attention_bwd(q, k, v, o, lse, do, cu_seqlens, causal: bool = True, window_l
     for h in range(hq):
         kh = h // G
         for a, b in zip(cu[:-1], cu[1:]):
-            K = k[a:b, kh]
-            V = v[a:b, kh]
             for i0, i1 in _doc_row_blocks(a, b, row_block):
+                ka, kb = _block_key_span(i0, i1, a, b, causal, window_left)
+                K = k[ka:kb, kh]
+                V = v[ka:kb, kh]
                 s = scale * (q[i0:i1, h] @ K.T)
-                vis = _visible(i0, i1, a, b, causal, window_left)
+                vis = _visible(i0, i1, ka, kb, causal, window_left, a, b)
                 Pm = np.where(vis, np.exp(s - lse[h, i0:i1][:, None]), 0.0)
-                dv[a:b, kh] += Pm.T @ do[i0:i1, h]
+                dv[ka:kb, kh] += Pm.T @ do[i0:i1, h]
                 dP = do[i0:i1, h] @ V.T
                 dS = Pm * (dP - Dvec[i0:i1, h][:, None])
                 dq[i0:i1, h] += scale * (dS @ K)
-                dk[a:b, kh] += scale * (dS.T @ q[i0:i1, h])
+                dk[ka:kb, kh] += scale * (dS.T @ q[i0:i1, h])
                 if dsinks is not None:
                     dsinks[h] += -np.sum(np.exp(float(sinks[h]) - lse[h, i0:i1]) * Dvec[i0:i1, h])
     return dq, dk, dv, dsinks

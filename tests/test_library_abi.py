@@ -1,0 +1,61 @@
+"""The C library builds, loads and exports every entry point include/usp.h
+declares; the host-side checks that need no GPU behave."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "usp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(usp_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from ulysses_sequence_long_gb300 import _build, binding
+    _build.build()
+    return binding.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "usp_attn_fwd" in names and "usp_relayout_fwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    from ulysses_sequence_long_gb300 import binding
+    assert sorted(binding.EXPORTED) == names
+
+
+def test_status_strings(lib):
+    from ulysses_sequence_long_gb300 import binding
+    for code in range(10):
+        s = binding.status_string(code)
+        assert s.startswith("USP_")
+    assert binding.status_string(999) == "USP_ERR_UNKNOWN"
+    assert lib.usp_version() >= 100
+
+
+def test_host_checks_without_gpu(lib):
+    from ulysses_sequence_long_gb300 import binding as B
+    # argument checks return before touching the device
+    assert lib.usp_relayout_fwd(None, None, 1, 8, 4, 8, 2, 2, None) == B.USP_ERR_INVALID_ARG
+    p = ctypes.c_void_p(16)
+    assert lib.usp_relayout_fwd(p, ctypes.c_void_p(1 << 20), 1, 8, 6, 8, 4, 2, None) == B.USP_ERR_INDIVISIBLE
+    assert lib.usp_relayout_fwd(p, ctypes.c_void_p(1 << 20), 1, 8, 2, 3, 2, 2, None) == B.USP_ERR_ALIGNMENT
+    assert lib.usp_relayout_fwd(p, ctypes.c_void_p(32), 1, 8, 2, 8, 2, 2, None) == B.USP_ERR_INVALID_ARG  # overlap
+    assert lib.usp_cu_seqlens_workspace_bytes(1, 4096) >= 16
+    prm = B.AttnParams(1, 256, 4, 2, 96, 2, 1, -1, 0.0, 16, 16, None)
+    assert lib.usp_attn_fwd(ctypes.byref(prm), p, p, p, p, p, None, None) == B.USP_ERR_UNSUPPORTED
+    prm = B.AttnParams(1, 256, 4, 2, 64, 4, 1, -1, 0.0, 16, 16, None)
+    assert lib.usp_attn_fwd(ctypes.byref(prm), p, p, p, p, p, None, None) == B.USP_ERR_INDIVISIBLE
+    prm = B.AttnParams(1, 256, 4, 2, 64, 2, 1, -5, 0.0, 16, 16, None)
+    assert lib.usp_attn_fwd(ctypes.byref(prm), p, p, p, p, p, None, None) == B.USP_ERR_UNSUPPORTED
+    prm = B.AttnParams(1, 256, 4, 2, 64, 2, 1, -1, -1.0, 16, 16, None)
+    assert lib.usp_attn_fwd(ctypes.byref(prm), p, p, p, p, p, None, None) == B.USP_ERR_INVALID_ARG
+    prm = B.AttnParams(1, 256, 4, 2, 64, 2, 1, -1, 0.0, 16, 16, None)
+    assert lib.usp_attn_fwd(ctypes.byref(prm), ctypes.c_void_p(18), p, p, p, p, None, None) == B.USP_ERR_ALIGNMENT

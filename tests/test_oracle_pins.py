@@ -392,3 +392,24 @@ def test_visible_pairs_closed_forms():
     assert oracle.visible_pairs([0, 100, 190, 256]) == 100 * 101 // 2 + 90 * 91 // 2 + 66 * 67 // 2
     L, w = 1000, 127
     assert oracle.visible_pairs([0, L], window_left=w) == sum(min(i + 1, w + 1) for i in range(L))
+
+
+def test_fwd_rows_agree_with_sdpa_rows():
+    q, k, v = _rand_qkv(45, 4, 2, 8, seed=20)
+    cu = [0, 20, 45]
+    rows = [0, 5, 19, 20, 33, 44]
+    t = np.array([0.2, -0.5, 1.0, 0.0])
+    for h in range(4):
+        O, L = oracle.attention_fwd_rows(q, k, v, cu, rows, h, window_left=6, sink=t[h])
+        # reference: the logits of the row written out with torch, hidden keys
+        # at -inf and the sink appended as one more logit (value row zero)
+        for n, i in enumerate(rows):
+            a, b = (0, 20) if i < 20 else (20, 45)
+            jj = np.arange(a, b)
+            seen = (jj <= i) & (i - jj <= 6)
+            logits = torch.from_numpy(k[a:b, h // 2] @ q[i, h] / np.sqrt(8))
+            logits = torch.where(torch.from_numpy(seen), logits, torch.tensor(-np.inf, dtype=torch.float64))
+            lg = torch.cat([logits, torch.tensor([t[h]], dtype=torch.float64)])
+            ref_o = torch.softmax(lg, 0)[:-1] @ torch.from_numpy(v[a:b, h // 2])
+            np.testing.assert_allclose(O[n], ref_o.numpy(), rtol=0, atol=1e-12)
+            np.testing.assert_allclose(L[n], torch.logsumexp(lg, 0).item(), rtol=1e-13)

@@ -1,0 +1,199 @@
+// usp_api.cu — the extern "C" entry points of include/usp.h: argument checks,
+// workspace carving, tensor-map encoding and dispatch to the kernels.  No
+// entry point allocates device memory or synchronises the stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "usp_attn_common.cuh"
+#include "usp_internal.h"
+
+namespace usp {
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> g(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+int check_launch() { return cudaGetLastError() == cudaSuccess ? USP_OK : USP_ERR_CUDA; }
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int make_head_tmap(CUtensorMap* m, const void* base, int P, int BS, int H, int D, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return USP_ERR_CUDA;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(BS),
+                        static_cast<cuuint64_t>(P)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                           static_cast<cuuint64_t>(BS) * H * D * 2};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult rc = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS ? USP_OK : USP_ERR_CUDA;
+}
+
+}  // namespace usp
+
+using namespace usp;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_relayout_args(const void* a, const void* b, int B, int S, int H, int D, int P, int eb) {
+  if (a == nullptr || b == nullptr) return USP_ERR_INVALID_ARG;
+  if (B <= 0 || S <= 0 || H <= 0 || D <= 0 || P <= 0) return USP_ERR_INVALID_ARG;
+  if (eb != 1 && eb != 2 && eb != 4 && eb != 8) return USP_ERR_INVALID_ARG;
+  if (H % P != 0 || S % P != 0) return USP_ERR_INDIVISIBLE;
+  uint64_t run = static_cast<uint64_t>(H / P) * D * eb;
+  if (run % 16 != 0 || !aligned16(a) || !aligned16(b)) return USP_ERR_ALIGNMENT;
+  uint64_t vec = static_cast<uint64_t>(B) * S * H * D * eb / 16;
+  if (vec >= (1ull << 32) || static_cast<uint64_t>(P) * B * S >= (1ull << 32)) return USP_ERR_UNSUPPORTED;
+  const char* pa = static_cast<const char*>(a);
+  const char* pb = static_cast<const char*>(b);
+  uint64_t bytes = vec * 16;
+  if (pa < pb + bytes && pb < pa + bytes) return USP_ERR_INVALID_ARG;  // buffers overlap
+  return USP_OK;
+}
+
+int check_attn_params(const usp_attn_params* p) {
+  if (p == nullptr) return USP_ERR_INVALID_ARG;
+  if (p->B <= 0 || p->S <= 0 || p->Hq <= 0 || p->Hkv <= 0 || p->D <= 0 || p->P <= 0) return USP_ERR_INVALID_ARG;
+  if (p->cu_seqlens == nullptr || p->n_docs == nullptr) return USP_ERR_INVALID_ARG;
+  if (p->causal != 0 && p->causal != 1) return USP_ERR_INVALID_ARG;
+  if (p->window_left < -1) return USP_ERR_UNSUPPORTED;
+  if (!(p->softmax_scale >= 0.f) || isinf(p->softmax_scale)) return USP_ERR_INVALID_ARG;
+  if (p->Hq % p->P != 0 || p->Hkv % p->P != 0 || p->Hq % p->Hkv != 0 || p->S % p->P != 0)
+    return USP_ERR_INDIVISIBLE;
+  if (p->D != 64 && p->D != 128) return USP_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(p->B) * p->S >= (1ll << 30)) return USP_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(p->P) * p->B * p->S * p->Hq * p->D >= (1ll << 40)) return USP_ERR_UNSUPPORTED;
+  return USP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* usp_status_string(int s) {
+  switch (s) {
+    case USP_OK: return "USP_OK";
+    case USP_ERR_INVALID_ARG: return "USP_ERR_INVALID_ARG: null pointer, bad size or flag, or overlapping buffers";
+    case USP_ERR_INDIVISIBLE: return "USP_ERR_INDIVISIBLE: sp size must divide S and the heads, Hkv must divide Hq";
+    case USP_ERR_UNSUPPORTED: return "USP_ERR_UNSUPPORTED: head dim, element size or problem size not supported";
+    case USP_ERR_ALIGNMENT: return "USP_ERR_ALIGNMENT: pointers and contiguous runs must be 16-byte aligned";
+    case USP_ERR_BAD_SEQLENS: return "USP_ERR_BAD_SEQLENS: cu_seqlens does not describe the gathered sequence";
+    case USP_ERR_BAD_POSITIONS: return "USP_ERR_BAD_POSITIONS: negative position id";
+    case USP_ERR_TIMEOUT: return "USP_ERR_TIMEOUT: a bounded wait inside a kernel gave up";
+    case USP_ERR_CUDA: return "USP_ERR_CUDA: CUDA call or launch failed";
+    case USP_ERR_WORKSPACE: return "USP_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    default: return "USP_ERR_UNKNOWN";
+  }
+}
+
+int usp_version(void) { return 100; }
+
+int usp_relayout_fwd(const void* x_seq, void* x_head, int B, int S, int H, int D, int P, int eb,
+                     usp_stream_t stream) {
+  int rc = check_relayout_args(x_seq, x_head, B, S, H, D, P, eb);
+  if (rc != USP_OK) return rc;
+  return launch_relayout(x_seq, x_head, B, S, H, D, P, eb, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_relayout_bwd(const void* x_head, void* x_seq, int B, int S, int H, int D, int P, int eb,
+                     usp_stream_t stream) {
+  int rc = check_relayout_args(x_head, x_seq, B, S, H, D, P, eb);
+  if (rc != USP_OK) return rc;
+  return launch_relayout(x_head, x_seq, B, S, H, D, P, eb, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_relayout_fwd_qkv(const void* q_seq, const void* k_seq, const void* v_seq, void* q_head, void* k_head,
+                         void* v_head, int B, int S, int Hq, int Hkv, int D, int P, int eb, usp_stream_t stream) {
+  int rc;
+  if ((rc = check_relayout_args(q_seq, q_head, B, S, Hq, D, P, eb)) != USP_OK) return rc;
+  if ((rc = check_relayout_args(k_seq, k_head, B, S, Hkv, D, P, eb)) != USP_OK) return rc;
+  if ((rc = check_relayout_args(v_seq, v_head, B, S, Hkv, D, P, eb)) != USP_OK) return rc;
+  const void* src[3] = {q_seq, k_seq, v_seq};
+  void* dst[3] = {q_head, k_head, v_head};
+  int H[3] = {Hq, Hkv, Hkv};
+  return launch_relayout_qkv(src, dst, H, B, S, D, P, eb, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t usp_cu_seqlens_workspace_bytes(int B, int S) {
+  if (B <= 0 || S <= 0) return 0;
+  return cu_seqlens_ws_bytes(B, S);
+}
+
+int usp_cu_seqlens_from_position_ids(const int32_t* pos, int B, int S, int P, int32_t* cu_seqlens, int32_t* n_docs,
+                                     int32_t* max_len, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                     usp_stream_t stream) {
+  if (pos == nullptr || cu_seqlens == nullptr || n_docs == nullptr || max_len == nullptr) return USP_ERR_INVALID_ARG;
+  if (B <= 0 || S <= 0 || P <= 0) return USP_ERR_INVALID_ARG;
+  if (S % P != 0) return USP_ERR_INDIVISIBLE;
+  if (static_cast<int64_t>(B) * S >= 0x7FFFFFFFll) return USP_ERR_UNSUPPORTED;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 15u) || ws_bytes < cu_seqlens_ws_bytes(B, S))
+    return USP_ERR_WORKSPACE;
+  return launch_cu_seqlens(pos, B, S, P, cu_seqlens, n_docs, max_len, static_cast<int32_t*>(ws), dev_status,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_attn_fwd(const usp_attn_params* params, const void* q, const void* k, const void* v, void* o, float* lse,
+                 int32_t* dev_status, usp_stream_t stream) {
+  int rc = check_attn_params(params);
+  if (rc != USP_OK) return rc;
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr) return USP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return USP_ERR_ALIGNMENT;
+  return launch_attn_fwd(*params, q, k, v, o, lse, dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t usp_attn_bwd_workspace_bytes(const usp_attn_params* params) {
+  if (check_attn_params(params) != USP_OK) return 0;
+  return attn_bwd_ws_bytes(*params);
+}
+
+int usp_attn_bwd(const usp_attn_params* params, const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const void* dO, void* dq, void* dk, void* dv, float* dsinks, void* ws,
+                 size_t ws_bytes, int32_t* dev_status, usp_stream_t stream) {
+  int rc = check_attn_params(params);
+  if (rc != USP_OK) return rc;
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr || dO == nullptr ||
+      dq == nullptr || dk == nullptr || dv == nullptr)
+    return USP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dO) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return USP_ERR_ALIGNMENT;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < attn_bwd_ws_bytes(*params))
+    return USP_ERR_WORKSPACE;
+  return launch_attn_bwd(*params, q, k, v, o, lse, dO, dq, dk, dv, params->sinks ? dsinks : nullptr, ws, dev_status,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,115 @@
+// usp_attn_common.cuh — pieces shared by the forward and backward attention
+// kernels: kernel parameters, document lookup in cu_seqlens, the visibility
+// rule, the validity check of cu_seqlens and the tensor-map encoder.
+//
+// Visibility (the varlen mask over the gathered sequence): token t of document
+// [a, b) sees key u when a <= u < b, u <= t if causal, and t - u <= window_left
+// (also u - t <= window_left when not causal) if window_left >= 0.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/usp.h"
+#include "usp_ptx.cuh"
+
+namespace usp {
+
+constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
+constexpr int kBN = 128;  // keys per tile
+
+struct AttnArgs {
+  int BS;           // tokens per rank: B*S
+  int S;            // row length
+  int B, P, hq, hk, G;
+  int causal, window_left;
+  float scale;       // softmax scale
+  float scale_log2;  // softmax scale * log2(e)
+  const int32_t* cu;
+  const int32_t* n_docs;
+  const float* sinks;  // global [Hq] or null
+  int32_t* status;
+};
+
+// Document index d with cu[d] <= t < cu[d+1] (cu assumed valid, n >= 1).
+__device__ __forceinline__ int find_doc(const int32_t* __restrict__ cu, int n, int t) {
+  int lo = 0, hi = n;  // invariant: cu[lo] <= t < cu[hi]
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (__ldg(cu + mid) <= t) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// [start, end) of the document holding token t, clamped so that a malformed
+// cu_seqlens (already reported) can never send an index out of [0, BS).
+__device__ __forceinline__ void doc_bounds(const int32_t* __restrict__ cu, int n, int BS, int t, int& a, int& b) {
+  int d = find_doc(cu, n, t);
+  a = __ldg(cu + d);
+  b = __ldg(cu + d + 1);
+  a = max(0, min(a, t));
+  b = min(BS, max(b, t + 1));
+}
+
+__device__ __forceinline__ bool visible(int t, int u, int a, int b, int causal, int wl) {
+  bool v = (u >= a) && (u < b);
+  if (causal) v = v && (u <= t);
+  if (wl >= 0) v = v && (t - u <= wl) && (causal || u - t <= wl);
+  return v;
+}
+
+// First and one-past-last key any of the rows [t_first, t_last] may see.
+__device__ __forceinline__ void key_range(const AttnArgs& p, int n, int t_first, int t_last, int& lo, int& hi) {
+  int a0, b0, a1, b1;
+  doc_bounds(p.cu, n, p.BS, t_first, a0, b0);
+  doc_bounds(p.cu, n, p.BS, t_last, a1, b1);
+  lo = a0;
+  hi = p.causal ? t_last + 1 : b1;
+  if (p.window_left >= 0) {
+    lo = max(lo, t_first - p.window_left);
+    if (!p.causal) hi = min(hi, t_last + p.window_left + 1);
+  }
+}
+
+// First and one-past-last query row that may see any of the keys [u_first, u_last].
+__device__ __forceinline__ void query_range(const AttnArgs& p, int n, int u_first, int u_last, int& lo, int& hi) {
+  int a0, b0, a1, b1;
+  doc_bounds(p.cu, n, p.BS, u_first, a0, b0);
+  doc_bounds(p.cu, n, p.BS, u_last, a1, b1);
+  lo = p.causal ? u_first : a0;
+  hi = b1;
+  if (p.window_left >= 0) {
+    hi = min(hi, u_last + p.window_left + 1);
+    if (!p.causal) lo = max(lo, u_first - p.window_left);
+  }
+}
+
+// Cheap per-CTA check of cu_seqlens: returns n_docs, or 0 (after recording
+// USP_ERR_BAD_SEQLENS) when it cannot describe the gathered sequence.  Block 0
+// also checks that every document is non-empty.
+__device__ __forceinline__ int checked_docs(const AttnArgs& p) {
+  int n = __ldg(p.n_docs);
+  bool ok = n >= 1 && n <= p.BS;
+  if (ok) ok = __ldg(p.cu) == 0 && __ldg(p.cu + n) == p.BS;
+  if (!ok) {
+    if (threadIdx.x == 0) set_status(p.status, USP_ERR_BAD_SEQLENS);
+    return 0;
+  }
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+    for (int d = threadIdx.x; d < n; d += blockDim.x)
+      if (__ldg(p.cu + d + 1) <= __ldg(p.cu + d)) set_status(p.status, USP_ERR_BAD_SEQLENS);
+  }
+  return n;
+}
+
+}  // namespace usp
+
+// ------------------------------------------------------------------ host side
+namespace usp {
+
+// Tensor map of a head-layout bf16 tensor [P][BS][H][D]: dims {D, H, BS, P},
+// box {64, 1, rows, 1}, 128-byte swizzle (one 128-byte row per token).
+int make_head_tmap(CUtensorMap* m, const void* base, int P, int BS, int H, int D, int box_rows);
+
+}  // namespace usp

@@ -1,0 +1,390 @@
+// usp_attn_fwd.cu — varlen causal GQA attention forward on the 5th-generation
+// tensor core (tcgen05), one launch for all P emulated ranks.
+//
+// What it computes (huggingface/accelerate PR #4209: attention runs on the
+// gathered sequence of the rank's heads; sinks are one logit per head sliced
+// to the rank's heads; sliding windows and packing keep working): for every
+// rank r, local query head j, token t,
+//     LSE_t = ln( sum_{u visible} exp(scale q_t.k_u) + exp(z_{r*hq+j}) )
+//     O_t   = sum_{u visible} exp(scale q_t.k_u - LSE_t) v_u
+//
+// CTA = one (rank, query head, block of 256 query rows) = two 128-row Q tiles
+// that share every K/V tile.  Warp roles (320 threads):
+//   warps 0-3   softmax for Q tile 0 (thread = query row = TMEM lane)
+//   warps 4-7   softmax for Q tile 1
+//   warp  8     TMA producer: Q tiles once, then a ring of K/V stages
+//   warp  9     MMA issuer (one thread): S_q = Q_q K^T into TMEM, then
+//               O_q += P_q V with P_q read from TMEM (bf16, written over S_q)
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
+// The MMA thread alternates the two tiles (PV_0, S_0 next, PV_1, S_1 next), so
+// the tensor core works on one tile while the other tile's softmax runs.
+//
+// Online softmax in the log2 domain with a lazy rescale: the running max only
+// moves when a row's new max exceeds it by more than 8 (a factor 256), and the
+// O row in TMEM is rescaled then.  Because S_q[n] is committed after
+// PV_q[n-1], waiting for S_q[n] also guarantees PV_q[n-1] has finished, so the
+// softmax threads may rescale O without another barrier.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "usp_attn_common.cuh"
+#include "usp_internal.h"
+
+namespace usp {
+
+namespace fwd {
+
+constexpr int kThreads = 320;
+constexpr int kAtomBytes = kBM * 128;  // one 64-column (128-byte) swizzle column of a 128-row tile
+
+template <int D>
+struct Cfg {
+  static constexpr int NCH = D / 64;                  // 64-wide column atoms per row
+  static constexpr int ST = (D == 128) ? 2 : 4;       // K/V pipeline stages
+  static constexpr int TILE = NCH * kAtomBytes;       // bytes of one 128-row tile
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * TILE;
+  static constexpr int OFF_V = OFF_K + ST * TILE;
+  static constexpr int OFF_BAR = OFF_V + ST * TILE;
+  static constexpr int SMEM = OFF_BAR + 1024 + 1024;  // barriers + alignment slack
+};
+
+struct Bars {
+  uint64_t q_full[2];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_final[2];
+  uint64_t mma_done;
+  uint64_t k_full[4];
+  uint64_t v_full[4];
+  uint64_t kv_empty[4];
+  uint32_t tmem;
+  int abort;
+};
+
+struct Out {
+  __nv_bfloat16* o;
+  float* lse;
+  int nqb;  // 256-row query blocks per (rank, head)
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, AttnArgs p, Out out) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- work unit: late query blocks first (they see the most keys); the
+  // query heads of one key/value head are adjacent, so they share K/V in L2.
+  const int per_blk = p.P * p.hq;
+  const int qb = out.nqb - 1 - static_cast<int>(blockIdx.x) / per_blk;
+  const int rem = static_cast<int>(blockIdx.x) % per_blk;
+  const int r = rem / p.hq, j = rem % p.hq, kvh = j / p.G;
+  const int t0 = qb * 2 * kBM;
+
+  const int n_docs = checked_docs(p);
+  if (n_docs == 0) return;
+
+  bool tile_ok[2];
+  int lo = 0x7FFFFFFF, hi = 0;
+  for (int q = 0; q < 2; ++q) {
+    int first = t0 + q * kBM;
+    tile_ok[q] = first < p.BS;
+    if (tile_ok[q]) {
+      int last = min(first + kBM, p.BS) - 1, l0, h0;
+      key_range(p, n_docs, first, last, l0, h0);
+      lo = min(lo, l0);
+      hi = max(hi, h0);
+    }
+  }
+  const int n_kv = (hi - lo + kBN - 1) / kBN;
+
+  if (tid == 0) {
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&bars->q_full[q], 1);
+      mbar_init(&bars->s_full[q], 1);
+      mbar_init(&bars->p_full[q], 4);
+      mbar_init(&bars->o_final[q], 1);
+    }
+    mbar_init(&bars->mma_done, 1);
+    for (int s = 0; s < C::ST; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem, 512);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  volatile int* abort = &bars->abort;
+  const uint32_t sbase = smem_u32(smem);
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      for (int q = 0; q < 2; ++q) {
+        if (!tile_ok[q]) continue;
+        mbar_arrive_expect_tx(&bars->q_full[q], C::TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_4d(smem + C::OFF_Q + q * C::TILE + c * kAtomBytes, &tq, &bars->q_full[q], c * 64, j,
+                      t0 + q * kBM, r);
+      }
+      int issued = 0;
+      for (int n = 0; n < n_kv; ++n) {
+        const int st = n % C::ST;
+        if (n >= C::ST && !mbar_wait(&bars->kv_empty[st], ((n / C::ST) - 1) & 1, abort, p.status)) break;
+        const int kv0 = lo + n * kBN;
+        mbar_arrive_expect_tx(&bars->k_full[st], C::TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_4d(smem + C::OFF_K + st * C::TILE + c * kAtomBytes, &tk, &bars->k_full[st], c * 64, kvh, kv0, r);
+        mbar_arrive_expect_tx(&bars->v_full[st], C::TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_4d(smem + C::OFF_V + st * C::TILE + c * kAtomBytes, &tv, &bars->v_full[st], c * 64, kvh, kv0, r);
+        issued = n + 1;
+      }
+      // Never leave the CTA with copies still landing in its shared memory.
+      for (int n = max(0, issued - C::ST); n < issued; ++n) {
+        mbar_wait(&bars->k_full[n % C::ST], (n / C::ST) & 1, abort, p.status);
+        mbar_wait(&bars->v_full[n % C::ST], (n / C::ST) & 1, abort, p.status);
+      }
+      for (int q = 0; q < 2; ++q)
+        if (tile_ok[q]) mbar_wait(&bars->q_full[q], 0, abort, p.status);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16(kBM, D, false, true);
+      bool ok = true;
+      for (int q = 0; q < 2 && ok; ++q)
+        if (tile_ok[q]) ok = mbar_wait(&bars->q_full[q], 0, abort, p.status);
+      auto issue_s = [&](int q, int st) {
+        const uint32_t qa = sbase + C::OFF_Q + q * C::TILE;
+        const uint32_t ka = sbase + C::OFF_K + st * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+          mma_ss(tmem + q * kBN, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_s,
+                 kk > 0);
+        }
+      };
+      auto issue_pv = [&](int q, int st, bool acc) {
+        const uint32_t va = sbase + C::OFF_V + st * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tmem + 256 + q * D, tmem + q * kBN + kk * 8, sdesc_sw128(va + kk * 16 * 128, kAtomBytes, 1024),
+                 idesc_o, (acc || kk > 0) ? 1u : 0u);
+      };
+      if (ok) ok = mbar_wait(&bars->k_full[0], 0, abort, p.status);
+      if (ok) {
+        tc_fence_after();
+        for (int q = 0; q < 2; ++q)
+          if (tile_ok[q]) {
+            issue_s(q, 0);
+            mma_commit(&bars->s_full[q]);
+          }
+      }
+      for (int n = 0; n < n_kv && ok; ++n) {
+        const int st = n % C::ST;
+        if (!(ok = mbar_wait(&bars->v_full[st], (n / C::ST) & 1, abort, p.status))) break;
+        bool next_k_ready = false;
+        for (int q = 0; q < 2 && ok; ++q) {
+          if (!tile_ok[q]) continue;
+          if (!(ok = mbar_wait(&bars->p_full[q], n & 1, abort, p.status))) break;
+          tc_fence_after();
+          issue_pv(q, st, n > 0);
+          if (n + 1 < n_kv) {
+            if (!next_k_ready) {
+              const int st1 = (n + 1) % C::ST;
+              if (!(ok = mbar_wait(&bars->k_full[st1], ((n + 1) / C::ST) & 1, abort, p.status))) break;
+              tc_fence_after();
+              next_k_ready = true;
+            }
+            issue_s(q, (n + 1) % C::ST);
+            mma_commit(&bars->s_full[q]);
+          } else {
+            mma_commit(&bars->o_final[q]);
+          }
+        }
+        mma_commit(&bars->kv_empty[st]);
+      }
+      // Every MMA issued above has finished before TMEM can be released.
+      mma_commit(&bars->mma_done);
+      mbar_wait(&bars->mma_done, 0, abort, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int q = warp >> 2;            // which Q tile
+    const int row = tid & 127;          // TMEM lane = row of the tile
+    const int t = t0 + q * kBM + row;   // rank-local token
+    const bool row_ok = t < p.BS;
+    const uint32_t lane_base = tmem + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
+    const uint32_t s_tm = lane_base + q * kBN;
+    const uint32_t o_tm = lane_base + 256 + q * D;
+    int a = 0, b = 0;
+    if (row_ok) doc_bounds(p.cu, n_docs, p.BS, t, a, b);
+    const int gh = r * p.hq + j;  // global query head: the sink slice of this rank
+    float m = -INFINITY, l = 0.f;
+    if (p.sinks != nullptr) {
+      m = __ldg(p.sinks + gh) * 1.4426950408889634f;
+      l = 1.f;
+    }
+    bool ok = tile_ok[q];
+    for (int n = 0; n < n_kv && ok; ++n) {
+      if (!(ok = mbar_wait(&bars->s_full[q], n & 1, abort, p.status))) break;
+      tc_fence_after();
+      uint32_t sr[kBN / 32][32];
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) tmem_ld32(s_tm + c * 32, sr[c]);
+      tmem_wait_ld();
+      float s[kBN];
+#pragma unroll
+      for (int c = 0; c < kBN; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+      const int kv0 = lo + n * kBN;
+      // rows whose keys in this tile are all visible skip the per-element mask
+      bool full = row_ok && kv0 >= a && kv0 + kBN <= b && (!p.causal || kv0 + kBN - 1 <= t);
+      if (p.window_left >= 0) full = full && (t - kv0 <= p.window_left) && (p.causal || kv0 + kBN - 1 - t <= p.window_left);
+      if (!full) {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          if (!(row_ok && visible(t, kv0 + c, a, b, p.causal, p.window_left))) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+      const float m_tile = mx * p.scale_log2;  // -inf stays -inf
+      const float m_new = fmaxf(m, m_tile);
+      const bool need = m_new > m + 8.f;
+      if (__any_sync(0xffffffffu, need)) {
+        const float alpha = need ? ex2(m - m_new) : 1.f;
+        if (need) {
+          l *= alpha;
+          m = m_new;
+        }
+        if (n > 0) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(o_tm + c * 32, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32(o_tm + c * 32, ov);
+          }
+        }
+      }
+      const float m_use = (m == -INFINITY) ? 0.f : m;
+      float rs = 0.f;
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int c = 0; c < kBN / 2; ++c) {
+        const float p0 = ex2(fmaf(s[2 * c], p.scale_log2, -m_use));
+        const float p1 = ex2(fmaf(s[2 * c + 1], p.scale_log2, -m_use));
+        rs += p0 + p1;
+        pk[c >> 5][c & 31] = pack_bf16x2(p0, p1);
+      }
+      l += rs;
+      tmem_st32(s_tm, pk[0]);
+      tmem_st32(s_tm + 32, pk[1]);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[q]);
+    }
+    // ---- epilogue: O /= l, bf16 out; LSE = ln(sum) including the sink
+    if (ok && (ok = mbar_wait(&bars->o_final[q], 0, abort, p.status))) {
+      tc_fence_after();
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = out.o + (static_cast<size_t>(r) * p.BS + (row_ok ? t : 0)) * p.hq * D +
+                            static_cast<size_t>(j) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(o_tm + c * 32, ov);
+        tmem_wait_ld();
+        uint32_t pkd[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pkd[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pkd[4 * e], pkd[4 * e + 1], pkd[4 * e + 2], pkd[4 * e + 3]);
+        }
+      }
+      if (row_ok) {
+        const int bb = t / p.S, ss = t - bb * p.S;
+        out.lse[(static_cast<size_t>(r * p.B + bb) * p.hq + j) * p.S + ss] =
+            l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace fwd
+
+template <int D>
+static int run_fwd(const usp_attn_params& prm, const AttnArgs& a, const void* q, const void* k, const void* v,
+                   void* o, float* lse, cudaStream_t st) {
+  CUtensorMap tq, tk, tv;
+  int rc;
+  if ((rc = make_head_tmap(&tq, q, a.P, a.BS, a.hq, D, kBM)) != USP_OK) return rc;
+  if ((rc = make_head_tmap(&tk, k, a.P, a.BS, a.hk, D, kBN)) != USP_OK) return rc;
+  if ((rc = make_head_tmap(&tv, v, a.P, a.BS, a.hk, D, kBN)) != USP_OK) return rc;
+  fwd::Out out{static_cast<__nv_bfloat16*>(o), lse, (a.BS + 2 * kBM - 1) / (2 * kBM)};
+  const int smem = fwd::Cfg<D>::SMEM;
+  if (cudaFuncSetAttribute(fwd::attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return USP_ERR_CUDA;
+  const unsigned grid = static_cast<unsigned>(out.nqb) * a.P * a.hq;
+  fwd::attn_fwd_kernel<D><<<grid, fwd::kThreads, smem, st>>>(tq, tk, tv, a, out);
+  (void)prm;
+  return check_launch();
+}
+
+int launch_attn_fwd(const usp_attn_params& prm, const void* q, const void* k, const void* v, void* o, float* lse,
+                    int32_t* status, cudaStream_t st) {
+  AttnArgs a;
+  a.B = prm.B;
+  a.S = prm.S;
+  a.BS = prm.B * prm.S;
+  a.P = prm.P;
+  a.hq = prm.Hq / prm.P;
+  a.hk = prm.Hkv / prm.P;
+  a.G = prm.Hq / prm.Hkv;
+  a.causal = prm.causal ? 1 : 0;
+  a.window_left = prm.window_left;
+  a.scale = prm.softmax_scale > 0.f ? prm.softmax_scale : 1.0f / sqrtf(static_cast<float>(prm.D));
+  a.scale_log2 = a.scale * 1.4426950408889634f;
+  a.cu = prm.cu_seqlens;
+  a.n_docs = prm.n_docs;
+  a.sinks = prm.sinks;
+  a.status = status;
+  if (prm.D == 128) return run_fwd<128>(prm, a, q, k, v, o, lse, st);
+  return run_fwd<64>(prm, a, q, k, v, o, lse, st);
+}
+
+}  // namespace usp

@@ -1,0 +1,53 @@
+// usp_internal.h — host-side declarations shared by the library's translation
+// units (launchers behind the C entry points of include/usp.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/usp.h"
+
+namespace usp {
+
+// SM count of the current device (cached per device).
+int device_sm_count();
+
+// Records a CUDA error of the last launch as USP_ERR_CUDA.
+int check_launch();
+
+// Exact unsigned 32-bit division by a runtime constant (multiply-high and
+// shift, Granlund & Montgomery 1994, "Division by invariant integers using
+// multiplication", round-up variant).
+struct FastDiv {
+  uint32_t d, m, s;
+  FastDiv() : d(1), m(0), s(0) {}
+  explicit FastDiv(uint32_t div) : d(div) {
+    s = 0;
+    while ((1ull << s) < div) ++s;
+    m = static_cast<uint32_t>(((1ull << 32) * ((1ull << s) - div)) / div + 1);
+  }
+#ifdef __CUDACC__
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    uint32_t hi = __umulhi(n, m);
+    return static_cast<uint32_t>((static_cast<uint64_t>(hi) + n) >> s);
+  }
+#endif
+};
+
+int launch_relayout(const void* src, void* dst, int B, int S, int H, int D, int P, int elem_bytes, bool to_head,
+                    cudaStream_t st);
+int launch_relayout_qkv(const void* const src[3], void* const dst[3], const int H[3], int B, int S, int D, int P,
+                        int elem_bytes, cudaStream_t st);
+int launch_cu_seqlens(const int32_t* pos, int B, int S, int P, int32_t* cu, int32_t* n_docs, int32_t* max_len,
+                      int32_t* ws, int32_t* status, cudaStream_t st);
+size_t cu_seqlens_ws_bytes(int B, int S);
+
+int launch_attn_fwd(const usp_attn_params& p, const void* q, const void* k, const void* v, void* o, float* lse,
+                    int32_t* status, cudaStream_t st);
+int launch_attn_bwd(const usp_attn_params& p, const void* q, const void* k, const void* v, const void* o,
+                    const float* lse, const void* dO, void* dq, void* dk, void* dv, float* dsinks, void* ws,
+                    int32_t* status, cudaStream_t st);
+size_t attn_bwd_ws_bytes(const usp_attn_params& p);
+
+}  // namespace usp
