@@ -56,7 +56,8 @@ __all__ = [
     "OracleError",
     "relayout_fwd", "relayout_bwd",
     "cu_seqlens_from_position_ids", "gather_position_ids",
-    "attention_fwd", "attention_fwd_rows", "attention_bwd",
+    "attention_fwd", "attention_fwd_rows", "attention_bwd", "attention_bwd_rows",
+    "attention_bwd_keys",
     "ulysses_fwd", "ulysses_bwd", "unsharded_fwd", "unsharded_bwd",
     "visible_pairs",
 ]
@@ -287,7 +288,7 @@ def attention_fwd_rows(q, k, v, cu_seqlens, rows, head: int, causal: bool = True
 
 def attention_bwd(q, k, v, o, lse, do, cu_seqlens, causal: bool = True, window_left: int = -1,
                   scale: Optional[float] = None, sinks: Optional[np.ndarray] = None,
-                  row_block: int = 512):
+                  row_block: int = 512, heads: Optional[list] = None):
     """Gradients of ``attention_fwd`` for the loss sum(O * dO).
 
     With P_ij = exp(s_ij - LSE_i) (zero where key j is hidden from i) and
@@ -301,7 +302,9 @@ def attention_bwd(q, k, v, o, lse, do, cu_seqlens, causal: bool = True, window_l
         dt    = -sum_i exp(t - LSE_i) D_i          (sink logit of the head)
 
     Key/value gradients of a GQA group sum over its query heads.  Returns
-    ``dq, dk, dv, dsinks`` (dsinks None without sinks), float64.
+    ``dq, dk, dv, dsinks`` (dsinks None without sinks), float64.  ``heads``
+    restricts the sums to those query heads (a whole GQA group gives that
+    key/value head's complete gradients).
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -319,7 +322,7 @@ def attention_bwd(q, k, v, o, lse, do, cu_seqlens, causal: bool = True, window_l
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
     dsinks = None if sinks is None else np.zeros(hq)
-    for h in range(hq):
+    for h in (range(hq) if heads is None else heads):
         kh = h // G
         for a, b in zip(cu[:-1], cu[1:]):
             for i0, i1 in _doc_row_blocks(a, b, row_block):
@@ -337,6 +340,71 @@ def attention_bwd(q, k, v, o, lse, do, cu_seqlens, causal: bool = True, window_l
                 if dsinks is not None:
                     dsinks[h] += -np.sum(np.exp(float(sinks[h]) - lse[h, i0:i1]) * Dvec[i0:i1, h])
     return dq, dk, dv, dsinks
+
+
+def attention_bwd_rows(q, k, v, do, cu_seqlens, rows, head: int, causal: bool = True,
+                       window_left: int = -1, scale: Optional[float] = None,
+                       sink: Optional[float] = None):
+    """dQ of the listed query rows of one head, each row from its own forward.
+
+    Row t needs only its own O_t, LSE_t and D_t = dO_t . O_t, so a single row
+    of a very long document is checked without the whole head.
+    """
+    T, hq, D = q.shape
+    kh = head // (hq // k.shape[1])
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    O, L = attention_fwd_rows(q, k, v, cu_seqlens, rows, head, causal, window_left, scale, sink)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    dq = np.empty((len(rows), D))
+    for n, t in enumerate(rows):
+        d = int(np.searchsorted(cu, t, side="right")) - 1
+        a, b = int(cu[d]), int(cu[d + 1])
+        ka, kb = _block_key_span(t, t + 1, a, b, causal, window_left)
+        K = np.asarray(k[ka:kb, kh], np.float64)
+        V = np.asarray(v[ka:kb, kh], np.float64)
+        dot = np.asarray(do[t, head], np.float64)
+        s = scale * (K @ np.asarray(q[t, head], np.float64))
+        Pm = np.where(_visible(t, t + 1, ka, kb, causal, window_left, a, b)[0], np.exp(s - L[n]), 0.0)
+        dS = Pm * (V @ dot - dot @ O[n])
+        dq[n] = scale * (dS @ K)
+    return dq
+
+
+def attention_bwd_keys(q, k, v, do, cu_seqlens, keys, kv_head: int, causal: bool = True,
+                       window_left: int = -1, scale: Optional[float] = None,
+                       sinks: Optional[np.ndarray] = None):
+    """dK and dV of the listed keys of one key/value head.
+
+    Every query row that sees one of the keys, in every query head of the
+    group, gets its O, LSE and D from its own forward (``attention_fwd_rows``);
+    then dV_u = sum P_tu dO_t and dK_u = scale sum dS_tu q_t over those rows.
+    Cheap when the keys sit near the end of their document.
+    """
+    T, hq, D = q.shape
+    G = hq // k.shape[1]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    dk = np.zeros((len(keys), D))
+    dv = np.zeros((len(keys), D))
+    for h in range(kv_head * G, (kv_head + 1) * G):
+        sink = None if sinks is None else float(sinks[h])
+        for n, u in enumerate(keys):
+            d = int(np.searchsorted(cu, u, side="right")) - 1
+            a, b = int(cu[d]), int(cu[d + 1])
+            rows = [t for t in range(a, b) if _visible(t, t + 1, u, u + 1, causal, window_left, a, b)[0, 0]]
+            if not rows:
+                continue
+            O, L = attention_fwd_rows(q, k, v, cu, rows, h, causal, window_left, scale, sink)
+            Qr = np.asarray(q[rows, h], np.float64)
+            dOr = np.asarray(do[rows, h], np.float64)
+            s = scale * (Qr @ np.asarray(k[u, kv_head], np.float64))
+            Pm = np.exp(s - L)
+            dS = Pm * (dOr @ np.asarray(v[u, kv_head], np.float64) - np.sum(dOr * O, axis=1))
+            dv[n] += Pm @ dOr
+            dk[n] += scale * (dS @ Qr)
+    return dk, dv
 
 
 def visible_pairs(cu_seqlens, causal: bool = True, window_left: int = -1) -> int:

@@ -1,0 +1,141 @@
+"""GPU parity of the backward path through the C ABI: dO exchanged seq->head,
+tcgen05 dK/dV and dQ kernels, dQ/dK/dV exchanged head->seq, dsinks; compared
+with the fp64 oracle (max-abs <= 2e-2, relative L2 <= 5e-3)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import usp_workloads as W
+from gpu_util import assert_close, built_lib, device_inputs, shape_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    built_lib()
+
+
+def _fwd_bwd(w):
+    from ulysses_sequence_long_gb300.pipeline import UlyssesAttention
+    dev, host = device_inputs(w)
+    ua = UlyssesAttention(shape_of(w), with_backward=True)
+    ua.forward(dev["q"], dev["k"], dev["v"], dev["pos"], dev["sinks"])
+    ua.backward(dev["do"], dev["sinks"])
+    torch.cuda.synchronize()
+    assert ua.read_status() == 0
+    return ua, dev, host
+
+
+SMALL = [
+    W.TINY,
+    W.MHA4K,
+    W.Workload("gqa_win_sink_d128", B=1, S=1024, Hq=8, Hkv=2, D=128, P=2, window_left=200, sinks=True,
+               doc_mode="explicit", doc_lens=(300, 1, 423, 300)),
+    W.Workload("gqa_win_sink_d64", B=1, S=1536, Hq=8, Hkv=4, D=64, P=4, window_left=127, sinks=True,
+               doc_mode="geometric", doc_mean=400, seed=3),
+    W.Workload("two_rows_ragged", B=2, S=640, Hq=4, Hkv=2, D=128, P=2, doc_mode="geometric", doc_mean=150,
+               seed=5),
+    W.Workload("noncausal_d64", B=1, S=512, Hq=2, Hkv=1, D=64, P=1, causal=False, doc_mode="explicit",
+               doc_lens=(100, 250, 162)),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_backward_full_parity_small(w):
+    ua, dev, host = _fwd_bwd(w)
+    snk = host["sinks"]
+    f = oracle.ulysses_fwd(host["q"], host["k"], host["v"], host["pos"], w.causal, w.window_left, None, snk)
+    g = oracle.ulysses_bwd(f, host["do"], w.causal, w.window_left, None, snk)
+    assert_close("dq", ua.dq_seq.float().cpu().numpy(), g["dq_seq"])
+    assert_close("dk", ua.dk_seq.float().cpu().numpy(), g["dk_seq"])
+    assert_close("dv", ua.dv_seq.float().cpu().numpy(), g["dv_seq"])
+    if snk is not None:
+        assert_close("dsinks", ua.dsinks.cpu().numpy(), g["dsinks"])
+
+
+def _rank_views(w, host, r):
+    hq, hk = w.Hq // w.P, w.Hkv // w.P
+    T = w.B * w.S
+    qh = oracle.relayout_fwd(host["q"], w.P)[r].reshape(T, hq, w.D)
+    kh = oracle.relayout_fwd(host["k"], w.P)[r].reshape(T, hk, w.D)
+    vh = oracle.relayout_fwd(host["v"], w.P)[r].reshape(T, hk, w.D)
+    doh = oracle.relayout_fwd(host["do"], w.P)[r].reshape(T, hq, w.D)
+    cu, _, _ = oracle.cu_seqlens_from_position_ids(host["pos"])
+    snk = None if host["sinks"] is None else host["sinks"][r * hq:(r + 1) * hq]
+    return qh, kh, vh, doh, cu, snk
+
+
+def _gpu_head(t, w, r, heads):
+    T = w.B * w.S
+    return t[r].reshape(T, heads, w.D).float().cpu().numpy()
+
+
+@pytest.mark.parametrize("w,groups", [
+    (W.GPTOSS_WIN, [(0, 0), (5, 0)]),
+    (W.LLAMA32K, [(2, 0), (7, 0)]),
+], ids=lambda x: x.name if hasattr(x, "name") else "")
+def test_backward_full_size_whole_groups(w, groups):
+    """Every query head of a GQA group on a rank: dQ of those heads and the
+    complete dK/dV of their key/value head, compared element by element."""
+    ua, dev, host = _fwd_bwd(w)
+    G = w.Hq // w.Hkv
+    for r, kvh in groups:
+        qh, kh, vh, doh, cu, snk = _rank_views(w, host, r)
+        heads = list(range(kvh * G, (kvh + 1) * G))
+        O, L = oracle.attention_fwd(qh, kh, vh, cu, w.causal, w.window_left, None, snk, heads=heads)
+        dq, dk, dv, ds = oracle.attention_bwd(qh, kh, vh, O, L, doh, cu, w.causal, w.window_left, None, snk,
+                                              heads=heads)
+        gq = _gpu_head(ua.dq_head, w, r, w.Hq // w.P)
+        gk = _gpu_head(ua.dk_head, w, r, w.Hkv // w.P)
+        gv = _gpu_head(ua.dv_head, w, r, w.Hkv // w.P)
+        assert_close(f"dq r{r}", gq[:, heads], dq[:, heads])
+        assert_close(f"dk r{r} kv{kvh}", gk[:, kvh], dk[:, kvh])
+        assert_close(f"dv r{r} kv{kvh}", gv[:, kvh], dv[:, kvh])
+        if ds is not None:
+            got = ua.dsinks.cpu().numpy()[r * (w.Hq // w.P):][heads]
+            assert_close(f"dsinks r{r}", got, ds[heads])
+
+
+@pytest.mark.parametrize("w", [W.GPTOSS_FULL, W.LONG128K], ids=lambda w: w.name)
+def test_backward_full_size_sampled(w):
+    """Long single documents: dQ at seeded rows, dK/dV at seeded keys near the
+    end of the document (few rows see them), all query heads of the group."""
+    ua, dev, host = _fwd_bwd(w)
+    rng = np.random.Generator(np.random.PCG64(17))
+    G = w.Hq // w.Hkv
+    r, kvh = w.P - 1, 0
+    qh, kh, vh, doh, cu, snk = _rank_views(w, host, r)
+    rows = np.sort(np.concatenate([rng.choice(w.S, 12, replace=False), [0, w.S - 1]]))
+    gq = _gpu_head(ua.dq_head, w, r, w.Hq // w.P)
+    for h in (kvh * G, kvh * G + G - 1):
+        dq = oracle.attention_bwd_rows(qh, kh, vh, doh, cu, rows, h, w.causal, w.window_left,
+                                       sink=None if snk is None else snk[h])
+        assert_close(f"dq rows h{h}", gq[rows, h], dq)
+    keys = np.sort(np.concatenate([w.S - 1 - rng.choice(384, 6, replace=False), [w.S - 1]]))
+    dk, dv = oracle.attention_bwd_keys(qh, kh, vh, doh, cu, keys, kvh, w.causal, w.window_left, sinks=snk)
+    gk = _gpu_head(ua.dk_head, w, r, w.Hkv // w.P)
+    gv = _gpu_head(ua.dv_head, w, r, w.Hkv // w.P)
+    assert_close("dk keys", gk[keys, kvh], dk)
+    assert_close("dv keys", gv[keys, kvh], dv)
+
+
+def test_backward_conservation_at_full_size():
+    """Properties that hold at any size, checked over every key of a 128K
+    document: without a sink each softmax row of dS sums to zero, so
+    sum_u dK_u = 0; and each row of P sums to one, so sum_u dV_u equals the sum
+    of dO over the group's query heads and rows."""
+    w = W.LONG128K
+    ua, dev, host = _fwd_bwd(w)
+    G = w.Hq // w.Hkv
+    for r in range(w.P):
+        gk = ua.dk_head[r].reshape(w.S, -1, w.D).double().sum(0).cpu().numpy()
+        ak = ua.dk_head[r].reshape(w.S, -1, w.D).double().abs().sum(0).cpu().numpy()
+        assert np.all(np.abs(gk) <= 5e-3 * ak + 1e-2), float(np.max(np.abs(gk) / ak))
+        gv = ua.dv_head[r].reshape(w.S, -1, w.D).double().sum(0).cpu().numpy()
+        av = ua.dv_head[r].reshape(w.S, -1, w.D).double().abs().sum(0).cpu().numpy()
+        hq = w.Hq // w.P
+        doh = oracle.relayout_fwd(host["do"], w.P)[r, 0]
+        want = doh.reshape(w.S, hq // G, G, w.D).sum(axis=(0, 2))
+        assert np.all(np.abs(gv - want) <= 5e-3 * (av + np.abs(want)) + 1e-2), float(np.max(np.abs(gv - want)))

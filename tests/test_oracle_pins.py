@@ -413,3 +413,30 @@ def test_fwd_rows_agree_with_sdpa_rows():
             ref_o = torch.softmax(lg, 0)[:-1] @ torch.from_numpy(v[a:b, h // 2])
             np.testing.assert_allclose(O[n], ref_o.numpy(), rtol=0, atol=1e-12)
             np.testing.assert_allclose(L[n], torch.logsumexp(lg, 0).item(), rtol=1e-13)
+
+
+@pytest.mark.parametrize("causal,window_left,use_sink", [(True, -1, False), (True, 5, True), (False, 4, False)])
+def test_bwd_rows_and_keys_agree_with_full_backward(causal, window_left, use_sink):
+    # the sampled forms are pinned to attention_bwd, itself pinned to torch
+    # autograd and finite differences above
+    q, k, v = _rand_qkv(40, 4, 2, 8, seed=21)
+    do = _rng(22).standard_normal(q.shape)
+    cu = [0, 11, 12, 40]
+    t = np.array([0.5, -0.2, 0.9, 0.1]) if use_sink else None
+    O, L = oracle.attention_fwd(q, k, v, cu, causal, window_left, sinks=t)
+    dq, dk, dv, _ = oracle.attention_bwd(q, k, v, O, L, do, cu, causal, window_left, sinks=t)
+    rows = [0, 10, 11, 12, 25, 39]
+    for h in range(4):
+        got = oracle.attention_bwd_rows(q, k, v, do, cu, rows, h, causal, window_left,
+                                        sink=None if t is None else t[h])
+        np.testing.assert_allclose(got, dq[rows, h], rtol=0, atol=1e-11)
+    keys = [0, 5, 11, 12, 30, 39]
+    for kh in range(2):
+        gk, gv = oracle.attention_bwd_keys(q, k, v, do, cu, keys, kh, causal, window_left, sinks=t)
+        np.testing.assert_allclose(gk, dk[keys, kh], rtol=0, atol=1e-11)
+        np.testing.assert_allclose(gv, dv[keys, kh], rtol=0, atol=1e-11)
+    # restricting to one GQA group gives that key/value head's full gradient
+    dq2, dk2, dv2, _ = oracle.attention_bwd(q, k, v, O, L, do, cu, causal, window_left, sinks=t, heads=[2, 3])
+    np.testing.assert_allclose(dk2[:, 1], dk[:, 1], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv2[:, 1], dv[:, 1], rtol=0, atol=1e-12)
+    assert np.all(dk2[:, 0] == 0) and np.all(dq2[:, :2] == 0)

@@ -1,14 +1,653 @@
-// usp_attn_bwd.cu — attention backward (placeholder until the kernels land).
+// usp_attn_bwd.cu — attention backward on the tcgen05 tensor core, all P
+// emulated ranks per launch, deterministic (no floating-point atomics).
+//
+// Gradients of O_t = sum_u exp(s_tu - LSE_t) v_u, s_tu = scale q_t.k_u, for the
+// loss sum(O * dO), with P_tu = exp(s_tu - LSE_t) and D_t = dO_t . O_t:
+//   dV_u = sum_t P_tu dO_t          dK_u = scale sum_t dS_tu q_t
+//   dQ_t = scale sum_u dS_tu k_u    dS_tu = P_tu (dO_t . v_u - D_t)
+//   dz   = -sum_t exp(z - LSE_t) D_t   (sink logit of the head)
+// Key/value gradients sum over the query heads of their GQA group; on each
+// rank those are its own heads (contiguous head blocks keep groups local).
+//
+// Four launches:
+//   1. preprocess   D_t for every (rank, query head, token): fp32 workspace
+//   2. dK/dV        CTA = (rank, kv head, 128 keys); loops over the group's
+//                   query heads and the 128-row query tiles that see the keys:
+//                     S^T = K Q^T, dP^T = V dO^T            (TMEM, fp32)
+//                     P^T, dS^T -> bf16 in TMEM over S^T / dP^T
+//                     dV += P^T dO, dK += dS^T Q           (A operand from TMEM)
+//   3. dQ           CTA = (rank, query head, 128 rows); loops over key tiles:
+//                     S = Q K^T, dP = dO V^T, dS -> bf16 in TMEM, dQ += dS K
+//   4. dsink        one block per (rank, head): a fixed-order tree reduction
+// Warp roles in 2 and 3 (320 threads): warps 0-7 compute (warp w owns TMEM lanes
+// 32*(w%4).. and column half w/4 of every 128-column tile), warp 8 feeds
+// shared memory (TMA), warp 9 issues the MMAs from one thread.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
 #include "usp_attn_common.cuh"
 #include "usp_internal.h"
 
 namespace usp {
+
+namespace bwd {
+
+constexpr int kThreads = 320;
+constexpr int kAtomBytes = kBM * 128;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// index of (rank r, local head j, rank-local token t) in a [P][B][hq][S] array
+__device__ __forceinline__ size_t stat_index(const AttnArgs& p, int r, int j, int t) {
+  const int b = t / p.S, s = t - b * p.S;
+  return (static_cast<size_t>(r * p.B + b) * p.hq + j) * p.S + s;
+}
+
+// --------------------------------------------------------------- preprocess
+// One row = D bf16 = D/8 lanes of 16 bytes.  Rows are (rank, token, head) in
+// head-layout order, so reads are contiguous.
+template <int D>
+__global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
+                                                         float* __restrict__ dvec, AttnArgs p, uint32_t n_rows) {
+  constexpr int LPR = D / 8;  // lanes per row
+  const uint32_t lane_row = threadIdx.x % LPR;
+  for (uint32_t row = (blockIdx.x * blockDim.x + threadIdx.x) / LPR; row < n_rows + (32 / LPR);
+       row += gridDim.x * blockDim.x / LPR) {
+    const bool ok = row < n_rows;
+    float acc = 0.f;
+    if (ok) {
+      const uint4 a = __ldg(o + static_cast<size_t>(row) * LPR + lane_row);
+      const uint4 b = __ldg(dO + static_cast<size_t>(row) * LPR + lane_row);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc += bf16lo(av[e]) * bf16lo(bv[e]) + bf16hi(av[e]) * bf16hi(bv[e]);
+    }
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (ok && lane_row == 0) {
+      const uint32_t j = row % p.hq;
+      const uint32_t rt = row / p.hq;
+      const uint32_t r = rt / p.BS, t = rt - r * p.BS;
+      dvec[stat_index(p, r, j, t)] = acc;
+    }
+  }
+}
+
+// --------------------------------------------------------------- dsink
+__global__ void __launch_bounds__(256) dsink_kernel(const float* __restrict__ lse, const float* __restrict__ dvec,
+                                                    float* __restrict__ dsinks, AttnArgs p) {
+  __shared__ float red[256];
+  const int r = blockIdx.x / p.hq, j = blockIdx.x % p.hq;
+  const float z = __ldg(p.sinks + r * p.hq + j);
+  float acc = 0.f;
+  for (int t = threadIdx.x; t < p.BS; t += blockDim.x) {
+    const size_t i = stat_index(p, r, j, t);
+    acc -= __expf(z - __ldg(lse + i)) * __ldg(dvec + i);
+  }
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) dsinks[r * p.hq + j] = red[0];
+}
+
+// --------------------------------------------------------------- helpers
+// A operand column of MMA step kk when the two column halves of a packed bf16
+// tile sit at [base, base+32) and [base+64, base+96).
+__device__ __forceinline__ uint32_t split_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
+
+__device__ __forceinline__ void ld64(uint32_t taddr, float (&x)[64]) {
+  uint32_t a[32], b[32];
+  tmem_ld32(taddr, a);
+  tmem_ld32(taddr + 32, b);
+  tmem_wait_ld();
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    x[e] = __uint_as_float(a[e]);
+    x[32 + e] = __uint_as_float(b[e]);
+  }
+}
+
+__device__ __forceinline__ void st_packed64(uint32_t taddr, const float (&x)[64]) {
+  uint32_t pk[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+  tmem_st32(taddr, pk);
+  tmem_wait_st();
+}
+
+// Write one TMEM row (D fp32 columns at `taddr`) times `mul` as bf16 to `dst` (if `ok`).
+template <int NCOL>
+__device__ __forceinline__ void store_row(uint32_t taddr, __nv_bfloat16* dst, float mul, bool ok) {
+#pragma unroll 1
+  for (int c = 0; c < NCOL / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld32(taddr + c * 32, v);
+    tmem_wait_ld();
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+    if (ok) {
+      uint4* d = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) d[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+    }
+  }
+}
+
+template <int D>
+struct Cfg {
+  static constexpr int NCH = D / 64;
+  static constexpr int TILE = NCH * kAtomBytes;  // one 128-row bf16 tile
+  static constexpr int QST = 2;                  // stages of (Q, dO) tiles in the dK/dV kernel
+  static constexpr int KST = 2;                  // stages of (K, V) tiles in the dQ kernel
+  // dK/dV kernel
+  static constexpr int A_K = 0;
+  static constexpr int A_V = A_K + TILE;
+  static constexpr int A_Q = A_V + TILE;              // [QST] Q tiles
+  static constexpr int A_DO = A_Q + QST * TILE;       // [QST] dO tiles
+  static constexpr int A_STAT = A_DO + QST * TILE;    // [QST][2][128] floats: LSE*log2e, D
+  static constexpr int A_BAR = A_STAT + QST * 2 * 128 * 4;
+  static constexpr int A_SMEM = A_BAR + 1024 + 1024;
+  // dQ kernel
+  static constexpr int B_Q = 0;
+  static constexpr int B_DO = B_Q + TILE;
+  static constexpr int B_K = B_DO + TILE;             // [KST]
+  static constexpr int B_V = B_K + KST * TILE;        // [KST]
+  static constexpr int B_BAR = B_V + KST * TILE;
+  static constexpr int B_SMEM = B_BAR + 1024 + 1024;
+};
+
+struct BarsA {
+  uint64_t kv_full;
+  uint64_t qdo_full[2];
+  uint64_t qdo_empty[2];
+  uint64_t st_full, dpt_full, p_full, ds_full, fin, mma_done;
+  uint32_t tmem;
+  int abort;
+};
+
+struct BarsB {
+  uint64_t q_full;
+  uint64_t k_full[2], v_full[2], kv_empty[2];
+  uint64_t s_full, dp_full, ds_full, fin, mma_done;
+  uint32_t tmem;
+  int abort;
+};
+
+struct Grads {
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  const float* lse;
+  const float* dvec;
+  int n_tiles;  // 128-token tiles per rank
+};
+
+// --------------------------------------------------------------- dK / dV
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, AttnArgs p, Grads g) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  BarsA* bars = reinterpret_cast<BarsA*>(smem + C::A_BAR);
+  float* stat = reinterpret_cast<float*>(smem + C::A_STAT);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // key tiles in order (early keys of a causal document see the most queries)
+  const int per = p.P * p.hk;
+  const int kt = static_cast<int>(blockIdx.x) / per;
+  const int rem = static_cast<int>(blockIdx.x) % per;
+  const int r = rem / p.hk, kh = rem % p.hk;
+  const int u0 = kt * kBN;
+
+  const int n_docs = checked_docs(p);
+  if (n_docs == 0) return;
+  int qlo, qhi;
+  query_range(p, n_docs, u0, min(u0 + kBN, p.BS) - 1, qlo, qhi);
+  const int n_q = (qhi - qlo + kBM - 1) / kBM;
+  const int n_it = p.G * n_q;
+
+  if (tid == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->qdo_full[s], 1);
+      mbar_init(&bars->qdo_empty[s], 1);
+    }
+    mbar_init(&bars->st_full, 1);
+    mbar_init(&bars->dpt_full, 1);
+    mbar_init(&bars->p_full, 8);
+    mbar_init(&bars->ds_full, 8);
+    mbar_init(&bars->fin, 1);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem, 512);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  volatile int* abort = &bars->abort;
+  const uint32_t sbase = smem_u32(smem);
+  // TMEM columns: S^T [0,128) dP^T [128,256) dV [256,256+D) dK [256+D,256+2D)
+  constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tdo);
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::TILE);
+      for (int c = 0; c < C::NCH; ++c) {
+        tma_load_4d(smem + C::A_K + c * kAtomBytes, &tk, &bars->kv_full, c * 64, kh, u0, r);
+        tma_load_4d(smem + C::A_V + c * kAtomBytes, &tv, &bars->kv_full, c * 64, kh, u0, r);
+      }
+    }
+    int issued = 0;
+    for (int i = 0; i < n_it; ++i) {
+      const int s = i & 1;
+      // lane 0 waits for the stage to drain; the warp follows its verdict
+      int go = 1;
+      if (lane == 0 && i >= 2) go = mbar_wait(&bars->qdo_empty[s], ((i >> 1) - 1) & 1, abort, p.status);
+      if (!__shfl_sync(0xffffffffu, go, 0)) break;
+      const int jq = kh * p.G + i / n_q;
+      const int q0 = qlo + (i % n_q) * kBM;
+      float* st = stat + s * 256;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = lane * 4 + e, t = q0 + c;
+        const bool ok = t < qhi;
+        const size_t idx = ok ? stat_index(p, r, jq, t) : 0;
+        st[c] = ok ? __ldg(g.lse + idx) * kLog2e : INFINITY;
+        st[128 + c] = ok ? __ldg(g.dvec + idx) : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->qdo_full[s], 2 * C::TILE);
+        for (int c = 0; c < C::NCH; ++c) {
+          tma_load_4d(smem + C::A_Q + s * C::TILE + c * kAtomBytes, &tq, &bars->qdo_full[s], c * 64, jq, q0, r);
+          tma_load_4d(smem + C::A_DO + s * C::TILE + c * kAtomBytes, &tdo, &bars->qdo_full[s], c * 64, jq, q0, r);
+        }
+      }
+      issued = i + 1;
+    }
+    if (lane == 0) {
+      mbar_wait(&bars->kv_full, 0, abort, p.status);
+      for (int i = max(0, issued - 2); i < issued; ++i) mbar_wait(&bars->qdo_full[i & 1], (i >> 1) & 1, abort, p.status);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(kBN, kBM, false, false);  // [keys x queries], K = D
+      constexpr uint32_t id_g = idesc_bf16(kBN, D, false, true);     // [keys x D], K = queries
+      auto issue_kmajor = [&](uint32_t dcol, uint32_t a_base, uint32_t b_base) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+          mma_ss(tmem + dcol, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), id_s, kk > 0);
+        }
+      };
+      auto issue_grad = [&](uint32_t dcol, uint32_t a_col, uint32_t b_base, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kBM / 16; ++kk)
+          mma_ts(tmem + dcol, tmem + a_col + split_col(kk), sdesc_sw128(b_base + kk * 16 * 128, kAtomBytes, 1024), id_g,
+                 (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(&bars->kv_full, 0, abort, p.status) && mbar_wait(&bars->qdo_full[0], 0, abort, p.status);
+      if (ok && n_it > 0) {
+        tc_fence_after();
+        issue_kmajor(T_S, sbase + C::A_K, sbase + C::A_Q);
+        mma_commit(&bars->st_full);
+        issue_kmajor(T_DP, sbase + C::A_V, sbase + C::A_DO);
+        mma_commit(&bars->dpt_full);
+      }
+      for (int i = 0; i < n_it && ok; ++i) {
+        const int s = i & 1, s1 = (i + 1) & 1;
+        if (!(ok = mbar_wait(&bars->p_full, i & 1, abort, p.status))) break;
+        tc_fence_after();
+        issue_grad(T_DV, T_S, sbase + C::A_DO + s * C::TILE, i > 0);
+        const bool more = i + 1 < n_it;
+        if (more) {
+          if (!(ok = mbar_wait(&bars->qdo_full[s1], ((i + 1) >> 1) & 1, abort, p.status))) break;
+          tc_fence_after();
+          issue_kmajor(T_S, sbase + C::A_K, sbase + C::A_Q + s1 * C::TILE);
+          mma_commit(&bars->st_full);
+        }
+        if (!(ok = mbar_wait(&bars->ds_full, i & 1, abort, p.status))) break;
+        tc_fence_after();
+        issue_grad(T_DK, T_DP, sbase + C::A_Q + s * C::TILE, i > 0);
+        mma_commit(&bars->qdo_empty[s]);
+        if (more) {
+          issue_kmajor(T_DP, sbase + C::A_V, sbase + C::A_DO + s1 * C::TILE);
+          mma_commit(&bars->dpt_full);
+        } else {
+          mma_commit(&bars->fin);
+        }
+      }
+      mma_commit(&bars->mma_done);
+      mbar_wait(&bars->mma_done, 0, abort, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ compute
+    const int half = warp >> 2;                     // query columns [64*half, 64*half+64)
+    const int krow = (warp & 3) * 32 + lane;        // TMEM lane = key row
+    const int u = u0 + krow;
+    const bool key_ok = u < p.BS;
+    int a = 0, b = 0;
+    if (key_ok) doc_bounds(p.cu, n_docs, p.BS, u, a, b);
+    const uint32_t lb = tmem + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
+    bool ok = true;
+    for (int i = 0; i < n_it && ok; ++i) {
+      const int s = i & 1;
+      const int q0 = qlo + (i % n_q) * kBM + half * 64;  // first query column of this half
+      if (!(ok = mbar_wait(&bars->qdo_full[s], (i >> 1) & 1, abort, p.status))) break;
+      const float* lse2 = stat + s * 256 + half * 64;
+      const float* dv = lse2 + 128;
+      if (!(ok = mbar_wait(&bars->st_full, i & 1, abort, p.status))) break;
+      tc_fence_after();
+      float x[64];
+      ld64(lb + T_S + half * 64, x);
+      bool full = key_ok && q0 >= a && q0 + 64 <= b && (!p.causal || q0 >= u);
+      if (p.window_left >= 0) full = full && (q0 + 63 - u <= p.window_left) && (p.causal || u - q0 <= p.window_left);
+      float pr[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const bool vis = full || (key_ok && visible(q0 + c, u, a, b, p.causal, p.window_left));
+        pr[c] = vis ? ex2(fmaf(x[c], p.scale_log2, -lse2[c])) : 0.f;
+      }
+      st_packed64(lb + T_S + half * 64, pr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full);
+      if (!(ok = mbar_wait(&bars->dpt_full, i & 1, abort, p.status))) break;
+      tc_fence_after();
+      ld64(lb + T_DP + half * 64, x);
+#pragma unroll
+      for (int c = 0; c < 64; ++c) x[c] = pr[c] * (x[c] - dv[c]);
+      st_packed64(lb + T_DP + half * 64, x);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->ds_full);
+    }
+    if (ok && n_it > 0 && (ok = mbar_wait(&bars->fin, 0, abort, p.status))) {
+      tc_fence_after();
+      const size_t row = (static_cast<size_t>(r) * p.BS + (key_ok ? u : 0)) * p.hk + kh;
+      if (half == 0)
+        store_row<D>(lb + T_DV, g.dv + row * D, 1.f, key_ok);
+      else
+        store_row<D>(lb + T_DK, g.dk + row * D, p.scale, key_ok);
+    } else if (ok && n_it == 0 && key_ok) {
+      // keys nobody sees (cannot happen for causal documents): zero gradients
+      const size_t row = (static_cast<size_t>(r) * p.BS + u) * p.hk + kh;
+      __nv_bfloat16* dst = (half == 0 ? g.dv : g.dk) + row * D;
+      for (int e = 0; e < D; e += 8) *reinterpret_cast<uint4*>(dst + e) = make_uint4(0, 0, 0, 0);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// --------------------------------------------------------------- dQ
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, AttnArgs p, Grads g) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  BarsB* bars = reinterpret_cast<BarsB*>(smem + C::B_BAR);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // late query tiles first (they see the most keys)
+  const int per = p.P * p.hq;
+  const int qt = g.n_tiles - 1 - static_cast<int>(blockIdx.x) / per;
+  const int rem = static_cast<int>(blockIdx.x) % per;
+  const int r = rem / p.hq, j = rem % p.hq, kvh = j / p.G;
+  const int t0 = qt * kBM;
+
+  const int n_docs = checked_docs(p);
+  if (n_docs == 0) return;
+  int lo, hi;
+  key_range(p, n_docs, t0, min(t0 + kBM, p.BS) - 1, lo, hi);
+  const int n_kv = (hi - lo + kBN - 1) / kBN;
+
+  if (tid == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->ds_full, 8);
+    mbar_init(&bars->fin, 1);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem, 512);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  volatile int* abort = &bars->abort;
+  const uint32_t sbase = smem_u32(smem);
+  constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256;
+
+  if (warp == 8) {
+    if (lane == 0) {
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      mbar_arrive_expect_tx(&bars->q_full, 2 * C::TILE);
+      for (int c = 0; c < C::NCH; ++c) {
+        tma_load_4d(smem + C::B_Q + c * kAtomBytes, &tq, &bars->q_full, c * 64, j, t0, r);
+        tma_load_4d(smem + C::B_DO + c * kAtomBytes, &tdo, &bars->q_full, c * 64, j, t0, r);
+      }
+      int issued = 0;
+      for (int n = 0; n < n_kv; ++n) {
+        const int s = n & 1;
+        if (n >= 2 && !mbar_wait(&bars->kv_empty[s], ((n >> 1) - 1) & 1, abort, p.status)) break;
+        const int kv0 = lo + n * kBN;
+        mbar_arrive_expect_tx(&bars->k_full[s], C::TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_4d(smem + C::B_K + s * C::TILE + c * kAtomBytes, &tk, &bars->k_full[s], c * 64, kvh, kv0, r);
+        mbar_arrive_expect_tx(&bars->v_full[s], C::TILE);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_4d(smem + C::B_V + s * C::TILE + c * kAtomBytes, &tv, &bars->v_full[s], c * 64, kvh, kv0, r);
+        issued = n + 1;
+      }
+      mbar_wait(&bars->q_full, 0, abort, p.status);
+      for (int n = max(0, issued - 2); n < issued; ++n) {
+        mbar_wait(&bars->k_full[n & 1], (n >> 1) & 1, abort, p.status);
+        mbar_wait(&bars->v_full[n & 1], (n >> 1) & 1, abort, p.status);
+      }
+    }
+  } else if (warp == 9) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(kBM, kBN, false, false);
+      constexpr uint32_t id_q = idesc_bf16(kBM, D, false, true);
+      auto issue_kmajor = [&](uint32_t dcol, uint32_t a_base, uint32_t b_base) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
+          mma_ss(tmem + dcol, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), id_s, kk > 0);
+        }
+      };
+      bool ok = mbar_wait(&bars->q_full, 0, abort, p.status);
+      auto issue_pair = [&](int n) -> bool {
+        const int s = n & 1;
+        if (!mbar_wait(&bars->k_full[s], (n >> 1) & 1, abort, p.status)) return false;
+        tc_fence_after();
+        issue_kmajor(T_S, sbase + C::B_Q, sbase + C::B_K + s * C::TILE);
+        mma_commit(&bars->s_full);
+        if (!mbar_wait(&bars->v_full[s], (n >> 1) & 1, abort, p.status)) return false;
+        tc_fence_after();
+        issue_kmajor(T_DP, sbase + C::B_DO, sbase + C::B_V + s * C::TILE);
+        mma_commit(&bars->dp_full);
+        return true;
+      };
+      if (ok && n_kv > 0) ok = issue_pair(0);
+      for (int n = 0; n < n_kv && ok; ++n) {
+        const int s = n & 1;
+        if (!(ok = mbar_wait(&bars->ds_full, n & 1, abort, p.status))) break;
+        tc_fence_after();
+        const uint32_t kb = sbase + C::B_K + s * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tmem + T_DQ, tmem + T_S + split_col(kk), sdesc_sw128(kb + kk * 16 * 128, kAtomBytes, 1024), id_q,
+                 (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars->kv_empty[s]);
+        if (n + 1 < n_kv)
+          ok = issue_pair(n + 1);
+        else
+          mma_commit(&bars->fin);
+      }
+      mma_commit(&bars->mma_done);
+      mbar_wait(&bars->mma_done, 0, abort, p.status);
+    }
+  } else {
+    const int half = warp >> 2;            // key columns [64*half, 64*half+64)
+    const int row = (warp & 3) * 32 + lane;
+    const int t = t0 + row;
+    const bool row_ok = t < p.BS;
+    int a = 0, b = 0;
+    float lse2 = INFINITY, dvt = 0.f;
+    if (row_ok) {
+      doc_bounds(p.cu, n_docs, p.BS, t, a, b);
+      const size_t idx = stat_index(p, r, j, t);
+      lse2 = __ldg(g.lse + idx) * kLog2e;
+      dvt = __ldg(g.dvec + idx);
+    }
+    const uint32_t lb = tmem + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
+    bool ok = true;
+    for (int n = 0; n < n_kv && ok; ++n) {
+      const int k0 = lo + n * kBN + half * 64;
+      if (!(ok = mbar_wait(&bars->s_full, n & 1, abort, p.status))) break;
+      tc_fence_after();
+      float x[64];
+      ld64(lb + T_S + half * 64, x);
+      bool full = row_ok && k0 >= a && k0 + 64 <= b && (!p.causal || k0 + 63 <= t);
+      if (p.window_left >= 0) full = full && (t - k0 <= p.window_left) && (p.causal || k0 + 63 - t <= p.window_left);
+      float pr[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const bool vis = full || (row_ok && visible(t, k0 + c, a, b, p.causal, p.window_left));
+        pr[c] = vis ? ex2(fmaf(x[c], p.scale_log2, -lse2)) : 0.f;
+      }
+      if (!(ok = mbar_wait(&bars->dp_full, n & 1, abort, p.status))) break;
+      tc_fence_after();
+      ld64(lb + T_DP + half * 64, x);
+#pragma unroll
+      for (int c = 0; c < 64; ++c) x[c] = pr[c] * (x[c] - dvt);
+      st_packed64(lb + T_S + half * 64, x);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->ds_full);
+    }
+    if (ok && n_kv > 0 && (ok = mbar_wait(&bars->fin, 0, abort, p.status))) {
+      tc_fence_after();
+      __nv_bfloat16* dst = g.dq + ((static_cast<size_t>(r) * p.BS + (row_ok ? t : 0)) * p.hq + j) * D + half * (D / 2);
+      store_row<D / 2>(lb + T_DQ + half * (D / 2), dst, p.scale, row_ok);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace bwd
+
 size_t attn_bwd_ws_bytes(const usp_attn_params& p) {
   size_t rows = static_cast<size_t>(p.B) * p.S * p.Hq;
   return (rows * sizeof(float) + 255) / 256 * 256;
 }
-int launch_attn_bwd(const usp_attn_params&, const void*, const void*, const void*, const void*, const float*,
-                    const void*, void*, void*, void*, float*, void*, int32_t*, cudaStream_t) {
-  return USP_ERR_UNSUPPORTED;
+
+template <int D>
+static int run_bwd(const AttnArgs& a, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, void* dq, void* dk, void* dv, float* dsinks, float* dvec, cudaStream_t st) {
+  using C = bwd::Cfg<D>;
+  // 1. D = rowsum(dO * O)
+  const uint32_t n_rows = static_cast<uint32_t>(static_cast<uint64_t>(a.P) * a.BS * a.hq);
+  {
+    const int per_block = 256 / (D / 8);
+    int grid = static_cast<int>((n_rows + per_block - 1) / per_block);
+    grid = grid < device_sm_count() * 8 ? grid : device_sm_count() * 8;
+    bwd::preprocess_kernel<D><<<grid, 256, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dO), dvec,
+                                                   a, n_rows);
+    if (check_launch() != USP_OK) return USP_ERR_CUDA;
+  }
+  CUtensorMap tq, tk, tv, tdo;
+  int rc;
+  if ((rc = make_head_tmap(&tq, q, a.P, a.BS, a.hq, D, kBM)) != USP_OK) return rc;
+  if ((rc = make_head_tmap(&tdo, dO, a.P, a.BS, a.hq, D, kBM)) != USP_OK) return rc;
+  if ((rc = make_head_tmap(&tk, k, a.P, a.BS, a.hk, D, kBN)) != USP_OK) return rc;
+  if ((rc = make_head_tmap(&tv, v, a.P, a.BS, a.hk, D, kBN)) != USP_OK) return rc;
+  bwd::Grads g{static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), lse,
+               dvec, (a.BS + kBM - 1) / kBM};
+  // 2. dK, dV
+  if (cudaFuncSetAttribute(bwd::dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::A_SMEM) != cudaSuccess)
+    return USP_ERR_CUDA;
+  bwd::dkdv_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hk, bwd::kThreads, C::A_SMEM, st>>>(tq, tk, tv, tdo,
+                                                                                                       a, g);
+  if (check_launch() != USP_OK) return USP_ERR_CUDA;
+  // 3. dQ
+  if (cudaFuncSetAttribute(bwd::dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::B_SMEM) != cudaSuccess)
+    return USP_ERR_CUDA;
+  bwd::dq_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hq, bwd::kThreads, C::B_SMEM, st>>>(tq, tk, tv, tdo,
+                                                                                                     a, g);
+  if (check_launch() != USP_OK) return USP_ERR_CUDA;
+  // 4. dsink
+  if (dsinks != nullptr && a.sinks != nullptr) {
+    bwd::dsink_kernel<<<a.P * a.hq, 256, 0, st>>>(lse, dvec, dsinks, a);
+    if (check_launch() != USP_OK) return USP_ERR_CUDA;
+  }
+  return USP_OK;
 }
+
+int launch_attn_bwd(const usp_attn_params& prm, const void* q, const void* k, const void* v, const void* o,
+                    const float* lse, const void* dO, void* dq, void* dk, void* dv, float* dsinks, void* ws,
+                    int32_t* status, cudaStream_t st) {
+  AttnArgs a;
+  a.B = prm.B;
+  a.S = prm.S;
+  a.BS = prm.B * prm.S;
+  a.P = prm.P;
+  a.hq = prm.Hq / prm.P;
+  a.hk = prm.Hkv / prm.P;
+  a.G = prm.Hq / prm.Hkv;
+  a.causal = prm.causal ? 1 : 0;
+  a.window_left = prm.window_left;
+  a.scale = prm.softmax_scale > 0.f ? prm.softmax_scale : 1.0f / sqrtf(static_cast<float>(prm.D));
+  a.scale_log2 = a.scale * 1.4426950408889634f;
+  a.cu = prm.cu_seqlens;
+  a.n_docs = prm.n_docs;
+  a.sinks = prm.sinks;
+  a.status = status;
+  float* dvec = static_cast<float*>(ws);
+  if (prm.D == 128) return run_bwd<128>(a, q, k, v, o, lse, dO, dq, dk, dv, dsinks, dvec, st);
+  return run_bwd<64>(a, q, k, v, o, lse, dO, dq, dk, dv, dsinks, dvec, st);
+}
+
 }  // namespace usp
