@@ -1,0 +1,435 @@
+"""Benchmark of the emulated Ulysses attention hot path on GB300.
+
+One step = the whole path of one attention layer, forward and backward, over
+one batch of seeded synthetic input already resident in HBM:
+  q/k/v exchange (seq -> head) · document boundaries from the gathered
+  position_ids · attention forward · O exchange (head -> seq) · dO exchange
+  (seq -> head) · attention backward (D rows, dK/dV, dQ, dsinks) · dQ/dK/dV
+  exchanges (head -> seq).
+
+The headline value is the attention's algorithmic fwd+bwd work,
+14 * D * Hq * (visible query/key pairs), divided by the whole step's time,
+in TFLOP/s.  The same JSON line carries the relayout bandwidth, per-call
+times, the roofline of the dominant kernel, an end-to-end figure measured
+through the C ABI with host buffers, and the fp64 oracle's CPU throughput.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+       python bench.py --impl reference ...   (the oracle on the host cores)
+For N > 1 each rank runs its own replica of the emulated P-rank job on its
+own GPU (no collective on the data path; barrier + max-over-ranks timing).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import usp_workloads as W  # noqa: E402
+
+DEFAULT_WORKLOAD = W.LLAMA32K.name
+METRIC = "varlen GQA attention fwd+bwd TFLOP/s at 1 GB300; relayout GB/s"
+
+
+# ----------------------------------------------------------------------------- host-side counts
+def visible_pairs(w: W.Workload) -> int:
+    """Query/key pairs the mask keeps, from the seeded document lengths (closed forms)."""
+    total = 0
+    for lens in W.document_lengths(w):
+        for L in lens:
+            if w.window_left < 0:
+                total += L * (L + 1) // 2 if w.causal else L * L
+            else:
+                wl = w.window_left
+                if w.causal:
+                    m = min(L, wl + 1)               # rows i < wl+1 see i+1 keys, the rest wl+1
+                    total += m * (m + 1) // 2 + (L - m) * (wl + 1)
+                else:
+                    total += sum(min(L - 1, i + wl) - max(0, i - wl) + 1 for i in range(L))
+    return total
+
+
+def attention_flops(w: W.Workload):
+    pairs = visible_pairs(w)
+    unit = w.D * w.Hq * pairs
+    # forward QK^T + PV = 4 flops per pair and dim; backward recompute S, dP, dV,
+    # dK, dQ = 10; of the backward, the dK/dV kernel does S, dP, dV, dK (8) and
+    # the dQ kernel does the one remaining algorithmic GEMM, dQ (2).
+    return {"pairs": pairs, "fwd": 4 * unit, "bwd": 10 * unit, "total": 14 * unit,
+            "dkdv": 8 * unit, "dq": 2 * unit}
+
+
+def relayout_bytes(w: W.Workload):
+    q = w.B * w.S * w.Hq * w.D * 2
+    kv = w.B * w.S * w.Hkv * w.D * 2
+    # every exchange reads and writes each element once
+    return {"qkv": 2 * (q + 2 * kv), "o": 2 * q, "do": 2 * q, "dqkv": 2 * (q + 2 * kv)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d["bf16_tflops_sustained"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- the step
+CALLS = ["relayout_qkv", "cu_seqlens", "attn_fwd", "relayout_o", "relayout_do", "attn_bwd_pre", "attn_bwd_dkdv",
+         "attn_bwd_dq", "relayout_dqkv"]
+
+
+class Step:
+    def __init__(self, w: W.Workload, device):
+        from ulysses_sequence_long_gb300 import binding as B
+        from ulysses_sequence_long_gb300.pipeline import Shape, UlyssesAttention
+        self.B_ = B
+        self.w = w
+        self.ua = UlyssesAttention(Shape(w.B, w.S, w.Hq, w.Hkv, w.D, w.P, w.causal, w.window_left), device=device)
+        t = W.qkv_do_shards(w)
+        self.host = t
+        self.dev = {n: x.to(device) for n, x in t.items()}
+        self.pos_host = torch.from_numpy(W.position_ids_shards(w))
+        self.pos = self.pos_host.to(device)
+        sk = W.sinks(w)
+        self.sinks = None if sk is None else sk.to(device)
+        self.stream = torch.cuda.current_stream(device)
+        self.n_events = 0
+
+    def run(self, events=None):
+        """One whole step; optional CUDA events recorded between the calls."""
+        ua, d, s = self.ua, self.dev, self.stream
+        sh = ua.shape
+        B = self.B_
+
+        def mark(i):
+            if events is not None:
+                events[i].record(s)
+
+        mark(0)
+        ua.exchange_qkv(d["q"], d["k"], d["v"], s)
+        mark(1)
+        ua.boundaries(self.pos, s)
+        mark(2)
+        ua.attention(self.sinks, s)
+        mark(3)
+        ua.exchange_out(s)
+        mark(4)
+        prm = ua.params(self.sinks)
+        if ua._bwd_ws is None:
+            n = B.usp_attn_bwd_workspace_bytes(prm)
+            ua._bwd_ws = torch.empty((max(n, 256),), dtype=torch.uint8, device=ua.o_head.device)
+        B.usp_relayout_fwd(d["do"], ua.do_head, sh.B, sh.S, sh.Hq, sh.D, sh.P, s)
+        mark(5)
+        B.usp_attn_bwd_preprocess(prm, ua.o_head, ua.lse, ua.do_head, ua.dsinks if self.sinks is not None else None,
+                                  ua._bwd_ws, ua.status, s)
+        mark(6)
+        B.usp_attn_bwd_dkdv(prm, ua.q_head, ua.k_head, ua.v_head, ua.lse, ua.do_head, ua.dk_head, ua.dv_head,
+                            ua._bwd_ws, ua.status, s)
+        mark(7)
+        B.usp_attn_bwd_dq(prm, ua.q_head, ua.k_head, ua.v_head, ua.lse, ua.do_head, ua.dq_head, ua._bwd_ws,
+                          ua.status, s)
+        mark(8)
+        B.usp_relayout_bwd(ua.dq_head, ua.dq_seq, sh.B, sh.S, sh.Hq, sh.D, sh.P, s)
+        B.usp_relayout_bwd(ua.dk_head, ua.dk_seq, sh.B, sh.S, sh.Hkv, sh.D, sh.P, s)
+        B.usp_relayout_bwd(ua.dv_head, ua.dv_seq, sh.B, sh.S, sh.Hkv, sh.D, sh.P, s)
+        mark(9)
+
+    def launches_per_step(self) -> int:
+        # relayout qkv 1, scan 3, fwd 1, relayout O 1, relayout dO 1, preprocess 1 (+ dsink 1),
+        # dK/dV 1, dQ 1, relayout dQ/dK/dV 3
+        return 13 + (1 if self.sinks is not None else 0)
+
+    # -- end to end: host buffers in and out, through the C ABI
+    def make_host_io(self):
+        pin = {n: x.pin_memory() for n, x in self.host.items()}
+        pin["pos"] = self.pos_host.pin_memory()
+        ua = self.ua
+        outs = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                for n, t in (("o", ua.o_seq), ("dq", ua.dq_seq), ("dk", ua.dk_seq), ("dv", ua.dv_seq))}
+        if self.sinks is not None:
+            outs["dsinks"] = torch.empty(ua.dsinks.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs.values())
+        return pin, outs, h2d, d2h
+
+    def run_e2e(self, pin, outs):
+        ua, d = self.ua, self.dev
+        for n in ("q", "k", "v", "do"):
+            d[n].copy_(pin[n], non_blocking=True)
+        self.pos.copy_(pin["pos"], non_blocking=True)
+        self.run()
+        outs["o"].copy_(ua.o_seq, non_blocking=True)
+        outs["dq"].copy_(ua.dq_seq, non_blocking=True)
+        outs["dk"].copy_(ua.dk_seq, non_blocking=True)
+        outs["dv"].copy_(ua.dv_seq, non_blocking=True)
+        if "dsinks" in outs:
+            outs["dsinks"].copy_(ua.dsinks, non_blocking=True)
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def oracle_sample(w: W.Workload, budget_s: float = 20.0):
+    """Time the fp64 oracle (as it stands) on a bounded sample of the workload.
+
+    The sample is the first document of the first key/value group of rank 0
+    (all of its query heads), forward and backward, truncated to at most
+    `rows` tokens so that it runs for roughly budget_s seconds.  Returns the
+    throughput in the bench's unit (algorithmic TFLOP/s of the sample).
+    """
+    import oracle
+    lens = W.document_lengths(w)[0]
+    L = lens[0]
+    G = w.Hq // w.Hkv
+    rng = np.random.Generator(np.random.PCG64(5))
+    # grow the sample until it takes a reasonable part of the budget
+    n = min(L, 512)
+    while True:
+        q = rng.standard_normal((n, G, w.D))
+        k = rng.standard_normal((n, 1, w.D))
+        v = rng.standard_normal((n, 1, w.D))
+        do = rng.standard_normal((n, G, w.D))
+        t0 = time.perf_counter()
+        O, Lse = oracle.attention_fwd(q, k, v, [0, n], w.causal, w.window_left)
+        oracle.attention_bwd(q, k, v, O, Lse, do, [0, n], w.causal, w.window_left)
+        dt = time.perf_counter() - t0
+        ww = W.Workload("sample", B=1, S=n, Hq=G, Hkv=1, D=w.D, P=1, causal=w.causal, window_left=w.window_left)
+        flops = attention_flops(ww)["total"]
+        if dt > budget_s / 4 or n >= L:
+            break
+        n = min(L, n * 2)
+    cores = os.cpu_count() or 1
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        pass
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"first document of rank 0, kv group 0 ({G} query heads, D={w.D}), first {n} tokens, "
+                      f"fp64 numpy forward+backward, {dt:.2f} s"}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    per = []
+    for _ in range(args.warmup):
+        oracle_sample(w, budget_s=8.0)
+    for _ in range(args.steps):
+        per.append(oracle_sample(w, budget_s=8.0))
+    val = statistics.median(p["value"] for p in per)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1))", "scaling": "weak",
+            "config": {"workload": w.name, **w.describe()},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": per[-1]["cores"], "kind": "oracle",
+                             "sample": per[-1]["sample"]},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="usp", choices=["usp", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    w = W.BY_NAME[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    from ulysses_sequence_long_gb300 import _build
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier()
+    _build.build()
+
+    step = Step(w, device)
+    fl = attention_flops(w)
+    rb = relayout_bytes(w)
+    for _ in range(max(args.warmup, 3)):
+        step.run()
+    torch.cuda.synchronize()
+    assert step.ua.read_status() == 0, "device status set during warm-up"
+
+    # ---- timed region: K whole steps, events between the calls
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        start.record()
+        for k in range(args.steps):
+            step.run(ev[k])
+        stop.record()
+        torch.cuda.synchronize()
+        barrier()
+    ms = start.elapsed_time(stop) / args.steps
+    ms = max_over_ranks(ms)
+    per_call = {}
+    for i, name in enumerate(CALLS):
+        per_call[name] = statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps))
+
+    value = fl["total"] * world / (ms * 1e-3) / 1e12
+    peaks = measured_peaks()
+    attn_ms = per_call["attn_fwd"] + per_call["attn_bwd_pre"] + per_call["attn_bwd_dkdv"] + per_call["attn_bwd_dq"]
+    relayout_ms = per_call["relayout_qkv"] + per_call["relayout_o"] + per_call["relayout_do"] + per_call["relayout_dqkv"]
+    relayout_total_bytes = rb["qkv"] + rb["o"] + rb["do"] + rb["dqkv"]
+    kernels = {"attn_fwd": fl["fwd"], "attn_bwd_dkdv": fl["dkdv"], "attn_bwd_dq": fl["dq"]}
+    dom = max(kernels, key=lambda n: per_call[n])
+    achieved = kernels[dom] / (per_call[dom] * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tr = json.load(f)
+        ent = tr.get(w.name, {}).get(dom)
+        if ent is not None and ent.get("source_hash") == _build.source_hash():
+            traffic = ent["bytes_per_launch"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": traffic,
+                "peak_source": peaks["source"] + " bf16 sustained"}
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), position_ids resets)",
+            "config": {"workload": w.name, "B": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "P": w.P,
+                       "causal": w.causal, "window_left": w.window_left, "sinks": w.sinks,
+                       "documents": len(W.document_lengths(w)[0]), "visible_pairs_per_head": fl["pairs"],
+                       "fwd_bwd_flop": fl["total"], "parallelism": f"emulated ulysses P={w.P}, replicas={world}",
+                       "l2": "inputs larger than L2 (no flush)"},
+            "relayout_gbs": relayout_total_bytes / (relayout_ms * 1e-3) / 1e9,
+            "relayout_frac_hbm": relayout_total_bytes / (relayout_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "attention_tflops": fl["total"] / (attn_ms * 1e-3) / 1e12,
+            "fwd_tflops": fl["fwd"] / (per_call["attn_fwd"] * 1e-3) / 1e12,
+            "bwd_tflops": fl["bwd"] / ((per_call["attn_bwd_pre"] + per_call["attn_bwd_dkdv"] +
+                                        per_call["attn_bwd_dq"]) * 1e-3) / 1e12,
+            "per_call_ms": per_call, "roofline": roofline, "gpu_launches": step.launches_per_step() * args.steps,
+            "clocks": clocks.summary()}
+
+    if not args.no_e2e:
+        pin, outs, h2d, d2h = step.make_host_io()
+        step.run_e2e(pin, outs)
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            step.run_e2e(pin, outs)
+        e1.record()
+        torch.cuda.synchronize()
+        barrier()
+        ems = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+        line["e2e"] = {"value": fl["total"] * world / (ems * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ems,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(w)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -191,6 +191,24 @@ int usp_attn_bwd(const usp_attn_params* params, const void* q, const void* k, co
                  void* dq, void* dk, void* dv, float* dsinks,
                  void* ws, size_t ws_bytes, int32_t* dev_status, usp_stream_t stream);
 
+/* The three phases usp_attn_bwd runs, in order, each one kernel launch (the
+ * preprocess adds one small reduction when sinks are given).  They are exposed
+ * so that a caller can time them or place the two gradient passes, which only
+ * read what the preprocess wrote, on different streams.  `ws` is
+ * usp_attn_bwd's workspace: the preprocess writes D_t there, the gradient
+ * passes read it.  Arguments and errors are as in usp_attn_bwd.
+ *   usp_attn_bwd_preprocess: D_t = sum_d dO_td O_td; dsinks (nullable).
+ *   usp_attn_bwd_dkdv:       dK, dV (every query head of each GQA group).
+ *   usp_attn_bwd_dq:         dQ. */
+int usp_attn_bwd_preprocess(const usp_attn_params* params, const void* o, const float* lse, const void* dO,
+                            float* dsinks, void* ws, size_t ws_bytes, int32_t* dev_status, usp_stream_t stream);
+int usp_attn_bwd_dkdv(const usp_attn_params* params, const void* q, const void* k, const void* v,
+                      const float* lse, const void* dO, void* dk, void* dv, const void* ws, size_t ws_bytes,
+                      int32_t* dev_status, usp_stream_t stream);
+int usp_attn_bwd_dq(const usp_attn_params* params, const void* q, const void* k, const void* v,
+                    const float* lse, const void* dO, void* dq, const void* ws, size_t ws_bytes,
+                    int32_t* dev_status, usp_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

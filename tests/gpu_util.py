@@ -39,6 +39,7 @@ def errors(got, ref):
 
 def assert_close(name, got, ref, max_abs=MAX_ABS, rel_l2=REL_L2):
     ma, rl = errors(got, ref)
+    print(f"[parity] {name}: max_abs={ma:.3e} rel_l2={rl:.3e} |ref|max={float(np.max(np.abs(ref))):.3e}")
     assert ma <= max_abs and rl <= rel_l2, f"{name}: max_abs={ma:.3e} (<= {max_abs}) rel_l2={rl:.3e} (<= {rel_l2})"
     return ma, rl
 

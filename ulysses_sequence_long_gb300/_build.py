@@ -42,6 +42,18 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
+def source_hash() -> str:
+    """Short hash of the library sources (csrc/ and include/usp.h)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    with open(os.path.join(ROOT, "include", "usp.h"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def _stale(objs) -> bool:
     if not os.path.exists(LIB):
         return True

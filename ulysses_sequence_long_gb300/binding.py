@@ -33,6 +33,7 @@ EXPORTED = [
     "usp_relayout_fwd", "usp_relayout_bwd", "usp_relayout_fwd_qkv",
     "usp_cu_seqlens_workspace_bytes", "usp_cu_seqlens_from_position_ids",
     "usp_attn_fwd", "usp_attn_bwd_workspace_bytes", "usp_attn_bwd",
+    "usp_attn_bwd_preprocess", "usp_attn_bwd_dkdv", "usp_attn_bwd_dq",
 ]
 
 
@@ -78,8 +79,12 @@ def load() -> ctypes.CDLL:
     L.usp_attn_bwd_workspace_bytes.restype = sz
     L.usp_attn_bwd_workspace_bytes.argtypes = [ctypes.POINTER(AttnParams)]
     L.usp_attn_bwd.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+    L.usp_attn_bwd_preprocess.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, sz, vp, vp]
+    L.usp_attn_bwd_dkdv.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+    L.usp_attn_bwd_dq.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     for name in ("usp_relayout_fwd", "usp_relayout_bwd", "usp_relayout_fwd_qkv",
-                 "usp_cu_seqlens_from_position_ids", "usp_attn_fwd", "usp_attn_bwd"):
+                 "usp_cu_seqlens_from_position_ids", "usp_attn_fwd", "usp_attn_bwd",
+                 "usp_attn_bwd_preprocess", "usp_attn_bwd_dkdv", "usp_attn_bwd_dq"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -170,3 +175,29 @@ def usp_attn_bwd(params: AttnParams, q, k, v, o, lse, dO, dq, dk, dv, dsinks, ws
         _dev(dv, "dv", torch.bfloat16), _dev(dsinks, "dsinks", torch.float32), _dev(ws, "ws"),
         ws.numel() * ws.element_size(), _dev(dev_status, "dev_status", torch.int32), _stream(stream)),
         "usp_attn_bwd")
+
+
+def usp_attn_bwd_preprocess(params: AttnParams, o, lse, dO, dsinks, ws, dev_status=None, stream=None):
+    _check(load().usp_attn_bwd_preprocess(
+        ctypes.byref(params), _dev(o, "o", torch.bfloat16), _dev(lse, "lse", torch.float32),
+        _dev(dO, "dO", torch.bfloat16), _dev(dsinks, "dsinks", torch.float32), _dev(ws, "ws"),
+        ws.numel() * ws.element_size(), _dev(dev_status, "dev_status", torch.int32), _stream(stream)),
+        "usp_attn_bwd_preprocess")
+
+
+def usp_attn_bwd_dkdv(params: AttnParams, q, k, v, lse, dO, dk, dv, ws, dev_status=None, stream=None):
+    _check(load().usp_attn_bwd_dkdv(
+        ctypes.byref(params), _dev(q, "q", torch.bfloat16), _dev(k, "k", torch.bfloat16),
+        _dev(v, "v", torch.bfloat16), _dev(lse, "lse", torch.float32), _dev(dO, "dO", torch.bfloat16),
+        _dev(dk, "dk", torch.bfloat16), _dev(dv, "dv", torch.bfloat16), _dev(ws, "ws"),
+        ws.numel() * ws.element_size(), _dev(dev_status, "dev_status", torch.int32), _stream(stream)),
+        "usp_attn_bwd_dkdv")
+
+
+def usp_attn_bwd_dq(params: AttnParams, q, k, v, lse, dO, dq, ws, dev_status=None, stream=None):
+    _check(load().usp_attn_bwd_dq(
+        ctypes.byref(params), _dev(q, "q", torch.bfloat16), _dev(k, "k", torch.bfloat16),
+        _dev(v, "v", torch.bfloat16), _dev(lse, "lse", torch.float32), _dev(dO, "dO", torch.bfloat16),
+        _dev(dq, "dq", torch.bfloat16), _dev(ws, "ws"), ws.numel() * ws.element_size(),
+        _dev(dev_status, "dev_status", torch.int32), _stream(stream)),
+        "usp_attn_bwd_dq")

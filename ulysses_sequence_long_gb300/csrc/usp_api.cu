@@ -196,4 +196,46 @@ int usp_attn_bwd(const usp_attn_params* params, const void* q, const void* k, co
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+int usp_attn_bwd_preprocess(const usp_attn_params* params, const void* o, const float* lse, const void* dO,
+                            float* dsinks, void* ws, size_t ws_bytes, int32_t* dev_status, usp_stream_t stream) {
+  int rc = check_attn_params(params);
+  if (rc != USP_OK) return rc;
+  if (o == nullptr || lse == nullptr || dO == nullptr) return USP_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(lse) || !aligned16(dO)) return USP_ERR_ALIGNMENT;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < attn_bwd_ws_bytes(*params))
+    return USP_ERR_WORKSPACE;
+  return launch_attn_bwd_preprocess(*params, o, lse, dO, params->sinks ? dsinks : nullptr, ws, dev_status,
+                                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_attn_bwd_dkdv(const usp_attn_params* params, const void* q, const void* k, const void* v, const float* lse,
+                      const void* dO, void* dk, void* dv, const void* ws, size_t ws_bytes, int32_t* dev_status,
+                      usp_stream_t stream) {
+  int rc = check_attn_params(params);
+  if (rc != USP_OK) return rc;
+  if (q == nullptr || k == nullptr || v == nullptr || lse == nullptr || dO == nullptr || dk == nullptr ||
+      dv == nullptr)
+    return USP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(lse) || !aligned16(dO) || !aligned16(dk) ||
+      !aligned16(dv))
+    return USP_ERR_ALIGNMENT;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < attn_bwd_ws_bytes(*params))
+    return USP_ERR_WORKSPACE;
+  return launch_attn_bwd_dkdv(*params, q, k, v, lse, dO, dk, dv, ws, dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_attn_bwd_dq(const usp_attn_params* params, const void* q, const void* k, const void* v, const float* lse,
+                    const void* dO, void* dq, const void* ws, size_t ws_bytes, int32_t* dev_status,
+                    usp_stream_t stream) {
+  int rc = check_attn_params(params);
+  if (rc != USP_OK) return rc;
+  if (q == nullptr || k == nullptr || v == nullptr || lse == nullptr || dO == nullptr || dq == nullptr)
+    return USP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(lse) || !aligned16(dO) || !aligned16(dq))
+    return USP_ERR_ALIGNMENT;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < attn_bwd_ws_bytes(*params))
+    return USP_ERR_WORKSPACE;
+  return launch_attn_bwd_dq(*params, q, k, v, lse, dO, dq, ws, dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

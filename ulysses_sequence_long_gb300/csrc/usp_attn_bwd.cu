@@ -19,6 +19,7 @@
 //   3. dQ           CTA = (rank, query head, 128 rows); loops over key tiles:
 //                     S = Q K^T, dP = dO V^T, dS -> bf16 in TMEM, dQ += dS K
 //   4. dsink        one block per (rank, head): a fixed-order tree reduction
+// (1 and 4 form the preprocess phase; each phase has its own entry point.)
 // Warp roles in 2 and 3 (320 threads): warps 0-7 compute (warp w owns TMEM lanes
 // 32*(w%4).. and column half w/4 of every 128-column tile), warp 8 feeds
 // shared memory (TMA), warp 9 issues the MMAs from one thread.
@@ -361,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float pr[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const bool vis = full || (key_ok && visible(q0 + c, u, a, b, p.causal, p.window_left));
+        const bool vis = full || (key_ok && visible_from_key(q0 + c, u, a, b, p.causal, p.window_left));
         pr[c] = vis ? ex2(fmaf(x[c], p.scale_log2, -lse2[c])) : 0.f;
       }
       st_packed64(lb + T_S + half * 64, pr);
@@ -584,51 +585,7 @@ size_t attn_bwd_ws_bytes(const usp_attn_params& p) {
   return (rows * sizeof(float) + 255) / 256 * 256;
 }
 
-template <int D>
-static int run_bwd(const AttnArgs& a, const void* q, const void* k, const void* v, const void* o, const float* lse,
-                   const void* dO, void* dq, void* dk, void* dv, float* dsinks, float* dvec, cudaStream_t st) {
-  using C = bwd::Cfg<D>;
-  // 1. D = rowsum(dO * O)
-  const uint32_t n_rows = static_cast<uint32_t>(static_cast<uint64_t>(a.P) * a.BS * a.hq);
-  {
-    const int per_block = 256 / (D / 8);
-    int grid = static_cast<int>((n_rows + per_block - 1) / per_block);
-    grid = grid < device_sm_count() * 8 ? grid : device_sm_count() * 8;
-    bwd::preprocess_kernel<D><<<grid, 256, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dO), dvec,
-                                                   a, n_rows);
-    if (check_launch() != USP_OK) return USP_ERR_CUDA;
-  }
-  CUtensorMap tq, tk, tv, tdo;
-  int rc;
-  if ((rc = make_head_tmap(&tq, q, a.P, a.BS, a.hq, D, kBM)) != USP_OK) return rc;
-  if ((rc = make_head_tmap(&tdo, dO, a.P, a.BS, a.hq, D, kBM)) != USP_OK) return rc;
-  if ((rc = make_head_tmap(&tk, k, a.P, a.BS, a.hk, D, kBN)) != USP_OK) return rc;
-  if ((rc = make_head_tmap(&tv, v, a.P, a.BS, a.hk, D, kBN)) != USP_OK) return rc;
-  bwd::Grads g{static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), lse,
-               dvec, (a.BS + kBM - 1) / kBM};
-  // 2. dK, dV
-  if (cudaFuncSetAttribute(bwd::dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::A_SMEM) != cudaSuccess)
-    return USP_ERR_CUDA;
-  bwd::dkdv_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hk, bwd::kThreads, C::A_SMEM, st>>>(tq, tk, tv, tdo,
-                                                                                                       a, g);
-  if (check_launch() != USP_OK) return USP_ERR_CUDA;
-  // 3. dQ
-  if (cudaFuncSetAttribute(bwd::dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::B_SMEM) != cudaSuccess)
-    return USP_ERR_CUDA;
-  bwd::dq_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hq, bwd::kThreads, C::B_SMEM, st>>>(tq, tk, tv, tdo,
-                                                                                                     a, g);
-  if (check_launch() != USP_OK) return USP_ERR_CUDA;
-  // 4. dsink
-  if (dsinks != nullptr && a.sinks != nullptr) {
-    bwd::dsink_kernel<<<a.P * a.hq, 256, 0, st>>>(lse, dvec, dsinks, a);
-    if (check_launch() != USP_OK) return USP_ERR_CUDA;
-  }
-  return USP_OK;
-}
-
-int launch_attn_bwd(const usp_attn_params& prm, const void* q, const void* k, const void* v, const void* o,
-                    const float* lse, const void* dO, void* dq, void* dk, void* dv, float* dsinks, void* ws,
-                    int32_t* status, cudaStream_t st) {
+static AttnArgs make_args(const usp_attn_params& prm, int32_t* status) {
   AttnArgs a;
   a.B = prm.B;
   a.S = prm.S;
@@ -645,9 +602,85 @@ int launch_attn_bwd(const usp_attn_params& prm, const void* q, const void* k, co
   a.n_docs = prm.n_docs;
   a.sinks = prm.sinks;
   a.status = status;
+  return a;
+}
+
+// 1. D = rowsum(dO * O) into the workspace, then the sink gradients.
+int launch_attn_bwd_preprocess(const usp_attn_params& prm, const void* o, const float* lse, const void* dO,
+                               float* dsinks, void* ws, int32_t* status, cudaStream_t st) {
+  const AttnArgs a = make_args(prm, status);
   float* dvec = static_cast<float*>(ws);
-  if (prm.D == 128) return run_bwd<128>(a, q, k, v, o, lse, dO, dq, dk, dv, dsinks, dvec, st);
-  return run_bwd<64>(a, q, k, v, o, lse, dO, dq, dk, dv, dsinks, dvec, st);
+  const uint32_t n_rows = static_cast<uint32_t>(static_cast<uint64_t>(a.P) * a.BS * a.hq);
+  const int per_block = 256 / (prm.D / 8);
+  int grid = static_cast<int>((n_rows + per_block - 1) / per_block);
+  grid = grid < device_sm_count() * 8 ? grid : device_sm_count() * 8;
+  if (prm.D == 128)
+    bwd::preprocess_kernel<128><<<grid, 256, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dO),
+                                                      dvec, a, n_rows);
+  else
+    bwd::preprocess_kernel<64><<<grid, 256, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dO),
+                                                     dvec, a, n_rows);
+  if (check_launch() != USP_OK) return USP_ERR_CUDA;
+  if (dsinks != nullptr && a.sinks != nullptr) {
+    bwd::dsink_kernel<<<a.P * a.hq, 256, 0, st>>>(lse, dvec, dsinks, a);
+    if (check_launch() != USP_OK) return USP_ERR_CUDA;
+  }
+  return USP_OK;
+}
+
+template <int D>
+static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const void* k, const void* v,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv, const float* dvec,
+                         cudaStream_t st) {
+  using C = bwd::Cfg<D>;
+  CUtensorMap tq, tk, tv, tdo;
+  int rc;
+  if ((rc = make_head_tmap(&tq, q, a.P, a.BS, a.hq, D, kBM)) != USP_OK) return rc;
+  if ((rc = make_head_tmap(&tdo, dO, a.P, a.BS, a.hq, D, kBM)) != USP_OK) return rc;
+  if ((rc = make_head_tmap(&tk, k, a.P, a.BS, a.hk, D, kBN)) != USP_OK) return rc;
+  if ((rc = make_head_tmap(&tv, v, a.P, a.BS, a.hk, D, kBN)) != USP_OK) return rc;
+  bwd::Grads g{static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), lse,
+               dvec, (a.BS + kBM - 1) / kBM};
+  if (!dq_pass) {
+    if (cudaFuncSetAttribute(bwd::dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::A_SMEM) !=
+        cudaSuccess)
+      return USP_ERR_CUDA;
+    bwd::dkdv_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hk, bwd::kThreads, C::A_SMEM, st>>>(
+        tq, tk, tv, tdo, a, g);
+  } else {
+    if (cudaFuncSetAttribute(bwd::dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::B_SMEM) != cudaSuccess)
+      return USP_ERR_CUDA;
+    bwd::dq_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hq, bwd::kThreads, C::B_SMEM, st>>>(tq, tk, tv,
+                                                                                                       tdo, a, g);
+  }
+  return check_launch();
+}
+
+// 2. dK, dV
+int launch_attn_bwd_dkdv(const usp_attn_params& prm, const void* q, const void* k, const void* v, const float* lse,
+                         const void* dO, void* dk, void* dv, const void* ws, int32_t* status, cudaStream_t st) {
+  const AttnArgs a = make_args(prm, status);
+  const float* dvec = static_cast<const float*>(ws);
+  if (prm.D == 128) return run_grad_pass<128>(false, a, q, k, v, lse, dO, nullptr, dk, dv, dvec, st);
+  return run_grad_pass<64>(false, a, q, k, v, lse, dO, nullptr, dk, dv, dvec, st);
+}
+
+// 3. dQ
+int launch_attn_bwd_dq(const usp_attn_params& prm, const void* q, const void* k, const void* v, const float* lse,
+                       const void* dO, void* dq, const void* ws, int32_t* status, cudaStream_t st) {
+  const AttnArgs a = make_args(prm, status);
+  const float* dvec = static_cast<const float*>(ws);
+  if (prm.D == 128) return run_grad_pass<128>(true, a, q, k, v, lse, dO, dq, nullptr, nullptr, dvec, st);
+  return run_grad_pass<64>(true, a, q, k, v, lse, dO, dq, nullptr, nullptr, dvec, st);
+}
+
+int launch_attn_bwd(const usp_attn_params& prm, const void* q, const void* k, const void* v, const void* o,
+                    const float* lse, const void* dO, void* dq, void* dk, void* dv, float* dsinks, void* ws,
+                    int32_t* status, cudaStream_t st) {
+  int rc;
+  if ((rc = launch_attn_bwd_preprocess(prm, o, lse, dO, dsinks, ws, status, st)) != USP_OK) return rc;
+  if ((rc = launch_attn_bwd_dkdv(prm, q, k, v, lse, dO, dk, dv, ws, status, st)) != USP_OK) return rc;
+  return launch_attn_bwd_dq(prm, q, k, v, lse, dO, dq, ws, status, st);
 }
 
 }  // namespace usp

@@ -59,6 +59,15 @@ __device__ __forceinline__ bool visible(int t, int u, int a, int b, int causal, 
   return v;
 }
 
+// The same rule seen from the key: query t sees key u of document [a, b) when
+// t lies in that document and the causal/window conditions hold.
+__device__ __forceinline__ bool visible_from_key(int t, int u, int a, int b, int causal, int wl) {
+  bool v = (t >= a) && (t < b);
+  if (causal) v = v && (u <= t);
+  if (wl >= 0) v = v && (t - u <= wl) && (causal || u - t <= wl);
+  return v;
+}
+
 // First and one-past-last key any of the rows [t_first, t_last] may see.
 __device__ __forceinline__ void key_range(const AttnArgs& p, int n, int t_first, int t_last, int& lo, int& hi) {
   int a0, b0, a1, b1;
