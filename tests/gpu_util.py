@@ -26,22 +26,59 @@ def built_lib():
     return binding.load()
 
 
-def errors(got, ref):
+def half_ulp_bf16(x):
+    """Half the bf16 spacing at |x|: the rounding error of storing x in bf16."""
+    a = np.maximum(np.abs(np.asarray(x, dtype=np.float64)), 2.0 ** -126)
+    return np.ldexp(1.0, np.floor(np.log2(a)).astype(np.int64) - 8)
+
+
+def errors(got, ref, bf16_out=True):
+    """(max-abs error, relative L2 error) of got against the fp64 reference.
+
+    For bf16 outputs the max-abs error leaves out the output format's own
+    rounding (half a bf16 ulp at the reference value): above |x| = 8 that
+    alone exceeds 2e-2, so no bf16-output implementation could meet the bound
+    otherwise.  The relative L2 error is taken as is.
+    """
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), "non-finite values in the GPU output"
-    d = got - ref
-    max_abs = float(np.max(np.abs(d))) if d.size else 0.0
-    rel = float(np.linalg.norm(d) / max(np.linalg.norm(ref), 1e-30))
+    d = np.abs(got - ref)
+    if bf16_out:
+        d = np.maximum(d - half_ulp_bf16(ref), 0.0)
+    max_abs = float(np.max(d)) if d.size else 0.0
+    rel = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
     return max_abs, rel
 
 
-def assert_close(name, got, ref, max_abs=MAX_ABS, rel_l2=REL_L2):
-    ma, rl = errors(got, ref)
-    print(f"[parity] {name}: max_abs={ma:.3e} rel_l2={rl:.3e} |ref|max={float(np.max(np.abs(ref))):.3e}")
+def assert_close(name, got, ref, max_abs=MAX_ABS, rel_l2=REL_L2, bf16_out=True):
+    ma, rl = errors(got, ref, bf16_out)
+    raw = float(np.max(np.abs(np.asarray(got, np.float64) - np.asarray(ref, np.float64))))
+    print(f"[parity] {name}: max_abs={ma:.3e} (raw {raw:.3e}) rel_l2={rl:.3e} "
+          f"|ref|max={float(np.max(np.abs(ref))):.3e}")
     assert ma <= max_abs and rl <= rel_l2, f"{name}: max_abs={ma:.3e} (<= {max_abs}) rel_l2={rl:.3e} (<= {rel_l2})"
     return ma, rl
+
+
+def dsink_bound(lse, sinks, o, do, hq):
+    """Error bound of dsinks, from the arithmetic (fp32 output, no stated tolerance).
+
+    dz_h = -sum_t exp(z_h - LSE_t) D_t with D_t = dO_t . O_t computed from the
+    bf16-rounded O the forward returns: each O element carries a relative
+    rounding error up to 2^-9, so |error| <= 2^-9 sum_t exp(z - LSE_t)
+    sum_d |dO_td O_td| to first order; twice that plus 1e-4 is allowed.
+    Arguments are the oracle's fp64 values in head layout: lse [P][B][hq][S],
+    sinks [Hq], o/do [P][B][S][hq][D].
+    """
+    P = lse.shape[0]
+    out = np.zeros(P * hq)
+    for r in range(P):
+        z = np.asarray(sinks[r * hq:(r + 1) * hq], np.float64)          # [hq]
+        w = np.exp(z[None, :, None] - lse[r])                           # [B][hq][S]
+        mag = np.abs(do[r] * o[r]).sum(-1).transpose(0, 2, 1)          # [B][hq][S]
+        out[r * hq:(r + 1) * hq] = (w * mag).sum(axis=(0, 2))
+    return 2.0 * 2.0 ** -9 * out + 1e-4
 
 
 def device_inputs(w: W.Workload, device="cuda"):

@@ -66,7 +66,7 @@ def test_forward_full_parity_small(w):
     snk = host["sinks"]
     ref = oracle.ulysses_fwd(host["q"], host["k"], host["v"], host["pos"], w.causal, w.window_left, None, snk)
     assert_close("o_seq", ua.o_seq.float().cpu().numpy(), ref["o_seq"])
-    assert_close("lse", ua.lse.cpu().numpy(), ref["lse"])
+    assert_close("lse", ua.lse.cpu().numpy(), ref["lse"], bf16_out=False)
     cu = ua.cu_seqlens[: ua.n_docs.item() + 1].cpu().numpy()
     assert np.array_equal(cu, ref["cu_seqlens"])
 
@@ -82,7 +82,7 @@ def test_forward_full_size_sampled_heads(w, pairs):
         O, L = _oracle_rank_head(w, host, ua, r, j)
         o, lse = _gpu_rank_head(w, ua, r, j)
         assert_close(f"O r{r} h{j}", o, O)
-        assert_close(f"LSE r{r} h{j}", lse, L)
+        assert_close(f"LSE r{r} h{j}", lse, L, bf16_out=False)
 
 
 def test_forward_long_context_sampled_rows():
@@ -98,7 +98,7 @@ def test_forward_long_context_sampled_rows():
         O, L = oracle.attention_fwd_rows(qh, kh, vh, [0, w.S], rows, j)
         o, lse = _gpu_rank_head(w, ua, r, j)
         assert_close(f"O r{r} h{j}", o[rows], O)
-        assert_close(f"LSE r{r} h{j}", lse[rows], L)
+        assert_close(f"LSE r{r} h{j}", lse[rows], L, bf16_out=False)
 
 
 def test_stale_per_shard_cu_seqlens_are_flagged():
