@@ -75,7 +75,11 @@ GPTOSS_FULL = Workload("gpt_oss_full_s16384", B=1, S=16384, Hq=64, Hkv=8, D=64, 
 LONG128K = Workload("long_context_s131072", B=1, S=131072, Hq=28, Hkv=4, D=128, P=4)
 
 ALL = [TINY, MHA4K, LLAMA32K, GPTOSS_WIN, GPTOSS_FULL, LONG128K]
-BY_NAME = {w.name: w for w in ALL}
+# A quarter-length Llama-shaped case for profiler captures: the same kernels and
+# tile mix, inputs still larger than L2 (168 MB of q/k/v/dO), far fewer launches.
+LLAMA8K_PROFILE = Workload("llama3_8b_gqa_packed_s8192", B=1, S=8192, Hq=32, Hkv=8, D=128, P=8,
+                           doc_mode="geometric", doc_mean=4096, seed=1)
+BY_NAME = {w.name: w for w in ALL + [LLAMA8K_PROFILE]}
 
 
 def document_lengths(w: Workload) -> List[List[int]]:
