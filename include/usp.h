@@ -136,6 +136,25 @@ int usp_cu_seqlens_from_position_ids(const int32_t* pos, int B, int S, int P,
                                      void* ws, size_t ws_bytes, int32_t* dev_status,
                                      usp_stream_t stream);
 
+/* Same result as usp_cu_seqlens_from_position_ids, for callers that cannot
+ * allocate device memory or hand over a workspace (for example code whose
+ * device memory is entirely reserved by another allocator, or a plugin
+ * interface that passes only input and output pointers).  It allocates
+ * nothing: the scan's scratch lives in a fixed 64 KiB device array inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  The pages have no counterpart of this call.
+ *   - B*S may be at most 2^24 tokens; larger sizes return USP_ERR_UNSUPPORTED.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array: calls whose kernels may overlap on the
+ *     GPU (other streams, other host threads) race and must be ordered by the
+ *     caller.  Leftover contents from an earlier call never matter.
+ * Other arguments, outputs and errors are those of
+ * usp_cu_seqlens_from_position_ids. */
+int usp_cu_seqlens_from_position_ids_noalloc(const int32_t* pos, int B, int S, int P, int32_t* cu_seqlens,
+                                             int32_t* n_docs, int32_t* max_len, int32_t* dev_status,
+                                             usp_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Attention over the gathered sequence, all P emulated ranks in one launch.
  *

@@ -32,6 +32,7 @@ EXPORTED = [
     "usp_status_string", "usp_version",
     "usp_relayout_fwd", "usp_relayout_bwd", "usp_relayout_fwd_qkv",
     "usp_cu_seqlens_workspace_bytes", "usp_cu_seqlens_from_position_ids",
+    "usp_cu_seqlens_from_position_ids_noalloc",
     "usp_attn_fwd", "usp_attn_bwd_workspace_bytes", "usp_attn_bwd",
     "usp_attn_bwd_preprocess", "usp_attn_bwd_dkdv", "usp_attn_bwd_dq",
 ]
@@ -75,6 +76,7 @@ def load() -> ctypes.CDLL:
     L.usp_cu_seqlens_workspace_bytes.restype = sz
     L.usp_cu_seqlens_workspace_bytes.argtypes = [i32, i32]
     L.usp_cu_seqlens_from_position_ids.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, sz, vp, vp]
+    L.usp_cu_seqlens_from_position_ids_noalloc.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp]
     L.usp_attn_fwd.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, vp, vp]
     L.usp_attn_bwd_workspace_bytes.restype = sz
     L.usp_attn_bwd_workspace_bytes.argtypes = [ctypes.POINTER(AttnParams)]
@@ -83,7 +85,8 @@ def load() -> ctypes.CDLL:
     L.usp_attn_bwd_dkdv.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     L.usp_attn_bwd_dq.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     for name in ("usp_relayout_fwd", "usp_relayout_bwd", "usp_relayout_fwd_qkv",
-                 "usp_cu_seqlens_from_position_ids", "usp_attn_fwd", "usp_attn_bwd",
+                 "usp_cu_seqlens_from_position_ids", "usp_cu_seqlens_from_position_ids_noalloc",
+                 "usp_attn_fwd", "usp_attn_bwd",
                  "usp_attn_bwd_preprocess", "usp_attn_bwd_dkdv", "usp_attn_bwd_dq"):
         getattr(L, name).restype = i32
     _lib = L
@@ -147,6 +150,16 @@ def usp_cu_seqlens_from_position_ids(pos, B, S, P, cu_seqlens, n_docs, max_len, 
         _dev(n_docs, "n_docs", torch.int32), _dev(max_len, "max_len", torch.int32), _dev(ws, "ws"),
         ws.numel() * ws.element_size(), _dev(dev_status, "dev_status", torch.int32), _stream(stream)),
         "usp_cu_seqlens_from_position_ids")
+
+
+def usp_cu_seqlens_from_position_ids_noalloc(pos, B, S, P, cu_seqlens, n_docs, max_len, dev_status=None,
+                                             stream=None):
+    """The scan without a workspace: its scratch is a fixed array inside the library (B*S <= 2^24)."""
+    _check(load().usp_cu_seqlens_from_position_ids_noalloc(
+        _dev(pos, "pos", torch.int32), B, S, P, _dev(cu_seqlens, "cu_seqlens", torch.int32),
+        _dev(n_docs, "n_docs", torch.int32), _dev(max_len, "max_len", torch.int32),
+        _dev(dev_status, "dev_status", torch.int32), _stream(stream)),
+        "usp_cu_seqlens_from_position_ids_noalloc")
 
 
 def attn_params(B, S, Hq, Hkv, D, P, cu_seqlens, n_docs, causal=True, window_left=-1, softmax_scale=0.0,
