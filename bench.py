@@ -103,7 +103,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except (FileNotFoundError, OSError):
@@ -149,18 +149,21 @@ CALLS = ["relayout_qkv", "cu_seqlens", "attn_fwd", "relayout_o", "relayout_do", 
 
 
 class Step:
-    def __init__(self, w: W.Workload, device):
+    def __init__(self, w: W.Workload, device, host=None):
         from ulysses_sequence_long_gb300 import binding as B
         from ulysses_sequence_long_gb300.pipeline import Shape, UlyssesAttention
         self.B_ = B
         self.w = w
+        self.device = device
         self.ua = UlyssesAttention(Shape(w.B, w.S, w.Hq, w.Hkv, w.D, w.P, w.causal, w.window_left), device=device)
-        t = W.qkv_do_shards(w)
-        self.host = t
-        self.dev = {n: x.to(device) for n, x in t.items()}
-        self.pos_host = torch.from_numpy(W.position_ids_shards(w))
+        if host is None:
+            host = {"t": W.qkv_do_shards(w), "pos": torch.from_numpy(W.position_ids_shards(w)), "sinks": W.sinks(w)}
+        self.shared_host = host
+        self.host = host["t"]
+        self.dev = {n: x.to(device) for n, x in self.host.items()}
+        self.pos_host = host["pos"]
         self.pos = self.pos_host.to(device)
-        sk = W.sinks(w)
+        sk = host["sinks"]
         self.sinks = None if sk is None else sk.to(device)
         self.stream = torch.cuda.current_stream(device)
         self.n_events = 0
@@ -222,18 +225,63 @@ class Step:
         d2h = sum(t.numel() * t.element_size() for t in outs.values())
         return pin, outs, h2d, d2h
 
-    def run_e2e(self, pin, outs):
-        ua, d = self.ua, self.dev
+    def upload(self, pin):
+        d = self.dev
         for n in ("q", "k", "v", "do"):
             d[n].copy_(pin[n], non_blocking=True)
         self.pos.copy_(pin["pos"], non_blocking=True)
-        self.run()
+
+    def download(self, outs):
+        ua = self.ua
         outs["o"].copy_(ua.o_seq, non_blocking=True)
         outs["dq"].copy_(ua.dq_seq, non_blocking=True)
         outs["dk"].copy_(ua.dk_seq, non_blocking=True)
         outs["dv"].copy_(ua.dv_seq, non_blocking=True)
         if "dsinks" in outs:
             outs["dsinks"].copy_(ua.dsinks, non_blocking=True)
+
+
+def run_e2e(slots, pin, outs, steps):
+    """`steps` whole steps with host buffers in and out, double-buffered.
+
+    Every step uploads its inputs from pinned host memory and downloads its
+    results (O, dQ, dK, dV, dsinks) to pinned host memory.  Step k computes on
+    slot k%2 while the inputs of step k+1 upload on one copy stream and the
+    results of step k-1 download on another.  Returns the elapsed ms between
+    CUDA events recorded before the first upload and after the last download.
+    """
+    comp = slots[0].stream
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_ready, done, out_read = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(comp)
+    up.wait_event(start)
+    with torch.cuda.stream(up):
+        slots[0].upload(pin)
+        in_ready[0].record(up)
+    for k in range(steps):
+        c, n = k % 2, (k + 1) % 2
+        comp.wait_event(in_ready[c])
+        if k >= 2:
+            comp.wait_event(out_read[c])         # results of step k-2 have left this slot
+        with torch.cuda.stream(comp):
+            slots[c].run()
+        done[c].record(comp)
+        if k + 1 < steps:
+            if k >= 1:
+                up.wait_event(done[n])           # step k-1 no longer reads that slot's inputs
+            with torch.cuda.stream(up):
+                slots[n].upload(pin)
+                in_ready[n].record(up)
+        down.wait_event(done[c])
+        with torch.cuda.stream(down):
+            slots[c].download(outs)
+            out_read[c].record(down)
+    comp.wait_stream(down)
+    stop.record(comp)
+    torch.cuda.synchronize()
+    return start.elapsed_time(stop)
 
 
 # ----------------------------------------------------------------------------- oracle timing
@@ -302,7 +350,7 @@ def run_reference(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="usp", choices=["usp", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))
@@ -407,18 +455,14 @@ def main():
 
     if not args.no_e2e:
         pin, outs, h2d, d2h = step.make_host_io()
-        step.run_e2e(pin, outs)
-        torch.cuda.synchronize()
+        twin = Step(w, device, host=step.shared_host)
+        slots = [step, twin]
+        run_e2e(slots, pin, outs, 3)               # warm-up of the copy path
         barrier()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            step.run_e2e(pin, outs)
-        e1.record()
-        torch.cuda.synchronize()
+        ems = run_e2e(slots, pin, outs, args.steps) / args.steps
         barrier()
-        ems = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+        ems = max_over_ranks(ems)
         line["e2e"] = {"value": fl["total"] * world / (ems * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ems,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

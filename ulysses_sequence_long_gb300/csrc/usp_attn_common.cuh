@@ -121,4 +121,8 @@ namespace usp {
 // box {64, 1, rows, 1}, 128-byte swizzle (one 128-byte row per token).
 int make_head_tmap(CUtensorMap* m, const void* base, int P, int BS, int H, int D, int box_rows);
 
+// Tensor map of the backward's per-row records, fp32 [P*hq][BS][4]: dims
+// {4, BS, P*hq}, box {4, box_rows, 1} (box_rows tokens of one head).
+int make_stats_tmap(CUtensorMap* m, const void* base, int BS, int rows, int box_rows);
+
 }  // namespace usp

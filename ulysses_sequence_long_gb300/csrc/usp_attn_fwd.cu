@@ -265,9 +265,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBN; ++c)
           if (!(row_ok && visible(t, kv0 + c, a, b, p.causal, p.window_left))) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // row max as 8 independent chains
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+      for (int e = 0; e < 8; ++e) mx8[e] = s[e];
+#pragma unroll
+      for (int c = 8; c < kBN; c += 8)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(mx8[e], s[c + e]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_tile = mx * p.scale_log2;  // -inf stays -inf
       const float m_new = fmaxf(m, m_tile);
       const bool need = m_new > m + 8.f;
@@ -290,16 +297,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float m_use = (m == -INFINITY) ? 0.f : m;
-      float rs = 0.f;
+      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
       uint32_t pk[2][32];
 #pragma unroll
       for (int c = 0; c < kBN / 2; ++c) {
         const float p0 = ex2(fmaf(s[2 * c], p.scale_log2, -m_use));
         const float p1 = ex2(fmaf(s[2 * c + 1], p.scale_log2, -m_use));
-        rs += p0 + p1;
+        rs8[c & 7] += p0 + p1;
         pk[c >> 5][c & 31] = pack_bf16x2(p0, p1);
       }
-      l += rs;
+      l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       tmem_st32(s_tm, pk[0]);
       tmem_st32(s_tm + 32, pk[1]);
       tmem_wait_st();
