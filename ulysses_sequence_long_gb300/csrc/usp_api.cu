@@ -59,12 +59,12 @@ int make_head_tmap(CUtensorMap* m, const void* base, int P, int BS, int H, int D
   return rc == CUDA_SUCCESS ? USP_OK : USP_ERR_CUDA;
 }
 
-int make_stats_tmap(CUtensorMap* m, const void* base, int BS, int rows, int box_rows) {
+int make_stats_tmap(CUtensorMap* m, const void* base, int BS, int pitch, int rows, int box_rows) {
   auto fn = encode_fn();
   if (fn == nullptr) return USP_ERR_CUDA;
-  cuuint64_t dims[3] = {4, static_cast<cuuint64_t>(BS), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[2] = {16, static_cast<cuuint64_t>(BS) * 16};
-  cuuint32_t box[3] = {4, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(BS), 2, static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch) * 4, static_cast<cuuint64_t>(pitch) * 8};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_rows), 2, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult rc = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,

@@ -9,20 +9,26 @@
 // Key/value gradients sum over the query heads of their GQA group; on each
 // rank those are its own heads (contiguous head blocks keep groups local).
 //
-// Four launches:
-//   1. preprocess   D_t for every (rank, query head, token): fp32 workspace
-//   2. dK/dV        CTA = (rank, kv head, 128 keys); loops over the group's
-//                   query heads and the 128-row query tiles that see the keys:
-//                     S^T = K Q^T, dP^T = V dO^T            (TMEM, fp32)
-//                     P^T, dS^T -> bf16 in TMEM over S^T / dP^T
-//                     dV += P^T dO, dK += dS^T Q           (A operand from TMEM)
-//   3. dQ           CTA = (rank, query head, 128 rows); loops over key tiles:
-//                     S = Q K^T, dP = dO V^T, dS -> bf16 in TMEM, dQ += dS K
-//   4. dsink        one block per (rank, head): a fixed-order tree reduction
-// (1 and 4 form the preprocess phase; each phase has its own entry point.)
-// Warp roles in 2 and 3 (320 threads): warps 0-7 compute (warp w owns TMEM lanes
-// 32*(w%4).. and column half w/4 of every 128-column tile), warp 8 feeds
-// shared memory (TMA), warp 9 issues the MMAs from one thread.
+// Launches (each phase has its own entry point):
+//   preprocess  D_t and LSE_t*log2(e) for every (rank, query head, token), in a
+//               planar fp32 workspace [P*hq][2][B*S padded to 4]; then the sink
+//               gradients (one block per head, fixed-order tree reduction).
+//   dK/dV       CTA = (rank, kv head, 128 keys).  K and V live in TMEM for the
+//               whole CTA and serve as the A operands of S^T = K Q^T and
+//               dP^T = V dO^T; 64-query slices of Q, dO and their statistics
+//               stream through shared memory; P^T and dS^T (bf16) are written
+//               over S^T / dP^T and feed dV += P^T dO, dK += dS^T Q.
+//   dQ          CTA = (rank, query head, 128 rows).  Q and dO live in TMEM as
+//               the A operands of S = Q K^T and dP = dO V^T; 64-key slices of
+//               K and V stream through shared memory; S/dP are double-buffered
+//               so one compute group works while the tensor core fills the
+//               other buffer; dS (bf16 over S) feeds dQ += dS K.
+// Every MMA takes its A operand from TMEM and only its B operand from shared
+// memory: that keeps the tensor core's shared-memory reads well under the
+// SM's bandwidth, which smem x smem MMAs at these tile widths exceed.
+// Warp roles (320 threads): warps 0-7 compute (warp w owns TMEM lanes
+// 32*(w%4)..+31), warp 8 feeds shared memory (TMA), warp 9 issues the MMAs
+// from one thread.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -36,7 +42,8 @@ namespace usp {
 namespace bwd {
 
 constexpr int kThreads = 320;
-constexpr int kAtomBytes = kBM * 128;
+constexpr int kSL = 64;                      // slice width (queries in dK/dV, keys in dQ)
+constexpr int kSliceBytes = kSL * 128;       // 64-row, 128-byte-wide swizzle column
 constexpr float kLog2e = 1.4426950408889634f;
 
 // index of (rank r, local head j, rank-local token t) in a [P][B][hq][S] array
@@ -45,15 +52,19 @@ __device__ __forceinline__ size_t stat_index(const AttnArgs& p, int r, int j, in
   return (static_cast<size_t>(r * p.B + b) * p.hq + j) * p.S + s;
 }
 
+// Planar statistics: plane 0 = LSE*log2(e), plane 1 = D, rows of `bsp`
+// (B*S rounded up to a multiple of 4, so every plane starts 16-byte aligned).
+__device__ __forceinline__ size_t plane_index(int bsp, int hq, int r, int j, int plane, int t) {
+  return ((static_cast<size_t>(r) * hq + j) * 2 + plane) * bsp + t;
+}
+
 // --------------------------------------------------------------- preprocess
 // One row = D bf16 = D/8 lanes of 16 bytes.  Rows are (rank, token, head) in
-// head-layout order, so reads are contiguous.  Output: one 16-byte record per
-// (rank, head, token), {LSE*log2(e), D, 0, 0}, laid out [P][hq][B*S] so that a
-// 128-token tile of one head is one contiguous 2 KB box for TMA.
+// head-layout order, so reads are contiguous.
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
-                                                         const float* __restrict__ lse, float4* __restrict__ stats,
-                                                         AttnArgs p, uint32_t n_rows) {
+                                                         const float* __restrict__ lse, float* __restrict__ stats,
+                                                         AttnArgs p, int bsp, uint32_t n_rows) {
   constexpr int LPR = D / 8;  // lanes per row
   const uint32_t lane_row = threadIdx.x % LPR;
   for (uint32_t row = (blockIdx.x * blockDim.x + threadIdx.x) / LPR; row < n_rows + (32 / LPR);
@@ -73,24 +84,22 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
       const uint32_t j = row % p.hq;
       const uint32_t rt = row / p.hq;
       const uint32_t r = rt / p.BS, t = rt - r * p.BS;
-      const float l2 = __ldg(lse + stat_index(p, r, j, t)) * kLog2e;
-      stats[(static_cast<size_t>(r) * p.hq + j) * p.BS + t] = make_float4(l2, acc, 0.f, 0.f);
+      stats[plane_index(bsp, p.hq, r, j, 0, t)] = __ldg(lse + stat_index(p, r, j, t)) * kLog2e;
+      stats[plane_index(bsp, p.hq, r, j, 1, t)] = acc;
     }
   }
 }
 
 // --------------------------------------------------------------- dsink
-__global__ void __launch_bounds__(256) dsink_kernel(const float4* __restrict__ stats, float* __restrict__ dsinks,
-                                                    AttnArgs p) {
+__global__ void __launch_bounds__(256) dsink_kernel(const float* __restrict__ stats, float* __restrict__ dsinks,
+                                                    AttnArgs p, int bsp) {
   __shared__ float red[256];
   const int r = blockIdx.x / p.hq, j = blockIdx.x % p.hq;
   const float z2 = __ldg(p.sinks + r * p.hq + j) * kLog2e;
-  const float4* row = stats + (static_cast<size_t>(r) * p.hq + j) * p.BS;
+  const float* l2 = stats + plane_index(bsp, p.hq, r, j, 0, 0);
+  const float* dd = stats + plane_index(bsp, p.hq, r, j, 1, 0);
   float acc = 0.f;
-  for (int t = threadIdx.x; t < p.BS; t += blockDim.x) {
-    const float4 st = __ldg(row + t);
-    acc -= ex2(z2 - st.x) * st.y;
-  }
+  for (int t = threadIdx.x; t < p.BS; t += blockDim.x) acc -= ex2(z2 - __ldg(l2 + t)) * __ldg(dd + t);
   red[threadIdx.x] = acc;
   __syncthreads();
   for (int s = 128; s > 0; s >>= 1) {
@@ -101,27 +110,60 @@ __global__ void __launch_bounds__(256) dsink_kernel(const float4* __restrict__ s
 }
 
 // --------------------------------------------------------------- helpers
-__device__ __forceinline__ void ld64(uint32_t taddr, float (&x)[64]) {
-  uint32_t a[32], b[32];
-  tmem_ld32(taddr, a);
-  tmem_ld32(taddr + 32, b);
-  tmem_wait_ld();
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&x)[N]) {
+  static_assert(N % 32 == 0, "");
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    x[e] = __uint_as_float(a[e]);
-    x[32 + e] = __uint_as_float(b[e]);
+  for (int c = 0; c < N / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld32(taddr + c * 32, v);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]);
   }
+  tmem_wait_ld();
 }
 
-__device__ __forceinline__ void st_packed64(uint32_t taddr, const float (&x)[64]) {
+// x[0..2M) as M packed bf16 pairs into TMEM columns [taddr, taddr + M).
+template <int M>
+__device__ __forceinline__ void tmem_st_packed(uint32_t taddr, const float* x) {
   uint32_t pk[32];
 #pragma unroll
-  for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
-  tmem_st32(taddr, pk);
+  for (int e = 0; e < 32; ++e) pk[e] = e < M ? pack_bf16x2(x[2 * e], x[2 * e + 1]) : 0u;
+  if constexpr (M == 32) {
+    tmem_st32(taddr, pk);
+  } else {
+    static_assert(M == 16, "");
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7]), "r"(pk[8]),
+        "r"(pk[9]), "r"(pk[10]), "r"(pk[11]), "r"(pk[12]), "r"(pk[13]), "r"(pk[14]), "r"(pk[15])
+        : "memory");
+  }
   tmem_wait_st();
 }
 
-// Write one TMEM row (D fp32 columns at `taddr`) times `mul` as bf16 to `dst` (if `ok`).
+// One bf16 row of D elements (global, 16-byte aligned) into TMEM as D/2 packed
+// columns: the A-operand layout (lane = row, column = pair of K elements).
+template <int D>
+__device__ __forceinline__ void row_to_tmem(uint32_t taddr, const __nv_bfloat16* src, bool ok) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    uint32_t v[32];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      uint4 w = ok ? __ldg(reinterpret_cast<const uint4*>(src + c * 64) + e) : make_uint4(0, 0, 0, 0);
+      v[4 * e] = w.x;
+      v[4 * e + 1] = w.y;
+      v[4 * e + 2] = w.z;
+      v[4 * e + 3] = w.w;
+    }
+    tmem_st32(taddr + c * 32, v);
+  }
+  tmem_wait_st();
+}
+
+// Write one TMEM row (NCOL fp32 columns at `taddr`) times `mul` as bf16 to `dst` (if `ok`).
 template <int NCOL>
 __device__ __forceinline__ void store_row(uint32_t taddr, __nv_bfloat16* dst, float mul, bool ok) {
 #pragma unroll 1
@@ -140,50 +182,47 @@ __device__ __forceinline__ void store_row(uint32_t taddr, __nv_bfloat16* dst, fl
   }
 }
 
-// Both gradient kernels work on 64-wide slices of the 128-lane tiles and keep
-// two slices in TMEM at once (buffers 0 and 1): while compute group g forms
-// P and dS for its slice, the tensor core computes the other group's next
-// slice and the gradient products of the previous one.
-constexpr int kSL = 64;                        // slice width (queries in dK/dV, keys in dQ)
-constexpr int kSliceBytes = kSL * 128;          // one 64-row, 128-byte-wide swizzle column
+// K-major B operand (rows x D, 128-byte swizzle, `atom_bytes` per 64-column
+// atom), MMA step kk over D.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int atom_bytes, int kk) {
+  return sdesc_sw128(base + (kk >> 2) * atom_bytes + (kk & 3) * 32, 16, 1024);
+}
+// MN-major B operand (rows = the MMA's K dimension, 128-byte rows of D), step kk over rows.
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int atom_bytes, int kk) {
+  return sdesc_sw128(base + kk * 16 * 128, atom_bytes, 1024);
+}
 
 template <int D>
 struct Cfg {
   static constexpr int NCH = D / 64;
-  static constexpr int TILE = NCH * kAtomBytes;   // 128-row bf16 tile
   static constexpr int SLICE = NCH * kSliceBytes;  // 64-row bf16 tile
-  static constexpr int STAT = kSL * 16;           // 64 records {LSE*log2e, D, 0, 0}
-  // dK/dV: K, V (128 keys) once; ring of (Q, dO, stats) 64-query slices
-  static constexpr int QST = (D == 128) ? 4 : 8;
-  static constexpr int A_K = 0;
-  static constexpr int A_V = A_K + TILE;
-  static constexpr int A_Q = A_V + TILE;
-  static constexpr int A_DO = A_Q + QST * SLICE;
-  static constexpr int A_STAT = A_DO + QST * SLICE;
-  static constexpr int A_BAR = A_STAT + QST * STAT;
+  static constexpr int STAT = 2 * kSL * 4;        // [2][64] fp32: LSE*log2e, D
+  static constexpr int NST = (D == 128) ? 6 : 8;  // stages of the streamed slices
+  // dK/dV: ring of (Q, dO, stats) 64-query slices
+  static constexpr int A_Q = 0;
+  static constexpr int A_DO = A_Q + NST * SLICE;
+  static constexpr int A_STAT = A_DO + NST * SLICE;
+  static constexpr int A_BAR = A_STAT + NST * STAT;
   static constexpr int A_SMEM = A_BAR + 1024 + 1024;
-  // dQ: Q, dO (128 rows) once; ring of (K, V) 64-key slices
-  static constexpr int KST = (D == 128) ? 4 : 8;
-  static constexpr int B_Q = 0;
-  static constexpr int B_DO = B_Q + TILE;
-  static constexpr int B_K = B_DO + TILE;
-  static constexpr int B_V = B_K + KST * SLICE;
-  static constexpr int B_BAR = B_V + KST * SLICE;
+  // dQ: ring of (K, V) 64-key slices
+  static constexpr int B_K = 0;
+  static constexpr int B_V = B_K + NST * SLICE;
+  static constexpr int B_BAR = B_V + NST * SLICE;
   static constexpr int B_SMEM = B_BAR + 1024 + 1024;
 };
 
 struct BarsA {
-  uint64_t kv_full;
+  uint64_t kv_ready;  // K, V rows stored into TMEM by the compute warps
   uint64_t qdo_full[8];
   uint64_t qdo_empty[8];
-  uint64_t st_full[2], dpt_full[2], p_full[2], ds_full[2];
+  uint64_t st_full, dpt_full, p_full, ds_full;
   uint64_t fin, mma_done;
   uint32_t tmem;
   int abort;
 };
 
 struct BarsB {
-  uint64_t q_full;
+  uint64_t qd_ready;  // Q, dO rows stored into TMEM by the compute warps
   uint64_t k_full[8], v_full[8], kv_empty[8];
   uint64_t s_full[2], dp_full[2], ds_full[2];
   uint64_t fin, mma_done;
@@ -192,37 +231,32 @@ struct BarsB {
 };
 
 struct Grads {
+  const __nv_bfloat16* q;  // head layout, read row by row into TMEM
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const __nv_bfloat16* dO;
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  const float4* stats;  // [P][hq][B*S] {LSE*log2e, D, 0, 0}
-  int n_tiles;          // 128-token tiles per rank
+  const float* stats;  // planar [P*hq][2][bsp]
+  int bsp;
+  int n_tiles;  // 128-token tiles per rank
 };
 
-// K-major operand (rows x D, 128-byte swizzle) of `rows_bytes` per 64-column
-// atom, MMA step kk over D.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int atom_bytes, int kk) {
-  return sdesc_sw128(base + (kk >> 2) * atom_bytes + (kk & 3) * 32, 16, 1024);
-}
-// MN-major operand (rows = K dimension, 128-byte rows of D), MMA step kk over rows.
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int atom_bytes, int kk) {
-  return sdesc_sw128(base + kk * 16 * 128, atom_bytes, 1024);
-}
-
 // --------------------------------------------------------------- dK / dV
-// CTA = (rank, kv head, 128 keys).  Iteration i covers 64 query rows of one
-// query head of the group; buffer b = i & 1 holds S^T_i (TMEM cols 64b..) and
-// dP^T_i (128 + 64b..); compute group g = b handles it.  dV at 256, dK at 256+D.
+// TMEM: S^T [0,64)  dP^T [64,128)  dV [128,128+D)  dK [128+D,128+2D)
+//       K [128+2D, 128+2D+D/2)  V [128+2D+D/2, 128+3D)        (D=128: 512 columns)
+// Compute warps w: TMEM lanes 32*(w%4).. = key rows; group g = w/4 takes query
+// columns [32g, 32g+32) of every slice and writes its 16 packed columns of
+// P^T / dS^T at column offset 32g (columns it has read itself).
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+    dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                 const __grid_constant__ CUtensorMap tst, AttnArgs p, Grads g) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   BarsA* bars = reinterpret_cast<BarsA*>(smem + C::A_BAR);
-  const float4* stat = reinterpret_cast<const float4*>(smem + C::A_STAT);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // key tiles in order (early keys of a causal document see the most queries)
@@ -236,21 +270,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n_docs == 0) return;
   int qlo, qhi;
   query_range(p, n_docs, u0, min(u0 + kBN, p.BS) - 1, qlo, qhi);
+  qlo &= ~3;  // statistics slices are fetched by TMA from 16-byte aligned tokens
   const int n_q = (qhi - qlo + kSL - 1) / kSL;
   const int n_it = p.G * n_q;
 
   if (tid == 0) {
-    mbar_init(&bars->kv_full, 1);
-    for (int s = 0; s < C::QST; ++s) {
+    mbar_init(&bars->kv_ready, 8);
+    for (int s = 0; s < C::NST; ++s) {
       mbar_init(&bars->qdo_full[s], 1);
       mbar_init(&bars->qdo_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->st_full[b], 1);
-      mbar_init(&bars->dpt_full[b], 1);
-      mbar_init(&bars->p_full[b], 4);
-      mbar_init(&bars->ds_full[b], 4);
-    }
+    mbar_init(&bars->st_full, 1);
+    mbar_init(&bars->dpt_full, 1);
+    mbar_init(&bars->p_full, 8);
+    mbar_init(&bars->ds_full, 8);
     mbar_init(&bars->fin, 1);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
@@ -266,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem;
   volatile int* abort = &bars->abort;
   const uint32_t sbase = smem_u32(smem);
-  constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
+  constexpr uint32_t T_S = 0, T_DP = 64, T_DV = 128, T_DK = 128 + D, T_K = 128 + 2 * D, T_V = T_K + D / 2;
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
@@ -274,15 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tq);
       prefetch_tmap(&tdo);
       prefetch_tmap(&tst);
-      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::TILE);
-      for (int c = 0; c < C::NCH; ++c) {
-        tma_load_4d(smem + C::A_K + c * kAtomBytes, &tk, &bars->kv_full, c * 64, kh, u0, r);
-        tma_load_4d(smem + C::A_V + c * kAtomBytes, &tv, &bars->kv_full, c * 64, kh, u0, r);
-      }
       int issued = 0;
       for (int i = 0; i < n_it; ++i) {
-        const int s = i % C::QST;
-        if (i >= C::QST && !mbar_wait(&bars->qdo_empty[s], ((i / C::QST) - 1) & 1, abort, p.status)) break;
+        const int s = i % C::NST;
+        if (i >= C::NST && !mbar_wait(&bars->qdo_empty[s], ((i / C::NST) - 1) & 1, abort, p.status)) break;
         const int jq = kh * p.G + i / n_q;
         const int q0 = qlo + (i % n_q) * kSL;
         mbar_arrive_expect_tx(&bars->qdo_full[s], 2 * C::SLICE + C::STAT);
@@ -290,106 +318,131 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(smem + C::A_Q + s * C::SLICE + c * kSliceBytes, &tq, &bars->qdo_full[s], c * 64, jq, q0, r);
           tma_load_4d(smem + C::A_DO + s * C::SLICE + c * kSliceBytes, &tdo, &bars->qdo_full[s], c * 64, jq, q0, r);
         }
-        tma_load_3d(smem + C::A_STAT + s * C::STAT, &tst, &bars->qdo_full[s], 0, q0, r * p.hq + jq);
+        tma_load_3d(smem + C::A_STAT + s * C::STAT, &tst, &bars->qdo_full[s], q0, 0, r * p.hq + jq);
         issued = i + 1;
       }
-      mbar_wait(&bars->kv_full, 0, abort, p.status);
-      for (int i = max(0, issued - C::QST); i < issued; ++i)
-        mbar_wait(&bars->qdo_full[i % C::QST], (i / C::QST) & 1, abort, p.status);
+      for (int i = max(0, issued - C::NST); i < issued; ++i)
+        mbar_wait(&bars->qdo_full[i % C::NST], (i / C::NST) & 1, abort, p.status);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(kBN, kSL, false, false);  // [128 keys x 64 queries], K = D
       constexpr uint32_t id_g = idesc_bf16(kBN, D, false, true);      // [128 keys x D], K = 64 queries
-      // S^T_i = K Q_i^T and dP^T_i = V dO_i^T into buffer i&1
-      auto issue_front = [&](int i) -> bool {
-        const int s = i % C::QST, b = i & 1;
-        if (!mbar_wait(&bars->qdo_full[s], (i / C::QST) & 1, abort, p.status)) return false;
+      auto issue_st = [&](int i) -> bool {  // S^T_i = K Q_i^T
+        const int s = i % C::NST;
+        if (!mbar_wait(&bars->qdo_full[s], (i / C::NST) & 1, abort, p.status)) return false;
         tc_fence_after();
-        const uint32_t qa = sbase + C::A_Q + s * C::SLICE, da = sbase + C::A_DO + s * C::SLICE;
+        const uint32_t qa = sbase + C::A_Q + s * C::SLICE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + T_S + b * kSL, kmajor_desc(sbase + C::A_K, kAtomBytes, kk), kmajor_desc(qa, kSliceBytes, kk),
-                 id_s, kk > 0);
-        mma_commit(&bars->st_full[b]);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + T_DP + b * kSL, kmajor_desc(sbase + C::A_V, kAtomBytes, kk), kmajor_desc(da, kSliceBytes, kk),
-                 id_s, kk > 0);
-        mma_commit(&bars->dpt_full[b]);
+          mma_ts(tmem + T_S, tmem + T_K + kk * 8, kmajor_desc(qa, kSliceBytes, kk), id_s, kk > 0);
+        mma_commit(&bars->st_full);
         return true;
       };
-      bool ok = mbar_wait(&bars->kv_full, 0, abort, p.status);
-      for (int i = 0; i < 2 && i < n_it && ok; ++i) ok = issue_front(i);
+      auto issue_dpt = [&](int i) {  // dP^T_i = V dO_i^T (its slice has landed: issue_st waited)
+        const uint32_t da = sbase + C::A_DO + (i % C::NST) * C::SLICE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ts(tmem + T_DP, tmem + T_V + kk * 8, kmajor_desc(da, kSliceBytes, kk), id_s, kk > 0);
+        mma_commit(&bars->dpt_full);
+      };
+      // A operand columns of a packed 64-query slice: the two halves sit at +0 and +32
+      auto acol = [](int kk) -> uint32_t { return kk < 2 ? kk * 8 : 32 + (kk - 2) * 8; };
+      bool ok = mbar_wait(&bars->kv_ready, 0, abort, p.status);
+      if (ok && n_it > 0) {
+        ok = issue_st(0);
+        if (ok) issue_dpt(0);
+      }
       for (int i = 0; i < n_it && ok; ++i) {
-        const int s = i % C::QST, b = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        // dV += P^T_i dO_i  (A: packed bf16 P^T in TMEM cols 64b..64b+32)
-        if (!(ok = mbar_wait(&bars->p_full[b], ph, abort, p.status))) break;
-        tc_fence_after();
+        const int s = i % C::NST;
+        const uint32_t ph = i & 1;
         const uint32_t da = sbase + C::A_DO + s * C::SLICE, qa = sbase + C::A_Q + s * C::SLICE;
-#pragma unroll
-        for (int kk = 0; kk < kSL / 16; ++kk)
-          mma_ts(tmem + T_DV, tmem + T_S + b * kSL + kk * 8, mnmajor_desc(da, kSliceBytes, kk), id_g,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T_i Q_i
-        if (!(ok = mbar_wait(&bars->ds_full[b], ph, abort, p.status))) break;
+        // dV += P^T_i dO_i
+        if (!(ok = mbar_wait(&bars->p_full, ph, abort, p.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kSL / 16; ++kk)
-          mma_ts(tmem + T_DK, tmem + T_DP + b * kSL + kk * 8, mnmajor_desc(qa, kSliceBytes, kk), id_g,
+          mma_ts(tmem + T_DV, tmem + T_S + acol(kk), mnmajor_desc(da, kSliceBytes, kk), id_g,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        const bool more = i + 1 < n_it;
+        if (more && !(ok = issue_st(i + 1))) break;  // S^T region is free once dV has read P^T
+        // dK += dS^T_i Q_i
+        if (!(ok = mbar_wait(&bars->ds_full, ph, abort, p.status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kSL / 16; ++kk)
+          mma_ts(tmem + T_DK, tmem + T_DP + acol(kk), mnmajor_desc(qa, kSliceBytes, kk), id_g,
                  (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->qdo_empty[s]);
-        if (i + 2 < n_it)
-          ok = issue_front(i + 2);
-        if (i == n_it - 1) mma_commit(&bars->fin);
+        if (more)
+          issue_dpt(i + 1);
+        else
+          mma_commit(&bars->fin);
       }
       mma_commit(&bars->mma_done);
       mbar_wait(&bars->mma_done, 0, abort, p.status);
     }
   } else {
     // ------------------------------------------------------------ compute
-    const int grp = warp >> 2;                      // handles iterations i with i & 1 == grp
+    const int grp = warp >> 2;                      // query columns [32*grp, 32*grp + 32) of each slice
     const int krow = (warp & 3) * 32 + lane;        // TMEM lane = key row
     const int u = u0 + krow;
     const bool key_ok = u < p.BS;
     int a = 0, b = 0;
     if (key_ok) doc_bounds(p.cu, n_docs, p.BS, u, a, b);
     const uint32_t lb = tmem + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
-    const uint32_t s_col = T_S + grp * kSL, dp_col = T_DP + grp * kSL;
+    // K (group 0) or V (group 1) row of this key into TMEM
+    {
+      const size_t row = (static_cast<size_t>(r) * p.BS + (key_ok ? u : 0)) * p.hk + kh;
+      row_to_tmem<D>(lb + (grp == 0 ? T_K : T_V), (grp == 0 ? g.k : g.v) + row * D, key_ok);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->kv_ready);
+    }
     bool ok = true;
-    for (int i = grp; i < n_it && ok; i += 2) {
-      const int s = i % C::QST;
-      const uint32_t ph = (i >> 1) & 1;
-      const int q0 = qlo + (i % n_q) * kSL;  // first query of the slice
-      if (!(ok = mbar_wait(&bars->qdo_full[s], (i / C::QST) & 1, abort, p.status))) break;
-      const float4* st4 = stat + s * kSL;
-      if (!(ok = mbar_wait(&bars->st_full[grp], ph, abort, p.status))) break;
+    for (int i = 0; i < n_it && ok; ++i) {
+      const int s = i % C::NST;
+      const uint32_t ph = i & 1;
+      const int q0 = qlo + (i % n_q) * kSL + grp * 32;  // first query column of this group
+      if (!(ok = mbar_wait(&bars->qdo_full[s], (i / C::NST) & 1, abort, p.status))) break;
+      const float* st = reinterpret_cast<const float*>(smem + C::A_STAT + s * C::STAT) + grp * 32;
+      if (!(ok = mbar_wait(&bars->st_full, ph, abort, p.status))) break;
       tc_fence_after();
-      float x[64];
-      ld64(lb + s_col, x);
-      bool full = key_ok && q0 >= a && q0 + kSL <= b && (!p.causal || q0 >= u);
-      if (p.window_left >= 0) full = full && (q0 + kSL - 1 - u <= p.window_left) && (p.causal || u - q0 <= p.window_left);
-      float pr[64];
+      float x[32];
+      tmem_ld_cols<32>(lb + T_S + grp * 32, x);
+      bool full = key_ok && q0 >= a && q0 + 32 <= b && (!p.causal || q0 >= u);
+      if (p.window_left >= 0) full = full && (q0 + 31 - u <= p.window_left) && (p.causal || u - q0 <= p.window_left);
+      float pr[32];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const bool vis = full || (key_ok && visible_from_key(q0 + c, u, a, b, p.causal, p.window_left));
-        pr[c] = vis ? ex2(fmaf(x[c], p.scale_log2, -st4[c].x)) : 0.f;
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(st + 4 * c4);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 4 * c4 + e;
+          const bool vis = full || (key_ok && visible_from_key(q0 + c, u, a, b, p.causal, p.window_left));
+          pr[c] = vis ? ex2(fmaf(x[c], p.scale_log2, -lv[e])) : 0.f;
+        }
       }
-      st_packed64(lb + s_col, pr);
+      tmem_st_packed<16>(lb + T_S + grp * 32, pr);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[grp]);
-      if (!(ok = mbar_wait(&bars->dpt_full[grp], ph, abort, p.status))) break;
+      if (lane == 0) mbar_arrive(&bars->p_full);
+      if (!(ok = mbar_wait(&bars->dpt_full, ph, abort, p.status))) break;
       tc_fence_after();
-      ld64(lb + dp_col, x);
+      tmem_ld_cols<32>(lb + T_DP + grp * 32, x);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) x[c] = pr[c] * (x[c] - st4[c].y);
-      st_packed64(lb + dp_col, x);
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 d4 = *reinterpret_cast<const float4*>(st + kSL + 4 * c4);
+        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[4 * c4 + e] = pr[4 * c4 + e] * (x[4 * c4 + e] - dv[e]);
+      }
+      tmem_st_packed<16>(lb + T_DP + grp * 32, x);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->ds_full[grp]);
+      if (lane == 0) mbar_arrive(&bars->ds_full);
     }
     if (ok && n_it > 0 && (ok = mbar_wait(&bars->fin, 0, abort, p.status))) {
       tc_fence_after();
@@ -414,13 +467,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // --------------------------------------------------------------- dQ
-// CTA = (rank, query head, 128 rows).  Iteration n covers 64 keys; buffer
-// b = n & 1 holds S_n (TMEM cols 64b..) and dP_n (128 + 64b..); compute group
-// g = b handles it.  dQ accumulates at 256.
+// TMEM: S_b [64b, 64b+64)  dP_b [128+64b, ...)  (b = 0, 1)  dQ [256, 256+D)
+//       Q [256+D, 256+D+D/2)  dO [256+D+D/2, 256+2D)          (D=128: 512 columns)
+// Iteration n covers 64 keys in buffer b = n & 1, handled by compute group b.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, AttnArgs p, Grads g) {
+    dq_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, AttnArgs p, Grads g) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -441,8 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_kv = (hi - lo + kSL - 1) / kSL;
 
   if (tid == 0) {
-    mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < C::KST; ++s) {
+    mbar_init(&bars->qd_ready, 8);
+    for (int s = 0; s < C::NST; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
@@ -467,21 +519,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem;
   volatile int* abort = &bars->abort;
   const uint32_t sbase = smem_u32(smem);
-  constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256;
+  constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256, T_Q = 256 + D, T_DO = T_Q + D / 2;
 
   if (warp == 8) {
     if (lane == 0) {
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
-      mbar_arrive_expect_tx(&bars->q_full, 2 * C::TILE);
-      for (int c = 0; c < C::NCH; ++c) {
-        tma_load_4d(smem + C::B_Q + c * kAtomBytes, &tq, &bars->q_full, c * 64, j, t0, r);
-        tma_load_4d(smem + C::B_DO + c * kAtomBytes, &tdo, &bars->q_full, c * 64, j, t0, r);
-      }
       int issued = 0;
       for (int n = 0; n < n_kv; ++n) {
-        const int s = n % C::KST;
-        if (n >= C::KST && !mbar_wait(&bars->kv_empty[s], ((n / C::KST) - 1) & 1, abort, p.status)) break;
+        const int s = n % C::NST;
+        if (n >= C::NST && !mbar_wait(&bars->kv_empty[s], ((n / C::NST) - 1) & 1, abort, p.status)) break;
         const int kv0 = lo + n * kSL;
         mbar_arrive_expect_tx(&bars->k_full[s], C::SLICE);
         for (int c = 0; c < C::NCH; ++c)
@@ -491,10 +538,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(smem + C::B_V + s * C::SLICE + c * kSliceBytes, &tv, &bars->v_full[s], c * 64, kvh, kv0, r);
         issued = n + 1;
       }
-      mbar_wait(&bars->q_full, 0, abort, p.status);
-      for (int n = max(0, issued - C::KST); n < issued; ++n) {
-        mbar_wait(&bars->k_full[n % C::KST], (n / C::KST) & 1, abort, p.status);
-        mbar_wait(&bars->v_full[n % C::KST], (n / C::KST) & 1, abort, p.status);
+      for (int n = max(0, issued - C::NST); n < issued; ++n) {
+        mbar_wait(&bars->k_full[n % C::NST], (n / C::NST) & 1, abort, p.status);
+        mbar_wait(&bars->v_full[n % C::NST], (n / C::NST) & 1, abort, p.status);
       }
     }
   } else if (warp == 9) {
@@ -502,29 +548,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_s = idesc_bf16(kBM, kSL, false, false);  // [128 rows x 64 keys], K = D
       constexpr uint32_t id_q = idesc_bf16(kBM, D, false, true);      // [128 rows x D], K = 64 keys
       auto issue_front = [&](int n) -> bool {
-        const int s = n % C::KST, b = n & 1;
-        const uint32_t ph = (n / C::KST) & 1;
+        const int s = n % C::NST, b = n & 1;
+        const uint32_t ph = (n / C::NST) & 1;
         if (!mbar_wait(&bars->k_full[s], ph, abort, p.status)) return false;
         tc_fence_after();
         const uint32_t ka = sbase + C::B_K + s * C::SLICE, va = sbase + C::B_V + s * C::SLICE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + T_S + b * kSL, kmajor_desc(sbase + C::B_Q, kAtomBytes, kk), kmajor_desc(ka, kSliceBytes, kk),
-                 id_s, kk > 0);
+          mma_ts(tmem + T_S + b * kSL, tmem + T_Q + kk * 8, kmajor_desc(ka, kSliceBytes, kk), id_s, kk > 0);
         mma_commit(&bars->s_full[b]);
         if (!mbar_wait(&bars->v_full[s], ph, abort, p.status)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + T_DP + b * kSL, kmajor_desc(sbase + C::B_DO, kAtomBytes, kk), kmajor_desc(va, kSliceBytes, kk),
-                 id_s, kk > 0);
+          mma_ts(tmem + T_DP + b * kSL, tmem + T_DO + kk * 8, kmajor_desc(va, kSliceBytes, kk), id_s, kk > 0);
         mma_commit(&bars->dp_full[b]);
         return true;
       };
-      bool ok = mbar_wait(&bars->q_full, 0, abort, p.status);
+      bool ok = mbar_wait(&bars->qd_ready, 0, abort, p.status);
       for (int n = 0; n < 2 && n < n_kv && ok; ++n) ok = issue_front(n);
       for (int n = 0; n < n_kv && ok; ++n) {
-        const int s = n % C::KST, b = n & 1;
+        const int s = n % C::NST, b = n & 1;
         if (!(ok = mbar_wait(&bars->ds_full[b], (n >> 1) & 1, abort, p.status))) break;
         tc_fence_after();
         const uint32_t ka = sbase + C::B_K + s * C::SLICE;
@@ -544,15 +588,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = (warp & 3) * 32 + lane;
     const int t = t0 + row;
     const bool row_ok = t < p.BS;
+    const uint32_t lb = tmem + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
+    // Q (group 0) or dO (group 1) row into TMEM
+    {
+      const size_t rrow = (static_cast<size_t>(r) * p.BS + (row_ok ? t : 0)) * p.hq + j;
+      row_to_tmem<D>(lb + (grp == 0 ? T_Q : T_DO), (grp == 0 ? g.q : g.dO) + rrow * D, row_ok);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->qd_ready);
+    }
     int a = 0, b = 0;
     float lse2 = INFINITY, dvt = 0.f;
     if (row_ok) {
       doc_bounds(p.cu, n_docs, p.BS, t, a, b);
-      const float4 st = __ldg(g.stats + (static_cast<size_t>(r) * p.hq + j) * p.BS + t);
-      lse2 = st.x;
-      dvt = st.y;
+      lse2 = __ldg(g.stats + plane_index(g.bsp, p.hq, r, j, 0, t));
+      dvt = __ldg(g.stats + plane_index(g.bsp, p.hq, r, j, 1, t));
     }
-    const uint32_t lb = tmem + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
     const uint32_t s_col = T_S + grp * kSL, dp_col = T_DP + grp * kSL;
     bool ok = true;
     for (int n = grp; n < n_kv && ok; n += 2) {
@@ -561,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait(&bars->s_full[grp], ph, abort, p.status))) break;
       tc_fence_after();
       float x[64];
-      ld64(lb + s_col, x);
+      tmem_ld_cols<64>(lb + s_col, x);
       bool full = row_ok && k0 >= a && k0 + kSL <= b && (!p.causal || k0 + kSL - 1 <= t);
       if (p.window_left >= 0) full = full && (t - k0 <= p.window_left) && (p.causal || k0 + kSL - 1 - t <= p.window_left);
       float pr[64];
@@ -572,10 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!(ok = mbar_wait(&bars->dp_full[grp], ph, abort, p.status))) break;
       tc_fence_after();
-      ld64(lb + dp_col, x);
+      tmem_ld_cols<64>(lb + dp_col, x);
 #pragma unroll
       for (int c = 0; c < 64; ++c) x[c] = pr[c] * (x[c] - dvt);
-      st_packed64(lb + s_col, x);
+      tmem_st_packed<32>(lb + s_col, x);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->ds_full[grp]);
@@ -597,9 +648,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace bwd
 
+static int stats_row_pitch(int BS) { return (BS + 3) & ~3; }
+
 size_t attn_bwd_ws_bytes(const usp_attn_params& p) {
-  size_t rows = static_cast<size_t>(p.B) * p.S * p.Hq;  // one {LSE*log2e, D, 0, 0} record per row and head
-  return (rows * 16 + 255) / 256 * 256;
+  // planar {LSE*log2e, D} per (rank, query head), rows padded to 4 tokens
+  size_t n = static_cast<size_t>(p.Hq) * 2 * stats_row_pitch(p.B * p.S);
+  return (n * sizeof(float) + 255) / 256 * 256;
 }
 
 static AttnArgs make_args(const usp_attn_params& prm, int32_t* status) {
@@ -622,24 +676,25 @@ static AttnArgs make_args(const usp_attn_params& prm, int32_t* status) {
   return a;
 }
 
-// 1. D = rowsum(dO * O) into the workspace, then the sink gradients.
+// 1. D = rowsum(dO * O) and LSE*log2e into the workspace, then the sink gradients.
 int launch_attn_bwd_preprocess(const usp_attn_params& prm, const void* o, const float* lse, const void* dO,
                                float* dsinks, void* ws, int32_t* status, cudaStream_t st) {
   const AttnArgs a = make_args(prm, status);
-  float4* stats = static_cast<float4*>(ws);
+  float* stats = static_cast<float*>(ws);
+  const int bsp = stats_row_pitch(a.BS);
   const uint32_t n_rows = static_cast<uint32_t>(static_cast<uint64_t>(a.P) * a.BS * a.hq);
   const int per_block = 256 / (prm.D / 8);
   int grid = static_cast<int>((n_rows + per_block - 1) / per_block);
   grid = grid < device_sm_count() * 8 ? grid : device_sm_count() * 8;
   if (prm.D == 128)
     bwd::preprocess_kernel<128><<<grid, 256, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dO),
-                                                      lse, stats, a, n_rows);
+                                                      lse, stats, a, bsp, n_rows);
   else
     bwd::preprocess_kernel<64><<<grid, 256, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dO),
-                                                     lse, stats, a, n_rows);
+                                                     lse, stats, a, bsp, n_rows);
   if (check_launch() != USP_OK) return USP_ERR_CUDA;
   if (dsinks != nullptr && a.sinks != nullptr) {
-    bwd::dsink_kernel<<<a.P * a.hq, 256, 0, st>>>(stats, dsinks, a);
+    bwd::dsink_kernel<<<a.P * a.hq, 256, 0, st>>>(stats, dsinks, a, bsp);
     if (check_launch() != USP_OK) return USP_ERR_CUDA;
   }
   return USP_OK;
@@ -647,31 +702,32 @@ int launch_attn_bwd_preprocess(const usp_attn_params& prm, const void* o, const 
 
 template <int D>
 static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const void* k, const void* v,
-                         const void* dO, void* dq, void* dk, void* dv, const float4* stats, cudaStream_t st) {
+                         const void* dO, void* dq, void* dk, void* dv, const float* stats, cudaStream_t st) {
   using C = bwd::Cfg<D>;
-  CUtensorMap tq, tk, tv, tdo, tst;
+  bwd::Grads g{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+               static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(dO),
+               static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
+               stats, stats_row_pitch(a.BS), (a.BS + kBM - 1) / kBM};
   int rc;
-  // dK/dV streams 64-row Q/dO/stats slices past 128-key K/V tiles; dQ streams
-  // 64-key K/V slices past 128-row Q/dO tiles.
-  const int q_rows = dq_pass ? kBM : bwd::kSL, kv_rows = dq_pass ? bwd::kSL : kBN;
-  if ((rc = make_stats_tmap(&tst, stats, a.BS, a.P * a.hq, bwd::kSL)) != USP_OK) return rc;
-  if ((rc = make_head_tmap(&tq, q, a.P, a.BS, a.hq, D, q_rows)) != USP_OK) return rc;
-  if ((rc = make_head_tmap(&tdo, dO, a.P, a.BS, a.hq, D, q_rows)) != USP_OK) return rc;
-  if ((rc = make_head_tmap(&tk, k, a.P, a.BS, a.hk, D, kv_rows)) != USP_OK) return rc;
-  if ((rc = make_head_tmap(&tv, v, a.P, a.BS, a.hk, D, kv_rows)) != USP_OK) return rc;
-  bwd::Grads g{static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), stats,
-               (a.BS + kBM - 1) / kBM};
   if (!dq_pass) {
+    // 64-query slices of Q, dO and their statistics stream past TMEM-resident K, V
+    CUtensorMap tq, tdo, tst;
+    if ((rc = make_head_tmap(&tq, q, a.P, a.BS, a.hq, D, bwd::kSL)) != USP_OK) return rc;
+    if ((rc = make_head_tmap(&tdo, dO, a.P, a.BS, a.hq, D, bwd::kSL)) != USP_OK) return rc;
+    if ((rc = make_stats_tmap(&tst, stats, a.BS, g.bsp, a.P * a.hq, bwd::kSL)) != USP_OK) return rc;
     if (cudaFuncSetAttribute(bwd::dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::A_SMEM) !=
         cudaSuccess)
       return USP_ERR_CUDA;
-    bwd::dkdv_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hk, bwd::kThreads, C::A_SMEM, st>>>(
-        tq, tk, tv, tdo, tst, a, g);
+    bwd::dkdv_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hk, bwd::kThreads, C::A_SMEM, st>>>(tq, tdo, tst,
+                                                                                                       a, g);
   } else {
+    // 64-key slices of K and V stream past TMEM-resident Q, dO
+    CUtensorMap tk, tv;
+    if ((rc = make_head_tmap(&tk, k, a.P, a.BS, a.hk, D, bwd::kSL)) != USP_OK) return rc;
+    if ((rc = make_head_tmap(&tv, v, a.P, a.BS, a.hk, D, bwd::kSL)) != USP_OK) return rc;
     if (cudaFuncSetAttribute(bwd::dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::B_SMEM) != cudaSuccess)
       return USP_ERR_CUDA;
-    bwd::dq_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hq, bwd::kThreads, C::B_SMEM, st>>>(tq, tk, tv,
-                                                                                                       tdo, a, g);
+    bwd::dq_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hq, bwd::kThreads, C::B_SMEM, st>>>(tk, tv, a, g);
   }
   return check_launch();
 }
@@ -680,8 +736,8 @@ static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const v
 int launch_attn_bwd_dkdv(const usp_attn_params& prm, const void* q, const void* k, const void* v, const float* lse,
                          const void* dO, void* dk, void* dv, const void* ws, int32_t* status, cudaStream_t st) {
   const AttnArgs a = make_args(prm, status);
-  const float4* stats = static_cast<const float4*>(ws);
-  (void)lse;  // read through the preprocess's records
+  const float* stats = static_cast<const float*>(ws);
+  (void)lse;  // read through the preprocess's statistics
   if (prm.D == 128) return run_grad_pass<128>(false, a, q, k, v, dO, nullptr, dk, dv, stats, st);
   return run_grad_pass<64>(false, a, q, k, v, dO, nullptr, dk, dv, stats, st);
 }
@@ -690,7 +746,7 @@ int launch_attn_bwd_dkdv(const usp_attn_params& prm, const void* q, const void* 
 int launch_attn_bwd_dq(const usp_attn_params& prm, const void* q, const void* k, const void* v, const float* lse,
                        const void* dO, void* dq, const void* ws, int32_t* status, cudaStream_t st) {
   const AttnArgs a = make_args(prm, status);
-  const float4* stats = static_cast<const float4*>(ws);
+  const float* stats = static_cast<const float*>(ws);
   (void)lse;
   if (prm.D == 128) return run_grad_pass<128>(true, a, q, k, v, dO, dq, nullptr, nullptr, stats, st);
   return run_grad_pass<64>(true, a, q, k, v, dO, dq, nullptr, nullptr, stats, st);

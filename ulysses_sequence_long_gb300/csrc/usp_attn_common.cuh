@@ -121,8 +121,9 @@ namespace usp {
 // box {64, 1, rows, 1}, 128-byte swizzle (one 128-byte row per token).
 int make_head_tmap(CUtensorMap* m, const void* base, int P, int BS, int H, int D, int box_rows);
 
-// Tensor map of the backward's per-row records, fp32 [P*hq][BS][4]: dims
-// {4, BS, P*hq}, box {4, box_rows, 1} (box_rows tokens of one head).
-int make_stats_tmap(CUtensorMap* m, const void* base, int BS, int rows, int box_rows);
+// Tensor map of the backward's planar statistics, fp32 [P*hq][2][pitch]: dims
+// {BS, 2, P*hq}, box {box_rows, 2, 1} (box_rows tokens of both planes of one
+// head); the token coordinate of a load must be a multiple of 4.
+int make_stats_tmap(CUtensorMap* m, const void* base, int BS, int pitch, int rows, int box_rows);
 
 }  // namespace usp
