@@ -183,13 +183,13 @@ __device__ __forceinline__ void store_row(uint32_t taddr, __nv_bfloat16* dst, fl
 }
 
 // K-major B operand (rows x D, 128-byte swizzle, `atom_bytes` per 64-column
-// atom), MMA step kk over D.
+// atom), MMA step kk over D: one descriptor per tile, moved per step.
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int atom_bytes, int kk) {
-  return sdesc_sw128(base + (kk >> 2) * atom_bytes + (kk & 3) * 32, 16, 1024);
+  return sdesc_add(sdesc_sw128(base, 16, 1024), (kk >> 2) * atom_bytes + (kk & 3) * 32);
 }
 // MN-major B operand (rows = the MMA's K dimension, 128-byte rows of D), step kk over rows.
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int atom_bytes, int kk) {
-  return sdesc_sw128(base + kk * 16 * 128, atom_bytes, 1024);
+  return sdesc_add(sdesc_sw128(base, atom_bytes, 1024), kk * 16 * 128);
 }
 
 template <int D>
@@ -413,17 +413,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_cols<32>(lb + T_S + grp * 32, x);
       bool full = key_ok && q0 >= a && q0 + 32 <= b && (!p.causal || q0 >= u);
       if (p.window_left >= 0) full = full && (q0 + 31 - u <= p.window_left) && (p.causal || u - q0 <= p.window_left);
+      // only slices that straddle a document, diagonal or window edge pay for
+      // the per-element mask (hidden scores become -inf, so exp2 gives 0)
+      if (!full) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (!(key_ok && visible_from_key(q0 + c, u, a, b, p.causal, p.window_left))) x[c] = -INFINITY;
+      }
       float pr[32];
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
         const float4 l4 = *reinterpret_cast<const float4*>(st + 4 * c4);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = 4 * c4 + e;
-          const bool vis = full || (key_ok && visible_from_key(q0 + c, u, a, b, p.causal, p.window_left));
-          pr[c] = vis ? ex2(fmaf(x[c], p.scale_log2, -lv[e])) : 0.f;
-        }
+        pr[4 * c4] = ex2(fmaf(x[4 * c4], p.scale_log2, -l4.x));
+        pr[4 * c4 + 1] = ex2(fmaf(x[4 * c4 + 1], p.scale_log2, -l4.y));
+        pr[4 * c4 + 2] = ex2(fmaf(x[4 * c4 + 2], p.scale_log2, -l4.z));
+        pr[4 * c4 + 3] = ex2(fmaf(x[4 * c4 + 3], p.scale_log2, -l4.w));
       }
       tmem_st_packed<16>(lb + T_S + grp * 32, pr);
       tc_fence_before();
@@ -615,12 +619,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_cols<64>(lb + s_col, x);
       bool full = row_ok && k0 >= a && k0 + kSL <= b && (!p.causal || k0 + kSL - 1 <= t);
       if (p.window_left >= 0) full = full && (t - k0 <= p.window_left) && (p.causal || k0 + kSL - 1 - t <= p.window_left);
+      if (!full) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (!(row_ok && visible(t, k0 + c, a, b, p.causal, p.window_left))) x[c] = -INFINITY;
+      }
       float pr[64];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const bool vis = full || (row_ok && visible(t, k0 + c, a, b, p.causal, p.window_left));
-        pr[c] = vis ? ex2(fmaf(x[c], p.scale_log2, -lse2)) : 0.f;
-      }
+      for (int c = 0; c < 64; ++c) pr[c] = ex2(fmaf(x[c], p.scale_log2, -lse2));
       if (!(ok = mbar_wait(&bars->dp_full[grp], ph, abort, p.status))) break;
       tc_fence_after();
       tmem_ld_cols<64>(lb + dp_col, x);

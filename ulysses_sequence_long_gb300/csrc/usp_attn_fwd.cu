@@ -174,22 +174,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int q = 0; q < 2 && ok; ++q)
         if (tile_ok[q]) ok = mbar_wait(&bars->q_full[q], 0, abort, p.status);
+      // descriptors are built once per tile and moved by a constant per MMA step
       auto issue_s = [&](int q, int st) {
-        const uint32_t qa = sbase + C::OFF_Q + q * C::TILE;
-        const uint32_t ka = sbase + C::OFF_K + st * C::TILE;
+        const uint64_t qd = sdesc_sw128(sbase + C::OFF_Q + q * C::TILE, 16, 1024);
+        const uint64_t kd = sdesc_sw128(sbase + C::OFF_K + st * C::TILE, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kAtomBytes + (kk & 3) * 32;
-          mma_ss(tmem + q * kBN, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_s,
-                 kk > 0);
+          mma_ss(tmem + q * kBN, sdesc_add(qd, off), sdesc_add(kd, off), idesc_s, kk > 0);
         }
       };
       auto issue_pv = [&](int q, int st, bool acc) {
-        const uint32_t va = sbase + C::OFF_V + st * C::TILE;
+        const uint64_t vd = sdesc_sw128(sbase + C::OFF_V + st * C::TILE, kAtomBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + 256 + q * D, tmem + q * kBN + kk * 8, sdesc_sw128(va + kk * 16 * 128, kAtomBytes, 1024),
-                 idesc_o, (acc || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + 256 + q * D, tmem + q * kBN + kk * 8, sdesc_add(vd, kk * 16 * 128), idesc_o,
+                 (acc || kk > 0) ? 1u : 0u);
       };
       if (ok) ok = mbar_wait(&bars->k_full[0], 0, abort, p.status);
       if (ok) {
@@ -278,37 +278,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_tile = mx * p.scale_log2;  // -inf stays -inf
       const float m_new = fmaxf(m, m_tile);
       const bool need = m_new > m + 8.f;
-      if (__any_sync(0xffffffffu, need)) {
-        const float alpha = need ? ex2(m - m_new) : 1.f;
-        if (need) {
-          l *= alpha;
-          m = m_new;
-        }
-        if (n > 0) {
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(o_tm + c * 32, ov);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32(o_tm + c * 32, ov);
-          }
-        }
+      const bool rescale = __any_sync(0xffffffffu, need);
+      const float alpha = need ? ex2(m - m_new) : 1.f;
+      if (need) {
+        l *= alpha;
+        m = m_new;
       }
       const float m_use = (m == -INFINITY) ? 0.f : m;
       float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
-      uint32_t pk[2][32];
 #pragma unroll
-      for (int c = 0; c < kBN / 2; ++c) {
-        const float p0 = ex2(fmaf(s[2 * c], p.scale_log2, -m_use));
-        const float p1 = ex2(fmaf(s[2 * c + 1], p.scale_log2, -m_use));
-        rs8[c & 7] += p0 + p1;
-        pk[c >> 5][c & 31] = pack_bf16x2(p0, p1);
+      for (int h = 0; h < 2; ++h) {  // each 64-column half is packed and stored as soon as it is done
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = ex2(fmaf(s[64 * h + 2 * c], p.scale_log2, -m_use));
+          const float p1 = ex2(fmaf(s[64 * h + 2 * c + 1], p.scale_log2, -m_use));
+          rs8[c & 7] += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(s_tm + 32 * h, pk);
       }
       l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-      tmem_st32(s_tm, pk[0]);
-      tmem_st32(s_tm + 32, pk[1]);
+      // The running max moved for some row of this warp: rescale the O rows.
+      // PV of the previous tile has finished (S of this tile was committed
+      // after it), and PV of this tile waits for this warp's arrival below.
+      if (rescale && n > 0) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(o_tm + c * 32, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st32(o_tm + c * 32, ov);
+        }
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

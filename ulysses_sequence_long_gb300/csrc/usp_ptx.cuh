@@ -67,6 +67,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same test, but a thread whose phase is not complete sleeps (up to the hint,
+// in ns) until the barrier completes instead of returning at once, so waiting
+// warps leave the issue slots to the warps that are working.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed.  Returns false
 // (and records USP_ERR_TIMEOUT) if it did not within USP_WAIT_NS, or if another
 // thread of the CTA already gave up (*abort != 0).
@@ -75,7 +90,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
       if (global_ns() - t0 > USP_WAIT_NS) {
@@ -127,6 +142,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   d |= static_cast<uint64_t>(2) << 61;  // SWIZZLE_128B
   return d;
 }
+
+// A descriptor moved by `bytes` (a multiple of 16): the start-address field is
+// the low 14 bits and shared-memory addresses stay far below 2^18, so a plain
+// add never carries out of it.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
