@@ -19,10 +19,9 @@
 //               stream through shared memory; P^T and dS^T (bf16) are written
 //               over S^T / dP^T and feed dV += P^T dO, dK += dS^T Q.
 //   dQ          CTA = (rank, query head, 128 rows).  Q and dO live in TMEM as
-//               the A operands of S = Q K^T and dP = dO V^T; 64-key slices of
-//               K and V stream through shared memory; S/dP are double-buffered
-//               so one compute group works while the tensor core fills the
-//               other buffer; dS (bf16 over S) feeds dQ += dS K.
+//               the A operands of S = Q K^T and dP = dO V^T; 128-key tiles of
+//               K and V stream through shared memory; dS (bf16 over S) feeds
+//               dQ += dS K.
 // Every MMA takes its A operand from TMEM and only its B operand from shared
 // memory: that keeps the tensor core's shared-memory reads well under the
 // SM's bandwidth, which smem x smem MMAs at these tile widths exceed.
@@ -44,6 +43,7 @@ namespace bwd {
 constexpr int kThreads = 320;
 constexpr int kSL = 64;                      // slice width (queries in dK/dV, keys in dQ)
 constexpr int kSliceBytes = kSL * 128;       // 64-row, 128-byte-wide swizzle column
+constexpr int kAtomBytes = kBN * 128;        // 128-row, 128-byte-wide swizzle column
 constexpr float kLog2e = 1.4426950408889634f;
 
 // index of (rank r, local head j, rank-local token t) in a [P][B][hq][S] array
@@ -204,10 +204,12 @@ struct Cfg {
   static constexpr int A_STAT = A_DO + NST * SLICE;
   static constexpr int A_BAR = A_STAT + NST * STAT;
   static constexpr int A_SMEM = A_BAR + 1024 + 1024;
-  // dQ: ring of (K, V) 64-key slices
+  // dQ: ring of (K, V) 128-key tiles
+  static constexpr int TILE = NCH * kBN * 128;       // 128-row bf16 tile
+  static constexpr int KST = (D == 128) ? 3 : 6;
   static constexpr int B_K = 0;
-  static constexpr int B_V = B_K + NST * SLICE;
-  static constexpr int B_BAR = B_V + NST * SLICE;
+  static constexpr int B_V = B_K + KST * TILE;
+  static constexpr int B_BAR = B_V + KST * TILE;
   static constexpr int B_SMEM = B_BAR + 1024 + 1024;
 };
 
@@ -224,7 +226,7 @@ struct BarsA {
 struct BarsB {
   uint64_t qd_ready;  // Q, dO rows stored into TMEM by the compute warps
   uint64_t k_full[8], v_full[8], kv_empty[8];
-  uint64_t s_full[2], dp_full[2], ds_full[2];
+  uint64_t s_full, dp_full, ds_full;
   uint64_t fin, mma_done;
   uint32_t tmem;
   int abort;
@@ -471,9 +473,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // --------------------------------------------------------------- dQ
-// TMEM: S_b [64b, 64b+64)  dP_b [128+64b, ...)  (b = 0, 1)  dQ [256, 256+D)
-//       Q [256+D, 256+D+D/2)  dO [256+D+D/2, 256+2D)          (D=128: 512 columns)
-// Iteration n covers 64 keys in buffer b = n & 1, handled by compute group b.
+// TMEM: S [0,128)  dP [128,256)  dQ [256,256+D)  Q [256+D, 256+D+D/2)
+//       dO [256+D+D/2, 256+2D)                                  (D=128: 512 columns)
+// Iteration n covers a 128-key tile.  Compute group g = warp/4 takes key
+// columns [64g, 64g+64) of S and dP and writes its 32 packed bf16 columns of dS
+// at column 64g of S (columns it has read itself).  The MMA thread issues
+// dQ(n), S(n+1), dP(n+1) as soon as dS(n) is complete: S is free once dQ(n)
+// has read dS(n) (in-order), dP once the compute warps have read it.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, AttnArgs p, Grads g) {
@@ -494,20 +500,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n_docs == 0) return;
   int lo, hi;
   key_range(p, n_docs, t0, min(t0 + kBM, p.BS) - 1, lo, hi);
-  const int n_kv = (hi - lo + kSL - 1) / kSL;
+  const int n_kv = (hi - lo + kBN - 1) / kBN;
 
   if (tid == 0) {
     mbar_init(&bars->qd_ready, 8);
-    for (int s = 0; s < C::NST; ++s) {
+    for (int s = 0; s < C::KST; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->dp_full[b], 1);
-      mbar_init(&bars->ds_full[b], 4);
-    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->ds_full, 8);
     mbar_init(&bars->fin, 1);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
@@ -531,64 +535,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tv);
       int issued = 0;
       for (int n = 0; n < n_kv; ++n) {
-        const int s = n % C::NST;
-        if (n >= C::NST && !mbar_wait(&bars->kv_empty[s], ((n / C::NST) - 1) & 1, abort, p.status)) break;
-        const int kv0 = lo + n * kSL;
-        mbar_arrive_expect_tx(&bars->k_full[s], C::SLICE);
+        const int s = n % C::KST;
+        if (n >= C::KST && !mbar_wait(&bars->kv_empty[s], ((n / C::KST) - 1) & 1, abort, p.status)) break;
+        const int kv0 = lo + n * kBN;
+        mbar_arrive_expect_tx(&bars->k_full[s], C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(smem + C::B_K + s * C::SLICE + c * kSliceBytes, &tk, &bars->k_full[s], c * 64, kvh, kv0, r);
-        mbar_arrive_expect_tx(&bars->v_full[s], C::SLICE);
+          tma_load_4d(smem + C::B_K + s * C::TILE + c * kAtomBytes, &tk, &bars->k_full[s], c * 64, kvh, kv0, r);
+        mbar_arrive_expect_tx(&bars->v_full[s], C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(smem + C::B_V + s * C::SLICE + c * kSliceBytes, &tv, &bars->v_full[s], c * 64, kvh, kv0, r);
+          tma_load_4d(smem + C::B_V + s * C::TILE + c * kAtomBytes, &tv, &bars->v_full[s], c * 64, kvh, kv0, r);
         issued = n + 1;
       }
-      for (int n = max(0, issued - C::NST); n < issued; ++n) {
-        mbar_wait(&bars->k_full[n % C::NST], (n / C::NST) & 1, abort, p.status);
-        mbar_wait(&bars->v_full[n % C::NST], (n / C::NST) & 1, abort, p.status);
+      for (int n = max(0, issued - C::KST); n < issued; ++n) {
+        mbar_wait(&bars->k_full[n % C::KST], (n / C::KST) & 1, abort, p.status);
+        mbar_wait(&bars->v_full[n % C::KST], (n / C::KST) & 1, abort, p.status);
       }
     }
   } else if (warp == 9) {
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(kBM, kSL, false, false);  // [128 rows x 64 keys], K = D
-      constexpr uint32_t id_q = idesc_bf16(kBM, D, false, true);      // [128 rows x D], K = 64 keys
-      auto issue_front = [&](int n) -> bool {
-        const int s = n % C::NST, b = n & 1;
-        const uint32_t ph = (n / C::NST) & 1;
-        if (!mbar_wait(&bars->k_full[s], ph, abort, p.status)) return false;
+      constexpr uint32_t id_s = idesc_bf16(kBM, kBN, false, false);  // [128 rows x 128 keys], K = D
+      constexpr uint32_t id_q = idesc_bf16(kBM, D, false, true);      // [128 rows x D], K = 128 keys
+      // A operand columns of the packed dS tile: the two 64-key halves sit at +0 and +64
+      auto acol = [](int kk) -> uint32_t { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; };
+      auto issue_s = [&](int n) -> bool {
+        const int s = n % C::KST;
+        if (!mbar_wait(&bars->k_full[s], (n / C::KST) & 1, abort, p.status)) return false;
         tc_fence_after();
-        const uint32_t ka = sbase + C::B_K + s * C::SLICE, va = sbase + C::B_V + s * C::SLICE;
+        const uint32_t ka = sbase + C::B_K + s * C::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts(tmem + T_S + b * kSL, tmem + T_Q + kk * 8, kmajor_desc(ka, kSliceBytes, kk), id_s, kk > 0);
-        mma_commit(&bars->s_full[b]);
-        if (!mbar_wait(&bars->v_full[s], ph, abort, p.status)) return false;
+          mma_ts(tmem + T_S, tmem + T_Q + kk * 8, kmajor_desc(ka, kAtomBytes, kk), id_s, kk > 0);
+        mma_commit(&bars->s_full);
+        return true;
+      };
+      auto issue_dp = [&](int n) -> bool {
+        const int s = n % C::KST;
+        if (!mbar_wait(&bars->v_full[s], (n / C::KST) & 1, abort, p.status)) return false;
         tc_fence_after();
+        const uint32_t va = sbase + C::B_V + s * C::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts(tmem + T_DP + b * kSL, tmem + T_DO + kk * 8, kmajor_desc(va, kSliceBytes, kk), id_s, kk > 0);
-        mma_commit(&bars->dp_full[b]);
+          mma_ts(tmem + T_DP, tmem + T_DO + kk * 8, kmajor_desc(va, kAtomBytes, kk), id_s, kk > 0);
+        mma_commit(&bars->dp_full);
         return true;
       };
       bool ok = mbar_wait(&bars->qd_ready, 0, abort, p.status);
-      for (int n = 0; n < 2 && n < n_kv && ok; ++n) ok = issue_front(n);
+      if (ok && n_kv > 0) ok = issue_s(0) && issue_dp(0);
       for (int n = 0; n < n_kv && ok; ++n) {
-        const int s = n % C::NST, b = n & 1;
-        if (!(ok = mbar_wait(&bars->ds_full[b], (n >> 1) & 1, abort, p.status))) break;
+        const int s = n % C::KST;
+        if (!(ok = mbar_wait(&bars->ds_full, n & 1, abort, p.status))) break;
         tc_fence_after();
-        const uint32_t ka = sbase + C::B_K + s * C::SLICE;
+        const uint32_t ka = sbase + C::B_K + s * C::TILE;
 #pragma unroll
-        for (int kk = 0; kk < kSL / 16; ++kk)
-          mma_ts(tmem + T_DQ, tmem + T_S + b * kSL + kk * 8, mnmajor_desc(ka, kSliceBytes, kk), id_q,
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tmem + T_DQ, tmem + T_S + acol(kk), mnmajor_desc(ka, kAtomBytes, kk), id_q,
                  (n > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->kv_empty[s]);
-        if (n + 2 < n_kv) ok = issue_front(n + 2);
-        if (n == n_kv - 1) mma_commit(&bars->fin);
+        if (n + 1 < n_kv)
+          ok = issue_s(n + 1) && issue_dp(n + 1);
+        else
+          mma_commit(&bars->fin);
       }
       mma_commit(&bars->mma_done);
       mbar_wait(&bars->mma_done, 0, abort, p.status);
     }
   } else {
-    const int grp = warp >> 2;             // handles iterations n with n & 1 == grp
+    const int grp = warp >> 2;             // key columns [64*grp, 64*grp + 64) of every tile
     const int row = (warp & 3) * 32 + lane;
     const int t = t0 + row;
     const bool row_ok = t < p.BS;
@@ -608,17 +620,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       lse2 = __ldg(g.stats + plane_index(g.bsp, p.hq, r, j, 0, t));
       dvt = __ldg(g.stats + plane_index(g.bsp, p.hq, r, j, 1, t));
     }
-    const uint32_t s_col = T_S + grp * kSL, dp_col = T_DP + grp * kSL;
+    const uint32_t s_col = T_S + grp * 64, dp_col = T_DP + grp * 64;
     bool ok = true;
-    for (int n = grp; n < n_kv && ok; n += 2) {
-      const uint32_t ph = (n >> 1) & 1;
-      const int k0 = lo + n * kSL;
-      if (!(ok = mbar_wait(&bars->s_full[grp], ph, abort, p.status))) break;
+    for (int n = 0; n < n_kv && ok; ++n) {
+      const uint32_t ph = n & 1;
+      const int k0 = lo + n * kBN + grp * 64;  // first key of this group's columns
+      if (!(ok = mbar_wait(&bars->s_full, ph, abort, p.status))) break;
       tc_fence_after();
       float x[64];
       tmem_ld_cols<64>(lb + s_col, x);
-      bool full = row_ok && k0 >= a && k0 + kSL <= b && (!p.causal || k0 + kSL - 1 <= t);
-      if (p.window_left >= 0) full = full && (t - k0 <= p.window_left) && (p.causal || k0 + kSL - 1 - t <= p.window_left);
+      bool full = row_ok && k0 >= a && k0 + 64 <= b && (!p.causal || k0 + 63 <= t);
+      if (p.window_left >= 0) full = full && (t - k0 <= p.window_left) && (p.causal || k0 + 63 - t <= p.window_left);
       if (!full) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
@@ -627,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float pr[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) pr[c] = ex2(fmaf(x[c], p.scale_log2, -lse2));
-      if (!(ok = mbar_wait(&bars->dp_full[grp], ph, abort, p.status))) break;
+      if (!(ok = mbar_wait(&bars->dp_full, ph, abort, p.status))) break;
       tc_fence_after();
       tmem_ld_cols<64>(lb + dp_col, x);
 #pragma unroll
@@ -635,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_packed<32>(lb + s_col, x);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->ds_full[grp]);
+      if (lane == 0) mbar_arrive(&bars->ds_full);
     }
     if (ok && n_kv > 0 && (ok = mbar_wait(&bars->fin, 0, abort, p.status))) {
       tc_fence_after();
@@ -727,10 +739,10 @@ static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const v
     bwd::dkdv_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hk, bwd::kThreads, C::A_SMEM, st>>>(tq, tdo, tst,
                                                                                                        a, g);
   } else {
-    // 64-key slices of K and V stream past TMEM-resident Q, dO
+    // 128-key tiles of K and V stream past TMEM-resident Q, dO
     CUtensorMap tk, tv;
-    if ((rc = make_head_tmap(&tk, k, a.P, a.BS, a.hk, D, bwd::kSL)) != USP_OK) return rc;
-    if ((rc = make_head_tmap(&tv, v, a.P, a.BS, a.hk, D, bwd::kSL)) != USP_OK) return rc;
+    if ((rc = make_head_tmap(&tk, k, a.P, a.BS, a.hk, D, kBN)) != USP_OK) return rc;
+    if ((rc = make_head_tmap(&tv, v, a.P, a.BS, a.hk, D, kBN)) != USP_OK) return rc;
     if (cudaFuncSetAttribute(bwd::dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::B_SMEM) != cudaSuccess)
       return USP_ERR_CUDA;
     bwd::dq_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hq, bwd::kThreads, C::B_SMEM, st>>>(tk, tv, a, g);
