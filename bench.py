@@ -148,14 +148,40 @@ CALLS = ["relayout_qkv", "cu_seqlens", "attn_fwd", "relayout_o", "relayout_do", 
          "attn_bwd_dq", "relayout_dqkv"]
 
 
+def relayout_bandwidth(w: W.Workload, device, t, steps: int):
+    """GB/s of the explicit exchange kernels alone: the q/k/v exchange
+    (seq -> head) and the O exchange (head -> seq), `steps` times each after
+    three warm-up rounds.  Every element is read once and written once."""
+    from ulysses_sequence_long_gb300.pipeline import Shape, UlyssesAttention
+    ua = UlyssesAttention(Shape(w.B, w.S, w.Hq, w.Hkv, w.D, w.P, w.causal, w.window_left), device=device,
+                          with_backward=False, fused=False)
+    s = torch.cuda.current_stream(device)
+    ua.o_head.zero_()
+    for _ in range(3):
+        ua.exchange_qkv(t["q"], t["k"], t["v"], s)
+        ua.exchange_out(s)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(s)
+    for _ in range(steps):
+        ua.exchange_qkv(t["q"], t["k"], t["v"], s)
+        ua.exchange_out(s)
+    stop.record(s)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(stop) / steps
+    rb = relayout_bytes(w)
+    del ua
+    torch.cuda.empty_cache()
+    return (rb["qkv"] + rb["o"]) / (ms * 1e-3) / 1e9, ms
+
+
 class Step:
-    def __init__(self, w: W.Workload, device, host=None):
-        from ulysses_sequence_long_gb300 import binding as B
+    def __init__(self, w: W.Workload, device, host=None, fused=None):
         from ulysses_sequence_long_gb300.pipeline import Shape, UlyssesAttention
-        self.B_ = B
         self.w = w
         self.device = device
-        self.ua = UlyssesAttention(Shape(w.B, w.S, w.Hq, w.Hkv, w.D, w.P, w.causal, w.window_left), device=device)
+        self.ua = UlyssesAttention(Shape(w.B, w.S, w.Hq, w.Hkv, w.D, w.P, w.causal, w.window_left), device=device,
+                                   fused=fused)
         if host is None:
             host = {"t": W.qkv_do_shards(w), "pos": torch.from_numpy(W.position_ids_shards(w)), "sinks": W.sinks(w)}
         self.shared_host = host
@@ -169,10 +195,10 @@ class Step:
         self.n_events = 0
 
     def run(self, events=None):
-        """One whole step; optional CUDA events recorded between the calls."""
+        """One whole step; optional CUDA events recorded between the calls
+        (event i+1 closes CALLS[i]; exchanges that the fused mode folds into
+        the attention kernels take ~0 ms)."""
         ua, d, s = self.ua, self.dev, self.stream
-        sh = ua.shape
-        B = self.B_
 
         def mark(i):
             if events is not None:
@@ -186,31 +212,12 @@ class Step:
         ua.attention(self.sinks, s)
         mark(3)
         ua.exchange_out(s)
-        mark(4)
-        prm = ua.params(self.sinks)
-        if ua._bwd_ws is None:
-            n = B.usp_attn_bwd_workspace_bytes(prm)
-            ua._bwd_ws = torch.empty((max(n, 256),), dtype=torch.uint8, device=ua.o_head.device)
-        B.usp_relayout_fwd(d["do"], ua.do_head, sh.B, sh.S, sh.Hq, sh.D, sh.P, s)
-        mark(5)
-        B.usp_attn_bwd_preprocess(prm, ua.o_head, ua.lse, ua.do_head, ua.dsinks if self.sinks is not None else None,
-                                  ua._bwd_ws, ua.status, s)
-        mark(6)
-        B.usp_attn_bwd_dkdv(prm, ua.q_head, ua.k_head, ua.v_head, ua.lse, ua.do_head, ua.dk_head, ua.dv_head,
-                            ua._bwd_ws, ua.status, s)
-        mark(7)
-        B.usp_attn_bwd_dq(prm, ua.q_head, ua.k_head, ua.v_head, ua.lse, ua.do_head, ua.dq_head, ua._bwd_ws,
-                          ua.status, s)
-        mark(8)
-        B.usp_relayout_bwd(ua.dq_head, ua.dq_seq, sh.B, sh.S, sh.Hq, sh.D, sh.P, s)
-        B.usp_relayout_bwd(ua.dk_head, ua.dk_seq, sh.B, sh.S, sh.Hkv, sh.D, sh.P, s)
-        B.usp_relayout_bwd(ua.dv_head, ua.dv_seq, sh.B, sh.S, sh.Hkv, sh.D, sh.P, s)
-        mark(9)
+        ua.backward_phases(d["do"], self.sinks, s, marks=lambda i: mark(4 + i))
 
     def launches_per_step(self) -> int:
-        # relayout qkv 1, scan 3, fwd 1, relayout O 1, relayout dO 1, preprocess 1 (+ dsink 1),
-        # dK/dV 1, dQ 1, relayout dQ/dK/dV 3
-        return 13 + (1 if self.sinks is not None else 0)
+        # scan 3, fwd 1, preprocess 1 (+ dsink 1), dK/dV 1, dQ 1; the explicit
+        # exchanges add relayout qkv 1, O 1, dO 1, dQ/dK/dV 3
+        return 7 + (1 if self.sinks is not None else 0) + (0 if self.ua.fused else 6)
 
     # -- end to end: host buffers in and out, through the C ABI
     def make_host_io(self):
@@ -358,6 +365,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--exchange", default="auto", choices=["auto", "fused", "explicit"],
+                    help="fused: attention kernels read/write the sequence shards; explicit: relayout kernels")
     args = ap.parse_args()
     w = W.BY_NAME[args.workload]
     if args.impl == "reference":
@@ -392,7 +401,8 @@ def main():
     barrier()
     _build.build()
 
-    step = Step(w, device)
+    fused = {"auto": None, "fused": True, "explicit": False}[args.exchange]
+    step = Step(w, device, fused=fused)
     fl = attention_flops(w)
     rb = relayout_bytes(w)
     for _ in range(max(args.warmup, 3)):
@@ -421,8 +431,14 @@ def main():
     value = fl["total"] * world / (ms * 1e-3) / 1e12
     peaks = measured_peaks()
     attn_ms = per_call["attn_fwd"] + per_call["attn_bwd_pre"] + per_call["attn_bwd_dkdv"] + per_call["attn_bwd_dq"]
-    relayout_ms = per_call["relayout_qkv"] + per_call["relayout_o"] + per_call["relayout_do"] + per_call["relayout_dqkv"]
-    relayout_total_bytes = rb["qkv"] + rb["o"] + rb["do"] + rb["dqkv"]
+    if step.ua.fused:
+        relayout_gbs, relayout_ms = relayout_bandwidth(w, device, step.dev, args.steps)
+        relayout_note = "explicit q/k/v + O exchanges timed apart (the step folds them into the attention I/O)"
+    else:
+        relayout_ms = (per_call["relayout_qkv"] + per_call["relayout_o"] + per_call["relayout_do"] +
+                       per_call["relayout_dqkv"])
+        relayout_gbs = (rb["qkv"] + rb["o"] + rb["do"] + rb["dqkv"]) / (relayout_ms * 1e-3) / 1e9
+        relayout_note = "the step's six exchange launches"
     kernels = {"attn_fwd": fl["fwd"], "attn_bwd_dkdv": fl["dkdv"], "attn_bwd_dq": fl["dq"]}
     dom = max(kernels, key=lambda n: per_call[n])
     achieved = kernels[dom] / (per_call[dom] * 1e-3) / 1e12
@@ -445,9 +461,10 @@ def main():
                        "causal": w.causal, "window_left": w.window_left, "sinks": w.sinks,
                        "documents": len(W.document_lengths(w)[0]), "visible_pairs_per_head": fl["pairs"],
                        "fwd_bwd_flop": fl["total"], "parallelism": f"emulated ulysses P={w.P}, replicas={world}",
+                       "exchanges": "fused" if step.ua.fused else "explicit",
                        "l2": "inputs larger than L2 (no flush)"},
-            "relayout_gbs": relayout_total_bytes / (relayout_ms * 1e-3) / 1e9,
-            "relayout_frac_hbm": relayout_total_bytes / (relayout_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "relayout_gbs": relayout_gbs, "relayout_frac_hbm": relayout_gbs / peaks["hbm_gbs"],
+            "relayout_measured": relayout_note,
             "attention_tflops": fl["total"] / (attn_ms * 1e-3) / 1e12,
             "fwd_tflops": fl["fwd"] / (per_call["attn_fwd"] * 1e-3) / 1e12,
             "bwd_tflops": fl["bwd"] / ((per_call["attn_bwd_pre"] + per_call["attn_bwd_dkdv"] +
@@ -457,7 +474,7 @@ def main():
 
     if not args.no_e2e:
         pin, outs, h2d, d2h = step.make_host_io()
-        twin = Step(w, device, host=step.shared_host)
+        twin = Step(w, device, host=step.shared_host, fused=fused)
         slots = [step, twin]
         run_e2e(slots, pin, outs, 3)               # warm-up of the copy path
         barrier()

@@ -177,16 +177,25 @@ typedef struct {
   const int32_t* cu_seqlens; /* device int32 [n_docs+1], from usp_cu_seqlens_from_position_ids */
   const int32_t* n_docs;     /* device int32 scalar */
   const float* sinks;        /* device fp32 [Hq] (global heads), or NULL */
+  int io_layout;             /* USP_IO_HEAD (0): q, k, v, dO, o, dq, dk, dv in head-layout;
+                                USP_IO_SEQ (1): the same tensors in seq-layout — the exchanges
+                                are fused into the kernels' loads and stores; needs (S/P) % 128 == 0 */
 } usp_attn_params;
 
+enum { USP_IO_HEAD = 0, USP_IO_SEQ = 1 };
+
 /* q:   bf16 head-layout [P][B][S][Hq/P][D];  k, v: bf16 [P][B][S][Hkv/P][D]
+ *      (with io_layout = USP_IO_SEQ: seq-layout [P][B][S/P][Hq][D] and [P][B][S/P][Hkv][D],
+ *      i.e. the shards each rank holds before the exchange; o then comes back in
+ *      seq-layout too, exactly what usp_relayout_bwd of the head-layout o gives)
  * o:   bf16 head-layout like q (output)
  * lse: fp32 [P][B][Hq/P][S] natural-log LSE (output; includes the sink)
  * dev_status: nullable device int32; USP_ERR_BAD_SEQLENS when cu_seqlens does
  *   not start at 0, is not strictly increasing, or does not end at B*S (the
  *   outputs are then left unwritten).
- * Errors: USP_ERR_INVALID_ARG, USP_ERR_INDIVISIBLE, USP_ERR_UNSUPPORTED (D not
- * 64/128, window_left < -1, B*S too large), USP_ERR_ALIGNMENT, USP_ERR_CUDA. */
+ * Errors: USP_ERR_INVALID_ARG (also an unknown io_layout), USP_ERR_INDIVISIBLE,
+ * USP_ERR_UNSUPPORTED (D not 64/128, window_left < -1, B*S >= 2^30 or
+ * B*S*Hq >= 2^31, USP_IO_SEQ with (S/P) % 128 != 0), USP_ERR_ALIGNMENT, USP_ERR_CUDA. */
 int usp_attn_fwd(const usp_attn_params* params, const void* q, const void* k, const void* v,
                  void* o, float* lse, int32_t* dev_status, usp_stream_t stream);
 

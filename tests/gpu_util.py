@@ -95,6 +95,24 @@ def device_inputs(w: W.Workload, device="cuda"):
     return dev, host
 
 
+def head_values(ua, name, r, j, heads_per_rank):
+    """float64 [B*S][D] of local head j of rank r for output `name` ("o", "dq",
+    "dk", "dv"), read from the head-layout buffer (explicit exchanges) or from
+    the seq-layout output (fused exchanges)."""
+    if not ua.fused:
+        t = getattr(ua, name + "_head")                      # [P][B][S][hpr][D]
+        return t[r].reshape(-1, heads_per_rank, t.shape[-1])[:, j].double().cpu().numpy()
+    t = getattr(ua, name + "_seq")                           # [P'][B][S/P][H][D]
+    P, Bb, Sl, H, D = t.shape
+    x = t.permute(1, 0, 2, 3, 4).reshape(Bb * P * Sl, H, D)  # token b*S + r'*Sl + s'
+    return x[:, r * heads_per_rank + j].double().cpu().numpy()
+
+
+def modes(w: W.Workload):
+    """Exchange modes a workload can run: explicit always, fused when S/P % 128 == 0."""
+    return [False] + ([True] if (w.S // w.P) % 128 == 0 else [])
+
+
 def shape_of(w: W.Workload):
     from ulysses_sequence_long_gb300.pipeline import Shape
     return Shape(B=w.B, S=w.S, Hq=w.Hq, Hkv=w.Hkv, D=w.D, P=w.P, causal=w.causal, window_left=w.window_left)

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import usp_workloads as W
-from gpu_util import assert_close, built_lib, device_inputs, dsink_bound, shape_of
+from gpu_util import assert_close, built_lib, device_inputs, dsink_bound, head_values, modes, shape_of
 
 pytestmark = pytest.mark.gpu
 
@@ -17,10 +17,10 @@ def _lib():
     built_lib()
 
 
-def _fwd_bwd(w):
+def _fwd_bwd(w, fused=False):
     from ulysses_sequence_long_gb300.pipeline import UlyssesAttention
     dev, host = device_inputs(w)
-    ua = UlyssesAttention(shape_of(w), with_backward=True)
+    ua = UlyssesAttention(shape_of(w), with_backward=True, fused=fused)
     ua.forward(dev["q"], dev["k"], dev["v"], dev["pos"], dev["sinks"])
     ua.backward(dev["do"], dev["sinks"])
     torch.cuda.synchronize()
@@ -42,9 +42,12 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
-def test_backward_full_parity_small(w):
-    ua, dev, host = _fwd_bwd(w)
+CASES = [(w, f) for w in SMALL for f in modes(w)]
+
+
+@pytest.mark.parametrize("w,fused", CASES, ids=[f"{w.name}-{'fused' if f else 'explicit'}" for w, f in CASES])
+def test_backward_full_parity_small(w, fused):
+    ua, dev, host = _fwd_bwd(w, fused)
     snk = host["sinks"]
     f = oracle.ulysses_fwd(host["q"], host["k"], host["v"], host["pos"], w.causal, w.window_left, None, snk)
     g = oracle.ulysses_bwd(f, host["do"], w.causal, w.window_left, None, snk)
@@ -70,19 +73,20 @@ def _rank_views(w, host, r):
     return qh, kh, vh, doh, cu, snk
 
 
-def _gpu_head(t, w, r, heads):
-    T = w.B * w.S
-    return t[r].reshape(T, heads, w.D).float().cpu().numpy()
+def _gpu_head(ua, name, w, r, heads):
+    """[T][heads][D] float64 of all local heads of rank r for output `name`."""
+    return np.stack([head_values(ua, name, r, j, heads) for j in range(heads)], axis=1)
 
 
-@pytest.mark.parametrize("w,groups", [
-    (W.GPTOSS_WIN, [(0, 0), (5, 0)]),
-    (W.LLAMA32K, [(2, 0), (7, 0)]),
-], ids=lambda x: x.name if hasattr(x, "name") else "")
-def test_backward_full_size_whole_groups(w, groups):
+@pytest.mark.parametrize("w,groups,fused", [
+    (W.GPTOSS_WIN, [(0, 0), (5, 0)], True),
+    (W.LLAMA32K, [(2, 0), (7, 0)], True),
+    (W.LLAMA32K, [(4, 0)], False),
+], ids=["gptoss_win-fused", "llama32k-fused", "llama32k-explicit"])
+def test_backward_full_size_whole_groups(w, groups, fused):
     """Every query head of a GQA group on a rank: dQ of those heads and the
     complete dK/dV of their key/value head, compared element by element."""
-    ua, dev, host = _fwd_bwd(w)
+    ua, dev, host = _fwd_bwd(w, fused)
     G = w.Hq // w.Hkv
     for r, kvh in groups:
         qh, kh, vh, doh, cu, snk = _rank_views(w, host, r)
@@ -90,9 +94,9 @@ def test_backward_full_size_whole_groups(w, groups):
         O, L = oracle.attention_fwd(qh, kh, vh, cu, w.causal, w.window_left, None, snk, heads=heads)
         dq, dk, dv, ds = oracle.attention_bwd(qh, kh, vh, O, L, doh, cu, w.causal, w.window_left, None, snk,
                                               heads=heads)
-        gq = _gpu_head(ua.dq_head, w, r, w.Hq // w.P)
-        gk = _gpu_head(ua.dk_head, w, r, w.Hkv // w.P)
-        gv = _gpu_head(ua.dv_head, w, r, w.Hkv // w.P)
+        gq = _gpu_head(ua, "dq", w, r, w.Hq // w.P)
+        gk = _gpu_head(ua, "dk", w, r, w.Hkv // w.P)
+        gv = _gpu_head(ua, "dv", w, r, w.Hkv // w.P)
         assert_close(f"dq r{r}", gq[:, heads], dq[:, heads])
         assert_close(f"dk r{r} kv{kvh}", gk[:, kvh], dk[:, kvh])
         assert_close(f"dv r{r} kv{kvh}", gv[:, kvh], dv[:, kvh])
@@ -110,7 +114,7 @@ def test_backward_full_size_whole_groups(w, groups):
 def test_backward_full_size_sampled(w):
     """Long single documents: dQ at seeded rows, dK/dV at seeded keys near the
     end of the document (few rows see them), all query heads of the group."""
-    ua, dev, host = _fwd_bwd(w)
+    ua, dev, host = _fwd_bwd(w, fused=True)
     rng = np.random.Generator(np.random.PCG64(17))
     G = w.Hq // w.Hkv
     r, kvh = w.P - 1, 0
@@ -121,7 +125,7 @@ def test_backward_full_size_sampled(w):
     # O, which D is computed from, is amplified there)
     rows = np.sort(rng.choice(w.S, 16, replace=False))
     edge = np.array([0, 1, w.S - 1])
-    gq = _gpu_head(ua.dq_head, w, r, w.Hq // w.P)
+    gq = _gpu_head(ua, "dq", w, r, w.Hq // w.P)
     for h in (kvh * G, kvh * G + G - 1):
         sink = None if snk is None else snk[h]
         dq = oracle.attention_bwd_rows(qh, kh, vh, doh, cu, rows, h, w.causal, w.window_left, sink=sink)
@@ -130,8 +134,8 @@ def test_backward_full_size_sampled(w):
         assert_close(f"dq edge rows h{h}", gq[edge, h], dq, rel_l2=np.inf)
     keys = np.sort(np.concatenate([w.S - 1 - rng.choice(384, 6, replace=False), [w.S - 1]]))
     dk, dv = oracle.attention_bwd_keys(qh, kh, vh, doh, cu, keys, kvh, w.causal, w.window_left, sinks=snk)
-    gk = _gpu_head(ua.dk_head, w, r, w.Hkv // w.P)
-    gv = _gpu_head(ua.dv_head, w, r, w.Hkv // w.P)
+    gk = _gpu_head(ua, "dk", w, r, w.Hkv // w.P)
+    gv = _gpu_head(ua, "dv", w, r, w.Hkv // w.P)
     assert_close("dk keys", gk[keys, kvh], dk)
     assert_close("dv keys", gv[keys, kvh], dv)
 
@@ -142,7 +146,7 @@ def test_backward_conservation_at_full_size():
     sum_u dK_u = 0; and each row of P sums to one, so sum_u dV_u equals the sum
     of dO over the group's query heads and rows."""
     w = W.LONG128K
-    ua, dev, host = _fwd_bwd(w)
+    ua, dev, host = _fwd_bwd(w, fused=False)
     G = w.Hq // w.Hkv
     for r in range(w.P):
         gk = ua.dk_head[r].reshape(w.S, -1, w.D).double().sum(0).cpu().numpy()

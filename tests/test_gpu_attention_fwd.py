@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import usp_workloads as W
-from gpu_util import assert_close, built_lib, device_inputs, shape_of
+from gpu_util import assert_close, built_lib, device_inputs, head_values, modes, shape_of
 
 pytestmark = pytest.mark.gpu
 
@@ -18,10 +18,10 @@ def _lib():
     built_lib()
 
 
-def _forward(w):
+def _forward(w, fused=False):
     from ulysses_sequence_long_gb300.pipeline import UlyssesAttention
     dev, host = device_inputs(w)
-    ua = UlyssesAttention(shape_of(w), with_backward=False)
+    ua = UlyssesAttention(shape_of(w), with_backward=False, fused=fused)
     ua.forward(dev["q"], dev["k"], dev["v"], dev["pos"], dev["sinks"])
     torch.cuda.synchronize()
     assert ua.read_status() == 0
@@ -41,7 +41,7 @@ def _oracle_rank_head(w, host, ua, r, j):
 
 
 def _gpu_rank_head(w, ua, r, j):
-    o = ua.o_head[r].reshape(w.B * w.S, w.Hq // w.P, w.D)[:, j].float().cpu().numpy()
+    o = head_values(ua, "o", r, j, w.Hq // w.P)
     lse = ua.lse[r][:, j].reshape(-1).cpu().numpy()
     return o, lse
 
@@ -60,9 +60,12 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
-def test_forward_full_parity_small(w):
-    ua, dev, host = _forward(w)
+CASES = [(w, f) for w in SMALL for f in modes(w)]
+
+
+@pytest.mark.parametrize("w,fused", CASES, ids=[f"{w.name}-{'fused' if f else 'explicit'}" for w, f in CASES])
+def test_forward_full_parity_small(w, fused):
+    ua, dev, host = _forward(w, fused)
     snk = host["sinks"]
     ref = oracle.ulysses_fwd(host["q"], host["k"], host["v"], host["pos"], w.causal, w.window_left, None, snk)
     assert_close("o_seq", ua.o_seq.float().cpu().numpy(), ref["o_seq"])
@@ -71,13 +74,14 @@ def test_forward_full_parity_small(w):
     assert np.array_equal(cu, ref["cu_seqlens"])
 
 
-@pytest.mark.parametrize("w,pairs", [
-    (W.GPTOSS_WIN, [(0, 0), (3, 5), (7, 7)]),
-    (W.GPTOSS_FULL, [(2, 1), (6, 6)]),
-    (W.LLAMA32K, [(0, 0), (5, 3), (7, 2)]),
-], ids=lambda x: x.name if hasattr(x, "name") else "")
-def test_forward_full_size_sampled_heads(w, pairs):
-    ua, dev, host = _forward(w)
+@pytest.mark.parametrize("w,pairs,fused", [
+    (W.GPTOSS_WIN, [(0, 0), (3, 5), (7, 7)], True),
+    (W.GPTOSS_FULL, [(2, 1), (6, 6)], False),
+    (W.LLAMA32K, [(0, 0), (5, 3), (7, 2)], True),
+    (W.LLAMA32K, [(1, 1)], False),
+], ids=["gptoss_win-fused", "gptoss_full-explicit", "llama32k-fused", "llama32k-explicit"])
+def test_forward_full_size_sampled_heads(w, pairs, fused):
+    ua, dev, host = _forward(w, fused)
     for r, j in pairs:
         O, L = _oracle_rank_head(w, host, ua, r, j)
         o, lse = _gpu_rank_head(w, ua, r, j)
@@ -87,7 +91,7 @@ def test_forward_full_size_sampled_heads(w, pairs):
 
 def test_forward_long_context_sampled_rows():
     w = W.LONG128K
-    ua, dev, host = _forward(w)
+    ua, dev, host = _forward(w, fused=True)
     rng = np.random.Generator(np.random.PCG64(11))
     hq, hk = w.Hq // w.P, w.Hkv // w.P
     for r, j in [(0, 0), (3, 6)]:
@@ -120,7 +124,7 @@ def test_stale_per_shard_cu_seqlens_are_flagged():
 def test_attention_refuses_indivisible_heads():
     from ulysses_sequence_long_gb300 import binding as B
     from ulysses_sequence_long_gb300.pipeline import Shape, UlyssesAttention
-    ua = UlyssesAttention(Shape(B=1, S=256, Hq=4, Hkv=2, D=64, P=2), with_backward=False)
+    ua = UlyssesAttention(Shape(B=1, S=256, Hq=4, Hkv=2, D=64, P=2), with_backward=False, fused=False)
     prm = B.attn_params(1, 256, 4, 2, 64, 4, ua.cu_seqlens, ua.n_docs)   # P=4 does not divide Hkv=2
     with pytest.raises(B.UspError) as e:
         B.usp_attn_fwd(prm, ua.q_head, ua.k_head, ua.v_head, ua.o_head, ua.lse)
@@ -128,4 +132,23 @@ def test_attention_refuses_indivisible_heads():
     prm = B.attn_params(1, 256, 4, 2, 96, 2, ua.cu_seqlens, ua.n_docs)   # head dim 96
     with pytest.raises(B.UspError) as e:
         B.usp_attn_fwd(prm, ua.q_head, ua.k_head, ua.v_head, ua.o_head, ua.lse)
+    assert e.value.code == B.USP_ERR_UNSUPPORTED
+
+
+@pytest.mark.gpu
+def test_fused_exchanges_need_shards_of_128_rows():
+    """Sequence-shard I/O tiles each shard in 128-row blocks: a shape whose
+    S/P is not a multiple of 128 is refused by the pipeline and by the C ABI."""
+    from ulysses_sequence_long_gb300 import binding as B
+    from ulysses_sequence_long_gb300.pipeline import Shape, UlyssesAttention
+    sh = Shape(B=1, S=320, Hq=4, Hkv=2, D=64, P=2)
+    with pytest.raises(ValueError):
+        UlyssesAttention(sh, with_backward=False, fused=True)
+    ua = UlyssesAttention(sh, with_backward=False)
+    assert not ua.fused
+    q = torch.zeros((2, 1, 160, 4, 64), dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros((2, 1, 160, 2, 64), dtype=torch.bfloat16, device="cuda")
+    prm = B.attn_params(1, 320, 4, 2, 64, 2, ua.cu_seqlens, ua.n_docs, io_layout=B.USP_IO_SEQ)
+    with pytest.raises(B.UspError) as e:
+        B.usp_attn_fwd(prm, q, kv, kv, q, ua.lse)
     assert e.value.code == B.USP_ERR_UNSUPPORTED

@@ -59,3 +59,12 @@ def test_host_checks_without_gpu(lib):
     assert lib.usp_attn_fwd(ctypes.byref(prm), p, p, p, p, p, None, None) == B.USP_ERR_INVALID_ARG
     prm = B.AttnParams(1, 256, 4, 2, 64, 2, 1, -1, 0.0, 16, 16, None)
     assert lib.usp_attn_fwd(ctypes.byref(prm), ctypes.c_void_p(18), p, p, p, p, None, None) == B.USP_ERR_ALIGNMENT
+    # sequence-shard I/O: unknown layouts are rejected; S/P must be a multiple of 128
+    prm = B.AttnParams(1, 256, 4, 2, 64, 2, 1, -1, 0.0, 16, 16, None, 7)
+    assert lib.usp_attn_fwd(ctypes.byref(prm), p, p, p, p, p, None, None) == B.USP_ERR_INVALID_ARG
+    prm = B.AttnParams(1, 320, 4, 2, 64, 2, 1, -1, 0.0, 16, 16, None, B.USP_IO_SEQ)
+    assert lib.usp_attn_fwd(ctypes.byref(prm), p, p, p, p, p, None, None) == B.USP_ERR_UNSUPPORTED
+    ws = ctypes.c_void_p(1 << 20)
+    assert lib.usp_attn_bwd_dkdv(ctypes.byref(prm), p, p, p, p, p, p, p, ws, 1 << 20, None, None) == \
+        B.USP_ERR_UNSUPPORTED
+    assert lib.usp_attn_bwd_dq(ctypes.byref(prm), p, p, p, p, p, p, ws, 1 << 20, None, None) == B.USP_ERR_UNSUPPORTED

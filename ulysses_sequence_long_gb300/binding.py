@@ -51,7 +51,12 @@ class AttnParams(ctypes.Structure):
         ("D", ctypes.c_int), ("P", ctypes.c_int), ("causal", ctypes.c_int),
         ("window_left", ctypes.c_int), ("softmax_scale", ctypes.c_float),
         ("cu_seqlens", ctypes.c_void_p), ("n_docs", ctypes.c_void_p), ("sinks", ctypes.c_void_p),
+        ("io_layout", ctypes.c_int),
     ]
+
+
+USP_IO_HEAD = 0
+USP_IO_SEQ = 1
 
 
 def lib_path() -> str:
@@ -163,10 +168,10 @@ def usp_cu_seqlens_from_position_ids_noalloc(pos, B, S, P, cu_seqlens, n_docs, m
 
 
 def attn_params(B, S, Hq, Hkv, D, P, cu_seqlens, n_docs, causal=True, window_left=-1, softmax_scale=0.0,
-                sinks=None) -> AttnParams:
+                sinks=None, io_layout=USP_IO_HEAD) -> AttnParams:
     return AttnParams(B, S, Hq, Hkv, D, P, 1 if causal else 0, window_left, softmax_scale,
                       _dev(cu_seqlens, "cu_seqlens", torch.int32), _dev(n_docs, "n_docs", torch.int32),
-                      _dev(sinks, "sinks", torch.float32))
+                      _dev(sinks, "sinks", torch.float32), int(io_layout))
 
 
 def usp_attn_fwd(params: AttnParams, q, k, v, o, lse, dev_status=None, stream=None):

@@ -59,6 +59,23 @@ int make_head_tmap(CUtensorMap* m, const void* base, int P, int BS, int H, int D
   return rc == CUDA_SUCCESS ? USP_OK : USP_ERR_CUDA;
 }
 
+// Tensor map of a seq-layout bf16 tensor [P][B][Sl][H][D]: dims {D, H, Sl, B, P},
+// box {64, 1, rows, 1, 1}; a box of `rows` tokens must lie in one shard of one row.
+int make_seq_tmap(CUtensorMap* m, const void* base, int P, int B, int Sl, int H, int D, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return USP_ERR_CUDA;
+  cuuint64_t dims[5] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(Sl),
+                        static_cast<cuuint64_t>(B), static_cast<cuuint64_t>(P)};
+  cuuint64_t strides[4] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                           static_cast<cuuint64_t>(Sl) * H * D * 2, static_cast<cuuint64_t>(B) * Sl * H * D * 2};
+  cuuint32_t box[5] = {64, 1, static_cast<cuuint32_t>(box_rows), 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult rc = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS ? USP_OK : USP_ERR_CUDA;
+}
+
 int make_stats_tmap(CUtensorMap* m, const void* base, int BS, int pitch, int rows, int box_rows) {
   auto fn = encode_fn();
   if (fn == nullptr) return USP_ERR_CUDA;
@@ -108,6 +125,10 @@ int check_attn_params(const usp_attn_params* p) {
   if (p->D != 64 && p->D != 128) return USP_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(p->B) * p->S >= (1ll << 30)) return USP_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(p->P) * p->B * p->S * p->Hq * p->D >= (1ll << 40)) return USP_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(p->B) * p->S * p->Hq >= (1ll << 31)) return USP_ERR_UNSUPPORTED;  // 32-bit row counters
+  if (p->io_layout != USP_IO_HEAD && p->io_layout != USP_IO_SEQ) return USP_ERR_INVALID_ARG;
+  // fused exchanges: tiles of 128 tokens must never straddle a rank's shard
+  if (p->io_layout == USP_IO_SEQ && (p->S / p->P) % 128 != 0) return USP_ERR_UNSUPPORTED;
   return USP_OK;
 }
 

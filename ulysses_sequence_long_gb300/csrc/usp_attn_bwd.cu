@@ -59,8 +59,9 @@ __device__ __forceinline__ size_t plane_index(int bsp, int hq, int r, int j, int
 }
 
 // --------------------------------------------------------------- preprocess
-// One row = D bf16 = D/8 lanes of 16 bytes.  Rows are (rank, token, head) in
-// head-layout order, so reads are contiguous.
+// One row = D bf16 = D/8 lanes of 16 bytes.  Rows are taken in statistics
+// order (rank, local head, token), so the LSE reads and the D/LSE writes are
+// contiguous; each row's D-vector is one contiguous run in either layout.
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
                                                          const float* __restrict__ lse, float* __restrict__ stats,
@@ -70,10 +71,13 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
   for (uint32_t row = (blockIdx.x * blockDim.x + threadIdx.x) / LPR; row < n_rows + (32 / LPR);
        row += gridDim.x * blockDim.x / LPR) {
     const bool ok = row < n_rows;
+    const uint32_t rj = ok ? row / p.BS : 0, t = ok ? row - rj * p.BS : 0;
+    const int r = static_cast<int>(rj) / p.hq, j = static_cast<int>(rj) - r * p.hq;
     float acc = 0.f;
     if (ok) {
-      const uint4 a = __ldg(o + static_cast<size_t>(row) * LPR + lane_row);
-      const uint4 b = __ldg(dO + static_cast<size_t>(row) * LPR + lane_row);
+      const size_t base = row_offset(p, r, j, p.hq, static_cast<int>(t), D) / 8;
+      const uint4 a = __ldg(o + base + lane_row);
+      const uint4 b = __ldg(dO + base + lane_row);
       const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc += bf16lo(av[e]) * bf16lo(bv[e]) + bf16hi(av[e]) * bf16hi(bv[e]);
@@ -81,9 +85,6 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
 #pragma unroll
     for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (ok && lane_row == 0) {
-      const uint32_t j = row % p.hq;
-      const uint32_t rt = row / p.hq;
-      const uint32_t r = rt / p.BS, t = rt - r * p.BS;
       stats[plane_index(bsp, p.hq, r, j, 0, t)] = __ldg(lse + stat_index(p, r, j, t)) * kLog2e;
       stats[plane_index(bsp, p.hq, r, j, 1, t)] = acc;
     }
@@ -272,7 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n_docs == 0) return;
   int qlo, qhi;
   query_range(p, n_docs, u0, min(u0 + kBN, p.BS) - 1, qlo, qhi);
-  qlo &= ~3;  // statistics slices are fetched by TMA from 16-byte aligned tokens
+  // statistics slices are fetched by TMA from 16-byte aligned tokens; with the
+  // exchanges fused, 64-token slices must also stay inside one rank's shard
+  qlo &= p.seq_io ? ~(kSL - 1) : ~3;
   const int n_q = (qhi - qlo + kSL - 1) / kSL;
   const int n_it = p.G * n_q;
 
@@ -317,8 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q0 = qlo + (i % n_q) * kSL;
         mbar_arrive_expect_tx(&bars->qdo_full[s], 2 * C::SLICE + C::STAT);
         for (int c = 0; c < C::NCH; ++c) {
-          tma_load_4d(smem + C::A_Q + s * C::SLICE + c * kSliceBytes, &tq, &bars->qdo_full[s], c * 64, jq, q0, r);
-          tma_load_4d(smem + C::A_DO + s * C::SLICE + c * kSliceBytes, &tdo, &bars->qdo_full[s], c * 64, jq, q0, r);
+          tma_load_rows(smem + C::A_Q + s * C::SLICE + c * kSliceBytes, &tq, &bars->qdo_full[s], p, c, r, jq, p.hq, q0);
+          tma_load_rows(smem + C::A_DO + s * C::SLICE + c * kSliceBytes, &tdo, &bars->qdo_full[s], p, c, r, jq, p.hq, q0);
         }
         tma_load_3d(smem + C::A_STAT + s * C::STAT, &tst, &bars->qdo_full[s], q0, 0, r * p.hq + jq);
         issued = i + 1;
@@ -396,8 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lb = tmem + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
     // K (group 0) or V (group 1) row of this key into TMEM
     {
-      const size_t row = (static_cast<size_t>(r) * p.BS + (key_ok ? u : 0)) * p.hk + kh;
-      row_to_tmem<D>(lb + (grp == 0 ? T_K : T_V), (grp == 0 ? g.k : g.v) + row * D, key_ok);
+      const size_t off = row_offset(p, r, kh, p.hk, key_ok ? u : 0, D);
+      row_to_tmem<D>(lb + (grp == 0 ? T_K : T_V), (grp == 0 ? g.k : g.v) + off, key_ok);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->kv_ready);
@@ -452,14 +455,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && n_it > 0 && (ok = mbar_wait(&bars->fin, 0, abort, p.status))) {
       tc_fence_after();
-      const size_t row = (static_cast<size_t>(r) * p.BS + (key_ok ? u : 0)) * p.hk + kh;
+      const size_t off = row_offset(p, r, kh, p.hk, key_ok ? u : 0, D);
       if (grp == 0)
-        store_row<D>(lb + T_DV, g.dv + row * D, 1.f, key_ok);
+        store_row<D>(lb + T_DV, g.dv + off, 1.f, key_ok);
       else
-        store_row<D>(lb + T_DK, g.dk + row * D, p.scale, key_ok);
+        store_row<D>(lb + T_DK, g.dk + off, p.scale, key_ok);
     } else if (ok && n_it == 0 && key_ok) {
-      const size_t row = (static_cast<size_t>(r) * p.BS + u) * p.hk + kh;
-      __nv_bfloat16* dst = (grp == 0 ? g.dv : g.dk) + row * D;
+      __nv_bfloat16* dst = (grp == 0 ? g.dv : g.dk) + row_offset(p, r, kh, p.hk, u, D);
       for (int e = 0; e < D; e += 8) *reinterpret_cast<uint4*>(dst + e) = make_uint4(0, 0, 0, 0);
     }
   }
@@ -500,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n_docs == 0) return;
   int lo, hi;
   key_range(p, n_docs, t0, min(t0 + kBM, p.BS) - 1, lo, hi);
+  if (p.seq_io) lo &= ~(kBN - 1);  // key tiles inside one rank's shard
   const int n_kv = (hi - lo + kBN - 1) / kBN;
 
   if (tid == 0) {
@@ -540,10 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kv0 = lo + n * kBN;
         mbar_arrive_expect_tx(&bars->k_full[s], C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(smem + C::B_K + s * C::TILE + c * kAtomBytes, &tk, &bars->k_full[s], c * 64, kvh, kv0, r);
+          tma_load_rows(smem + C::B_K + s * C::TILE + c * kAtomBytes, &tk, &bars->k_full[s], p, c, r, kvh, p.hk, kv0);
         mbar_arrive_expect_tx(&bars->v_full[s], C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(smem + C::B_V + s * C::TILE + c * kAtomBytes, &tv, &bars->v_full[s], c * 64, kvh, kv0, r);
+          tma_load_rows(smem + C::B_V + s * C::TILE + c * kAtomBytes, &tv, &bars->v_full[s], p, c, r, kvh, p.hk, kv0);
         issued = n + 1;
       }
       for (int n = max(0, issued - C::KST); n < issued; ++n) {
@@ -607,8 +610,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lb = tmem + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
     // Q (group 0) or dO (group 1) row into TMEM
     {
-      const size_t rrow = (static_cast<size_t>(r) * p.BS + (row_ok ? t : 0)) * p.hq + j;
-      row_to_tmem<D>(lb + (grp == 0 ? T_Q : T_DO), (grp == 0 ? g.q : g.dO) + rrow * D, row_ok);
+      const size_t off = row_offset(p, r, j, p.hq, row_ok ? t : 0, D);
+      row_to_tmem<D>(lb + (grp == 0 ? T_Q : T_DO), (grp == 0 ? g.q : g.dO) + off, row_ok);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->qd_ready);
@@ -651,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && n_kv > 0 && (ok = mbar_wait(&bars->fin, 0, abort, p.status))) {
       tc_fence_after();
-      __nv_bfloat16* dst = g.dq + ((static_cast<size_t>(r) * p.BS + (row_ok ? t : 0)) * p.hq + j) * D + grp * (D / 2);
+      __nv_bfloat16* dst = g.dq + row_offset(p, r, j, p.hq, row_ok ? t : 0, D) + grp * (D / 2);
       store_row<D / 2>(lb + T_DQ + grp * (D / 2), dst, p.scale, row_ok);
     }
   }
@@ -691,6 +694,8 @@ static AttnArgs make_args(const usp_attn_params& prm, int32_t* status) {
   a.n_docs = prm.n_docs;
   a.sinks = prm.sinks;
   a.status = status;
+  a.seq_io = prm.io_layout == USP_IO_SEQ ? 1 : 0;
+  a.Sl = prm.S / prm.P;
   return a;
 }
 
@@ -730,8 +735,8 @@ static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const v
   if (!dq_pass) {
     // 64-query slices of Q, dO and their statistics stream past TMEM-resident K, V
     CUtensorMap tq, tdo, tst;
-    if ((rc = make_head_tmap(&tq, q, a.P, a.BS, a.hq, D, bwd::kSL)) != USP_OK) return rc;
-    if ((rc = make_head_tmap(&tdo, dO, a.P, a.BS, a.hq, D, bwd::kSL)) != USP_OK) return rc;
+    if ((rc = make_rows_tmap(&tq, q, a, a.hq, D, bwd::kSL)) != USP_OK) return rc;
+    if ((rc = make_rows_tmap(&tdo, dO, a, a.hq, D, bwd::kSL)) != USP_OK) return rc;
     if ((rc = make_stats_tmap(&tst, stats, a.BS, g.bsp, a.P * a.hq, bwd::kSL)) != USP_OK) return rc;
     if (cudaFuncSetAttribute(bwd::dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::A_SMEM) !=
         cudaSuccess)
@@ -741,8 +746,8 @@ static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const v
   } else {
     // 128-key tiles of K and V stream past TMEM-resident Q, dO
     CUtensorMap tk, tv;
-    if ((rc = make_head_tmap(&tk, k, a.P, a.BS, a.hk, D, kBN)) != USP_OK) return rc;
-    if ((rc = make_head_tmap(&tv, v, a.P, a.BS, a.hk, D, kBN)) != USP_OK) return rc;
+    if ((rc = make_rows_tmap(&tk, k, a, a.hk, D, kBN)) != USP_OK) return rc;
+    if ((rc = make_rows_tmap(&tv, v, a, a.hk, D, kBN)) != USP_OK) return rc;
     if (cudaFuncSetAttribute(bwd::dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::B_SMEM) != cudaSuccess)
       return USP_ERR_CUDA;
     bwd::dq_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hq, bwd::kThreads, C::B_SMEM, st>>>(tk, tv, a, g);

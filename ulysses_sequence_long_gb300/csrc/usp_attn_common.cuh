@@ -30,7 +30,36 @@ struct AttnArgs {
   const int32_t* n_docs;
   const float* sinks;  // global [Hq] or null
   int32_t* status;
+  int seq_io;  // 1: inputs and outputs in seq-layout [P][B][S/P][H][D] (exchanges fused)
+  int Sl;      // S/P
 };
+
+// Element offset of the D-vector of (rank r, local head j of `hpr` per rank,
+// rank-local token t = b*S + s) in either layout:
+//   head-layout [P][B][S][hpr][D]      ((r*B*S + t)*hpr + j)*D
+//   seq-layout  [P][B][S/P][P*hpr][D]  (((r'*B + b)*Sl + s')*P*hpr + r*hpr + j)*D, s = r'*Sl + s'
+__device__ __forceinline__ size_t row_offset(const AttnArgs& p, int r, int j, int hpr, int t, int D) {
+  if (!p.seq_io) return ((static_cast<size_t>(r) * p.BS + t) * hpr + j) * D;
+  const int b = t / p.S, s = t - b * p.S;
+  const int rp = s / p.Sl, sp = s - rp * p.Sl;
+  return ((static_cast<size_t>(rp * p.B + b) * p.Sl + sp) * (static_cast<size_t>(p.P) * hpr) +
+          static_cast<size_t>(r) * hpr + j) * D;
+}
+
+// TMA load of `rows` tokens starting at rank-local token t (64 columns of the
+// D-vectors starting at column c64*64) of local head j of rank r, from either
+// layout's tensor map.  In seq-layout the rows must lie in one shard of one
+// row of the batch (the kernels align tiles to make sure).
+__device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* m, uint64_t* bar, const AttnArgs& p,
+                                              int c64, int r, int j, int hpr, int t) {
+  if (!p.seq_io) {
+    tma_load_4d(dst, m, bar, c64 * 64, j, t, r);
+  } else {
+    const int b = t / p.S, s = t - b * p.S;
+    const int rp = s / p.Sl, sp = s - rp * p.Sl;
+    tma_load_5d(dst, m, bar, c64 * 64, r * hpr + j, sp, b, rp);
+  }
+}
 
 // Document index d with cu[d] <= t < cu[d+1] (cu assumed valid, n >= 1).
 __device__ __forceinline__ int find_doc(const int32_t* __restrict__ cu, int n, int t) {
@@ -120,6 +149,13 @@ namespace usp {
 // Tensor map of a head-layout bf16 tensor [P][BS][H][D]: dims {D, H, BS, P},
 // box {64, 1, rows, 1}, 128-byte swizzle (one 128-byte row per token).
 int make_head_tmap(CUtensorMap* m, const void* base, int P, int BS, int H, int D, int box_rows);
+int make_seq_tmap(CUtensorMap* m, const void* base, int P, int B, int Sl, int H, int D, int box_rows);
+
+// The map for either layout: head-layout (hpr heads per rank) or seq-layout (P*hpr heads).
+inline int make_rows_tmap(CUtensorMap* m, const void* base, const AttnArgs& a, int hpr, int D, int box_rows) {
+  return a.seq_io ? make_seq_tmap(m, base, a.P, a.B, a.Sl, a.P * hpr, D, box_rows)
+                  : make_head_tmap(m, base, a.P, a.BS, hpr, D, box_rows);
+}
 
 // Tensor map of the backward's planar statistics, fp32 [P*hq][2][pitch]: dims
 // {BS, 2, P*hq}, box {box_rows, 2, 1} (box_rows tokens of both planes of one

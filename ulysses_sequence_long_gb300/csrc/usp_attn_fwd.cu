@@ -103,6 +103,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       hi = max(hi, h0);
     }
   }
+  // With the exchanges fused, key tiles are aligned to 128 tokens so that a
+  // tile never straddles a rank's shard (keys before the document are masked).
+  if (p.seq_io) lo &= ~(kBN - 1);
   const int n_kv = (hi - lo + kBN - 1) / kBN;
 
   if (tid == 0) {
@@ -142,8 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!tile_ok[q]) continue;
         mbar_arrive_expect_tx(&bars->q_full[q], C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(smem + C::OFF_Q + q * C::TILE + c * kAtomBytes, &tq, &bars->q_full[q], c * 64, j,
-                      t0 + q * kBM, r);
+          tma_load_rows(smem + C::OFF_Q + q * C::TILE + c * kAtomBytes, &tq, &bars->q_full[q], p, c, r, j, p.hq,
+                        t0 + q * kBM);
       }
       int issued = 0;
       for (int n = 0; n < n_kv; ++n) {
@@ -152,10 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kv0 = lo + n * kBN;
         mbar_arrive_expect_tx(&bars->k_full[st], C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(smem + C::OFF_K + st * C::TILE + c * kAtomBytes, &tk, &bars->k_full[st], c * 64, kvh, kv0, r);
+          tma_load_rows(smem + C::OFF_K + st * C::TILE + c * kAtomBytes, &tk, &bars->k_full[st], p, c, r, kvh, p.hk, kv0);
         mbar_arrive_expect_tx(&bars->v_full[st], C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_4d(smem + C::OFF_V + st * C::TILE + c * kAtomBytes, &tv, &bars->v_full[st], c * 64, kvh, kv0, r);
+          tma_load_rows(smem + C::OFF_V + st * C::TILE + c * kAtomBytes, &tv, &bars->v_full[st], p, c, r, kvh, p.hk, kv0);
         issued = n + 1;
       }
       // Never leave the CTA with copies still landing in its shared memory.
@@ -322,8 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && (ok = mbar_wait(&bars->o_final[q], 0, abort, p.status))) {
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = out.o + (static_cast<size_t>(r) * p.BS + (row_ok ? t : 0)) * p.hq * D +
-                            static_cast<size_t>(j) * D;
+      __nv_bfloat16* orow = out.o + row_offset(p, r, j, p.hq, row_ok ? t : 0, D);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
@@ -362,9 +364,9 @@ static int run_fwd(const usp_attn_params& prm, const AttnArgs& a, const void* q,
                    void* o, float* lse, cudaStream_t st) {
   CUtensorMap tq, tk, tv;
   int rc;
-  if ((rc = make_head_tmap(&tq, q, a.P, a.BS, a.hq, D, kBM)) != USP_OK) return rc;
-  if ((rc = make_head_tmap(&tk, k, a.P, a.BS, a.hk, D, kBN)) != USP_OK) return rc;
-  if ((rc = make_head_tmap(&tv, v, a.P, a.BS, a.hk, D, kBN)) != USP_OK) return rc;
+  if ((rc = make_rows_tmap(&tq, q, a, a.hq, D, kBM)) != USP_OK) return rc;
+  if ((rc = make_rows_tmap(&tk, k, a, a.hk, D, kBN)) != USP_OK) return rc;
+  if ((rc = make_rows_tmap(&tv, v, a, a.hk, D, kBN)) != USP_OK) return rc;
   fwd::Out out{static_cast<__nv_bfloat16*>(o), lse, (a.BS + 2 * kBM - 1) / (2 * kBM)};
   const int smem = fwd::Cfg<D>::SMEM;
   if (cudaFuncSetAttribute(fwd::attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
@@ -394,6 +396,8 @@ int launch_attn_fwd(const usp_attn_params& prm, const void* q, const void* k, co
   a.n_docs = prm.n_docs;
   a.sinks = prm.sinks;
   a.status = status;
+  a.seq_io = prm.io_layout == USP_IO_SEQ ? 1 : 0;
+  a.Sl = prm.S / prm.P;
   if (prm.D == 128) return run_fwd<128>(prm, a, q, k, v, o, lse, st);
   return run_fwd<64>(prm, a, q, k, v, o, lse, st);
 }

@@ -5,6 +5,16 @@ the library in the order of the attention wrapper of huggingface/accelerate
 PR #4209: the q/k/v exchange (gather sequence, scatter heads), document
 boundaries from the gathered position_ids, attention over the gathered
 sequence, and the output exchange back; the backward swaps the exchanges.
+
+Two ways to run the exchanges:
+
+* fused (default when S/P is a multiple of 128): the attention kernels read
+  q/k/v/dO straight from the sequence shards and write O/dQ/dK/dV straight
+  back (``io_layout = USP_IO_SEQ``); the permutation happens in their TMA
+  loads and stores, so no exchange kernel runs;
+* explicit: ``usp_relayout_*`` kernels move the tensors between the shard
+  layout and the head layout around head-layout attention.
+
 torch only allocates the buffers and supplies the stream; every step runs in
 the library's kernels.
 """
@@ -38,21 +48,31 @@ class Shape:
     def hk(self):
         return self.Hkv // self.P
 
+    @property
+    def can_fuse(self) -> bool:
+        return (self.S // self.P) % 128 == 0
+
 
 class UlyssesAttention:
     """Buffers and calls for one shape on one device."""
 
-    def __init__(self, shape: Shape, device="cuda", with_backward: bool = True):
+    def __init__(self, shape: Shape, device="cuda", with_backward: bool = True, fused: Optional[bool] = None):
         s = self.shape = shape
+        self.fused = shape.can_fuse if fused is None else bool(fused)
+        if self.fused and not shape.can_fuse:
+            raise ValueError("fused exchanges need S/P to be a multiple of 128")
         dev = torch.device(device)
         bf = torch.bfloat16
         P, Bb, S, D = s.P, s.B, s.S, s.D
-        self.q_head = torch.empty((P, Bb, S, s.hq, D), dtype=bf, device=dev)
-        self.k_head = torch.empty((P, Bb, S, s.hk, D), dtype=bf, device=dev)
-        self.v_head = torch.empty((P, Bb, S, s.hk, D), dtype=bf, device=dev)
-        self.o_head = torch.empty((P, Bb, S, s.hq, D), dtype=bf, device=dev)
+        seq_q = (P, Bb, S // P, s.Hq, D)
+        seq_kv = (P, Bb, S // P, s.Hkv, D)
+        if not self.fused:
+            self.q_head = torch.empty((P, Bb, S, s.hq, D), dtype=bf, device=dev)
+            self.k_head = torch.empty((P, Bb, S, s.hk, D), dtype=bf, device=dev)
+            self.v_head = torch.empty((P, Bb, S, s.hk, D), dtype=bf, device=dev)
+            self.o_head = torch.empty((P, Bb, S, s.hq, D), dtype=bf, device=dev)
         self.lse = torch.empty((P, Bb, s.hq, S), dtype=torch.float32, device=dev)
-        self.o_seq = torch.empty((P, Bb, S // P, s.Hq, D), dtype=bf, device=dev)
+        self.o_seq = torch.empty(seq_q, dtype=bf, device=dev)
         self.cu_seqlens = torch.empty((Bb * S + 1,), dtype=torch.int32, device=dev)
         self.n_docs = torch.zeros((1,), dtype=torch.int32, device=dev)
         self.max_len = torch.zeros((1,), dtype=torch.int32, device=dev)
@@ -61,26 +81,39 @@ class UlyssesAttention:
         self.scan_ws = torch.empty((ws,), dtype=torch.uint8, device=dev)
         self.with_backward = with_backward
         if with_backward:
-            self.do_head = torch.empty_like(self.o_head)
-            self.dq_head = torch.empty_like(self.q_head)
-            self.dk_head = torch.empty_like(self.k_head)
-            self.dv_head = torch.empty_like(self.v_head)
-            self.dq_seq = torch.empty((P, Bb, S // P, s.Hq, D), dtype=bf, device=dev)
-            self.dk_seq = torch.empty((P, Bb, S // P, s.Hkv, D), dtype=bf, device=dev)
-            self.dv_seq = torch.empty((P, Bb, S // P, s.Hkv, D), dtype=bf, device=dev)
+            if not self.fused:
+                self.do_head = torch.empty((P, Bb, S, s.hq, D), dtype=bf, device=dev)
+                self.dq_head = torch.empty((P, Bb, S, s.hq, D), dtype=bf, device=dev)
+                self.dk_head = torch.empty((P, Bb, S, s.hk, D), dtype=bf, device=dev)
+                self.dv_head = torch.empty((P, Bb, S, s.hk, D), dtype=bf, device=dev)
+            self.dq_seq = torch.empty(seq_q, dtype=bf, device=dev)
+            self.dk_seq = torch.empty(seq_kv, dtype=bf, device=dev)
+            self.dv_seq = torch.empty(seq_kv, dtype=bf, device=dev)
             self.dsinks = torch.zeros((s.Hq,), dtype=torch.float32, device=dev)
         self._bwd_ws = None
+        self._inputs = None  # the forward's q/k/v as the attention kernels read them
 
     def params(self, sinks: Optional[torch.Tensor]) -> B_.AttnParams:
         s = self.shape
         return B_.attn_params(s.B, s.S, s.Hq, s.Hkv, s.D, s.P, self.cu_seqlens, self.n_docs, s.causal,
-                              s.window_left, s.softmax_scale, sinks)
+                              s.window_left, s.softmax_scale, sinks,
+                              B_.USP_IO_SEQ if self.fused else B_.USP_IO_HEAD)
+
+    def _ws(self, prm):
+        if self._bwd_ws is None:
+            n = B_.usp_attn_bwd_workspace_bytes(prm)
+            self._bwd_ws = torch.empty((max(n, 256),), dtype=torch.uint8, device=self.lse.device)
+        return self._bwd_ws
 
     # -- steps ---------------------------------------------------------------
     def exchange_qkv(self, q_seq, k_seq, v_seq, stream=None):
         s = self.shape
+        if self.fused:
+            self._inputs = (q_seq, k_seq, v_seq)
+            return
         B_.usp_relayout_fwd_qkv(q_seq, k_seq, v_seq, self.q_head, self.k_head, self.v_head,
                                 s.B, s.S, s.Hq, s.Hkv, s.D, s.P, stream)
+        self._inputs = (self.q_head, self.k_head, self.v_head)
 
     def boundaries(self, pos_shards, stream=None):
         s = self.shape
@@ -88,12 +121,14 @@ class UlyssesAttention:
                                             self.max_len, self.scan_ws, self.status, stream)
 
     def attention(self, sinks=None, stream=None):
-        B_.usp_attn_fwd(self.params(sinks), self.q_head, self.k_head, self.v_head, self.o_head, self.lse,
-                        self.status, stream)
+        q, k, v = self._inputs
+        out = self.o_seq if self.fused else self.o_head
+        B_.usp_attn_fwd(self.params(sinks), q, k, v, out, self.lse, self.status, stream)
 
     def exchange_out(self, stream=None):
         s = self.shape
-        B_.usp_relayout_bwd(self.o_head, self.o_seq, s.B, s.S, s.Hq, s.D, s.P, stream)
+        if not self.fused:
+            B_.usp_relayout_bwd(self.o_head, self.o_seq, s.B, s.S, s.Hq, s.D, s.P, stream)
 
     def forward(self, q_seq, k_seq, v_seq, pos_shards, sinks=None, stream=None):
         """Sequence shards in, sequence shards out (``self.o_seq``)."""
@@ -103,17 +138,48 @@ class UlyssesAttention:
         self.exchange_out(stream)
         return self.o_seq
 
-    def backward(self, do_seq, sinks=None, stream=None):
-        """dO shards in; dQ/dK/dV shards out (``self.dq_seq`` ...), dsinks."""
+    def backward_phases(self, do_seq, sinks=None, stream=None, marks=None):
+        """The backward as its separate library calls; `marks(i)` is called
+        between them (for timing): 0 before, 1 after the dO exchange, 2 after
+        the preprocess, 3 after dK/dV, 4 after dQ, 5 after the output exchanges."""
         s = self.shape
         prm = self.params(sinks)
-        if self._bwd_ws is None:
-            n = B_.usp_attn_bwd_workspace_bytes(prm)
-            self._bwd_ws = torch.empty((max(n, 256),), dtype=torch.uint8, device=self.o_head.device)
+        ws = self._ws(prm)
+        mark = marks or (lambda i: None)
+        q, k, v = self._inputs
+        mark(0)
+        if self.fused:
+            do, o, dq, dk, dv = do_seq, self.o_seq, self.dq_seq, self.dk_seq, self.dv_seq
+        else:
+            B_.usp_relayout_fwd(do_seq, self.do_head, s.B, s.S, s.Hq, s.D, s.P, stream)
+            do, o, dq, dk, dv = self.do_head, self.o_head, self.dq_head, self.dk_head, self.dv_head
+        mark(1)
+        B_.usp_attn_bwd_preprocess(prm, o, self.lse, do, self.dsinks if sinks is not None else None, ws,
+                                   self.status, stream)
+        mark(2)
+        B_.usp_attn_bwd_dkdv(prm, q, k, v, self.lse, do, dk, dv, ws, self.status, stream)
+        mark(3)
+        B_.usp_attn_bwd_dq(prm, q, k, v, self.lse, do, dq, ws, self.status, stream)
+        mark(4)
+        if not self.fused:
+            B_.usp_relayout_bwd(self.dq_head, self.dq_seq, s.B, s.S, s.Hq, s.D, s.P, stream)
+            B_.usp_relayout_bwd(self.dk_head, self.dk_seq, s.B, s.S, s.Hkv, s.D, s.P, stream)
+            B_.usp_relayout_bwd(self.dv_head, self.dv_seq, s.B, s.S, s.Hkv, s.D, s.P, stream)
+        mark(5)
+        return self.dq_seq, self.dk_seq, self.dv_seq
+
+    def backward(self, do_seq, sinks=None, stream=None):
+        """dO shards in; dQ/dK/dV shards out (``self.dq_seq`` ...), dsinks.
+        In explicit mode this is the single ``usp_attn_bwd`` call."""
+        if self.fused:
+            return self.backward_phases(do_seq, sinks, stream)
+        s = self.shape
+        prm = self.params(sinks)
+        ws = self._ws(prm)
+        q, k, v = self._inputs
         B_.usp_relayout_fwd(do_seq, self.do_head, s.B, s.S, s.Hq, s.D, s.P, stream)
-        B_.usp_attn_bwd(prm, self.q_head, self.k_head, self.v_head, self.o_head, self.lse, self.do_head,
-                        self.dq_head, self.dk_head, self.dv_head, self.dsinks if sinks is not None else None,
-                        self._bwd_ws, self.status, stream)
+        B_.usp_attn_bwd(prm, q, k, v, self.o_head, self.lse, self.do_head, self.dq_head, self.dk_head,
+                        self.dv_head, self.dsinks if sinks is not None else None, ws, self.status, stream)
         B_.usp_relayout_bwd(self.dq_head, self.dq_seq, s.B, s.S, s.Hq, s.D, s.P, stream)
         B_.usp_relayout_bwd(self.dk_head, self.dk_seq, s.B, s.S, s.Hkv, s.D, s.P, stream)
         B_.usp_relayout_bwd(self.dv_head, self.dv_seq, s.B, s.S, s.Hkv, s.D, s.P, stream)
