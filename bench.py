@@ -72,8 +72,10 @@ def attention_flops(w: W.Workload):
 def relayout_bytes(w: W.Workload):
     q = w.B * w.S * w.Hq * w.D * 2
     kv = w.B * w.S * w.Hkv * w.D * 2
-    # every exchange reads and writes each element once
-    return {"qkv": 2 * (q + 2 * kv), "o": 2 * q, "do": 2 * q, "dqkv": 2 * (q + 2 * kv)}
+    rep = max(1, w.P // w.Hkv)  # key/value heads replicated when there are fewer than ranks
+    # every exchange reads and writes each element once; a replicated head is
+    # written (forward) or read (backward) once per replica
+    return {"qkv": 2 * q + 2 * (kv + rep * kv), "o": 2 * q, "do": 2 * q, "dqkv": 2 * q + 2 * (rep * kv + kv)}
 
 
 def measured_peaks():

@@ -82,18 +82,31 @@ int usp_version(void);
  * P ranks' buffers).  accelerate PR #4209, the comment on the four
  * _SeqAllToAll.apply call sites: queries/keys/values go from the local
  * sequence chunk with all heads to the whole sequence with H/P heads, and the
- * output comes back as [batch, seq, heads/sp_size, head_dim] per rank.
+ * output comes back per rank as its sequence chunk with the heads of every rank.
  *
  *   usp_relayout_fwd:  x_head[r][b][r'*S/P + s'][j][d] = x_seq[r'][b][s'][r*H/P + j][d]
  *   usp_relayout_bwd:  x_seq[r'][b][s'][r*H/P + j][d]  = x_head[r][b][r'*S/P + s'][j][d]
  *
  * x_seq:  [P][B][S/P][H][D] elements of elem_bytes bytes (input of fwd, output of bwd)
  * x_head: [P][B][S][H/P][D]                          (output of fwd, input of bwd)
+ *
+ * Fewer heads than ranks (H < P, P a multiple of H; kv-head replication, a
+ * follow-up listed in PR #4209): every head is replicated on P/H ranks, rank r
+ * holding head r / (P/H), so x_head is [P][B][S][1][D] and
+ *   usp_relayout_fwd:  x_head[r][b][r'*S/P + s'][0][d] = x_seq[r'][b][s'][r / (P/H)][d]
+ *   usp_relayout_bwd:  x_seq[r'][b][s'][h][d] = sum over the P/H ranks r with r / (P/H) == h of
+ *                      x_head[r][b][r'*S/P + s'][0][d]
+ * (the exchange back of a gradient is the adjoint of the copy: the replicas'
+ * gradients add up).  The sum is taken in fp32 in rank order and rounded once;
+ * it is defined for bf16 only (elem_bytes 2, else USP_ERR_UNSUPPORTED).
+ *
  * The two buffers must not overlap.  Each contiguous run, (H/P)*D*elem_bytes
- * bytes, must be a multiple of 16 (USP_ERR_ALIGNMENT otherwise).
+ * bytes (D*elem_bytes when replicated), must be a multiple of 16
+ * (USP_ERR_ALIGNMENT otherwise).
  * Errors: USP_ERR_INVALID_ARG (null pointer, size <= 0, elem_bytes not 1/2/4/8),
- *         USP_ERR_INDIVISIBLE (H % P or S % P), USP_ERR_ALIGNMENT, USP_ERR_CUDA.
- * The result is a bit-exact copy of every element.
+ *         USP_ERR_INDIVISIBLE (S % P, or H % P when H >= P, or P % H when H < P),
+ *         USP_ERR_ALIGNMENT, USP_ERR_UNSUPPORTED, USP_ERR_CUDA.
+ * Apart from the replica sum the result is a bit-exact copy of every element.
  * ---------------------------------------------------------------------- */
 int usp_relayout_fwd(const void* x_seq, void* x_head, int B, int S, int H, int D, int P,
                      int elem_bytes, usp_stream_t stream);
@@ -101,8 +114,9 @@ int usp_relayout_bwd(const void* x_head, void* x_seq, int B, int S, int H, int D
                      int elem_bytes, usp_stream_t stream);
 
 /* Same permutation for three tensors in one launch: q (Hq heads) and k, v
- * (Hkv heads), all with head dim D.  Equivalent to three usp_relayout_fwd
- * calls; meant for the q/k/v exchange of one attention layer. */
+ * (Hkv heads, replicated when Hkv < P), all with head dim D.  Equivalent to
+ * three usp_relayout_fwd calls; meant for the q/k/v exchange of one attention
+ * layer.  Hq % P != 0 is USP_ERR_INDIVISIBLE (query heads are never replicated). */
 int usp_relayout_fwd_qkv(const void* q_seq, const void* k_seq, const void* v_seq,
                          void* q_head, void* k_head, void* v_head,
                          int B, int S, int Hq, int Hkv, int D, int P, int elem_bytes,
@@ -165,9 +179,9 @@ int usp_cu_seqlens_from_position_ids_noalloc(const int32_t* pos, int B, int S, i
  * logit z = sinks[r*hq + j] (not scaled; absent when sinks == NULL):
  *     LSE_t = ln( sum_u exp(s_tu) + exp(z) )
  *     O_t   = sum_u exp(s_tu - LSE_t) v_u
- * (softmax over the keys plus one value-less sink logit; accelerate PR #4209
- * gpt-oss finding: "attention sinks are one logit per head, so slice s_aux to
- * the heads each rank holds").
+ * (softmax over the keys plus one value-less sink logit; accelerate PR #4209,
+ * the gpt-oss finding: each head has a single sink logit, so after the exchange
+ * a rank uses the slice of the sinks for the heads it holds).
  * ---------------------------------------------------------------------- */
 typedef struct {
   int B, S, Hq, Hkv, D, P;   /* global sizes; D must be 64 or 128 */
@@ -195,7 +209,8 @@ enum { USP_IO_HEAD = 0, USP_IO_SEQ = 1 };
  *   outputs are then left unwritten).
  * Errors: USP_ERR_INVALID_ARG (also an unknown io_layout), USP_ERR_INDIVISIBLE,
  * USP_ERR_UNSUPPORTED (D not 64/128, window_left < -1, B*S >= 2^30 or
- * B*S*Hq >= 2^31, USP_IO_SEQ with (S/P) % 128 != 0), USP_ERR_ALIGNMENT, USP_ERR_CUDA. */
+ * B*S*Hq >= 2^31, Hq > 1024, USP_IO_SEQ with (S/P) % 128 != 0), USP_ERR_ALIGNMENT,
+ * USP_ERR_CUDA. */
 int usp_attn_fwd(const usp_attn_params* params, const void* q, const void* k, const void* v,
                  void* o, float* lse, int32_t* dev_status, usp_stream_t stream);
 

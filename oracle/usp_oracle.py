@@ -29,9 +29,13 @@ Everything here is the plain definition, written out in float64 with numpy:
   that function.
 * ``ulysses_fwd`` / ``ulysses_bwd``: the whole emulated P-rank path, and
   ``unsharded_fwd`` / ``unsharded_bwd``: the same attention run on the
-  unsharded tensors, the pages' correctness reference ("tested against an
-  unsharded forward/backward", PR #4209; the yunchang script compares against
+  unsharded tensors, the pages' correctness reference (PR #4209 checks the
+  sharded forward and backward against an unsharded run; the yunchang script compares against
   ``flash_attn_func`` on the full tensors).
+
+With fewer key/value heads than ranks (P a multiple of Hkv), each key/value
+head is replicated on P/Hkv ranks and the exchange back of dK/dV sums the
+replicas (kv-head replication, a follow-up listed in PR #4209).
 
 Readings where the pages are silent (each is listed in the design notes):
 the softmax scale defaults to 1/sqrt(D) (``flash_attn_func`` is called with no
@@ -72,16 +76,21 @@ class OracleError(ValueError):
 # _gather_heads_scatter_seq)
 # ---------------------------------------------------------------------------
 
-def _check_divisible(S: int, H: int, P: int) -> None:
-    # The torch backend refuses an sp_size that does not divide the heads
+def _check_divisible(S: int, H: int, P: int, replicate: bool = False) -> None:
+    # The torch backend refuses an sp size that does not divide the heads
     # (accelerate PR #4209, "What does this PR do?", the list under "How").
-    if P <= 0 or H % P != 0:
+    # Key/value heads fewer than the ranks are replicated instead when the
+    # ranks are a multiple of them (the kv-head replication the same PR lists
+    # as a follow-up).
+    if P <= 0:
+        raise OracleError("sp size must be positive")
+    if H % P != 0 and not (replicate and H < P and P % H == 0):
         raise OracleError(f"sp size {P} does not divide {H} heads")
     if S % P != 0:
         raise OracleError(f"sp size {P} does not divide sequence length {S}")
 
 
-def relayout_fwd(x_seq: np.ndarray, P: int) -> np.ndarray:
+def relayout_fwd(x_seq: np.ndarray, P: int, replicate: bool = False) -> np.ndarray:
     """Gather the sequence, scatter the heads.
 
     ``x_seq`` is ``[P][B][S/P][H][D]``: rank r' holds positions
@@ -93,29 +102,54 @@ def relayout_fwd(x_seq: np.ndarray, P: int) -> np.ndarray:
 
     Written as a reshape that names the two rank axes and a transpose that
     swaps them, which is that formula.
+
+    With ``replicate`` and fewer heads than ranks (H < P, P a multiple of H),
+    each head goes to the P/H ranks r with r // (P/H) equal to it, and every
+    rank holds one head::
+
+        out[r][b][r'*S/P + s'][0][d] = x_seq[r'][b][s'][r // (P/H)][d]
     """
     Px, B, Sl, H, D = x_seq.shape
     if Px != P:
         raise OracleError("leading axis must be the rank axis")
-    _check_divisible(Sl * P, H, P)
+    _check_divisible(Sl * P, H, P, replicate)
+    if H < P:
+        owner = np.arange(P) // (P // H)        # the head rank r receives
+        y = x_seq[:, :, :, owner, :]            # [r'][b][s'][r][d]
+        y = y.transpose(3, 1, 0, 2, 4)          # [r][b][r'][s'][d]
+        return np.ascontiguousarray(y).reshape(P, B, P * Sl, 1, D)
     Hp = H // P
     y = x_seq.reshape(P, B, Sl, P, Hp, D)       # [r'][b][s'][r][j][d]
     y = y.transpose(3, 1, 0, 2, 4, 5)           # [r][b][r'][s'][j][d]
     return np.ascontiguousarray(y).reshape(P, B, P * Sl, Hp, D)
 
 
-def relayout_bwd(x_head: np.ndarray, P: int) -> np.ndarray:
+def relayout_bwd(x_head: np.ndarray, P: int, heads: Optional[int] = None) -> np.ndarray:
     """Gather the heads, scatter the sequence: the inverse exchange.
 
     ``x_head`` is ``[P][B][S][H/P][D]``; the result is ``[P][B][S/P][H][D]``::
 
         out[r'][b][s'][r*H/P + j][d] = x_head[r][b][r'*S/P + s'][j][d]
+
+    With ``heads`` = H < P (replicated heads, one per rank) the exchange back
+    of a gradient is the adjoint of the replication: the replicas are summed::
+
+        out[r'][b][s'][h][d] = sum over r with r // (P/H) == h of x_head[r][b][r'*S/P + s'][0][d]
     """
     Px, B, S, Hp, D = x_head.shape
     if Px != P:
         raise OracleError("leading axis must be the rank axis")
-    _check_divisible(S, Hp * P, P)
+    H = Hp * P if heads is None else heads
+    _check_divisible(S, H, P, replicate=True)
     Sl = S // P
+    if H < P:
+        if Hp != 1:
+            raise OracleError("replicated heads hold one head per rank")
+        y = x_head.reshape(H, P // H, B, P, Sl, D).sum(axis=1)   # [h][b][r'][s'][d]
+        y = y.transpose(2, 1, 3, 0, 4)                           # [r'][b][s'][h][d]
+        return np.ascontiguousarray(y)
+    if H != Hp * P:
+        raise OracleError("head count does not match the head-layout tensor")
     y = x_head.reshape(P, B, P, Sl, Hp, D)      # [r][b][r'][s'][j][d]
     y = y.transpose(2, 1, 3, 0, 4, 5)           # [r'][b][s'][r][j][d]
     return np.ascontiguousarray(y).reshape(P, B, Sl, P * Hp, D)
@@ -429,7 +463,7 @@ def visible_pairs(cu_seqlens, causal: bool = True, window_left: int = -1) -> int
 # ---------------------------------------------------------------------------
 
 def _rank_sinks(sinks, r, hq):
-    # Sinks are one logit per head; after the exchange rank r holds heads
+    # Each head has a single sink logit; after the exchange rank r holds heads
     # [r*hq, (r+1)*hq), so it uses that slice (accelerate PR #4209, gpt-oss).
     return None if sinks is None else np.asarray(sinks, dtype=np.float64)[r * hq:(r + 1) * hq]
 
@@ -446,8 +480,9 @@ def ulysses_fwd(q_seq, k_seq, v_seq, pos_shards, causal=True, window_left=-1, sc
     P, B, Sl, Hq, D = q_seq.shape
     S = P * Sl
     qh = relayout_fwd(np.asarray(q_seq, np.float64), P)
-    kh = relayout_fwd(np.asarray(k_seq, np.float64), P)
-    vh = relayout_fwd(np.asarray(v_seq, np.float64), P)
+    # key/value heads fewer than the ranks are replicated (one per rank)
+    kh = relayout_fwd(np.asarray(k_seq, np.float64), P, replicate=True)
+    vh = relayout_fwd(np.asarray(v_seq, np.float64), P, replicate=True)
     cu, n, max_len = cu_seqlens_from_position_ids(pos_shards)
     hq, hk = Hq // P, kh.shape[3]
     o_head = np.empty((P, B, S, hq, D))
@@ -459,7 +494,7 @@ def ulysses_fwd(q_seq, k_seq, v_seq, pos_shards, causal=True, window_left=-1, sc
         o_head[r] = O.reshape(B, S, hq, D)
         lse[r] = L.reshape(hq, B, S).transpose(1, 0, 2)
     return dict(q_head=qh, k_head=kh, v_head=vh, cu_seqlens=cu, n_docs=n, max_len=max_len,
-                o_head=o_head, lse=lse, o_seq=relayout_bwd(o_head, P))
+                o_head=o_head, lse=lse, o_seq=relayout_bwd(o_head, P), Hkv=k_seq.shape[3])
 
 
 def ulysses_bwd(fwd: dict, do_seq, causal=True, window_left=-1, scale=None, sinks=None):
@@ -485,9 +520,11 @@ def ulysses_bwd(fwd: dict, do_seq, causal=True, window_left=-1, scale=None, sink
         dvh[r] = dv.reshape(B, S, hk, D)
         if ds is not None:
             dsinks[r * hq:(r + 1) * hq] = ds
+    Hkv = fwd.get("Hkv", hk * P)
+    # replicated key/value heads: the exchange back sums the replicas' gradients
     return dict(do_head=doh, dq_head=dqh, dk_head=dkh, dv_head=dvh, dsinks=dsinks,
-                dq_seq=relayout_bwd(dqh, P), dk_seq=relayout_bwd(dkh, P),
-                dv_seq=relayout_bwd(dvh, P))
+                dq_seq=relayout_bwd(dqh, P), dk_seq=relayout_bwd(dkh, P, Hkv),
+                dv_seq=relayout_bwd(dvh, P, Hkv))
 
 
 def _unshard(x_seq):

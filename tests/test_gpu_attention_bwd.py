@@ -7,7 +7,8 @@ import torch
 
 import oracle
 import usp_workloads as W
-from gpu_util import assert_close, built_lib, device_inputs, dsink_bound, head_values, modes, shape_of
+from gpu_util import (assert_close, built_lib, device_inputs, dsink_bound, half_ulp_bf16, head_values, modes,
+                      seq_head_values, shape_of)
 
 pytestmark = pytest.mark.gpu
 
@@ -39,6 +40,10 @@ SMALL = [
                seed=5),
     W.Workload("noncausal_d64", B=1, S=512, Hq=2, Hkv=1, D=64, P=1, causal=False, doc_mode="explicit",
                doc_lens=(100, 250, 162)),
+    # kv-head replication: more ranks than key/value heads
+    W.Workload("kv_rep_d64", B=1, S=512, Hq=8, Hkv=2, D=64, P=4, doc_mode="explicit", doc_lens=(200, 180, 132)),
+    W.Workload("mqa_rep_win_sink_d128", B=1, S=1024, Hq=8, Hkv=1, D=128, P=8, window_left=150, sinks=True,
+               doc_mode="explicit", doc_lens=(300, 1, 400, 323)),
 ]
 
 
@@ -52,8 +57,14 @@ def test_backward_full_parity_small(w, fused):
     f = oracle.ulysses_fwd(host["q"], host["k"], host["v"], host["pos"], w.causal, w.window_left, None, snk)
     g = oracle.ulysses_bwd(f, host["do"], w.causal, w.window_left, None, snk)
     assert_close("dq", ua.dq_seq.float().cpu().numpy(), g["dq_seq"])
-    assert_close("dk", ua.dk_seq.float().cpu().numpy(), g["dk_seq"])
-    assert_close("dv", ua.dv_seq.float().cpu().numpy(), g["dv_seq"])
+    sk = sv = None
+    if not fused and w.Hkv < w.P:
+        # replicated key/value heads, explicit exchange: each rank's partial
+        # dK/dV is stored in bf16 before the exchange back sums the replicas
+        sk = oracle.relayout_bwd(half_ulp_bf16(g["dk_head"]), w.P, w.Hkv)
+        sv = oracle.relayout_bwd(half_ulp_bf16(g["dv_head"]), w.P, w.Hkv)
+    assert_close("dk", ua.dk_seq.float().cpu().numpy(), g["dk_seq"], slack=sk)
+    assert_close("dv", ua.dv_seq.float().cpu().numpy(), g["dv_seq"], slack=sv)
     if snk is not None:
         got = ua.dsinks.cpu().numpy().astype(np.float64)
         bound = dsink_bound(f["lse"], snk, f["o_head"], g["do_head"], w.Hq // w.P)
@@ -62,11 +73,11 @@ def test_backward_full_parity_small(w, fused):
 
 
 def _rank_views(w, host, r):
-    hq, hk = w.Hq // w.P, w.Hkv // w.P
+    hq = w.Hq // w.P
     T = w.B * w.S
     qh = oracle.relayout_fwd(host["q"], w.P)[r].reshape(T, hq, w.D)
-    kh = oracle.relayout_fwd(host["k"], w.P)[r].reshape(T, hk, w.D)
-    vh = oracle.relayout_fwd(host["v"], w.P)[r].reshape(T, hk, w.D)
+    kh = oracle.relayout_fwd(host["k"], w.P, replicate=True)[r].reshape(T, -1, w.D)
+    vh = oracle.relayout_fwd(host["v"], w.P, replicate=True)[r].reshape(T, -1, w.D)
     doh = oracle.relayout_fwd(host["do"], w.P)[r].reshape(T, hq, w.D)
     cu, _, _ = oracle.cu_seqlens_from_position_ids(host["pos"])
     snk = None if host["sinks"] is None else host["sinks"][r * hq:(r + 1) * hq]
@@ -108,6 +119,33 @@ def test_backward_full_size_whole_groups(w, groups, fused):
             do_r = doh.reshape(1, w.B, w.S, hq, w.D)
             bound = dsink_bound(lse_r, snk, o_r, do_r, hq)[heads]
             assert np.all(np.abs(got - ds[heads]) <= bound), (np.abs(got - ds[heads]), bound)
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "explicit"])
+def test_backward_full_size_replicated_kv_head(fused):
+    """Sp size 16 over 8 key/value heads: one key/value head, held by two
+    ranks.  dQ of both ranks' query heads element by element; dK/dV of the
+    head equal the sum of the two ranks' partial gradients (each rank's
+    partial checked too in explicit mode, where it is a separate buffer)."""
+    w = W.LLAMA32K_P16
+    ua, dev, host = _fwd_bwd(w, fused)
+    rep, hq, h = w.P // w.Hkv, w.Hq // w.P, 5
+    dk_sum, dv_sum = 0.0, 0.0
+    sk, sv = 0.0, 0.0      # explicit exchange: the partials are rounded to bf16 before the sum
+    for r in range(h * rep, (h + 1) * rep):
+        qh, kh, vh, doh, cu, snk = _rank_views(w, host, r)
+        O, L = oracle.attention_fwd(qh, kh, vh, cu, w.causal, w.window_left, None, snk)
+        dq, dk, dv, _ = oracle.attention_bwd(qh, kh, vh, O, L, doh, cu, w.causal, w.window_left, None, snk)
+        assert_close(f"dq r{r}", _gpu_head(ua, "dq", w, r, hq), dq)
+        if not fused:
+            assert_close(f"dk partial r{r}", ua.dk_head[r].reshape(-1, w.D).double().cpu().numpy(), dk[:, 0])
+            assert_close(f"dv partial r{r}", ua.dv_head[r].reshape(-1, w.D).double().cpu().numpy(), dv[:, 0])
+        dk_sum = dk_sum + dk[:, 0]
+        dv_sum = dv_sum + dv[:, 0]
+        sk = sk + half_ulp_bf16(dk[:, 0])
+        sv = sv + half_ulp_bf16(dv[:, 0])
+    assert_close(f"dk head {h}", seq_head_values(ua.dk_seq, h), dk_sum, slack=None if fused else sk)
+    assert_close(f"dv head {h}", seq_head_values(ua.dv_seq, h), dv_sum, slack=None if fused else sv)
 
 
 @pytest.mark.parametrize("w", [W.GPTOSS_FULL, W.LONG128K], ids=lambda w: w.name)

@@ -30,10 +30,10 @@ def _forward(w, fused=False):
 
 def _oracle_rank_head(w, host, ua, r, j):
     """fp64 O [T][D] and LSE [T] of rank r, local head j, from the oracle alone."""
-    hq, hk = w.Hq // w.P, w.Hkv // w.P
+    hq = w.Hq // w.P
     qh = oracle.relayout_fwd(host["q"], w.P)[r].reshape(w.B * w.S, hq, w.D)
-    kh = oracle.relayout_fwd(host["k"], w.P)[r].reshape(w.B * w.S, hk, w.D)
-    vh = oracle.relayout_fwd(host["v"], w.P)[r].reshape(w.B * w.S, hk, w.D)
+    kh = oracle.relayout_fwd(host["k"], w.P, replicate=True)[r].reshape(w.B * w.S, -1, w.D)
+    vh = oracle.relayout_fwd(host["v"], w.P, replicate=True)[r].reshape(w.B * w.S, -1, w.D)
     cu, _, _ = oracle.cu_seqlens_from_position_ids(host["pos"])
     snk = None if host["sinks"] is None else host["sinks"][r * hq:(r + 1) * hq]
     O, L = oracle.attention_fwd(qh, kh, vh, cu, w.causal, w.window_left, None, snk, heads=[j])
@@ -57,6 +57,10 @@ SMALL = [
                seed=5),
     W.Workload("noncausal_d64", B=1, S=512, Hq=2, Hkv=1, D=64, P=1, causal=False, doc_mode="explicit",
                doc_lens=(100, 250, 162)),
+    # kv-head replication: more ranks than key/value heads
+    W.Workload("kv_rep_d64", B=1, S=512, Hq=8, Hkv=2, D=64, P=4, doc_mode="explicit", doc_lens=(200, 180, 132)),
+    W.Workload("mqa_rep_win_sink_d128", B=1, S=1024, Hq=8, Hkv=1, D=128, P=8, window_left=150, sinks=True,
+               doc_mode="explicit", doc_lens=(300, 1, 400, 323)),
 ]
 
 
@@ -79,7 +83,10 @@ def test_forward_full_parity_small(w, fused):
     (W.GPTOSS_FULL, [(2, 1), (6, 6)], False),
     (W.LLAMA32K, [(0, 0), (5, 3), (7, 2)], True),
     (W.LLAMA32K, [(1, 1)], False),
-], ids=["gptoss_win-fused", "gptoss_full-explicit", "llama32k-fused", "llama32k-explicit"])
+    (W.LLAMA32K_P16, [(0, 0), (9, 1), (15, 1)], True),
+    (W.LLAMA32K_P16, [(6, 1)], False),
+], ids=["gptoss_win-fused", "gptoss_full-explicit", "llama32k-fused", "llama32k-explicit", "llama32k_p16-fused",
+        "llama32k_p16-explicit"])
 def test_forward_full_size_sampled_heads(w, pairs, fused):
     ua, dev, host = _forward(w, fused)
     for r, j in pairs:
@@ -108,7 +115,7 @@ def test_forward_long_context_sampled_rows():
 def test_stale_per_shard_cu_seqlens_are_flagged():
     """The per-shard boundaries a collator computes describe S/P tokens; the
     kernel runs on the gathered S (accelerate PR #4209: 41.8% of logits
-    mismatched and nothing raised).  Here the device check reports it."""
+    were wrong, silently).  Here the device check reports it."""
     from ulysses_sequence_long_gb300 import binding as B
     w = W.TINY
     ua, dev, host = _forward(w)
@@ -125,7 +132,11 @@ def test_attention_refuses_indivisible_heads():
     from ulysses_sequence_long_gb300 import binding as B
     from ulysses_sequence_long_gb300.pipeline import Shape, UlyssesAttention
     ua = UlyssesAttention(Shape(B=1, S=256, Hq=4, Hkv=2, D=64, P=2), with_backward=False, fused=False)
-    prm = B.attn_params(1, 256, 4, 2, 64, 4, ua.cu_seqlens, ua.n_docs)   # P=4 does not divide Hkv=2
+    prm = B.attn_params(1, 256, 4, 2, 64, 8, ua.cu_seqlens, ua.n_docs)   # P=8 does not divide Hq=4
+    with pytest.raises(B.UspError) as e:
+        B.usp_attn_fwd(prm, ua.q_head, ua.k_head, ua.v_head, ua.o_head, ua.lse)
+    assert e.value.code == B.USP_ERR_INDIVISIBLE
+    prm = B.attn_params(1, 256, 12, 3, 64, 4, ua.cu_seqlens, ua.n_docs)  # 3 kv heads cannot replicate over 4 ranks
     with pytest.raises(B.UspError) as e:
         B.usp_attn_fwd(prm, ua.q_head, ua.k_head, ua.v_head, ua.o_head, ua.lse)
     assert e.value.code == B.USP_ERR_INDIVISIBLE

@@ -67,6 +67,44 @@ def test_relayout_ragged_shapes(P, B, S, H, D):
     assert np.array_equal(_bits(y), oracle.relayout_fwd(_bits(x), P))
 
 
+@pytest.mark.parametrize("P,S,H,D", [(4, 512, 2, 64), (8, 1024, 1, 128), (16, 32768, 8, 128)])
+def test_relayout_replicated_heads(P, S, H, D):
+    """Fewer heads than ranks: the exchange copies head r // (P/H) to rank r
+    (bit-exact), and the exchange back sums the replicas in fp32, rounded
+    once to bf16."""
+    from ulysses_sequence_long_gb300 import binding as B
+    g = torch.Generator(device="cpu").manual_seed(P * 7 + H)
+    x = torch.randn((P, 1, S // P, H, D), generator=g).to(torch.bfloat16)
+    y = torch.empty((P, 1, S, 1, D), dtype=torch.bfloat16, device="cuda")
+    B.usp_relayout_fwd(x.cuda(), y, 1, S, H, D, P)
+    gy = torch.randn((P, 1, S, 1, D), generator=g).to(torch.bfloat16)
+    z = torch.empty((P, 1, S // P, H, D), dtype=torch.bfloat16, device="cuda")
+    B.usp_relayout_bwd(gy.cuda(), z, 1, S, H, D, P)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(y), oracle.relayout_fwd(_bits(x), P, replicate=True))
+    want = oracle.relayout_bwd(W.bf16_to_f64(gy), P, H)
+    got = z.double().cpu().numpy()
+    # fp32 sum of P/H bf16 values, one rounding to bf16: within half an ulp
+    # of bf16 at the exact sum (plus the fp32 rounding of the sum)
+    a = np.maximum(np.abs(want), 2.0 ** -126)
+    half_ulp = np.ldexp(1.0, np.floor(np.log2(a)).astype(np.int64) - 8)
+    assert np.all(np.abs(got - want) <= half_ulp * (1 + 2.0 ** -6)), float(np.max(np.abs(got - want) / half_ulp))
+
+
+def test_relayout_qkv_replicated_kv():
+    from ulysses_sequence_long_gb300 import binding as B
+    w = W.LLAMA32K_P16
+    t = W.qkv_do_shards(w, names=("q", "k", "v"))
+    d = {n: x.cuda() for n, x in t.items()}
+    heads = {n: torch.empty((w.P, w.B, w.S, w.Hq // w.P if n == "q" else 1, w.D), dtype=torch.bfloat16,
+                            device="cuda") for n in d}
+    B.usp_relayout_fwd_qkv(d["q"], d["k"], d["v"], heads["q"], heads["k"], heads["v"],
+                           w.B, w.S, w.Hq, w.Hkv, w.D, w.P)
+    torch.cuda.synchronize()
+    for n in ("q", "k", "v"):
+        assert np.array_equal(_bits(heads[n]), oracle.relayout_fwd(_bits(t[n]), w.P, replicate=(n != "q"))), n
+
+
 def test_relayout_refusals():
     from ulysses_sequence_long_gb300 import binding as B
     x = torch.zeros((4, 1, 4, 6, 8), dtype=torch.bfloat16, device="cuda")
@@ -81,6 +119,16 @@ def test_relayout_refusals():
     assert e.value.code == B.USP_ERR_ALIGNMENT
     with pytest.raises(TypeError):
         B.usp_relayout_fwd(x.cpu(), y, 1, 16, 6, 8, 4)  # no CPU path
+    x3 = torch.zeros((4, 1, 4, 3, 8), dtype=torch.bfloat16, device="cuda")
+    y3 = torch.zeros((4, 1, 16, 1, 8), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(B.UspError) as e:
+        B.usp_relayout_fwd(x3, y3, 1, 16, 3, 8, 4)      # 3 heads cannot be replicated over 4 ranks
+    assert e.value.code == B.USP_ERR_INDIVISIBLE
+    x4 = torch.zeros((4, 1, 4, 2, 8), dtype=torch.float32, device="cuda")
+    y4 = torch.zeros((4, 1, 16, 1, 8), dtype=torch.float32, device="cuda")
+    with pytest.raises(B.UspError) as e:
+        B.usp_relayout_bwd(y4, x4, 1, 16, 2, 8, 4)      # summing replicas is defined for bf16 only
+    assert e.value.code == B.USP_ERR_UNSUPPORTED
 
 
 # ------------------------------------------------------------------ cu_seqlens

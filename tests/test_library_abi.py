@@ -51,7 +51,9 @@ def test_host_checks_without_gpu(lib):
     assert lib.usp_cu_seqlens_workspace_bytes(1, 4096) >= 16
     prm = B.AttnParams(1, 256, 4, 2, 96, 2, 1, -1, 0.0, 16, 16, None)
     assert lib.usp_attn_fwd(ctypes.byref(prm), p, p, p, p, p, None, None) == B.USP_ERR_UNSUPPORTED
-    prm = B.AttnParams(1, 256, 4, 2, 64, 4, 1, -1, 0.0, 16, 16, None)
+    prm = B.AttnParams(1, 256, 4, 2, 64, 8, 1, -1, 0.0, 16, 16, None)   # 8 ranks, 4 query heads
+    assert lib.usp_attn_fwd(ctypes.byref(prm), p, p, p, p, p, None, None) == B.USP_ERR_INDIVISIBLE
+    prm = B.AttnParams(1, 258, 6, 2, 64, 3, 1, -1, 0.0, 16, 16, None)   # 2 kv heads cannot replicate over 3 ranks
     assert lib.usp_attn_fwd(ctypes.byref(prm), p, p, p, p, p, None, None) == B.USP_ERR_INDIVISIBLE
     prm = B.AttnParams(1, 256, 4, 2, 64, 2, 1, -5, 0.0, 16, 16, None)
     assert lib.usp_attn_fwd(ctypes.byref(prm), p, p, p, p, p, None, None) == B.USP_ERR_UNSUPPORTED

@@ -89,6 +89,41 @@ def test_relayout_refuses_indivisible_heads():
     # "sp_size not dividing the heads" is refused (accelerate PR #4209)
     with pytest.raises(oracle.OracleError):
         oracle.relayout_fwd(np.zeros((4, 1, 2, 6, 2)), 4)
+    # fewer heads than ranks are replicated only when asked and when P is a multiple of H
+    with pytest.raises(oracle.OracleError):
+        oracle.relayout_fwd(np.zeros((4, 1, 2, 2, 2)), 4)
+    with pytest.raises(oracle.OracleError):
+        oracle.relayout_fwd(np.zeros((4, 1, 2, 3, 2)), 4, replicate=True)
+
+
+@pytest.mark.parametrize("P,B,S,H,D", [(4, 1, 8, 2, 3), (4, 2, 8, 1, 2), (8, 1, 16, 2, 1)])
+def test_relayout_replicated_rank_holds_a_copy_of_its_head(P, B, S, H, D):
+    x = _encoded_seq_tensor(P, B, S, H, D)
+    y = oracle.relayout_fwd(x, P, replicate=True)
+    assert y.shape == (P, B, S, 1, D)
+    rep = P // H
+    for r in range(P):
+        for b in range(B):
+            for pos in range(S):
+                for d in range(D):
+                    # rank r sees every position of row b, and head r // (P/H)
+                    assert _decode(int(y[r, b, pos, 0, d]), S, H, D) == (b, pos, r // rep, d)
+
+
+@pytest.mark.parametrize("P,H", [(4, 2), (4, 1), (8, 2)])
+def test_relayout_replicated_bwd_is_the_adjoint_of_fwd(P, H):
+    # The exchange back of a gradient must be the adjoint (transpose) of the
+    # forward exchange: <fwd(x), y> = <x, bwd(y)> for all x, y.  For a copy to
+    # P/H ranks that is the sum over the replicas.
+    B, S, D = 2, 8, 3
+    x = _rng(21).standard_normal((P, B, S // P, H, D))
+    y = _rng(22).standard_normal((P, B, S, 1, D))
+    lhs = float(np.sum(oracle.relayout_fwd(x, P, replicate=True) * y))
+    rhs = float(np.sum(x * oracle.relayout_bwd(y, P, H)))
+    assert abs(lhs - rhs) <= 1e-12 * max(1.0, abs(lhs))
+    # a gradient that is the same on every replica comes back P/H times
+    xi = _rng(23).integers(-100, 100, size=(P, B, S // P, H, D)).astype(np.float64)
+    assert np.array_equal(oracle.relayout_bwd(oracle.relayout_fwd(xi, P, replicate=True), P, H), (P // H) * xi)
 
 
 # ---------------------------------------------------------------------------
@@ -364,6 +399,10 @@ def _small_workload_tensors(w):
     W.Workload("gqa_p4", B=1, S=64, Hq=8, Hkv=4, D=16, P=4, doc_mode="explicit", doc_lens=(5, 40, 19)),
     W.Workload("sink_win_p2", B=2, S=32, Hq=4, Hkv=2, D=8, P=2, window_left=6, sinks=True,
                doc_mode="explicit", doc_lens=(20, 12)),
+    # kv-head replication: fewer key/value heads than ranks
+    W.Workload("kv_rep_p4", B=1, S=64, Hq=8, Hkv=2, D=8, P=4, doc_mode="explicit", doc_lens=(30, 34)),
+    W.Workload("mqa_rep_sink_win_p4", B=1, S=48, Hq=4, Hkv=1, D=8, P=4, window_left=9, sinks=True,
+               doc_mode="explicit", doc_lens=(7, 41)),
 ], ids=lambda w: w.name)
 def test_ulysses_equals_unsharded(w):
     x = _small_workload_tensors(w)

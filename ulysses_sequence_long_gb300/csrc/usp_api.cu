@@ -97,19 +97,26 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int check_relayout_args(const void* a, const void* b, int B, int S, int H, int D, int P, int eb) {
+// H % P == 0: H/P heads per rank.  H < P with P % H == 0: every head is
+// replicated on P/H ranks (the head-layout tensor is P/H times larger); the
+// exchange back then sums the replicas, which needs bf16 elements.
+int check_relayout_args(const void* a, const void* b, int B, int S, int H, int D, int P, int eb, bool to_head) {
   if (a == nullptr || b == nullptr) return USP_ERR_INVALID_ARG;
   if (B <= 0 || S <= 0 || H <= 0 || D <= 0 || P <= 0) return USP_ERR_INVALID_ARG;
   if (eb != 1 && eb != 2 && eb != 4 && eb != 8) return USP_ERR_INVALID_ARG;
-  if (H % P != 0 || S % P != 0) return USP_ERR_INDIVISIBLE;
-  uint64_t run = static_cast<uint64_t>(H / P) * D * eb;
+  const bool replicated = H < P;
+  if ((replicated ? P % H : H % P) != 0 || S % P != 0) return USP_ERR_INDIVISIBLE;
+  if (replicated && !to_head && eb != 2) return USP_ERR_UNSUPPORTED;
+  const uint64_t hpr = replicated ? 1 : static_cast<uint64_t>(H / P);
+  uint64_t run = hpr * D * eb;
   if (run % 16 != 0 || !aligned16(a) || !aligned16(b)) return USP_ERR_ALIGNMENT;
-  uint64_t vec = static_cast<uint64_t>(B) * S * H * D * eb / 16;
-  if (vec >= (1ull << 32) || static_cast<uint64_t>(P) * B * S >= (1ull << 32)) return USP_ERR_UNSUPPORTED;
+  uint64_t seq_vec = static_cast<uint64_t>(B) * S * H * D * eb / 16;
+  uint64_t head_vec = static_cast<uint64_t>(P) * B * S * hpr * D * eb / 16;
+  if (head_vec >= (1ull << 32) || static_cast<uint64_t>(P) * B * S >= (1ull << 32)) return USP_ERR_UNSUPPORTED;
   const char* pa = static_cast<const char*>(a);
   const char* pb = static_cast<const char*>(b);
-  uint64_t bytes = vec * 16;
-  if (pa < pb + bytes && pb < pa + bytes) return USP_ERR_INVALID_ARG;  // buffers overlap
+  const uint64_t bytes_a = (to_head ? seq_vec : head_vec) * 16, bytes_b = (to_head ? head_vec : seq_vec) * 16;
+  if (pa < pb + bytes_b && pb < pa + bytes_a) return USP_ERR_INVALID_ARG;  // buffers overlap
   return USP_OK;
 }
 
@@ -120,12 +127,15 @@ int check_attn_params(const usp_attn_params* p) {
   if (p->causal != 0 && p->causal != 1) return USP_ERR_INVALID_ARG;
   if (p->window_left < -1) return USP_ERR_UNSUPPORTED;
   if (!(p->softmax_scale >= 0.f) || isinf(p->softmax_scale)) return USP_ERR_INVALID_ARG;
-  if (p->Hq % p->P != 0 || p->Hkv % p->P != 0 || p->Hq % p->Hkv != 0 || p->S % p->P != 0)
-    return USP_ERR_INDIVISIBLE;
+  // query heads split over the ranks; key/value heads either split too or,
+  // when there are fewer of them than ranks, are replicated P/Hkv times
+  if (p->Hq % p->P != 0 || p->Hq % p->Hkv != 0 || p->S % p->P != 0) return USP_ERR_INDIVISIBLE;
+  if (p->Hkv >= p->P ? p->Hkv % p->P != 0 : p->P % p->Hkv != 0) return USP_ERR_INDIVISIBLE;
   if (p->D != 64 && p->D != 128) return USP_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(p->B) * p->S >= (1ll << 30)) return USP_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(p->P) * p->B * p->S * p->Hq * p->D >= (1ll << 40)) return USP_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(p->B) * p->S * p->Hq >= (1ll << 31)) return USP_ERR_UNSUPPORTED;  // 32-bit row counters
+  if (p->Hq > 1024) return USP_ERR_UNSUPPORTED;  // the preprocess stages 32 tokens x Hq row sums in shared memory
   if (p->io_layout != USP_IO_HEAD && p->io_layout != USP_IO_SEQ) return USP_ERR_INVALID_ARG;
   // fused exchanges: tiles of 128 tokens must never straddle a rank's shard
   if (p->io_layout == USP_IO_SEQ && (p->S / p->P) % 128 != 0) return USP_ERR_UNSUPPORTED;
@@ -156,14 +166,14 @@ int usp_version(void) { return 100; }
 
 int usp_relayout_fwd(const void* x_seq, void* x_head, int B, int S, int H, int D, int P, int eb,
                      usp_stream_t stream) {
-  int rc = check_relayout_args(x_seq, x_head, B, S, H, D, P, eb);
+  int rc = check_relayout_args(x_seq, x_head, B, S, H, D, P, eb, true);
   if (rc != USP_OK) return rc;
   return launch_relayout(x_seq, x_head, B, S, H, D, P, eb, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int usp_relayout_bwd(const void* x_head, void* x_seq, int B, int S, int H, int D, int P, int eb,
                      usp_stream_t stream) {
-  int rc = check_relayout_args(x_head, x_seq, B, S, H, D, P, eb);
+  int rc = check_relayout_args(x_head, x_seq, B, S, H, D, P, eb, false);
   if (rc != USP_OK) return rc;
   return launch_relayout(x_head, x_seq, B, S, H, D, P, eb, false, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -171,9 +181,10 @@ int usp_relayout_bwd(const void* x_head, void* x_seq, int B, int S, int H, int D
 int usp_relayout_fwd_qkv(const void* q_seq, const void* k_seq, const void* v_seq, void* q_head, void* k_head,
                          void* v_head, int B, int S, int Hq, int Hkv, int D, int P, int eb, usp_stream_t stream) {
   int rc;
-  if ((rc = check_relayout_args(q_seq, q_head, B, S, Hq, D, P, eb)) != USP_OK) return rc;
-  if ((rc = check_relayout_args(k_seq, k_head, B, S, Hkv, D, P, eb)) != USP_OK) return rc;
-  if ((rc = check_relayout_args(v_seq, v_head, B, S, Hkv, D, P, eb)) != USP_OK) return rc;
+  if (Hq % P != 0) return USP_ERR_INDIVISIBLE;  // query heads are never replicated
+  if ((rc = check_relayout_args(q_seq, q_head, B, S, Hq, D, P, eb, true)) != USP_OK) return rc;
+  if ((rc = check_relayout_args(k_seq, k_head, B, S, Hkv, D, P, eb, true)) != USP_OK) return rc;
+  if ((rc = check_relayout_args(v_seq, v_head, B, S, Hkv, D, P, eb, true)) != USP_OK) return rc;
   const void* src[3] = {q_seq, k_seq, v_seq};
   void* dst[3] = {q_head, k_head, v_head};
   int H[3] = {Hq, Hkv, Hkv};

@@ -59,35 +59,67 @@ __device__ __forceinline__ size_t plane_index(int bsp, int hq, int r, int j, int
 }
 
 // --------------------------------------------------------------- preprocess
-// One row = D bf16 = D/8 lanes of 16 bytes.  Rows are taken in statistics
-// order (rank, local head, token), so the LSE reads and the D/LSE writes are
-// contiguous; each row's D-vector is one contiguous run in either layout.
+// A block takes a chunk of kPreTok consecutive tokens with every head stored
+// next to them (seq-layout: all H heads of the shard; head-layout: the hq
+// heads of one rank), so its O/dO reads are one contiguous run.  Row sums go
+// to shared memory, then each head's kPreTok statistics are written (and its
+// LSE read) as one contiguous 128-byte run.
+constexpr int kPreTok = 32;
+
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
                                                          const float* __restrict__ lse, float* __restrict__ stats,
-                                                         AttnArgs p, int bsp, uint32_t n_rows) {
-  constexpr int LPR = D / 8;  // lanes per row
-  const uint32_t lane_row = threadIdx.x % LPR;
-  for (uint32_t row = (blockIdx.x * blockDim.x + threadIdx.x) / LPR; row < n_rows + (32 / LPR);
-       row += gridDim.x * blockDim.x / LPR) {
-    const bool ok = row < n_rows;
-    const uint32_t rj = ok ? row / p.BS : 0, t = ok ? row - rj * p.BS : 0;
-    const int r = static_cast<int>(rj) / p.hq, j = static_cast<int>(rj) - r * p.hq;
-    float acc = 0.f;
-    if (ok) {
-      const size_t base = row_offset(p, r, j, p.hq, static_cast<int>(t), D) / 8;
-      const uint4 a = __ldg(o + base + lane_row);
-      const uint4 b = __ldg(dO + base + lane_row);
-      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc += bf16lo(av[e]) * bf16lo(bv[e]) + bf16hi(av[e]) * bf16hi(bv[e]);
+                                                         AttnArgs p, int bsp, int n_chunks) {
+  constexpr int LPR = D / 8;           // 16-byte lanes per row
+  constexpr int RPP = 256 / LPR;       // rows per pass of the block
+  extern __shared__ float dsum[];      // [Hb][kPreTok]
+  const int Hb = p.seq_io ? p.P * p.hq : p.hq;
+  const int tid = threadIdx.x, lane_row = tid % LPR;
+  const int nct = (p.BS + kPreTok - 1) / kPreTok;  // head-layout chunks per rank
+  for (int c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+    // chunk -> first token t0 (rank-local, b*S + s), its rank (head-layout) and
+    // the element offset of its first row
+    int r0 = 0, t0, ntok;
+    size_t base;
+    if (p.seq_io) {
+      const int g0 = c * kPreTok;                    // token index in memory order (shard, row, position)
+      const int rp = g0 / (p.B * p.Sl), rem = g0 - rp * p.B * p.Sl;
+      const int b = rem / p.Sl, sp = rem - b * p.Sl;
+      t0 = b * p.S + rp * p.Sl + sp;
+      ntok = kPreTok;                                // S/P is a multiple of 128
+      base = static_cast<size_t>(g0) * Hb * D;
+    } else {
+      r0 = c / nct;
+      t0 = (c - r0 * nct) * kPreTok;
+      ntok = min(kPreTok, p.BS - t0);
+      base = (static_cast<size_t>(r0) * p.BS + t0) * Hb * D;
     }
+    const int nrows = ntok * Hb;
+    for (int i0 = 0; i0 < nrows; i0 += RPP) {
+      const int i = i0 + tid / LPR;
+      float acc = 0.f;
+      if (i < nrows) {
+        const size_t e = (base + static_cast<size_t>(i) * D) / 8 + lane_row;
+        const uint4 a = __ldg(o + e);
+        const uint4 bq = __ldg(dO + e);
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {bq.x, bq.y, bq.z, bq.w};
 #pragma unroll
-    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (ok && lane_row == 0) {
-      stats[plane_index(bsp, p.hq, r, j, 0, t)] = __ldg(lse + stat_index(p, r, j, t)) * kLog2e;
-      stats[plane_index(bsp, p.hq, r, j, 1, t)] = acc;
+        for (int k = 0; k < 4; ++k) acc += bf16lo(av[k]) * bf16lo(bv[k]) + bf16hi(av[k]) * bf16hi(bv[k]);
+      }
+#pragma unroll
+      for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (i < nrows && lane_row == 0) dsum[(i % Hb) * kPreTok + i / Hb] = acc;
     }
+    __syncthreads();
+    for (int idx = tid; idx < Hb * kPreTok; idx += 256) {
+      const int h = idx / kPreTok, k = idx - h * kPreTok;
+      if (k < ntok) {
+        const int r = p.seq_io ? h / p.hq : r0, j = p.seq_io ? h - r * p.hq : h, t = t0 + k;
+        stats[plane_index(bsp, p.hq, r, j, 0, t)] = __ldg(lse + stat_index(p, r, j, t)) * kLog2e;
+        stats[plane_index(bsp, p.hq, r, j, 1, t)] = dsum[idx];
+      }
+    }
+    __syncthreads();
   }
 }
 
@@ -262,11 +294,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   BarsA* bars = reinterpret_cast<BarsA*>(smem + C::A_BAR);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // key tiles in order (early keys of a causal document see the most queries)
-  const int per = p.P * p.hk;
+  // key tiles in order (early keys of a causal document see the most queries).
+  // A CTA owns one key/value head: in head-layout the local head kl of rank r
+  // (its gradient sums that rank's G query heads; replicas of a head are
+  // summed by the exchange back), in seq-layout the global head, whose
+  // gradient sums the whole group of Hq/Hkv query heads over the ranks.
+  const int per = p.seq_io ? p.Hkv : p.P * p.hk;
   const int kt = static_cast<int>(blockIdx.x) / per;
-  const int rem = static_cast<int>(blockIdx.x) % per;
-  const int r = rem / p.hk, kh = rem % p.hk;
+  const int unit = static_cast<int>(blockIdx.x) % per;
+  const HeadRef kvh = p.seq_io ? HeadRef{0, 0, unit} : kv_head_ref(p, unit / p.hk, unit % p.hk);
+  const int n_heads = p.seq_io ? p.Hq / p.Hkv : p.G;
+  const int hg0 = p.seq_io ? unit * n_heads : kvh.r * p.hq + kvh.j * p.G;  // global index of the first query head
   const int u0 = kt * kBN;
 
   const int n_docs = checked_docs(p);
@@ -277,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // exchanges fused, 64-token slices must also stay inside one rank's shard
   qlo &= p.seq_io ? ~(kSL - 1) : ~3;
   const int n_q = (qhi - qlo + kSL - 1) / kSL;
-  const int n_it = p.G * n_q;
+  const int n_it = n_heads * n_q;
 
   if (tid == 0) {
     mbar_init(&bars->kv_ready, 8);
@@ -316,14 +354,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < n_it; ++i) {
         const int s = i % C::NST;
         if (i >= C::NST && !mbar_wait(&bars->qdo_empty[s], ((i / C::NST) - 1) & 1, abort, p.status)) break;
-        const int jq = kh * p.G + i / n_q;
+        const int hg = hg0 + i / n_q;
+        const HeadRef qh{hg / p.hq, hg % p.hq, hg};
         const int q0 = qlo + (i % n_q) * kSL;
         mbar_arrive_expect_tx(&bars->qdo_full[s], 2 * C::SLICE + C::STAT);
         for (int c = 0; c < C::NCH; ++c) {
-          tma_load_rows(smem + C::A_Q + s * C::SLICE + c * kSliceBytes, &tq, &bars->qdo_full[s], p, c, r, jq, p.hq, q0);
-          tma_load_rows(smem + C::A_DO + s * C::SLICE + c * kSliceBytes, &tdo, &bars->qdo_full[s], p, c, r, jq, p.hq, q0);
+          tma_load_rows(smem + C::A_Q + s * C::SLICE + c * kSliceBytes, &tq, &bars->qdo_full[s], p, c, qh, q0);
+          tma_load_rows(smem + C::A_DO + s * C::SLICE + c * kSliceBytes, &tdo, &bars->qdo_full[s], p, c, qh, q0);
         }
-        tma_load_3d(smem + C::A_STAT + s * C::STAT, &tst, &bars->qdo_full[s], q0, 0, r * p.hq + jq);
+        tma_load_3d(smem + C::A_STAT + s * C::STAT, &tst, &bars->qdo_full[s], q0, 0, hg);
         issued = i + 1;
       }
       for (int i = max(0, issued - C::NST); i < issued; ++i)
@@ -399,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lb = tmem + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
     // K (group 0) or V (group 1) row of this key into TMEM
     {
-      const size_t off = row_offset(p, r, kh, p.hk, key_ok ? u : 0, D);
+      const size_t off = row_offset(p, kvh, p.hk, p.Hkv, key_ok ? u : 0, D);
       row_to_tmem<D>(lb + (grp == 0 ? T_K : T_V), (grp == 0 ? g.k : g.v) + off, key_ok);
       tc_fence_before();
       __syncwarp();
@@ -455,13 +494,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && n_it > 0 && (ok = mbar_wait(&bars->fin, 0, abort, p.status))) {
       tc_fence_after();
-      const size_t off = row_offset(p, r, kh, p.hk, key_ok ? u : 0, D);
+      const size_t off = row_offset(p, kvh, p.hk, p.Hkv, key_ok ? u : 0, D);
       if (grp == 0)
         store_row<D>(lb + T_DV, g.dv + off, 1.f, key_ok);
       else
         store_row<D>(lb + T_DK, g.dk + off, p.scale, key_ok);
     } else if (ok && n_it == 0 && key_ok) {
-      __nv_bfloat16* dst = (grp == 0 ? g.dv : g.dk) + row_offset(p, r, kh, p.hk, u, D);
+      __nv_bfloat16* dst = (grp == 0 ? g.dv : g.dk) + row_offset(p, kvh, p.hk, p.Hkv, u, D);
       for (int e = 0; e < D; e += 8) *reinterpret_cast<uint4*>(dst + e) = make_uint4(0, 0, 0, 0);
     }
   }
@@ -495,7 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int per = p.P * p.hq;
   const int qt = g.n_tiles - 1 - static_cast<int>(blockIdx.x) / per;
   const int rem = static_cast<int>(blockIdx.x) % per;
-  const int r = rem / p.hq, j = rem % p.hq, kvh = j / p.G;
+  const int r = rem / p.hq, j = rem % p.hq;
+  const HeadRef qh = q_head_ref(p, r, j), kvh = kv_head_ref(p, r, j / p.G);
   const int t0 = qt * kBM;
 
   const int n_docs = checked_docs(p);
@@ -543,10 +583,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kv0 = lo + n * kBN;
         mbar_arrive_expect_tx(&bars->k_full[s], C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_rows(smem + C::B_K + s * C::TILE + c * kAtomBytes, &tk, &bars->k_full[s], p, c, r, kvh, p.hk, kv0);
+          tma_load_rows(smem + C::B_K + s * C::TILE + c * kAtomBytes, &tk, &bars->k_full[s], p, c, kvh, kv0);
         mbar_arrive_expect_tx(&bars->v_full[s], C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_rows(smem + C::B_V + s * C::TILE + c * kAtomBytes, &tv, &bars->v_full[s], p, c, r, kvh, p.hk, kv0);
+          tma_load_rows(smem + C::B_V + s * C::TILE + c * kAtomBytes, &tv, &bars->v_full[s], p, c, kvh, kv0);
         issued = n + 1;
       }
       for (int n = max(0, issued - C::KST); n < issued; ++n) {
@@ -610,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lb = tmem + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
     // Q (group 0) or dO (group 1) row into TMEM
     {
-      const size_t off = row_offset(p, r, j, p.hq, row_ok ? t : 0, D);
+      const size_t off = row_offset(p, qh, p.hq, p.Hq, row_ok ? t : 0, D);
       row_to_tmem<D>(lb + (grp == 0 ? T_Q : T_DO), (grp == 0 ? g.q : g.dO) + off, row_ok);
       tc_fence_before();
       __syncwarp();
@@ -654,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && n_kv > 0 && (ok = mbar_wait(&bars->fin, 0, abort, p.status))) {
       tc_fence_after();
-      __nv_bfloat16* dst = g.dq + row_offset(p, r, j, p.hq, row_ok ? t : 0, D) + grp * (D / 2);
+      __nv_bfloat16* dst = g.dq + row_offset(p, qh, p.hq, p.Hq, row_ok ? t : 0, D) + grp * (D / 2);
       store_row<D / 2>(lb + T_DQ + grp * (D / 2), dst, p.scale, row_ok);
     }
   }
@@ -684,8 +724,10 @@ static AttnArgs make_args(const usp_attn_params& prm, int32_t* status) {
   a.BS = prm.B * prm.S;
   a.P = prm.P;
   a.hq = prm.Hq / prm.P;
-  a.hk = prm.Hkv / prm.P;
-  a.G = prm.Hq / prm.Hkv;
+  a.hk = prm.Hkv >= prm.P ? prm.Hkv / prm.P : 1;
+  a.G = a.hq / a.hk;
+  a.Hq = prm.Hq;
+  a.Hkv = prm.Hkv;
   a.causal = prm.causal ? 1 : 0;
   a.window_left = prm.window_left;
   a.scale = prm.softmax_scale > 0.f ? prm.softmax_scale : 1.0f / sqrtf(static_cast<float>(prm.D));
@@ -705,16 +747,15 @@ int launch_attn_bwd_preprocess(const usp_attn_params& prm, const void* o, const 
   const AttnArgs a = make_args(prm, status);
   float* stats = static_cast<float*>(ws);
   const int bsp = stats_row_pitch(a.BS);
-  const uint32_t n_rows = static_cast<uint32_t>(static_cast<uint64_t>(a.P) * a.BS * a.hq);
-  const int per_block = 256 / (prm.D / 8);
-  int grid = static_cast<int>((n_rows + per_block - 1) / per_block);
-  grid = grid < device_sm_count() * 8 ? grid : device_sm_count() * 8;
-  if (prm.D == 128)
-    bwd::preprocess_kernel<128><<<grid, 256, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dO),
-                                                      lse, stats, a, bsp, n_rows);
-  else
-    bwd::preprocess_kernel<64><<<grid, 256, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dO),
-                                                     lse, stats, a, bsp, n_rows);
+  const int Hb = a.seq_io ? a.P * a.hq : a.hq;
+  const int n_chunks = a.seq_io ? a.BS / bwd::kPreTok : a.P * ((a.BS + bwd::kPreTok - 1) / bwd::kPreTok);
+  const int smem = Hb * bwd::kPreTok * static_cast<int>(sizeof(float));
+  int grid = n_chunks < device_sm_count() * 8 ? n_chunks : device_sm_count() * 8;
+  auto kern = prm.D == 128 ? bwd::preprocess_kernel<128> : bwd::preprocess_kernel<64>;
+  if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return USP_ERR_CUDA;
+  kern<<<grid, 256, smem, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse, stats, a, bsp,
+                                n_chunks);
   if (check_launch() != USP_OK) return USP_ERR_CUDA;
   if (dsinks != nullptr && a.sinks != nullptr) {
     bwd::dsink_kernel<<<a.P * a.hq, 256, 0, st>>>(stats, dsinks, a, bsp);
@@ -735,19 +776,19 @@ static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const v
   if (!dq_pass) {
     // 64-query slices of Q, dO and their statistics stream past TMEM-resident K, V
     CUtensorMap tq, tdo, tst;
-    if ((rc = make_rows_tmap(&tq, q, a, a.hq, D, bwd::kSL)) != USP_OK) return rc;
-    if ((rc = make_rows_tmap(&tdo, dO, a, a.hq, D, bwd::kSL)) != USP_OK) return rc;
+    if ((rc = make_rows_tmap(&tq, q, a, a.hq, a.Hq, D, bwd::kSL)) != USP_OK) return rc;
+    if ((rc = make_rows_tmap(&tdo, dO, a, a.hq, a.Hq, D, bwd::kSL)) != USP_OK) return rc;
     if ((rc = make_stats_tmap(&tst, stats, a.BS, g.bsp, a.P * a.hq, bwd::kSL)) != USP_OK) return rc;
     if (cudaFuncSetAttribute(bwd::dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::A_SMEM) !=
         cudaSuccess)
       return USP_ERR_CUDA;
-    bwd::dkdv_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hk, bwd::kThreads, C::A_SMEM, st>>>(tq, tdo, tst,
+    bwd::dkdv_kernel<D><<<static_cast<unsigned>(g.n_tiles) * (a.seq_io ? a.Hkv : a.P * a.hk), bwd::kThreads, C::A_SMEM, st>>>(tq, tdo, tst,
                                                                                                        a, g);
   } else {
     // 128-key tiles of K and V stream past TMEM-resident Q, dO
     CUtensorMap tk, tv;
-    if ((rc = make_rows_tmap(&tk, k, a, a.hk, D, kBN)) != USP_OK) return rc;
-    if ((rc = make_rows_tmap(&tv, v, a, a.hk, D, kBN)) != USP_OK) return rc;
+    if ((rc = make_rows_tmap(&tk, k, a, a.hk, a.Hkv, D, kBN)) != USP_OK) return rc;
+    if ((rc = make_rows_tmap(&tv, v, a, a.hk, a.Hkv, D, kBN)) != USP_OK) return rc;
     if (cudaFuncSetAttribute(bwd::dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::B_SMEM) != cudaSuccess)
       return USP_ERR_CUDA;
     bwd::dq_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hq, bwd::kThreads, C::B_SMEM, st>>>(tk, tv, a, g);

@@ -22,7 +22,8 @@ constexpr int kBN = 128;  // keys per tile
 struct AttnArgs {
   int BS;           // tokens per rank: B*S
   int S;            // row length
-  int B, P, hq, hk, G;
+  int B, P, hq, hk, G;  // hk: key/value heads per rank (1 when Hkv < P: replicated); G = hq / hk
+  int Hq, Hkv;          // global head counts
   int causal, window_left;
   float scale;       // softmax scale
   float scale_log2;  // softmax scale * log2(e)
@@ -34,30 +35,43 @@ struct AttnArgs {
   int Sl;      // S/P
 };
 
-// Element offset of the D-vector of (rank r, local head j of `hpr` per rank,
-// rank-local token t = b*S + s) in either layout:
-//   head-layout [P][B][S][hpr][D]      ((r*B*S + t)*hpr + j)*D
-//   seq-layout  [P][B][S/P][P*hpr][D]  (((r'*B + b)*Sl + s')*P*hpr + r*hpr + j)*D, s = r'*Sl + s'
-__device__ __forceinline__ size_t row_offset(const AttnArgs& p, int r, int j, int hpr, int t, int D) {
-  if (!p.seq_io) return ((static_cast<size_t>(r) * p.BS + t) * hpr + j) * D;
+// A head as the kernels address it: rank r and local index j in the
+// head-layout [P][B][S][hpr][D], global index g in the seq-layout
+// [P][B][S/P][H][D].
+struct HeadRef {
+  int r, j, g;
+};
+
+__device__ __forceinline__ HeadRef q_head_ref(const AttnArgs& p, int r, int j) { return {r, j, r * p.hq + j}; }
+// Local key/value head kl of rank r: global head r*Hkv/P + kl (with Hkv < P the
+// P/Hkv ranks r*Hkv/P == h all hold a replica of head h).
+__device__ __forceinline__ HeadRef kv_head_ref(const AttnArgs& p, int r, int kl) {
+  return {r, kl, (r * p.Hkv) / p.P + kl};
+}
+
+// Element offset of the D-vector of head h at rank-local token t = b*S + s in
+// either layout (hpr heads per rank in head-layout, H heads in seq-layout):
+//   head-layout  ((r*B*S + t)*hpr + j)*D
+//   seq-layout   (((r'*B + b)*Sl + s')*H + g)*D,   s = r'*Sl + s'
+__device__ __forceinline__ size_t row_offset(const AttnArgs& p, HeadRef h, int hpr, int H, int t, int D) {
+  if (!p.seq_io) return ((static_cast<size_t>(h.r) * p.BS + t) * hpr + h.j) * D;
   const int b = t / p.S, s = t - b * p.S;
   const int rp = s / p.Sl, sp = s - rp * p.Sl;
-  return ((static_cast<size_t>(rp * p.B + b) * p.Sl + sp) * (static_cast<size_t>(p.P) * hpr) +
-          static_cast<size_t>(r) * hpr + j) * D;
+  return ((static_cast<size_t>(rp * p.B + b) * p.Sl + sp) * H + h.g) * D;
 }
 
 // TMA load of `rows` tokens starting at rank-local token t (64 columns of the
-// D-vectors starting at column c64*64) of local head j of rank r, from either
-// layout's tensor map.  In seq-layout the rows must lie in one shard of one
-// row of the batch (the kernels align tiles to make sure).
+// D-vectors starting at column c64*64) of head h, from either layout's tensor
+// map.  In seq-layout the rows must lie in one shard of one row of the batch
+// (the kernels align tiles to make sure).
 __device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* m, uint64_t* bar, const AttnArgs& p,
-                                              int c64, int r, int j, int hpr, int t) {
+                                              int c64, HeadRef h, int t) {
   if (!p.seq_io) {
-    tma_load_4d(dst, m, bar, c64 * 64, j, t, r);
+    tma_load_4d(dst, m, bar, c64 * 64, h.j, t, h.r);
   } else {
     const int b = t / p.S, s = t - b * p.S;
     const int rp = s / p.Sl, sp = s - rp * p.Sl;
-    tma_load_5d(dst, m, bar, c64 * 64, r * hpr + j, sp, b, rp);
+    tma_load_5d(dst, m, bar, c64 * 64, h.g, sp, b, rp);
   }
 }
 
@@ -151,9 +165,9 @@ namespace usp {
 int make_head_tmap(CUtensorMap* m, const void* base, int P, int BS, int H, int D, int box_rows);
 int make_seq_tmap(CUtensorMap* m, const void* base, int P, int B, int Sl, int H, int D, int box_rows);
 
-// The map for either layout: head-layout (hpr heads per rank) or seq-layout (P*hpr heads).
-inline int make_rows_tmap(CUtensorMap* m, const void* base, const AttnArgs& a, int hpr, int D, int box_rows) {
-  return a.seq_io ? make_seq_tmap(m, base, a.P, a.B, a.Sl, a.P * hpr, D, box_rows)
+// The map for either layout: head-layout (hpr heads per rank) or seq-layout (H heads).
+inline int make_rows_tmap(CUtensorMap* m, const void* base, const AttnArgs& a, int hpr, int H, int D, int box_rows) {
+  return a.seq_io ? make_seq_tmap(m, base, a.P, a.B, a.Sl, H, D, box_rows)
                   : make_head_tmap(m, base, a.P, a.BS, hpr, D, box_rows);
 }
 

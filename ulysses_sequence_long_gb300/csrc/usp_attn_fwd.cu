@@ -2,8 +2,9 @@
 // tensor core (tcgen05), one launch for all P emulated ranks.
 //
 // What it computes (huggingface/accelerate PR #4209: attention runs on the
-// gathered sequence of the rank's heads; sinks are one logit per head sliced
-// to the rank's heads; sliding windows and packing keep working): for every
+// gathered sequence of the rank's heads; each head has a single sink logit,
+// taken from the slice of the rank's heads; sliding windows and packing keep
+// working): for every
 // rank r, local query head j, token t,
 //     LSE_t = ln( sum_{u visible} exp(scale q_t.k_u) + exp(z_{r*hq+j}) )
 //     O_t   = sum_{u visible} exp(scale q_t.k_u - LSE_t) v_u
@@ -85,7 +86,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int per_blk = p.P * p.hq;
   const int qb = out.nqb - 1 - static_cast<int>(blockIdx.x) / per_blk;
   const int rem = static_cast<int>(blockIdx.x) % per_blk;
-  const int r = rem / p.hq, j = rem % p.hq, kvh = j / p.G;
+  const int r = rem / p.hq, j = rem % p.hq;
+  const HeadRef qh = q_head_ref(p, r, j), kvh = kv_head_ref(p, r, j / p.G);
   const int t0 = qb * 2 * kBM;
 
   const int n_docs = checked_docs(p);
@@ -145,8 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!tile_ok[q]) continue;
         mbar_arrive_expect_tx(&bars->q_full[q], C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_rows(smem + C::OFF_Q + q * C::TILE + c * kAtomBytes, &tq, &bars->q_full[q], p, c, r, j, p.hq,
-                        t0 + q * kBM);
+          tma_load_rows(smem + C::OFF_Q + q * C::TILE + c * kAtomBytes, &tq, &bars->q_full[q], p, c, qh, t0 + q * kBM);
       }
       int issued = 0;
       for (int n = 0; n < n_kv; ++n) {
@@ -155,10 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kv0 = lo + n * kBN;
         mbar_arrive_expect_tx(&bars->k_full[st], C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_rows(smem + C::OFF_K + st * C::TILE + c * kAtomBytes, &tk, &bars->k_full[st], p, c, r, kvh, p.hk, kv0);
+          tma_load_rows(smem + C::OFF_K + st * C::TILE + c * kAtomBytes, &tk, &bars->k_full[st], p, c, kvh, kv0);
         mbar_arrive_expect_tx(&bars->v_full[st], C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_rows(smem + C::OFF_V + st * C::TILE + c * kAtomBytes, &tv, &bars->v_full[st], p, c, r, kvh, p.hk, kv0);
+          tma_load_rows(smem + C::OFF_V + st * C::TILE + c * kAtomBytes, &tv, &bars->v_full[st], p, c, kvh, kv0);
         issued = n + 1;
       }
       // Never leave the CTA with copies still landing in its shared memory.
@@ -325,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && (ok = mbar_wait(&bars->o_final[q], 0, abort, p.status))) {
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = out.o + row_offset(p, r, j, p.hq, row_ok ? t : 0, D);
+      __nv_bfloat16* orow = out.o + row_offset(p, qh, p.hq, p.Hq, row_ok ? t : 0, D);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
@@ -364,9 +365,9 @@ static int run_fwd(const usp_attn_params& prm, const AttnArgs& a, const void* q,
                    void* o, float* lse, cudaStream_t st) {
   CUtensorMap tq, tk, tv;
   int rc;
-  if ((rc = make_rows_tmap(&tq, q, a, a.hq, D, kBM)) != USP_OK) return rc;
-  if ((rc = make_rows_tmap(&tk, k, a, a.hk, D, kBN)) != USP_OK) return rc;
-  if ((rc = make_rows_tmap(&tv, v, a, a.hk, D, kBN)) != USP_OK) return rc;
+  if ((rc = make_rows_tmap(&tq, q, a, a.hq, a.Hq, D, kBM)) != USP_OK) return rc;
+  if ((rc = make_rows_tmap(&tk, k, a, a.hk, a.Hkv, D, kBN)) != USP_OK) return rc;
+  if ((rc = make_rows_tmap(&tv, v, a, a.hk, a.Hkv, D, kBN)) != USP_OK) return rc;
   fwd::Out out{static_cast<__nv_bfloat16*>(o), lse, (a.BS + 2 * kBM - 1) / (2 * kBM)};
   const int smem = fwd::Cfg<D>::SMEM;
   if (cudaFuncSetAttribute(fwd::attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
@@ -386,8 +387,10 @@ int launch_attn_fwd(const usp_attn_params& prm, const void* q, const void* k, co
   a.BS = prm.B * prm.S;
   a.P = prm.P;
   a.hq = prm.Hq / prm.P;
-  a.hk = prm.Hkv / prm.P;
-  a.G = prm.Hq / prm.Hkv;
+  a.hk = prm.Hkv >= prm.P ? prm.Hkv / prm.P : 1;
+  a.G = a.hq / a.hk;
+  a.Hq = prm.Hq;
+  a.Hkv = prm.Hkv;
   a.causal = prm.causal ? 1 : 0;
   a.window_left = prm.window_left;
   a.scale = prm.softmax_scale > 0.f ? prm.softmax_scale : 1.0f / sqrtf(static_cast<float>(prm.D));

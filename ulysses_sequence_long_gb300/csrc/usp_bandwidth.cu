@@ -16,15 +16,17 @@ namespace usp {
 
 // ============================================================== relayout
 //
-// Sizes are counted in 16-byte vectors.  A "run" is the (H/P)*D elements one
-// rank's block of heads occupies at one position: contiguous in both layouts.
-//   head-layout run index  hr = (r*B + b)*S + s          (rank r, row b, position s)
-//   seq-layout  run index  sr = ((r'*B + b)*Sl + s')*P + r  (s = r'*Sl + s')
+// Sizes are counted in 16-byte vectors.  A "run" is the hpr*D elements one
+// rank's block of heads occupies at one position: contiguous in both layouts
+// (hpr = H/P heads per rank; when H < P each head is replicated on P/H ranks,
+// hpr = 1, and rank r holds head r/(P/H)).
+//   head-layout run index  hr = (r*B + b)*S + s              (rank r, row b, position s)
+//   seq-layout  run index  sr = ((r'*B + b)*Sl + s')*R + r/rep  (s = r'*Sl + s', R = H/hpr runs per token)
 struct RelayoutGeom {
-  uint32_t n_vec;      // vectors in the whole tensor
+  uint32_t n_vec;      // vectors in the destination tensor
   FastDiv run_vec;     // vectors per run
-  FastDiv S, B, Sl, P;
-  uint32_t Sl_u, B_u, S_u, P_u;
+  FastDiv S, B, Sl, R, rep;
+  uint32_t Sl_u, B_u, S_u, R_u, rep_u;
 };
 
 __device__ __forceinline__ uint32_t head_run_to_seq_run(const RelayoutGeom& g, uint32_t hr) {
@@ -34,12 +36,13 @@ __device__ __forceinline__ uint32_t head_run_to_seq_run(const RelayoutGeom& g, u
   uint32_t b = rb - r * g.B_u;
   uint32_t rp = g.Sl.div(s);
   uint32_t sp = s - rp * g.Sl_u;
-  return ((rp * g.B_u + b) * g.Sl_u + sp) * g.P_u + r;
+  return ((rp * g.B_u + b) * g.Sl_u + sp) * g.R_u + g.rep.div(r);
 }
 
-__device__ __forceinline__ uint32_t seq_run_to_head_run(const RelayoutGeom& g, uint32_t sr) {
-  uint32_t t = g.P.div(sr);
-  uint32_t r = sr - t * g.P_u;
+// Head-layout run of replica `rr` (0 <= rr < rep) of seq-layout run sr.
+__device__ __forceinline__ uint32_t seq_run_to_head_run(const RelayoutGeom& g, uint32_t sr, uint32_t rr) {
+  uint32_t t = g.R.div(sr);
+  uint32_t r = (sr - t * g.R_u) * g.rep_u + rr;
   uint32_t t2 = g.Sl.div(t);
   uint32_t sp = t - t2 * g.Sl_u;
   uint32_t rp = g.B.div(t2);
@@ -52,7 +55,8 @@ constexpr int kRelayoutUnroll = 4;
 
 // Destination-ordered: every thread-iteration writes consecutive vectors of
 // the destination, so stores are fully coalesced; loads come from runs of at
-// least 128 bytes in every configuration this path is used with.
+// least 128 bytes in every configuration this path is used with.  Towards the
+// head layout a replicated head is simply read by each of its replicas.
 template <bool kToHead>
 __device__ __forceinline__ void relayout_body(const int4* __restrict__ src, int4* __restrict__ dst,
                                               const RelayoutGeom& g, uint32_t first, uint32_t stride) {
@@ -66,7 +70,7 @@ __device__ __forceinline__ void relayout_body(const int4* __restrict__ src, int4
       if (v < g.n_vec) {
         uint32_t run = g.run_vec.div(v);
         uint32_t k = v - run * g.run_vec.d;
-        uint32_t srun = kToHead ? head_run_to_seq_run(g, run) : seq_run_to_head_run(g, run);
+        uint32_t srun = kToHead ? head_run_to_seq_run(g, run) : seq_run_to_head_run(g, run, 0);
         val[u] = __ldg(src + static_cast<size_t>(srun) * g.run_vec.d + k);
       }
     }
@@ -80,6 +84,35 @@ template <bool kToHead>
 __global__ void __launch_bounds__(kRelayoutThreads) relayout_kernel(const int4* __restrict__ src,
                                                                     int4* __restrict__ dst, RelayoutGeom g) {
   relayout_body<kToHead>(src, dst, g, blockIdx.x * blockDim.x + threadIdx.x, gridDim.x * blockDim.x);
+}
+
+// Head layout -> seq layout when heads are replicated (bf16 only): the
+// exchange back sums the rep replicas of every head (the adjoint of the
+// replication), in fp32 in replica order, rounded once to bf16.
+__global__ void __launch_bounds__(kRelayoutThreads) relayout_reduce_kernel(const int4* __restrict__ src,
+                                                                           int4* __restrict__ dst, RelayoutGeom g) {
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t v = blockIdx.x * blockDim.x + threadIdx.x; v < g.n_vec; v += stride) {
+    const uint32_t run = g.run_vec.div(v);
+    const uint32_t k = v - run * g.run_vec.d;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (uint32_t rr = 0; rr < g.rep_u; ++rr) {
+      const int4 x = __ldg(src + static_cast<size_t>(seq_run_to_head_run(g, run, rr)) * g.run_vec.d + k);
+      const uint32_t w[4] = {static_cast<uint32_t>(x.x), static_cast<uint32_t>(x.y), static_cast<uint32_t>(x.z),
+                             static_cast<uint32_t>(x.w)};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[2 * e] += bf16lo(w[e]);
+        acc[2 * e + 1] += bf16hi(w[e]);
+      }
+    }
+    int4 out;
+    out.x = static_cast<int>(pack_bf16x2(acc[0], acc[1]));
+    out.y = static_cast<int>(pack_bf16x2(acc[2], acc[3]));
+    out.z = static_cast<int>(pack_bf16x2(acc[4], acc[5]));
+    out.w = static_cast<int>(pack_bf16x2(acc[6], acc[7]));
+    __stcs(dst + v, out);
+  }
 }
 
 // q, k and v in one launch: the grid is split in proportion to their sizes.
@@ -98,20 +131,23 @@ __global__ void __launch_bounds__(kRelayoutThreads) relayout_qkv_kernel(Relayout
                       nb * blockDim.x);
 }
 
-static RelayoutGeom make_geom(int B, int S, int H, int D, int P, int eb) {
+static RelayoutGeom make_geom(int B, int S, int H, int D, int P, int eb, bool to_head) {
   RelayoutGeom g;
-  uint64_t run_bytes = static_cast<uint64_t>(H / P) * D * eb;
-  uint64_t nv = static_cast<uint64_t>(B) * S * H * D * eb / 16;
-  g.n_vec = static_cast<uint32_t>(nv);
+  const int hpr = H >= P ? H / P : 1, rep = H >= P ? 1 : P / H;
+  uint64_t run_bytes = static_cast<uint64_t>(hpr) * D * eb;
+  uint64_t seq_vec = static_cast<uint64_t>(B) * S * H * D * eb / 16;
+  g.n_vec = static_cast<uint32_t>(to_head ? seq_vec * rep : seq_vec);
   g.run_vec = FastDiv(static_cast<uint32_t>(run_bytes / 16));
   g.S = FastDiv(S);
   g.B = FastDiv(B);
   g.Sl = FastDiv(S / P);
-  g.P = FastDiv(P);
+  g.R = FastDiv(H / hpr);
+  g.rep = FastDiv(rep);
   g.Sl_u = S / P;
   g.B_u = B;
   g.S_u = S;
-  g.P_u = P;
+  g.R_u = H / hpr;
+  g.rep_u = rep;
   return g;
 }
 
@@ -125,10 +161,12 @@ static int relayout_grid(uint64_t n_vec) {
 
 int launch_relayout(const void* src, void* dst, int B, int S, int H, int D, int P, int eb, bool to_head,
                     cudaStream_t st) {
-  RelayoutGeom g = make_geom(B, S, H, D, P, eb);
+  RelayoutGeom g = make_geom(B, S, H, D, P, eb, to_head);
   if (g.n_vec == 0) return USP_OK;
   int grid = relayout_grid(g.n_vec);
-  if (to_head)
+  if (!to_head && g.rep_u > 1)
+    relayout_reduce_kernel<<<grid, kRelayoutThreads, 0, st>>>(static_cast<const int4*>(src), static_cast<int4*>(dst), g);
+  else if (to_head)
     relayout_kernel<true><<<grid, kRelayoutThreads, 0, st>>>(static_cast<const int4*>(src), static_cast<int4*>(dst), g);
   else
     relayout_kernel<false><<<grid, kRelayoutThreads, 0, st>>>(static_cast<const int4*>(src), static_cast<int4*>(dst), g);
@@ -142,7 +180,7 @@ int launch_relayout_qkv(const void* const src[3], void* const dst[3], const int 
   for (int t = 0; t < 3; ++t) {
     a.src[t] = static_cast<const int4*>(src[t]);
     a.dst[t] = static_cast<int4*>(dst[t]);
-    a.g[t] = make_geom(B, S, H[t], D, P, eb);
+    a.g[t] = make_geom(B, S, H[t], D, P, eb, true);
     nv[t] = a.g[t].n_vec;
     total += nv[t];
   }

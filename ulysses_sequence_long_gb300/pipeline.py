@@ -15,6 +15,11 @@ Two ways to run the exchanges:
 * explicit: ``usp_relayout_*`` kernels move the tensors between the shard
   layout and the head layout around head-layout attention.
 
+With fewer key/value heads than ranks (P a multiple of Hkv) every key/value
+head is replicated on P/Hkv ranks; the exchange back of dK/dV sums the
+replicas (explicit mode), or the dK/dV kernel sums the whole query group
+directly (fused mode).
+
 torch only allocates the buffers and supplies the stream; every step runs in
 the library's kernels.
 """
@@ -46,7 +51,9 @@ class Shape:
 
     @property
     def hk(self):
-        return self.Hkv // self.P
+        """Key/value heads per rank; with fewer of them than ranks each rank
+        holds one replicated head."""
+        return self.Hkv // self.P if self.Hkv >= self.P else 1
 
     @property
     def can_fuse(self) -> bool:

@@ -79,7 +79,11 @@ ALL = [TINY, MHA4K, LLAMA32K, GPTOSS_WIN, GPTOSS_FULL, LONG128K]
 # tile mix, inputs still larger than L2 (168 MB of q/k/v/dO), far fewer launches.
 LLAMA8K_PROFILE = Workload("llama3_8b_gqa_packed_s8192", B=1, S=8192, Hq=32, Hkv=8, D=128, P=8,
                            doc_mode="geometric", doc_mean=4096, seed=1)
-BY_NAME = {w.name: w for w in ALL + [LLAMA8K_PROFILE]}
+# kv-head replication (more ranks than key/value heads): the Llama-shaped
+# packed case at sp size 16, each of the 8 key/value heads on 2 ranks.
+LLAMA32K_P16 = Workload("llama3_8b_gqa_packed_s32768_p16", B=1, S=32768, Hq=32, Hkv=8, D=128, P=16,
+                        doc_mode="geometric", doc_mean=4096)
+BY_NAME = {w.name: w for w in ALL + [LLAMA8K_PROFILE, LLAMA32K_P16]}
 
 
 def document_lengths(w: Workload) -> List[List[int]]:
