@@ -27,6 +27,12 @@ Everything here is the plain definition, written out in float64 with numpy:
   and one sink logit per head sliced to the rank's heads (PR #4209, the
   gpt-oss finding about ``s_aux``).  The gradients are the textbook ones of
   that function.
+* ``hybrid_fwd`` / ``hybrid_bwd``: yunchang's ring x Ulysses hybrid (USP):
+  the ranks form a (ring, ulysses) mesh with the Ulysses dimension innermost
+  and contiguous ("basic") sequence chunks; the Ulysses exchange runs inside
+  each ring group, then the ring passes key/value super-chunks around and
+  merges the partial outputs through their log-sum-exp
+  (feifeibear/long-context-attention issue #135, the device-mesh script).
 * ``ulysses_fwd`` / ``ulysses_bwd``: the whole emulated P-rank path, and
   ``unsharded_fwd`` / ``unsharded_bwd``: the same attention run on the
   unsharded tensors, the pages' correctness reference (PR #4209 checks the
@@ -64,6 +70,8 @@ __all__ = [
     "attention_bwd_keys",
     "ulysses_fwd", "ulysses_bwd", "unsharded_fwd", "unsharded_bwd",
     "visible_pairs",
+    "hybrid_relayout_fwd", "hybrid_relayout_bwd", "ring_block_fwd", "ring_merge",
+    "hybrid_fwd", "hybrid_bwd",
 ]
 
 
@@ -557,3 +565,246 @@ def unsharded_bwd(q_seq, k_seq, v_seq, do_seq, pos_shards, causal=True, window_l
     O, L = attention_fwd(q, k, v, cu, causal, window_left, scale, sinks)
     dq, dk, dv, ds = attention_bwd(q, k, v, O, L, do, cu, causal, window_left, scale, sinks)
     return (dq.reshape(B, S, Hq, D), dk.reshape(B, S, -1, D), dv.reshape(B, S, -1, D), ds)
+
+
+# ---------------------------------------------------------------------------
+# ring x Ulysses (USP hybrid): feifeibear/long-context-attention issue #135,
+# the device-mesh script (mesh (ring, ulysses) with the Ulysses dimension
+# innermost, "basic" contiguous chunks, the result compared with a
+# non-distributed flash attention over the full tensors)
+# ---------------------------------------------------------------------------
+
+def hybrid_relayout_fwd(x_seq: np.ndarray, ring: int, ulysses: int, replicate: bool = False) -> np.ndarray:
+    """The Ulysses exchange inside each ring group.
+
+    ``x_seq`` is ``[P][B][S/P][H][D]`` with P = ring * ulysses; rank
+    p = rho * ulysses + u holds positions ``[p*S/P, (p+1)*S/P)``.  The ranks of
+    ring group rho (p = rho*U .. rho*U + U - 1) exchange among themselves, so
+    that rank (rho, w) holds the super-chunk ``[rho*C, (rho+1)*C)``
+    (C = S/ring) for heads ``[w*H/U, (w+1)*H/U)``.  The result is laid out
+    ``[U][B][S][H/U][D]``: for each Ulysses index w the ring ranks'
+    super-chunks end to end::
+
+        out[w][b][rho*C + u*S/P + s'][j][d] = x_seq[rho*U + u][b][s'][w*H/U + j][d]
+
+    With ``replicate`` and fewer heads than ``ulysses`` (U a multiple of H),
+    rank (rho, w) receives head w // (U/H) as its one head.  ring = 1 is
+    ``relayout_fwd``.
+    """
+    P, B, Sp, H, D = x_seq.shape
+    U = ulysses
+    if ring <= 0 or U <= 0 or P != ring * U:
+        raise OracleError("the rank axis must hold ring * ulysses shards")
+    _check_divisible(Sp * U, H, U, replicate)
+    if H < U:
+        owner = np.arange(U) // (U // H)
+        y = x_seq[:, :, :, owner, :]                          # [p][b][s'][w][d]
+        y = y.reshape(ring, U, B, Sp, U, D).transpose(4, 2, 0, 1, 3, 5)   # [w][b][rho][u][s'][d]
+        return np.ascontiguousarray(y).reshape(U, B, P * Sp, 1, D)
+    Hp = H // U
+    y = x_seq.reshape(ring, U, B, Sp, U, Hp, D)               # [rho][u][b][s'][w][j][d]
+    y = y.transpose(4, 2, 0, 1, 3, 5, 6)                      # [w][b][rho][u][s'][j][d]
+    return np.ascontiguousarray(y).reshape(U, B, P * Sp, Hp, D)
+
+
+def hybrid_relayout_bwd(x_head: np.ndarray, ring: int, ulysses: int, heads: Optional[int] = None) -> np.ndarray:
+    """The inverse exchange inside each ring group::
+
+        out[rho*U + u][b][s'][w*H/U + j][d] = x_head[w][b][rho*C + u*S/P + s'][j][d]
+
+    With ``heads`` = H < U (replicated heads) the replicas' values are summed
+    (the adjoint of the replication), as in ``relayout_bwd``.
+    """
+    U, B, S, Hp, D = x_head.shape
+    if U != ulysses or ring <= 0 or S % (ring * U) != 0:
+        raise OracleError("head-layout tensor does not match ring * ulysses")
+    P = ring * U
+    Sp = S // P
+    H = Hp * U if heads is None else heads
+    _check_divisible(S, H, U, replicate=True)
+    if H < U:
+        if Hp != 1:
+            raise OracleError("replicated heads hold one head per rank")
+        y = x_head.reshape(H, U // H, B, ring, U, Sp, D).sum(axis=1)     # [h][b][rho][u][s'][d]
+        y = y.transpose(2, 3, 1, 4, 0, 5)                                # [rho][u][b][s'][h][d]
+        return np.ascontiguousarray(y).reshape(P, B, Sp, H, D)
+    y = x_head.reshape(U, B, ring, U, Sp, Hp, D)              # [w][b][rho][u][s'][j][d]
+    y = y.transpose(2, 3, 1, 4, 0, 5, 6)                      # [rho][u][b][s'][w][j][d]
+    return np.ascontiguousarray(y).reshape(P, B, Sp, U * Hp, D)
+
+
+def _block_mask(i0, i1, k0, k1, cu, causal, window_left):
+    """Boolean [i1-i0][k1-k0]: query i may see key j (same document, causal,
+    window), for the query rows [i0, i1) and the keys [k0, k1)."""
+    cu = np.asarray(cu, dtype=np.int64)
+    i = np.arange(i0, i1)
+    j = np.arange(k0, k1)
+    di = np.searchsorted(cu, i, side="right") - 1
+    dj = np.searchsorted(cu, j, side="right") - 1
+    vis = di[:, None] == dj[None, :]
+    if causal:
+        vis &= j[None, :] <= i[:, None]
+    if window_left >= 0:
+        vis &= (i[:, None] - j[None, :]) <= window_left
+        if not causal:
+            vis &= (j[None, :] - i[:, None]) <= window_left
+    return vis
+
+
+def ring_block_fwd(q, k, v, cu_seqlens, rows, keys, causal: bool = True, window_left: int = -1,
+                   scale: Optional[float] = None):
+    """One ring step's attention: the query rows ``rows = (i0, i1)`` over the
+    keys ``keys = (k0, k1)`` only (the key/value super-chunk the rank holds at
+    that step), with the document, causal and window masks of
+    ``attention_fwd`` and no sink.  ``q`` [T][hq][D], ``k``/``v`` [T][hk][D].
+    Returns ``O`` [i1-i0][hq][D] and ``LSE`` [hq][i1-i0]; a row that sees no
+    key of the block has O = 0 and LSE = -inf."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    T, hq, D = q.shape
+    G = hq // k.shape[1]
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    i0, i1 = rows
+    k0, k1 = keys
+    vis = _block_mask(i0, i1, k0, k1, cu_seqlens, causal, window_left)
+    O = np.zeros((i1 - i0, hq, D))
+    L = np.full((hq, i1 - i0), -np.inf)
+    seen = vis.any(axis=1)
+    for h in range(hq):
+        s = np.where(vis, scale * (q[i0:i1, h] @ k[k0:k1, h // G].T), -np.inf)
+        m = np.where(seen, s.max(axis=1), 0.0)
+        e = np.where(vis, np.exp(s - m[:, None]), 0.0)
+        z = e.sum(axis=1)
+        L[h, seen] = m[seen] + np.log(z[seen])
+        O[seen, h] = (e[seen] / z[seen, None]) @ v[k0:k1, h // G]
+    return O, L
+
+
+def ring_merge(O1, L1, O2, L2):
+    """Combine two softmax-normalised partial outputs over disjoint key sets
+    into the one over their union: LSE = log(e^L1 + e^L2) and
+    O = e^(L1-LSE) O1 + e^(L2-LSE) O2 (a part with LSE = -inf adds nothing).
+    ``O`` [..., hq, D] with ``L`` [hq, ...] matching its leading row axis."""
+    L = np.logaddexp(L1, L2)
+    fin = np.isfinite(L)
+    w1 = np.where(fin, np.exp(np.where(fin, L1 - L, 0.0)), 0.0)
+    w2 = np.where(fin, np.exp(np.where(fin, L2 - L, 0.0)), 0.0)
+    # L is [hq][rows]; O is [rows][hq][D]
+    return O1 * w1.T[:, :, None] + O2 * w2.T[:, :, None], L
+
+
+def hybrid_fwd(q_seq, k_seq, v_seq, pos_shards, ring: int, causal=True, window_left=-1, scale=None,
+               sinks=None):
+    """Forward of the ring x Ulysses hybrid over P = ring * ulysses emulated ranks.
+
+    1. Ulysses exchange inside each ring group (``hybrid_relayout_fwd``).
+    2. For each Ulysses index w, ``ring`` steps: at step s ring rank rho
+       attends its query super-chunk rho to the key/value super-chunk
+       (rho - s) mod ring (``ring_block_fwd``) and merges the result into its
+       running (O, LSE) (``ring_merge``).
+    3. The sink logit of each head, if any, joins the softmax once, as a
+       final part with LSE = sink and no value.
+    4. The inverse exchange brings O back to the sequence shards.
+
+    Document boundaries come from the gathered position_ids as in
+    ``ulysses_fwd``.  Returns the head-layout tensors, ``o_head``
+    [U][B][S][hq][D], ``lse`` [U][B][hq][S] and ``o_seq``.
+    """
+    P, B, Sp, Hq, D = q_seq.shape
+    if P % ring != 0:
+        raise OracleError("ring degree must divide the ranks")
+    U = P // ring
+    S = P * Sp
+    if Hq % U != 0:
+        raise OracleError(f"ulysses degree {U} does not divide {Hq} heads")
+    C = S // ring
+    qh = hybrid_relayout_fwd(np.asarray(q_seq, np.float64), ring, U)
+    kh = hybrid_relayout_fwd(np.asarray(k_seq, np.float64), ring, U, replicate=True)
+    vh = hybrid_relayout_fwd(np.asarray(v_seq, np.float64), ring, U, replicate=True)
+    cu, n, max_len = cu_seqlens_from_position_ids(pos_shards)
+    hq, T = Hq // U, B * S
+    o_head = np.empty((U, B, S, hq, D))
+    lse = np.empty((U, B, hq, S))
+    for w in range(U):
+        Q = qh[w].reshape(T, hq, D)
+        K = kh[w].reshape(T, -1, D)
+        V = vh[w].reshape(T, -1, D)
+        O = np.zeros((T, hq, D))
+        L = np.full((hq, T), -np.inf)
+        for step in range(ring):
+            for rho in range(ring):
+                kc = (rho - step) % ring
+                for b in range(B):
+                    rows = (b * S + rho * C, b * S + (rho + 1) * C)
+                    keys = (b * S + kc * C, b * S + (kc + 1) * C)
+                    Ob, Lb = ring_block_fwd(Q, K, V, cu, rows, keys, causal, window_left, scale)
+                    sl = slice(*rows)
+                    O[sl], L[:, sl] = ring_merge(O[sl], L[:, sl], Ob, Lb)
+        if sinks is not None:
+            z = np.asarray(sinks, np.float64)[w * hq:(w + 1) * hq]
+            O, L = ring_merge(O, L, np.zeros_like(O), np.repeat(z[:, None], T, axis=1))
+        o_head[w] = O.reshape(B, S, hq, D)
+        lse[w] = L.reshape(hq, B, S).transpose(1, 0, 2)
+    return dict(q_head=qh, k_head=kh, v_head=vh, cu_seqlens=cu, n_docs=n, max_len=max_len,
+                o_head=o_head, lse=lse, o_seq=hybrid_relayout_bwd(o_head, ring, U), Hkv=k_seq.shape[3],
+                ring=ring)
+
+
+def hybrid_bwd(fwd: dict, do_seq, causal=True, window_left=-1, scale=None, sinks=None):
+    """Backward of the ring x Ulysses hybrid: dO goes through the Ulysses
+    exchange; every ring step recomputes its block's probabilities from the
+    final LSE and adds its share to dQ (kept by the query's rank) and to dK/dV
+    (carried with the key/value super-chunk back to its owner); the inverse
+    exchange returns dQ/dK/dV (replicas summed)."""
+    ring = fwd["ring"]
+    P = do_seq.shape[0]
+    U = P // ring
+    doh = hybrid_relayout_fwd(np.asarray(do_seq, np.float64), ring, U)
+    _, B, S, hq, D = doh.shape
+    T, C = B * S, S // ring
+    hk = fwd["k_head"].shape[3]
+    G = hq // hk
+    sc = 1.0 / np.sqrt(D) if scale is None else scale
+    cu = fwd["cu_seqlens"]
+    dqh = np.zeros_like(fwd["q_head"])
+    dkh = np.zeros_like(fwd["k_head"])
+    dvh = np.zeros_like(fwd["v_head"])
+    dsinks = None if sinks is None else np.zeros(hq * U)
+    for w in range(U):
+        Q = fwd["q_head"][w].reshape(T, hq, D)
+        K = fwd["k_head"][w].reshape(T, hk, D)
+        V = fwd["v_head"][w].reshape(T, hk, D)
+        O = fwd["o_head"][w].reshape(T, hq, D)
+        dO = doh[w].reshape(T, hq, D)
+        L = fwd["lse"][w].transpose(1, 0, 2).reshape(hq, T)
+        Dvec = np.sum(dO * O, axis=2)                     # [T][hq]
+        dq = np.zeros((T, hq, D))
+        dk = np.zeros((T, hk, D))
+        dv = np.zeros((T, hk, D))
+        for step in range(ring):
+            for rho in range(ring):
+                kc = (rho - step) % ring
+                for b in range(B):
+                    i0, i1 = b * S + rho * C, b * S + (rho + 1) * C
+                    k0, k1 = b * S + kc * C, b * S + (kc + 1) * C
+                    vis = _block_mask(i0, i1, k0, k1, cu, causal, window_left)
+                    for h in range(hq):
+                        kv = h // G
+                        s = sc * (Q[i0:i1, h] @ K[k0:k1, kv].T)
+                        Pm = np.where(vis, np.exp(np.where(vis, s, 0.0) - L[h, i0:i1][:, None]), 0.0)
+                        dv[k0:k1, kv] += Pm.T @ dO[i0:i1, h]
+                        dS = Pm * (dO[i0:i1, h] @ V[k0:k1, kv].T - Dvec[i0:i1, h][:, None])
+                        dq[i0:i1, h] += sc * (dS @ K[k0:k1, kv])
+                        dk[k0:k1, kv] += sc * (dS.T @ Q[i0:i1, h])
+        if dsinks is not None:
+            z = np.asarray(sinks, np.float64)[w * hq:(w + 1) * hq]
+            dsinks[w * hq:(w + 1) * hq] = -np.sum(np.exp(z[:, None] - L) * Dvec.T, axis=1)
+        dqh[w] = dq.reshape(B, S, hq, D)
+        dkh[w] = dk.reshape(B, S, hk, D)
+        dvh[w] = dv.reshape(B, S, hk, D)
+    Hkv = fwd["Hkv"]
+    return dict(do_head=doh, dq_head=dqh, dk_head=dkh, dv_head=dvh, dsinks=dsinks,
+                dq_seq=hybrid_relayout_bwd(dqh, ring, U), dk_seq=hybrid_relayout_bwd(dkh, ring, U, Hkv),
+                dv_seq=hybrid_relayout_bwd(dvh, ring, U, Hkv))

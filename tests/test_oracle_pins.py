@@ -479,3 +479,95 @@ def test_bwd_rows_and_keys_agree_with_full_backward(causal, window_left, use_sin
     np.testing.assert_allclose(dk2[:, 1], dk[:, 1], rtol=0, atol=1e-12)
     np.testing.assert_allclose(dv2[:, 1], dv[:, 1], rtol=0, atol=1e-12)
     assert np.all(dk2[:, 0] == 0) and np.all(dq2[:, :2] == 0)
+
+
+# ---------------------------------------------------------------------------
+# ring x Ulysses hybrid (USP)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("ring,U,B,S,H,D", [(2, 2, 1, 16, 4, 2), (3, 2, 2, 24, 2, 1), (4, 1, 1, 8, 3, 2),
+                                            (1, 4, 2, 8, 4, 1)])
+def test_hybrid_relayout_rank_holds_its_super_chunk_for_its_heads(ring, U, B, S, H, D):
+    P = ring * U
+    x = _encoded_seq_tensor(P, B, S, H, D)
+    y = oracle.hybrid_relayout_fwd(x, ring, U)
+    Hp = H // U
+    assert y.shape == (U, B, S, Hp, D)
+    for w in range(U):
+        for b in range(B):
+            for pos in range(S):
+                for j in range(Hp):
+                    for d in range(D):
+                        # Ulysses rank w of every ring group: global position pos, heads block w
+                        assert _decode(int(y[w, b, pos, j, d]), S, H, D) == (b, pos, w * Hp + j, d)
+    assert np.array_equal(oracle.hybrid_relayout_bwd(y, ring, U), x)
+    if ring == 1:
+        assert np.array_equal(y, oracle.relayout_fwd(x, U))
+
+
+def test_hybrid_relayout_replicated_is_adjoint():
+    ring, U, H = 2, 4, 2
+    x = _rng(31).standard_normal((ring * U, 2, 3, H, 4))
+    y = _rng(32).standard_normal((U, 2, ring * U * 3, 1, 4))
+    lhs = float(np.sum(oracle.hybrid_relayout_fwd(x, ring, U, replicate=True) * y))
+    rhs = float(np.sum(x * oracle.hybrid_relayout_bwd(y, ring, U, H)))
+    assert abs(lhs - rhs) <= 1e-12 * max(1.0, abs(lhs))
+
+
+def test_ring_merge_of_two_key_blocks_is_the_union():
+    # softmax over a key set = log-sum-exp merge of the softmaxes over a split of it
+    q, k, v = _rand_qkv(40, 2, 1, 8, seed=33)
+    cu = [0, 13, 40]
+    for causal in (True, False):
+        Oa, La = oracle.ring_block_fwd(q, k, v, cu, (20, 40), (0, 20), causal)
+        Ob, Lb = oracle.ring_block_fwd(q, k, v, cu, (20, 40), (20, 40), causal)
+        Ou, Lu = oracle.ring_block_fwd(q, k, v, cu, (20, 40), (0, 40), causal)
+        Om, Lm = oracle.ring_merge(Oa, La, Ob, Lb)
+        np.testing.assert_allclose(Om, Ou, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(Lm, Lu, rtol=0, atol=1e-13)
+        # and the whole-range block is plain attention over those rows
+        O, L = oracle.attention_fwd(q, k, v, cu, causal)
+        np.testing.assert_allclose(Ou, O[20:40], rtol=0, atol=1e-13)
+    # rows with no key in the block: O = 0, LSE = -inf
+    O0, L0 = oracle.ring_block_fwd(q, k, v, cu, (0, 10), (20, 40), True)
+    assert np.all(O0 == 0) and np.all(L0 == -np.inf)
+
+
+HYBRID = [
+    (W.Workload("usp_r2u2", B=1, S=64, Hq=4, Hkv=2, D=8, P=4, ring=2, doc_mode="explicit", doc_lens=(23, 41)), ),
+    (W.Workload("usp_r4u1_noncausal", B=1, S=32, Hq=2, Hkv=1, D=4, P=4, ring=4, causal=False,
+                doc_mode="explicit", doc_lens=(32,)), ),
+    (W.Workload("usp_r2u2_win_sink_b2", B=2, S=48, Hq=4, Hkv=2, D=8, P=4, ring=2, window_left=9, sinks=True,
+                doc_mode="explicit", doc_lens=(30, 18)), ),
+    (W.Workload("usp_r2u4_kv_rep", B=1, S=64, Hq=8, Hkv=2, D=4, P=8, ring=2, doc_mode="explicit",
+                doc_lens=(5, 50, 9)), ),
+    (W.Workload("usp_r1u2", B=1, S=32, Hq=4, Hkv=2, D=4, P=2, ring=1, doc_mode="explicit", doc_lens=(20, 12)), ),
+]
+
+
+@pytest.mark.parametrize("w", [c[0] for c in HYBRID], ids=lambda w: w.name)
+def test_hybrid_equals_unsharded(w):
+    """The pages validate the hybrid against a non-distributed attention over
+    the full tensors; the oracle's hybrid must agree with the unsharded
+    definition in the forward and the backward."""
+    x = _small_workload_tensors(w)
+    pos = W.position_ids_shards(w)
+    snk = None if W.sinks(w) is None else W.sinks(w).double().numpy()
+    kw = dict(causal=w.causal, window_left=w.window_left, sinks=snk)
+    f = oracle.hybrid_fwd(x["q"], x["k"], x["v"], pos, w.ring, **kw)
+    O, L = oracle.unsharded_fwd(x["q"], x["k"], x["v"], pos, **kw)
+    np.testing.assert_allclose(f["o_seq"], W.shard_sequence(O, w.P), rtol=0, atol=1e-12)
+    U, hq = w.P // w.ring, w.Hq // (w.P // w.ring)
+    for u in range(U):
+        np.testing.assert_allclose(f["lse"][u].transpose(1, 0, 2).reshape(hq, -1), L[u * hq:(u + 1) * hq],
+                                   rtol=0, atol=1e-12)
+    g = oracle.hybrid_bwd(f, x["do"], **kw)
+    dq, dk, dv, ds = oracle.unsharded_bwd(x["q"], x["k"], x["v"], x["do"], pos, **kw)
+    np.testing.assert_allclose(g["dq_seq"], W.shard_sequence(dq, w.P), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(g["dk_seq"], W.shard_sequence(dk, w.P), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(g["dv_seq"], W.shard_sequence(dv, w.P), rtol=0, atol=1e-11)
+    if snk is not None:
+        np.testing.assert_allclose(g["dsinks"], ds, rtol=0, atol=1e-11)
+    if w.ring == 1:
+        u = oracle.ulysses_fwd(x["q"], x["k"], x["v"], pos, **kw)
+        np.testing.assert_allclose(f["o_seq"], u["o_seq"], rtol=0, atol=1e-13)

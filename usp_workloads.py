@@ -46,6 +46,7 @@ class Workload:
     doc_mode: str = "single"       # "single" | "explicit" | "geometric"
     doc_mean: int = 4096           # mean length for doc_mode == "geometric"
     seed: int = 0
+    ring: int = 1                  # ring degree of the ring x Ulysses hybrid (P = ring * ulysses)
 
     @property
     def G(self) -> int:
