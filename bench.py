@@ -179,11 +179,15 @@ def relayout_bandwidth(w: W.Workload, device, t, steps: int):
 
 class Step:
     def __init__(self, w: W.Workload, device, host=None, fused=None):
-        from ulysses_sequence_long_gb300.pipeline import Shape, UlyssesAttention
+        from ulysses_sequence_long_gb300.pipeline import HybridAttention, Shape, UlyssesAttention
         self.w = w
         self.device = device
-        self.ua = UlyssesAttention(Shape(w.B, w.S, w.Hq, w.Hkv, w.D, w.P, w.causal, w.window_left), device=device,
-                                   fused=fused)
+        shape = Shape(w.B, w.S, w.Hq, w.Hkv, w.D, w.P, w.causal, w.window_left)
+        self.hybrid = w.ring > 1
+        if self.hybrid:   # ring x Ulysses: explicit exchanges inside each ring group
+            self.ua = HybridAttention(shape, w.ring, device=device)
+        else:
+            self.ua = UlyssesAttention(shape, device=device, fused=fused)
         if host is None:
             host = {"t": W.qkv_do_shards(w), "pos": torch.from_numpy(W.position_ids_shards(w)), "sinks": W.sinks(w)}
         self.shared_host = host
@@ -206,6 +210,10 @@ class Step:
             if events is not None:
                 events[i].record(s)
 
+        if self.hybrid:
+            ua.forward_phases(d["q"], d["k"], d["v"], self.pos, self.sinks, s, marks=mark)
+            ua.backward_phases(d["do"], self.sinks, s, marks=lambda i: mark(4 + i))
+            return
         mark(0)
         ua.exchange_qkv(d["q"], d["k"], d["v"], s)
         mark(1)
@@ -217,9 +225,14 @@ class Step:
         ua.backward_phases(d["do"], self.sinks, s, marks=lambda i: mark(4 + i))
 
     def launches_per_step(self) -> int:
+        sink = 1 if self.sinks is not None else 0
+        if self.hybrid:
+            # exchanges 1 + 1 + 1 + 3, scan 3, preprocess 1 (+ dsink); per ring
+            # step: forward + merge, dK/dV + 2 sums, dQ + 1 sum
+            return 10 + sink + 7 * self.w.ring
         # scan 3, fwd 1, preprocess 1 (+ dsink 1), dK/dV 1, dQ 1; the explicit
         # exchanges add relayout qkv 1, O 1, dO 1, dQ/dK/dV 3
-        return 7 + (1 if self.sinks is not None else 0) + (0 if self.ua.fused else 6)
+        return 7 + sink + (0 if self.ua.fused else 6)
 
     # -- end to end: host buffers in and out, through the C ABI
     def make_host_io(self):
@@ -463,7 +476,7 @@ def main():
                        "causal": w.causal, "window_left": w.window_left, "sinks": w.sinks,
                        "documents": len(W.document_lengths(w)[0]), "visible_pairs_per_head": fl["pairs"],
                        "fwd_bwd_flop": fl["total"], "parallelism": f"emulated ulysses P={w.P}, replicas={world}",
-                       "exchanges": "fused" if step.ua.fused else "explicit",
+                       "exchanges": "fused" if step.ua.fused else "explicit", "ring": w.ring,
                        "l2": "inputs larger than L2 (no flush)"},
             "relayout_gbs": relayout_gbs, "relayout_frac_hbm": relayout_gbs / peaks["hbm_gbs"],
             "relayout_measured": relayout_note,

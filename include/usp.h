@@ -194,6 +194,12 @@ typedef struct {
   int io_layout;             /* USP_IO_HEAD (0): q, k, v, dO, o, dq, dk, dv in head-layout;
                                 USP_IO_SEQ (1): the same tensors in seq-layout — the exchanges
                                 are fused into the kernels' loads and stores; needs (S/P) % 128 == 0 */
+  int ring;                  /* ring x Ulysses hybrid: ring degree R (0 or 1: no ring).  With R > 1,
+                                P is the Ulysses degree, the tensors are the hybrid head-layout of
+                                usp_hybrid_relayout_fwd, and a call computes one ring step: rows of
+                                super-chunk a (S/R positions each) see only the keys of super-chunk
+                                (a - ring_step) mod R.  Needs (S/R) % 256 == 0 and USP_IO_HEAD. */
+  int ring_step;             /* 0 <= ring_step < R */
 } usp_attn_params;
 
 enum { USP_IO_HEAD = 0, USP_IO_SEQ = 1 };
@@ -213,6 +219,56 @@ enum { USP_IO_HEAD = 0, USP_IO_SEQ = 1 };
  * USP_ERR_CUDA. */
 int usp_attn_fwd(const usp_attn_params* params, const void* q, const void* k, const void* v,
                  void* o, float* lse, int32_t* dev_status, usp_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Ring x Ulysses hybrid (USP; feifeibear/long-context-attention issue #135,
+ * the device-mesh script: ranks form a (ring, ulysses) mesh with the Ulysses
+ * dimension innermost and contiguous ("basic") sequence chunks).
+ *
+ * P = ring * ulysses ranks; rank p = rho*ulysses + u holds positions
+ * [p*S/P, (p+1)*S/P).  The Ulysses exchange runs inside each ring group
+ * rho, after which rank (rho, w) holds super-chunk rho (positions
+ * [rho*C, (rho+1)*C), C = S/ring) for heads [w*H/U, (w+1)*H/U), U = ulysses.
+ * The hybrid head-layout [U][B][S][H/U][D] lays the ring ranks' super-chunks
+ * end to end for each w:
+ *   x_head[w][b][rho*C + u*S/P + s'][j][d] = x_seq[rho*U + u][b][s'][w*H/U + j][d]
+ * (H < U: replicated heads as in usp_relayout_fwd; the bwd exchange sums them).
+ * ring = 1 is usp_relayout_fwd/bwd with P = ulysses.  Errors as usp_relayout_fwd,
+ * with S % (ring*ulysses) for USP_ERR_INDIVISIBLE.
+ * ---------------------------------------------------------------------- */
+int usp_hybrid_relayout_fwd(const void* x_seq, void* x_head, int B, int S, int H, int D, int ring, int ulysses,
+                            int elem_bytes, usp_stream_t stream);
+int usp_hybrid_relayout_bwd(const void* x_head, void* x_seq, int B, int S, int H, int D, int ring, int ulysses,
+                            int elem_bytes, usp_stream_t stream);
+int usp_hybrid_relayout_fwd_qkv(const void* q_seq, const void* k_seq, const void* v_seq,
+                                void* q_head, void* k_head, void* v_head,
+                                int B, int S, int Hq, int Hkv, int D, int ring, int ulysses, int elem_bytes,
+                                usp_stream_t stream);
+
+enum { USP_RING_FIRST = 1, USP_RING_LAST = 2 };
+
+/* Forward of one ring step's result into the running output: with the step's
+ * o_step (bf16, head layout like o) and lse_step (fp32 [P][B][hq][S], -inf for
+ * rows that saw no key) from usp_attn_fwd with params->ring_step = s:
+ *   L = ln(e^L_acc + e^L_step),  O = e^(L_acc - L) O_acc + e^(L_step - L) O_step
+ * flags USP_RING_FIRST: the running values start as the step's (o_acc/lse_acc
+ * are not read).  USP_RING_LAST: the sink logit z = sinks[r*hq + j] (if
+ * params->sinks) joins once, L' = ln(e^L + e^z), O' = e^(L - L') O, and the
+ * result goes to o (bf16) and lse (fp32), o_acc/lse_acc are not written;
+ * otherwise it goes to o_acc (fp32, shaped like o) and lse_acc.  params is the
+ * step call's (ring and ring_step are not read; sinks are, at the last step).
+ * Pointers 16-byte aligned.  Errors: as usp_attn_fwd. */
+int usp_ring_fwd_merge(const usp_attn_params* params, const void* o_step, const float* lse_step,
+                       float* o_acc, float* lse_acc, void* o, float* lse, int flags, usp_stream_t stream);
+
+/* Backward of the ring: g_acc (fp32) += g_step (bf16), n elements (a multiple
+ * of 8).  USP_RING_FIRST: g_acc starts at zero (not read).  USP_RING_LAST: the
+ * sum is rounded once to bf16 into g_out and g_acc is not written.  Every
+ * step's dQ (kept by its rank) and dK/dV (carried with their super-chunk) is
+ * summed at the element's own address.  Pointers 16-byte aligned.
+ * Errors: USP_ERR_INVALID_ARG, USP_ERR_ALIGNMENT, USP_ERR_UNSUPPORTED (n/8 >= 2^32), USP_ERR_CUDA. */
+int usp_ring_grad_accumulate(const void* g_step, float* g_acc, void* g_out, size_t n, int flags,
+                             usp_stream_t stream);
 
 /* Bytes of workspace usp_attn_bwd needs: the fp32 row statistic
  * D_t = sum_d dO_td O_td for every query row and head, 256-byte aligned. */

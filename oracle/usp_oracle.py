@@ -386,11 +386,13 @@ def attention_bwd(q, k, v, o, lse, do, cu_seqlens, causal: bool = True, window_l
 
 def attention_bwd_rows(q, k, v, do, cu_seqlens, rows, head: int, causal: bool = True,
                        window_left: int = -1, scale: Optional[float] = None,
-                       sink: Optional[float] = None):
+                       sink: Optional[float] = None, key_window: Optional[Tuple[int, int]] = None):
     """dQ of the listed query rows of one head, each row from its own forward.
 
     Row t needs only its own O_t, LSE_t and D_t = dO_t . O_t, so a single row
-    of a very long document is checked without the whole head.
+    of a very long document is checked without the whole head.  With
+    ``key_window = (k0, k1)`` only the keys in [k0, k1) contribute to the sum
+    (one ring step's share of dQ); O, LSE and D stay those of the whole row.
     """
     T, hq, D = q.shape
     kh = head // (hq // k.shape[1])
@@ -407,7 +409,11 @@ def attention_bwd_rows(q, k, v, do, cu_seqlens, rows, head: int, causal: bool = 
         V = np.asarray(v[ka:kb, kh], np.float64)
         dot = np.asarray(do[t, head], np.float64)
         s = scale * (K @ np.asarray(q[t, head], np.float64))
-        Pm = np.where(_visible(t, t + 1, ka, kb, causal, window_left, a, b)[0], np.exp(s - L[n]), 0.0)
+        vis = _visible(t, t + 1, ka, kb, causal, window_left, a, b)[0]
+        if key_window is not None:
+            kk = np.arange(ka, kb)
+            vis = vis & (kk >= key_window[0]) & (kk < key_window[1])
+        Pm = np.where(vis, np.exp(s - L[n]), 0.0)
         dS = Pm * (V @ dot - dot @ O[n])
         dq[n] = scale * (dS @ K)
     return dq
@@ -415,13 +421,15 @@ def attention_bwd_rows(q, k, v, do, cu_seqlens, rows, head: int, causal: bool = 
 
 def attention_bwd_keys(q, k, v, do, cu_seqlens, keys, kv_head: int, causal: bool = True,
                        window_left: int = -1, scale: Optional[float] = None,
-                       sinks: Optional[np.ndarray] = None):
+                       sinks: Optional[np.ndarray] = None, row_window: Optional[Tuple[int, int]] = None):
     """dK and dV of the listed keys of one key/value head.
 
     Every query row that sees one of the keys, in every query head of the
     group, gets its O, LSE and D from its own forward (``attention_fwd_rows``);
     then dV_u = sum P_tu dO_t and dK_u = scale sum dS_tu q_t over those rows.
-    Cheap when the keys sit near the end of their document.
+    Cheap when the keys sit near the end of their document.  With
+    ``row_window = (q0, q1)`` only the rows in [q0, q1) contribute (one ring
+    step's share of dK/dV).
     """
     T, hq, D = q.shape
     G = hq // k.shape[1]
@@ -435,7 +443,8 @@ def attention_bwd_keys(q, k, v, do, cu_seqlens, keys, kv_head: int, causal: bool
         for n, u in enumerate(keys):
             d = int(np.searchsorted(cu, u, side="right")) - 1
             a, b = int(cu[d]), int(cu[d + 1])
-            rows = [t for t in range(a, b) if _visible(t, t + 1, u, u + 1, causal, window_left, a, b)[0, 0]]
+            rows = [t for t in range(a, b) if _visible(t, t + 1, u, u + 1, causal, window_left, a, b)[0, 0]
+                    and (row_window is None or row_window[0] <= t < row_window[1])]
             if not rows:
                 continue
             O, L = attention_fwd_rows(q, k, v, cu, rows, h, causal, window_left, scale, sink)
@@ -752,12 +761,13 @@ def hybrid_fwd(q_seq, k_seq, v_seq, pos_shards, ring: int, causal=True, window_l
                 ring=ring)
 
 
-def hybrid_bwd(fwd: dict, do_seq, causal=True, window_left=-1, scale=None, sinks=None):
+def hybrid_bwd(fwd: dict, do_seq, causal=True, window_left=-1, scale=None, sinks=None, return_steps=False):
     """Backward of the ring x Ulysses hybrid: dO goes through the Ulysses
     exchange; every ring step recomputes its block's probabilities from the
     final LSE and adds its share to dQ (kept by the query's rank) and to dK/dV
     (carried with the key/value super-chunk back to its owner); the inverse
-    exchange returns dQ/dK/dV (replicas summed)."""
+    exchange returns dQ/dK/dV (replicas summed).  ``return_steps`` also
+    returns each step's block gradients (head layout) under ``steps``."""
     ring = fwd["ring"]
     P = do_seq.shape[0]
     U = P // ring
@@ -772,6 +782,8 @@ def hybrid_bwd(fwd: dict, do_seq, causal=True, window_left=-1, scale=None, sinks
     dkh = np.zeros_like(fwd["k_head"])
     dvh = np.zeros_like(fwd["v_head"])
     dsinks = None if sinks is None else np.zeros(hq * U)
+    steps = [dict(dq_head=np.zeros_like(dqh), dk_head=np.zeros_like(dkh), dv_head=np.zeros_like(dvh))
+             for _ in range(ring)] if return_steps else None
     for w in range(U):
         Q = fwd["q_head"][w].reshape(T, hq, D)
         K = fwd["k_head"][w].reshape(T, hk, D)
@@ -794,10 +806,18 @@ def hybrid_bwd(fwd: dict, do_seq, causal=True, window_left=-1, scale=None, sinks
                         kv = h // G
                         s = sc * (Q[i0:i1, h] @ K[k0:k1, kv].T)
                         Pm = np.where(vis, np.exp(np.where(vis, s, 0.0) - L[h, i0:i1][:, None]), 0.0)
-                        dv[k0:k1, kv] += Pm.T @ dO[i0:i1, h]
+                        bv = Pm.T @ dO[i0:i1, h]
                         dS = Pm * (dO[i0:i1, h] @ V[k0:k1, kv].T - Dvec[i0:i1, h][:, None])
-                        dq[i0:i1, h] += sc * (dS @ K[k0:k1, kv])
-                        dk[k0:k1, kv] += sc * (dS.T @ Q[i0:i1, h])
+                        bq = sc * (dS @ K[k0:k1, kv])
+                        bk = sc * (dS.T @ Q[i0:i1, h])
+                        dv[k0:k1, kv] += bv
+                        dq[i0:i1, h] += bq
+                        dk[k0:k1, kv] += bk
+                        if steps is not None:
+                            st = steps[step]
+                            st["dv_head"][w].reshape(T, hk, D)[k0:k1, kv] += bv
+                            st["dq_head"][w].reshape(T, hq, D)[i0:i1, h] += bq
+                            st["dk_head"][w].reshape(T, hk, D)[k0:k1, kv] += bk
         if dsinks is not None:
             z = np.asarray(sinks, np.float64)[w * hq:(w + 1) * hq]
             dsinks[w * hq:(w + 1) * hq] = -np.sum(np.exp(z[:, None] - L) * Dvec.T, axis=1)
@@ -807,4 +827,4 @@ def hybrid_bwd(fwd: dict, do_seq, causal=True, window_left=-1, scale=None, sinks
     Hkv = fwd["Hkv"]
     return dict(do_head=doh, dq_head=dqh, dk_head=dkh, dv_head=dvh, dsinks=dsinks,
                 dq_seq=hybrid_relayout_bwd(dqh, ring, U), dk_seq=hybrid_relayout_bwd(dkh, ring, U, Hkv),
-                dv_seq=hybrid_relayout_bwd(dvh, ring, U, Hkv))
+                dv_seq=hybrid_relayout_bwd(dvh, ring, U, Hkv), steps=steps)

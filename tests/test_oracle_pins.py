@@ -571,3 +571,27 @@ def test_hybrid_equals_unsharded(w):
     if w.ring == 1:
         u = oracle.ulysses_fwd(x["q"], x["k"], x["v"], pos, **kw)
         np.testing.assert_allclose(f["o_seq"], u["o_seq"], rtol=0, atol=1e-13)
+    # the per-step block gradients add up to the result
+    gs = oracle.hybrid_bwd(f, x["do"], return_steps=True, **kw)
+    for n in ("dq_head", "dk_head", "dv_head"):
+        np.testing.assert_allclose(sum(st[n] for st in gs["steps"]), g[n], rtol=0, atol=1e-12)
+
+
+def test_bwd_rows_and_keys_split_over_windows_add_up():
+    # one ring step's share of dQ (keys of a window) and of dK/dV (rows of a
+    # window): the shares over a partition of the sequence add up to the whole
+    q, k, v = _rand_qkv(48, 2, 1, 8, seed=34)
+    do = _rng(35).standard_normal(q.shape)
+    cu = [0, 20, 48]
+    rows = [5, 19, 20, 33, 47]
+    whole = oracle.attention_bwd_rows(q, k, v, do, cu, rows, 1)
+    parts = [oracle.attention_bwd_rows(q, k, v, do, cu, rows, 1, key_window=wd) for wd in ((0, 24), (24, 48))]
+    np.testing.assert_allclose(parts[0] + parts[1], whole, rtol=0, atol=1e-12)
+    keys = [0, 10, 21, 30, 47]
+    dk, dv = oracle.attention_bwd_keys(q, k, v, do, cu, keys, 0)
+    p0 = oracle.attention_bwd_keys(q, k, v, do, cu, keys, 0, row_window=(0, 24))
+    p1 = oracle.attention_bwd_keys(q, k, v, do, cu, keys, 0, row_window=(24, 48))
+    np.testing.assert_allclose(p0[0] + p1[0], dk, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(p0[1] + p1[1], dv, rtol=0, atol=1e-12)
+    # and a key window that excludes every key of a row gives it no gradient
+    assert np.all(oracle.attention_bwd_rows(q, k, v, do, cu, [5], 0, key_window=(24, 48)) == 0)

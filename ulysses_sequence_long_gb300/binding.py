@@ -35,7 +35,12 @@ EXPORTED = [
     "usp_cu_seqlens_from_position_ids_noalloc",
     "usp_attn_fwd", "usp_attn_bwd_workspace_bytes", "usp_attn_bwd",
     "usp_attn_bwd_preprocess", "usp_attn_bwd_dkdv", "usp_attn_bwd_dq",
+    "usp_hybrid_relayout_fwd", "usp_hybrid_relayout_bwd", "usp_hybrid_relayout_fwd_qkv",
+    "usp_ring_fwd_merge", "usp_ring_grad_accumulate",
 ]
+
+USP_RING_FIRST = 1
+USP_RING_LAST = 2
 
 
 class UspError(RuntimeError):
@@ -51,7 +56,7 @@ class AttnParams(ctypes.Structure):
         ("D", ctypes.c_int), ("P", ctypes.c_int), ("causal", ctypes.c_int),
         ("window_left", ctypes.c_int), ("softmax_scale", ctypes.c_float),
         ("cu_seqlens", ctypes.c_void_p), ("n_docs", ctypes.c_void_p), ("sinks", ctypes.c_void_p),
-        ("io_layout", ctypes.c_int),
+        ("io_layout", ctypes.c_int), ("ring", ctypes.c_int), ("ring_step", ctypes.c_int),
     ]
 
 
@@ -89,10 +94,17 @@ def load() -> ctypes.CDLL:
     L.usp_attn_bwd_preprocess.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, sz, vp, vp]
     L.usp_attn_bwd_dkdv.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     L.usp_attn_bwd_dq.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+    L.usp_hybrid_relayout_fwd.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp]
+    L.usp_hybrid_relayout_bwd.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp]
+    L.usp_hybrid_relayout_fwd_qkv.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp]
+    L.usp_ring_fwd_merge.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, vp, i32, vp]
+    L.usp_ring_grad_accumulate.argtypes = [vp, vp, vp, sz, i32, vp]
     for name in ("usp_relayout_fwd", "usp_relayout_bwd", "usp_relayout_fwd_qkv",
                  "usp_cu_seqlens_from_position_ids", "usp_cu_seqlens_from_position_ids_noalloc",
                  "usp_attn_fwd", "usp_attn_bwd",
-                 "usp_attn_bwd_preprocess", "usp_attn_bwd_dkdv", "usp_attn_bwd_dq"):
+                 "usp_attn_bwd_preprocess", "usp_attn_bwd_dkdv", "usp_attn_bwd_dq",
+                 "usp_hybrid_relayout_fwd", "usp_hybrid_relayout_bwd", "usp_hybrid_relayout_fwd_qkv",
+                 "usp_ring_fwd_merge", "usp_ring_grad_accumulate"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -168,10 +180,10 @@ def usp_cu_seqlens_from_position_ids_noalloc(pos, B, S, P, cu_seqlens, n_docs, m
 
 
 def attn_params(B, S, Hq, Hkv, D, P, cu_seqlens, n_docs, causal=True, window_left=-1, softmax_scale=0.0,
-                sinks=None, io_layout=USP_IO_HEAD) -> AttnParams:
+                sinks=None, io_layout=USP_IO_HEAD, ring=1, ring_step=0) -> AttnParams:
     return AttnParams(B, S, Hq, Hkv, D, P, 1 if causal else 0, window_left, softmax_scale,
                       _dev(cu_seqlens, "cu_seqlens", torch.int32), _dev(n_docs, "n_docs", torch.int32),
-                      _dev(sinks, "sinks", torch.float32), int(io_layout))
+                      _dev(sinks, "sinks", torch.float32), int(io_layout), int(ring), int(ring_step))
 
 
 def usp_attn_fwd(params: AttnParams, q, k, v, o, lse, dev_status=None, stream=None):
@@ -219,3 +231,35 @@ def usp_attn_bwd_dq(params: AttnParams, q, k, v, lse, dO, dq, ws, dev_status=Non
         _dev(dq, "dq", torch.bfloat16), _dev(ws, "ws"), ws.numel() * ws.element_size(),
         _dev(dev_status, "dev_status", torch.int32), _stream(stream)),
         "usp_attn_bwd_dq")
+
+
+def usp_hybrid_relayout_fwd(x_seq, x_head, B, S, H, D, ring, ulysses, stream=None):
+    _check(load().usp_hybrid_relayout_fwd(_dev(x_seq, "x_seq"), _dev(x_head, "x_head"), B, S, H, D, ring, ulysses,
+                                          x_seq.element_size(), _stream(stream)), "usp_hybrid_relayout_fwd")
+
+
+def usp_hybrid_relayout_bwd(x_head, x_seq, B, S, H, D, ring, ulysses, stream=None):
+    _check(load().usp_hybrid_relayout_bwd(_dev(x_head, "x_head"), _dev(x_seq, "x_seq"), B, S, H, D, ring, ulysses,
+                                          x_head.element_size(), _stream(stream)), "usp_hybrid_relayout_bwd")
+
+
+def usp_hybrid_relayout_fwd_qkv(q_seq, k_seq, v_seq, q_head, k_head, v_head, B, S, Hq, Hkv, D, ring, ulysses,
+                                stream=None):
+    _check(load().usp_hybrid_relayout_fwd_qkv(
+        _dev(q_seq, "q_seq"), _dev(k_seq, "k_seq"), _dev(v_seq, "v_seq"), _dev(q_head, "q_head"),
+        _dev(k_head, "k_head"), _dev(v_head, "v_head"), B, S, Hq, Hkv, D, ring, ulysses, q_seq.element_size(),
+        _stream(stream)), "usp_hybrid_relayout_fwd_qkv")
+
+
+def usp_ring_fwd_merge(params: AttnParams, o_step, lse_step, o_acc, lse_acc, o, lse, flags, stream=None):
+    _check(load().usp_ring_fwd_merge(
+        ctypes.byref(params), _dev(o_step, "o_step", torch.bfloat16), _dev(lse_step, "lse_step", torch.float32),
+        _dev(o_acc, "o_acc", torch.float32), _dev(lse_acc, "lse_acc", torch.float32), _dev(o, "o", torch.bfloat16),
+        _dev(lse, "lse", torch.float32), int(flags), _stream(stream)), "usp_ring_fwd_merge")
+
+
+def usp_ring_grad_accumulate(g_step, g_acc, g_out, flags, stream=None):
+    _check(load().usp_ring_grad_accumulate(
+        _dev(g_step, "g_step", torch.bfloat16), _dev(g_acc, "g_acc", torch.float32),
+        _dev(g_out, "g_out", torch.bfloat16), g_step.numel(), int(flags), _stream(stream)),
+        "usp_ring_grad_accumulate")

@@ -97,27 +97,36 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// H % P == 0: H/P heads per rank.  H < P with P % H == 0: every head is
-// replicated on P/H ranks (the head-layout tensor is P/H times larger); the
+// Ps sequence shards, Ph head blocks (Ps = Ph = P for the Ulysses exchange).
+// H % Ph == 0: H/Ph heads per block.  H < Ph with Ph % H == 0: every head is
+// replicated on Ph/H blocks (the head-layout tensor is Ph/H times larger); the
 // exchange back then sums the replicas, which needs bf16 elements.
-int check_relayout_args(const void* a, const void* b, int B, int S, int H, int D, int P, int eb, bool to_head) {
+int check_relayout_args(const void* a, const void* b, int B, int S, int H, int D, int Ps, int Ph, int eb,
+                        bool to_head) {
   if (a == nullptr || b == nullptr) return USP_ERR_INVALID_ARG;
-  if (B <= 0 || S <= 0 || H <= 0 || D <= 0 || P <= 0) return USP_ERR_INVALID_ARG;
+  if (B <= 0 || S <= 0 || H <= 0 || D <= 0 || Ps <= 0 || Ph <= 0) return USP_ERR_INVALID_ARG;
   if (eb != 1 && eb != 2 && eb != 4 && eb != 8) return USP_ERR_INVALID_ARG;
-  const bool replicated = H < P;
-  if ((replicated ? P % H : H % P) != 0 || S % P != 0) return USP_ERR_INDIVISIBLE;
+  const bool replicated = H < Ph;
+  if ((replicated ? Ph % H : H % Ph) != 0 || S % Ps != 0) return USP_ERR_INDIVISIBLE;
   if (replicated && !to_head && eb != 2) return USP_ERR_UNSUPPORTED;
-  const uint64_t hpr = replicated ? 1 : static_cast<uint64_t>(H / P);
+  const uint64_t hpr = replicated ? 1 : static_cast<uint64_t>(H / Ph);
   uint64_t run = hpr * D * eb;
   if (run % 16 != 0 || !aligned16(a) || !aligned16(b)) return USP_ERR_ALIGNMENT;
   uint64_t seq_vec = static_cast<uint64_t>(B) * S * H * D * eb / 16;
-  uint64_t head_vec = static_cast<uint64_t>(P) * B * S * hpr * D * eb / 16;
-  if (head_vec >= (1ull << 32) || static_cast<uint64_t>(P) * B * S >= (1ull << 32)) return USP_ERR_UNSUPPORTED;
+  uint64_t head_vec = static_cast<uint64_t>(Ph) * B * S * hpr * D * eb / 16;
+  if (head_vec >= (1ull << 32) || static_cast<uint64_t>(Ph) * B * S >= (1ull << 32)) return USP_ERR_UNSUPPORTED;
   const char* pa = static_cast<const char*>(a);
   const char* pb = static_cast<const char*>(b);
   const uint64_t bytes_a = (to_head ? seq_vec : head_vec) * 16, bytes_b = (to_head ? head_vec : seq_vec) * 16;
   if (pa < pb + bytes_b && pb < pa + bytes_a) return USP_ERR_INVALID_ARG;  // buffers overlap
   return USP_OK;
+}
+
+// ring x ulysses shards; 0 when the product is not a positive int
+int hybrid_shards(int ring, int ulysses) {
+  if (ring <= 0 || ulysses <= 0) return 0;
+  const int64_t ps = static_cast<int64_t>(ring) * ulysses;
+  return ps > (1 << 30) ? 0 : static_cast<int>(ps);
 }
 
 int check_attn_params(const usp_attn_params* p) {
@@ -139,6 +148,15 @@ int check_attn_params(const usp_attn_params* p) {
   if (p->io_layout != USP_IO_HEAD && p->io_layout != USP_IO_SEQ) return USP_ERR_INVALID_ARG;
   // fused exchanges: tiles of 128 tokens must never straddle a rank's shard
   if (p->io_layout == USP_IO_SEQ && (p->S / p->P) % 128 != 0) return USP_ERR_UNSUPPORTED;
+  // ring x Ulysses step: the kernels' 256-row blocks never straddle a super-chunk
+  if (p->ring < 0) return USP_ERR_INVALID_ARG;
+  if (p->ring > 1) {
+    if (p->ring_step < 0 || p->ring_step >= p->ring) return USP_ERR_INVALID_ARG;
+    if (p->S % p->ring != 0 || (p->S / p->ring) % 256 != 0 || p->io_layout != USP_IO_HEAD)
+      return USP_ERR_UNSUPPORTED;
+  } else if (p->ring_step != 0) {
+    return USP_ERR_INVALID_ARG;
+  }
   return USP_OK;
 }
 
@@ -166,29 +184,61 @@ int usp_version(void) { return 100; }
 
 int usp_relayout_fwd(const void* x_seq, void* x_head, int B, int S, int H, int D, int P, int eb,
                      usp_stream_t stream) {
-  int rc = check_relayout_args(x_seq, x_head, B, S, H, D, P, eb, true);
+  int rc = check_relayout_args(x_seq, x_head, B, S, H, D, P, P, eb, true);
   if (rc != USP_OK) return rc;
-  return launch_relayout(x_seq, x_head, B, S, H, D, P, eb, true, reinterpret_cast<cudaStream_t>(stream));
+  return launch_relayout(x_seq, x_head, B, S, H, D, P, P, eb, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int usp_relayout_bwd(const void* x_head, void* x_seq, int B, int S, int H, int D, int P, int eb,
                      usp_stream_t stream) {
-  int rc = check_relayout_args(x_head, x_seq, B, S, H, D, P, eb, false);
+  int rc = check_relayout_args(x_head, x_seq, B, S, H, D, P, P, eb, false);
   if (rc != USP_OK) return rc;
-  return launch_relayout(x_head, x_seq, B, S, H, D, P, eb, false, reinterpret_cast<cudaStream_t>(stream));
+  return launch_relayout(x_head, x_seq, B, S, H, D, P, P, eb, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static int relayout_qkv(const void* q_seq, const void* k_seq, const void* v_seq, void* q_head, void* k_head,
+                        void* v_head, int B, int S, int Hq, int Hkv, int D, int Ps, int Ph, int eb,
+                        usp_stream_t stream) {
+  int rc;
+  if (Hq % Ph != 0) return USP_ERR_INDIVISIBLE;  // query heads are never replicated
+  if ((rc = check_relayout_args(q_seq, q_head, B, S, Hq, D, Ps, Ph, eb, true)) != USP_OK) return rc;
+  if ((rc = check_relayout_args(k_seq, k_head, B, S, Hkv, D, Ps, Ph, eb, true)) != USP_OK) return rc;
+  if ((rc = check_relayout_args(v_seq, v_head, B, S, Hkv, D, Ps, Ph, eb, true)) != USP_OK) return rc;
+  const void* src[3] = {q_seq, k_seq, v_seq};
+  void* dst[3] = {q_head, k_head, v_head};
+  int H[3] = {Hq, Hkv, Hkv};
+  return launch_relayout_qkv(src, dst, H, B, S, D, Ps, Ph, eb, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int usp_relayout_fwd_qkv(const void* q_seq, const void* k_seq, const void* v_seq, void* q_head, void* k_head,
                          void* v_head, int B, int S, int Hq, int Hkv, int D, int P, int eb, usp_stream_t stream) {
-  int rc;
-  if (Hq % P != 0) return USP_ERR_INDIVISIBLE;  // query heads are never replicated
-  if ((rc = check_relayout_args(q_seq, q_head, B, S, Hq, D, P, eb, true)) != USP_OK) return rc;
-  if ((rc = check_relayout_args(k_seq, k_head, B, S, Hkv, D, P, eb, true)) != USP_OK) return rc;
-  if ((rc = check_relayout_args(v_seq, v_head, B, S, Hkv, D, P, eb, true)) != USP_OK) return rc;
-  const void* src[3] = {q_seq, k_seq, v_seq};
-  void* dst[3] = {q_head, k_head, v_head};
-  int H[3] = {Hq, Hkv, Hkv};
-  return launch_relayout_qkv(src, dst, H, B, S, D, P, eb, reinterpret_cast<cudaStream_t>(stream));
+  return relayout_qkv(q_seq, k_seq, v_seq, q_head, k_head, v_head, B, S, Hq, Hkv, D, P, P, eb, stream);
+}
+
+int usp_hybrid_relayout_fwd(const void* x_seq, void* x_head, int B, int S, int H, int D, int ring, int ulysses,
+                            int eb, usp_stream_t stream) {
+  const int ps = hybrid_shards(ring, ulysses);
+  if (ps == 0) return USP_ERR_INVALID_ARG;
+  int rc = check_relayout_args(x_seq, x_head, B, S, H, D, ps, ulysses, eb, true);
+  if (rc != USP_OK) return rc;
+  return launch_relayout(x_seq, x_head, B, S, H, D, ps, ulysses, eb, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_hybrid_relayout_bwd(const void* x_head, void* x_seq, int B, int S, int H, int D, int ring, int ulysses,
+                            int eb, usp_stream_t stream) {
+  const int ps = hybrid_shards(ring, ulysses);
+  if (ps == 0) return USP_ERR_INVALID_ARG;
+  int rc = check_relayout_args(x_head, x_seq, B, S, H, D, ps, ulysses, eb, false);
+  if (rc != USP_OK) return rc;
+  return launch_relayout(x_head, x_seq, B, S, H, D, ps, ulysses, eb, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_hybrid_relayout_fwd_qkv(const void* q_seq, const void* k_seq, const void* v_seq, void* q_head,
+                                void* k_head, void* v_head, int B, int S, int Hq, int Hkv, int D, int ring,
+                                int ulysses, int eb, usp_stream_t stream) {
+  const int ps = hybrid_shards(ring, ulysses);
+  if (ps == 0) return USP_ERR_INVALID_ARG;
+  return relayout_qkv(q_seq, k_seq, v_seq, q_head, k_head, v_head, B, S, Hq, Hkv, D, ps, ulysses, eb, stream);
 }
 
 size_t usp_cu_seqlens_workspace_bytes(int B, int S) {
@@ -213,6 +263,8 @@ int usp_attn_fwd(const usp_attn_params* params, const void* q, const void* k, co
                  int32_t* dev_status, usp_stream_t stream) {
   int rc = check_attn_params(params);
   if (rc != USP_OK) return rc;
+  // a ring step leaves the sink out; usp_ring_fwd_merge adds it once at the last step
+  if (params->ring > 1 && params->sinks != nullptr) return USP_ERR_INVALID_ARG;
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr) return USP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return USP_ERR_ALIGNMENT;
@@ -281,6 +333,35 @@ int usp_attn_bwd_dq(const usp_attn_params* params, const void* q, const void* k,
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < attn_bwd_ws_bytes(*params))
     return USP_ERR_WORKSPACE;
   return launch_attn_bwd_dq(*params, q, k, v, lse, dO, dq, ws, dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_ring_fwd_merge(const usp_attn_params* params, const void* o_step, const float* lse_step, float* o_acc,
+                       float* lse_acc, void* o, float* lse, int flags, usp_stream_t stream) {
+  int rc = check_attn_params(params);
+  if (rc != USP_OK) return rc;
+  if (flags & ~(USP_RING_FIRST | USP_RING_LAST)) return USP_ERR_INVALID_ARG;
+  const bool first = flags & USP_RING_FIRST, last = flags & USP_RING_LAST;
+  if (o_step == nullptr || lse_step == nullptr) return USP_ERR_INVALID_ARG;
+  if ((!first || !last) && (o_acc == nullptr || lse_acc == nullptr)) return USP_ERR_INVALID_ARG;
+  if (last && (o == nullptr || lse == nullptr)) return USP_ERR_INVALID_ARG;
+  if (!aligned16(o_step) || (o_acc && !aligned16(o_acc)) || (o && !aligned16(o))) return USP_ERR_ALIGNMENT;
+  if (static_cast<uint64_t>(params->P) * params->B * params->S * (params->Hq / params->P) * (params->D / 8) >=
+      (1ull << 32))
+    return USP_ERR_UNSUPPORTED;
+  return launch_ring_fwd_merge(*params, o_step, lse_step, o_acc, lse_acc, o, lse, flags,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_ring_grad_accumulate(const void* g_step, float* g_acc, void* g_out, size_t n, int flags,
+                             usp_stream_t stream) {
+  if (flags & ~(USP_RING_FIRST | USP_RING_LAST)) return USP_ERR_INVALID_ARG;
+  const bool first = flags & USP_RING_FIRST, last = flags & USP_RING_LAST;
+  if (g_step == nullptr || ((!first || !last) && g_acc == nullptr) || (last && g_out == nullptr))
+    return USP_ERR_INVALID_ARG;
+  if (n % 8 != 0) return USP_ERR_ALIGNMENT;
+  if (!aligned16(g_step) || (g_acc && !aligned16(g_acc)) || (g_out && !aligned16(g_out))) return USP_ERR_ALIGNMENT;
+  if (n / 8 >= (1ull << 32)) return USP_ERR_UNSUPPORTED;
+  return launch_ring_grad_accumulate(g_step, g_acc, g_out, n, flags, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -311,10 +311,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n_docs == 0) return;
   int qlo, qhi;
   query_range(p, n_docs, u0, min(u0 + kBN, p.BS) - 1, qlo, qhi);
+  // ring x Ulysses step: only the queries of the super-chunk that holds this
+  // key/value block at this step
+  int rq0 = 0, rq1 = 0x7FFFFFFF;
+  if (p.ring > 1) {
+    ring_query_window(p, u0, rq0, rq1);
+    qlo = max(qlo, rq0);
+    qhi = min(qhi, rq1);
+  }
   // statistics slices are fetched by TMA from 16-byte aligned tokens; with the
   // exchanges fused, 64-token slices must also stay inside one rank's shard
   qlo &= p.seq_io ? ~(kSL - 1) : ~3;
-  const int n_q = (qhi - qlo + kSL - 1) / kSL;
+  const int n_q = qhi > qlo ? (qhi - qlo + kSL - 1) / kSL : 0;
   const int n_it = n_heads * n_q;
 
   if (tid == 0) {
@@ -435,6 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool key_ok = u < p.BS;
     int a = 0, b = 0;
     if (key_ok) doc_bounds(p.cu, n_docs, p.BS, u, a, b);
+    a = max(a, rq0);  // a ring step: queries of one super-chunk only
+    b = min(b, rq1);
     const uint32_t lb = tmem + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
     // K (group 0) or V (group 1) row of this key into TMEM
     {
@@ -542,8 +552,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n_docs == 0) return;
   int lo, hi;
   key_range(p, n_docs, t0, min(t0 + kBM, p.BS) - 1, lo, hi);
+  int rk0 = 0, rk1 = 0x7FFFFFFF;  // ring x Ulysses step: one key/value super-chunk
+  if (p.ring > 1) {
+    ring_key_window(p, t0, rk0, rk1);
+    lo = max(lo, rk0);
+    hi = min(hi, rk1);
+  }
   if (p.seq_io) lo &= ~(kBN - 1);  // key tiles inside one rank's shard
-  const int n_kv = (hi - lo + kBN - 1) / kBN;
+  const int n_kv = hi > lo ? (hi - lo + kBN - 1) / kBN : 0;
 
   if (tid == 0) {
     mbar_init(&bars->qd_ready, 8);
@@ -663,6 +679,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       lse2 = __ldg(g.stats + plane_index(g.bsp, p.hq, r, j, 0, t));
       dvt = __ldg(g.stats + plane_index(g.bsp, p.hq, r, j, 1, t));
     }
+    a = max(a, rk0);  // a ring step: one key/value super-chunk only
+    b = min(b, rk1);
     const uint32_t s_col = T_S + grp * 64, dp_col = T_DP + grp * 64;
     bool ok = true;
     for (int n = 0; n < n_kv && ok; ++n) {
@@ -696,6 +714,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       __nv_bfloat16* dst = g.dq + row_offset(p, qh, p.hq, p.Hq, row_ok ? t : 0, D) + grp * (D / 2);
       store_row<D / 2>(lb + T_DQ + grp * (D / 2), dst, p.scale, row_ok);
+    } else if (ok && n_kv == 0 && row_ok) {  // no key at this ring step: dQ = 0
+      __nv_bfloat16* dst = g.dq + row_offset(p, qh, p.hq, p.Hq, t, D) + grp * (D / 2);
+      for (int e = 0; e < D / 2; e += 8) *reinterpret_cast<uint4*>(dst + e) = make_uint4(0, 0, 0, 0);
     }
   }
 
@@ -738,6 +759,9 @@ static AttnArgs make_args(const usp_attn_params& prm, int32_t* status) {
   a.status = status;
   a.seq_io = prm.io_layout == USP_IO_SEQ ? 1 : 0;
   a.Sl = prm.S / prm.P;
+  a.ring = prm.ring > 1 ? prm.ring : 1;
+  a.ring_step = a.ring > 1 ? prm.ring_step : 0;
+  a.C = prm.S / a.ring;
   return a;
 }
 

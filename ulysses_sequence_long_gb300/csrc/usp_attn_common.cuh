@@ -33,7 +33,26 @@ struct AttnArgs {
   int32_t* status;
   int seq_io;  // 1: inputs and outputs in seq-layout [P][B][S/P][H][D] (exchanges fused)
   int Sl;      // S/P
+  int ring, ring_step, C;  // ring x Ulysses: ring degree (1: none), step, super-chunk length S/ring
 };
+
+// Ring x Ulysses: at ring step `ring_step` the rows of super-chunk a (of
+// C = S/ring positions) see only the keys of super-chunk (a - ring_step) mod
+// ring, the key/value block their ring rank holds at that step.  Key window
+// [k0, k1) of rank-local token t, and the query window [q0, q1) of key u.
+__device__ __forceinline__ void ring_key_window(const AttnArgs& p, int t, int& k0, int& k1) {
+  const int b = t / p.S, s = t - b * p.S;
+  const int kc = (s / p.C + p.ring - p.ring_step) % p.ring;
+  k0 = b * p.S + kc * p.C;
+  k1 = k0 + p.C;
+}
+
+__device__ __forceinline__ void ring_query_window(const AttnArgs& p, int u, int& q0, int& q1) {
+  const int b = u / p.S, s = u - b * p.S;
+  const int qc = (s / p.C + p.ring_step) % p.ring;
+  q0 = b * p.S + qc * p.C;
+  q1 = q0 + p.C;
+}
 
 // A head as the kernels address it: rank r and local index j in the
 // head-layout [P][B][S][hpr][D], global index g in the seq-layout

@@ -105,10 +105,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       hi = max(hi, h0);
     }
   }
+  // Ring x Ulysses step: only the key/value super-chunk held at this step (the
+  // CTA's 256 rows lie in one super-chunk).
+  int rk0 = 0, rk1 = 0x7FFFFFFF;
+  if (p.ring > 1) {
+    ring_key_window(p, t0, rk0, rk1);
+    lo = max(lo, rk0);
+    hi = min(hi, rk1);
+  }
   // With the exchanges fused, key tiles are aligned to 128 tokens so that a
   // tile never straddles a rank's shard (keys before the document are masked).
   if (p.seq_io) lo &= ~(kBN - 1);
-  const int n_kv = (hi - lo + kBN - 1) / kBN;
+  const int n_kv = hi > lo ? (hi - lo + kBN - 1) / kBN : 0;
+  if (n_kv == 0) {
+    // no key to see (a ring step whose block lies after these rows): O = 0 and
+    // LSE = the sink logit alone, or -inf
+    if (warp < 8) {
+      const int q = warp >> 2, t = t0 + q * kBM + (tid & 127);
+      if (tile_ok[q] && t < p.BS) {
+        uint4* dst = reinterpret_cast<uint4*>(out.o + row_offset(p, qh, p.hq, p.Hq, t, D));
+        for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+        const int bb = t / p.S, ss = t - bb * p.S;
+        out.lse[(static_cast<size_t>(r * p.B + bb) * p.hq + j) * p.S + ss] =
+            p.sinks != nullptr ? __ldg(p.sinks + r * p.hq + j) : -INFINITY;
+      }
+    }
+    return;
+  }
 
   if (tid == 0) {
     for (int q = 0; q < 2; ++q) {
@@ -243,6 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_tm = lane_base + 256 + q * D;
     int a = 0, b = 0;
     if (row_ok) doc_bounds(p.cu, n_docs, p.BS, t, a, b);
+    a = max(a, rk0);  // a ring step sees one key/value super-chunk
+    b = min(b, rk1);
     const int gh = r * p.hq + j;  // global query head: the sink slice of this rank
     float m = -INFINITY, l = 0.f;
     if (p.sinks != nullptr) {
@@ -401,6 +426,9 @@ int launch_attn_fwd(const usp_attn_params& prm, const void* q, const void* k, co
   a.status = status;
   a.seq_io = prm.io_layout == USP_IO_SEQ ? 1 : 0;
   a.Sl = prm.S / prm.P;
+  a.ring = prm.ring > 1 ? prm.ring : 1;
+  a.ring_step = a.ring > 1 ? prm.ring_step : 0;
+  a.C = prm.S / a.ring;
   if (prm.D == 128) return run_fwd<128>(prm, a, q, k, v, o, lse, st);
   return run_fwd<64>(prm, a, q, k, v, o, lse, st);
 }

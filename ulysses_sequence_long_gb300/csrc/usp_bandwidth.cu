@@ -131,8 +131,13 @@ __global__ void __launch_bounds__(kRelayoutThreads) relayout_qkv_kernel(Relayout
                       nb * blockDim.x);
 }
 
-static RelayoutGeom make_geom(int B, int S, int H, int D, int P, int eb, bool to_head) {
+// Ps sequence shards, Ph head blocks: Ps = Ph = P for the Ulysses exchange;
+// for the ring x Ulysses hybrid Ps = ring*ulysses shards and Ph = ulysses
+// blocks, each block holding the whole sequence (the ring ranks' super-chunks
+// end to end).  The shard of a position is s / (S/Ps) in both cases.
+static RelayoutGeom make_geom(int B, int S, int H, int D, int Ps, int Ph, int eb, bool to_head) {
   RelayoutGeom g;
+  const int P = Ph;
   const int hpr = H >= P ? H / P : 1, rep = H >= P ? 1 : P / H;
   uint64_t run_bytes = static_cast<uint64_t>(hpr) * D * eb;
   uint64_t seq_vec = static_cast<uint64_t>(B) * S * H * D * eb / 16;
@@ -140,10 +145,10 @@ static RelayoutGeom make_geom(int B, int S, int H, int D, int P, int eb, bool to
   g.run_vec = FastDiv(static_cast<uint32_t>(run_bytes / 16));
   g.S = FastDiv(S);
   g.B = FastDiv(B);
-  g.Sl = FastDiv(S / P);
+  g.Sl = FastDiv(S / Ps);
   g.R = FastDiv(H / hpr);
   g.rep = FastDiv(rep);
-  g.Sl_u = S / P;
+  g.Sl_u = S / Ps;
   g.B_u = B;
   g.S_u = S;
   g.R_u = H / hpr;
@@ -159,9 +164,9 @@ static int relayout_grid(uint64_t n_vec) {
   return static_cast<int>(want < 1 ? 1 : want);
 }
 
-int launch_relayout(const void* src, void* dst, int B, int S, int H, int D, int P, int eb, bool to_head,
+int launch_relayout(const void* src, void* dst, int B, int S, int H, int D, int Ps, int Ph, int eb, bool to_head,
                     cudaStream_t st) {
-  RelayoutGeom g = make_geom(B, S, H, D, P, eb, to_head);
+  RelayoutGeom g = make_geom(B, S, H, D, Ps, Ph, eb, to_head);
   if (g.n_vec == 0) return USP_OK;
   int grid = relayout_grid(g.n_vec);
   if (!to_head && g.rep_u > 1)
@@ -173,14 +178,14 @@ int launch_relayout(const void* src, void* dst, int B, int S, int H, int D, int 
   return check_launch();
 }
 
-int launch_relayout_qkv(const void* const src[3], void* const dst[3], const int H[3], int B, int S, int D, int P,
-                        int eb, cudaStream_t st) {
+int launch_relayout_qkv(const void* const src[3], void* const dst[3], const int H[3], int B, int S, int D, int Ps,
+                        int Ph, int eb, cudaStream_t st) {
   Relayout3 a;
   uint64_t total = 0, nv[3];
   for (int t = 0; t < 3; ++t) {
     a.src[t] = static_cast<const int4*>(src[t]);
     a.dst[t] = static_cast<int4*>(dst[t]);
-    a.g[t] = make_geom(B, S, H[t], D, P, eb, true);
+    a.g[t] = make_geom(B, S, H[t], D, Ps, Ph, eb, true);
     nv[t] = a.g[t].n_vec;
     total += nv[t];
   }

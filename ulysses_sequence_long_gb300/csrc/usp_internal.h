@@ -35,10 +35,15 @@ struct FastDiv {
 #endif
 };
 
-int launch_relayout(const void* src, void* dst, int B, int S, int H, int D, int P, int elem_bytes, bool to_head,
-                    cudaStream_t st);
-int launch_relayout_qkv(const void* const src[3], void* const dst[3], const int H[3], int B, int S, int D, int P,
-                        int elem_bytes, cudaStream_t st);
+// Ps sequence shards, Ph head blocks (Ps = Ph = P: the Ulysses exchange;
+// Ps = ring*ulysses, Ph = ulysses: the exchange of the ring x Ulysses hybrid).
+int launch_relayout(const void* src, void* dst, int B, int S, int H, int D, int Ps, int Ph, int elem_bytes,
+                    bool to_head, cudaStream_t st);
+int launch_relayout_qkv(const void* const src[3], void* const dst[3], const int H[3], int B, int S, int D, int Ps,
+                        int Ph, int elem_bytes, cudaStream_t st);
+int launch_ring_fwd_merge(const usp_attn_params& p, const void* o_step, const float* lse_step, float* o_acc,
+                          float* lse_acc, void* o, float* lse, int flags, cudaStream_t st);
+int launch_ring_grad_accumulate(const void* g_step, float* g_acc, void* g_out, size_t n, int flags, cudaStream_t st);
 int launch_cu_seqlens(const int32_t* pos, int B, int S, int P, int32_t* cu, int32_t* n_docs, int32_t* max_len,
                       int32_t* ws, int32_t* status, cudaStream_t st);
 size_t cu_seqlens_ws_bytes(int B, int S);

@@ -84,7 +84,11 @@ LLAMA8K_PROFILE = Workload("llama3_8b_gqa_packed_s8192", B=1, S=8192, Hq=32, Hkv
 # packed case at sp size 16, each of the 8 key/value heads on 2 ranks.
 LLAMA32K_P16 = Workload("llama3_8b_gqa_packed_s32768_p16", B=1, S=32768, Hq=32, Hkv=8, D=128, P=16,
                         doc_mode="geometric", doc_mean=4096)
-BY_NAME = {w.name: w for w in ALL + [LLAMA8K_PROFILE, LLAMA32K_P16]}
+# ring x Ulysses hybrid: the same Llama-shaped workload over 8 ranks as ring 2
+# x ulysses 4 (the yunchang test's mesh shape with the degrees swapped).
+LLAMA32K_RING2 = Workload("llama3_8b_gqa_packed_s32768_ring2x4", B=1, S=32768, Hq=32, Hkv=8, D=128, P=8,
+                          ring=2, doc_mode="geometric", doc_mean=4096)
+BY_NAME = {w.name: w for w in ALL + [LLAMA8K_PROFILE, LLAMA32K_P16, LLAMA32K_RING2]}
 
 
 def document_lengths(w: Workload) -> List[List[int]]:
