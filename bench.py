@@ -477,6 +477,7 @@ def main():
                        "documents": len(W.document_lengths(w)[0]), "visible_pairs_per_head": fl["pairs"],
                        "fwd_bwd_flop": fl["total"], "parallelism": f"emulated ulysses P={w.P}, replicas={world}",
                        "exchanges": "fused" if step.ua.fused else "explicit", "ring": w.ring,
+                       "dq_pass": "stored dS" if step.ua.stored_ds else "recomputed S and dP",
                        "l2": "inputs larger than L2 (no flush)"},
             "relayout_gbs": relayout_gbs, "relayout_frac_hbm": relayout_gbs / peaks["hbm_gbs"],
             "relayout_measured": relayout_note,

@@ -270,6 +270,19 @@ int usp_ring_fwd_merge(const usp_attn_params* params, const void* o_step, const 
 int usp_ring_grad_accumulate(const void* g_step, float* g_acc, void* g_out, size_t n, int flags,
                              usp_stream_t stream);
 
+/* Workspace that enables the faster backward: the dK/dV pass also stores dS
+ * (bf16 blocks of [128 keys][64 queries] for every (query head, row, key tile,
+ * query slice) pair a causal mask can reach) and the dQ pass computes
+ * dQ = scale * dS K from them instead of recomputing S and dP.  Returns the
+ * whole workspace size (the statistics of usp_attn_bwd_workspace_bytes plus
+ * the blocks), or 0 when the shape has no such path (causal == 0, or S not a
+ * multiple of 128).  The blocks' count depends only on the shape (the longest
+ * possible document), so it is known without reading cu_seqlens.  Any
+ * backward call given ws_bytes >= this size takes the stored-dS path; the
+ * dK/dV and dQ calls of one backward must get the same ws and ws_bytes, with
+ * the dK/dV call first. */
+size_t usp_attn_bwd_fast_workspace_bytes(const usp_attn_params* params);
+
 /* Bytes of workspace usp_attn_bwd needs: the fp32 row statistic
  * D_t = sum_d dO_td O_td for every query row and head, 256-byte aligned. */
 size_t usp_attn_bwd_workspace_bytes(const usp_attn_params* params);

@@ -18,10 +18,10 @@ def _lib():
     built_lib()
 
 
-def _fwd_bwd(w, fused=False):
+def _fwd_bwd(w, fused=False, stored_ds=None):
     from ulysses_sequence_long_gb300.pipeline import UlyssesAttention
     dev, host = device_inputs(w)
-    ua = UlyssesAttention(shape_of(w), with_backward=True, fused=fused)
+    ua = UlyssesAttention(shape_of(w), with_backward=True, fused=fused, stored_ds=stored_ds)
     ua.forward(dev["q"], dev["k"], dev["v"], dev["pos"], dev["sinks"])
     ua.backward(dev["do"], dev["sinks"])
     torch.cuda.synchronize()
@@ -47,12 +47,16 @@ SMALL = [
 ]
 
 
-CASES = [(w, f) for w in SMALL for f in modes(w)]
+# both dQ passes: from the stored dS blocks (causal shapes) and by recomputing S and dP
+CASES = [(w, f, d) for w in SMALL for f in modes(w) for d in ([True, False] if w.causal else [False])]
 
 
-@pytest.mark.parametrize("w,fused", CASES, ids=[f"{w.name}-{'fused' if f else 'explicit'}" for w, f in CASES])
-def test_backward_full_parity_small(w, fused):
-    ua, dev, host = _fwd_bwd(w, fused)
+@pytest.mark.parametrize("w,fused,stored_ds", CASES,
+                         ids=[f"{w.name}-{'fused' if f else 'explicit'}-{'stored_ds' if d else 'recompute'}"
+                              for w, f, d in CASES])
+def test_backward_full_parity_small(w, fused, stored_ds):
+    ua, dev, host = _fwd_bwd(w, fused, stored_ds)
+    assert ua.stored_ds == stored_ds
     snk = host["sinks"]
     f = oracle.ulysses_fwd(host["q"], host["k"], host["v"], host["pos"], w.causal, w.window_left, None, snk)
     g = oracle.ulysses_bwd(f, host["do"], w.causal, w.window_left, None, snk)
@@ -89,15 +93,15 @@ def _gpu_head(ua, name, w, r, heads):
     return np.stack([head_values(ua, name, r, j, heads) for j in range(heads)], axis=1)
 
 
-@pytest.mark.parametrize("w,groups,fused", [
-    (W.GPTOSS_WIN, [(0, 0), (5, 0)], True),
-    (W.LLAMA32K, [(2, 0), (7, 0)], True),
-    (W.LLAMA32K, [(4, 0)], False),
-], ids=["gptoss_win-fused", "llama32k-fused", "llama32k-explicit"])
-def test_backward_full_size_whole_groups(w, groups, fused):
+@pytest.mark.parametrize("w,groups,fused,stored_ds", [
+    (W.GPTOSS_WIN, [(0, 0), (5, 0)], True, True),
+    (W.LLAMA32K, [(2, 0), (7, 0)], True, True),
+    (W.LLAMA32K, [(4, 0)], False, False),
+], ids=["gptoss_win-fused-stored_ds", "llama32k-fused-stored_ds", "llama32k-explicit-recompute"])
+def test_backward_full_size_whole_groups(w, groups, fused, stored_ds):
     """Every query head of a GQA group on a rank: dQ of those heads and the
     complete dK/dV of their key/value head, compared element by element."""
-    ua, dev, host = _fwd_bwd(w, fused)
+    ua, dev, host = _fwd_bwd(w, fused, stored_ds)
     G = w.Hq // w.Hkv
     for r, kvh in groups:
         qh, kh, vh, doh, cu, snk = _rank_views(w, host, r)

@@ -24,10 +24,10 @@ def _bits(t):
     return t.contiguous().view(torch.int16).cpu().numpy()
 
 
-def _run(w, backward=True):
+def _run(w, backward=True, stored_ds=None):
     from ulysses_sequence_long_gb300.pipeline import HybridAttention
     dev, host = device_inputs(w)
-    ha = HybridAttention(shape_of(w), w.ring, with_backward=backward)
+    ha = HybridAttention(shape_of(w), w.ring, with_backward=backward, stored_ds=stored_ds)
     ha.forward(dev["q"], dev["k"], dev["v"], dev["pos"], dev["sinks"])
     if backward:
         ha.backward(dev["do"], dev["sinks"])
@@ -73,9 +73,14 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
-def test_hybrid_full_parity_small(w):
-    ha, dev, host = _run(w)
+CASES = [(w, d) for w in SMALL for d in ([True, False] if w.causal else [False])]
+
+
+@pytest.mark.parametrize("w,stored_ds", CASES,
+                         ids=[f"{w.name}-{'stored_ds' if d else 'recompute'}" for w, d in CASES])
+def test_hybrid_full_parity_small(w, stored_ds):
+    ha, dev, host = _run(w, stored_ds=stored_ds)
+    assert ha.stored_ds == stored_ds
     snk = host["sinks"]
     kw = dict(causal=w.causal, window_left=w.window_left, sinks=snk)
     f = oracle.hybrid_fwd(host["q"], host["k"], host["v"], host["pos"], w.ring, **kw)

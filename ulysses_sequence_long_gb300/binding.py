@@ -36,7 +36,7 @@ EXPORTED = [
     "usp_attn_fwd", "usp_attn_bwd_workspace_bytes", "usp_attn_bwd",
     "usp_attn_bwd_preprocess", "usp_attn_bwd_dkdv", "usp_attn_bwd_dq",
     "usp_hybrid_relayout_fwd", "usp_hybrid_relayout_bwd", "usp_hybrid_relayout_fwd_qkv",
-    "usp_ring_fwd_merge", "usp_ring_grad_accumulate",
+    "usp_ring_fwd_merge", "usp_ring_grad_accumulate", "usp_attn_bwd_fast_workspace_bytes",
 ]
 
 USP_RING_FIRST = 1
@@ -90,6 +90,8 @@ def load() -> ctypes.CDLL:
     L.usp_attn_fwd.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, vp, vp]
     L.usp_attn_bwd_workspace_bytes.restype = sz
     L.usp_attn_bwd_workspace_bytes.argtypes = [ctypes.POINTER(AttnParams)]
+    L.usp_attn_bwd_fast_workspace_bytes.restype = sz
+    L.usp_attn_bwd_fast_workspace_bytes.argtypes = [ctypes.POINTER(AttnParams)]
     L.usp_attn_bwd.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     L.usp_attn_bwd_preprocess.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, sz, vp, vp]
     L.usp_attn_bwd_dkdv.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
@@ -195,6 +197,10 @@ def usp_attn_fwd(params: AttnParams, q, k, v, o, lse, dev_status=None, stream=No
 
 def usp_attn_bwd_workspace_bytes(params: AttnParams) -> int:
     return int(load().usp_attn_bwd_workspace_bytes(ctypes.byref(params)))
+
+
+def usp_attn_bwd_fast_workspace_bytes(params: AttnParams) -> int:
+    return int(load().usp_attn_bwd_fast_workspace_bytes(ctypes.byref(params)))
 
 
 def usp_attn_bwd(params: AttnParams, q, k, v, o, lse, dO, dq, dk, dv, dsinks, ws, dev_status=None, stream=None):

@@ -89,6 +89,37 @@ int make_stats_tmap(CUtensorMap* m, const void* base, int BS, int pitch, int row
   return rc == CUDA_SUCCESS ? USP_OK : USP_ERR_CUDA;
 }
 
+// Tensor map of the stored dS blocks, bf16 [n_blocks][128 keys][64 queries]:
+// dims {64, 128, n_blocks}, box {64, 128, 2} (the two 64-query blocks of one
+// 128-row query tile, stored next to each other), 128-byte swizzle.
+int make_ds_tmap(CUtensorMap* m, const void* base, long long n_blocks) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return USP_ERR_CUDA;
+  cuuint64_t dims[3] = {64, 128, static_cast<cuuint64_t>(n_blocks)};
+  cuuint64_t strides[2] = {128, 128 * 128};
+  cuuint32_t box[3] = {64, 128, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult rc = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS ? USP_OK : USP_ERR_CUDA;
+}
+
+// The same blocks as store targets of one compute warp: box {32, 32, 1} (32
+// query columns of 32 key rows, 64-byte rows), 64-byte swizzle.
+int make_ds_store_tmap(CUtensorMap* m, void* base, long long n_blocks) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return USP_ERR_CUDA;
+  cuuint64_t dims[3] = {64, 128, static_cast<cuuint64_t>(n_blocks)};
+  cuuint64_t strides[2] = {128, 128 * 128};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult rc = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS ? USP_OK : USP_ERR_CUDA;
+}
+
 }  // namespace usp
 
 using namespace usp;
@@ -271,6 +302,12 @@ int usp_attn_fwd(const usp_attn_params* params, const void* q, const void* k, co
   return launch_attn_fwd(*params, q, k, v, o, lse, dev_status, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t usp_attn_bwd_fast_workspace_bytes(const usp_attn_params* params) {
+  if (check_attn_params(params) != USP_OK) return 0;
+  const size_t ds = attn_bwd_ds_bytes(*params);
+  return ds == 0 ? 0 : attn_bwd_ws_bytes(*params) + ds;
+}
+
 size_t usp_attn_bwd_workspace_bytes(const usp_attn_params* params) {
   if (check_attn_params(params) != USP_OK) return 0;
   return attn_bwd_ws_bytes(*params);
@@ -289,8 +326,8 @@ int usp_attn_bwd(const usp_attn_params* params, const void* q, const void* k, co
     return USP_ERR_ALIGNMENT;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < attn_bwd_ws_bytes(*params))
     return USP_ERR_WORKSPACE;
-  return launch_attn_bwd(*params, q, k, v, o, lse, dO, dq, dk, dv, params->sinks ? dsinks : nullptr, ws, dev_status,
-                         reinterpret_cast<cudaStream_t>(stream));
+  return launch_attn_bwd(*params, q, k, v, o, lse, dO, dq, dk, dv, params->sinks ? dsinks : nullptr, ws, ws_bytes,
+                         dev_status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int usp_attn_bwd_preprocess(const usp_attn_params* params, const void* o, const float* lse, const void* dO,
@@ -318,7 +355,8 @@ int usp_attn_bwd_dkdv(const usp_attn_params* params, const void* q, const void* 
     return USP_ERR_ALIGNMENT;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < attn_bwd_ws_bytes(*params))
     return USP_ERR_WORKSPACE;
-  return launch_attn_bwd_dkdv(*params, q, k, v, lse, dO, dk, dv, ws, dev_status, reinterpret_cast<cudaStream_t>(stream));
+  return launch_attn_bwd_dkdv(*params, q, k, v, lse, dO, dk, dv, ws, ws_bytes, dev_status,
+                              reinterpret_cast<cudaStream_t>(stream));
 }
 
 int usp_attn_bwd_dq(const usp_attn_params* params, const void* q, const void* k, const void* v, const float* lse,
@@ -332,7 +370,8 @@ int usp_attn_bwd_dq(const usp_attn_params* params, const void* q, const void* k,
     return USP_ERR_ALIGNMENT;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < attn_bwd_ws_bytes(*params))
     return USP_ERR_WORKSPACE;
-  return launch_attn_bwd_dq(*params, q, k, v, lse, dO, dq, ws, dev_status, reinterpret_cast<cudaStream_t>(stream));
+  return launch_attn_bwd_dq(*params, q, k, v, lse, dO, dq, ws, ws_bytes, dev_status,
+                            reinterpret_cast<cudaStream_t>(stream));
 }
 
 int usp_ring_fwd_merge(const usp_attn_params* params, const void* o_step, const float* lse_step, float* o_acc,

@@ -32,6 +32,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "usp_attn_common.cuh"
 #include "usp_internal.h"
@@ -230,12 +231,14 @@ struct Cfg {
   static constexpr int NCH = D / 64;
   static constexpr int SLICE = NCH * kSliceBytes;  // 64-row bf16 tile
   static constexpr int STAT = 2 * kSL * 4;        // [2][64] fp32: LSE*log2e, D
-  static constexpr int NST = (D == 128) ? 6 : 8;  // stages of the streamed slices
-  // dK/dV: ring of (Q, dO, stats) 64-query slices
+  static constexpr int NST = (D == 128) ? 5 : 8;  // stages of the streamed slices
+  // dK/dV: ring of (Q, dO, stats) 64-query slices, then two 2 KB dS staging
+  // buffers per compute warp (its [32 keys][32 queries] part of a dS block)
   static constexpr int A_Q = 0;
   static constexpr int A_DO = A_Q + NST * SLICE;
   static constexpr int A_STAT = A_DO + NST * SLICE;
-  static constexpr int A_BAR = A_STAT + NST * STAT;
+  static constexpr int A_DS = (A_STAT + NST * STAT + 1023) / 1024 * 1024;
+  static constexpr int A_BAR = A_DS + 8 * 2 * 2048;
   static constexpr int A_SMEM = A_BAR + 1024 + 1024;
   // dQ: ring of (K, V) 128-key tiles
   static constexpr int TILE = NCH * kBN * 128;       // 128-row bf16 tile
@@ -265,6 +268,31 @@ struct BarsB {
   int abort;
 };
 
+// Stored dS blocks (the dK/dV pass writes them, the dQ pass reads them): one
+// block = [128 keys][64 queries] bf16 of one (query head, batch row, key tile
+// kt, 64-query slice qs), dS^T rows of 128 bytes.  Causal masks only: key tile
+// kt meets the slices qs in [2kt, 2kt + n(kt)), n(kt) = min(N - 2kt, Wc), with
+// N = S/64 slices per row and Wc = 2 (1 + ceil(window_left/128)) (N without a
+// window).  Blocks of one (head, row) are numbered by key tile, then slice:
+//   off(kt) = sum_{k < kt} n(k),  block(kt, qs) = off(kt) + qs - 2kt.
+struct DsGeom {
+  int N;              // 64-query slices per row
+  int Wc;             // slices a key tile may meet (N without a window)
+  int kc;             // key tiles [0, kc) meet Wc slices, later ones N - 2k
+  long long per_row;  // blocks per (query head, batch row)
+};
+
+__host__ __device__ __forceinline__ int ds_count(const DsGeom& g, int kt) {
+  const int n = g.N - 2 * kt;
+  return n < g.Wc ? n : g.Wc;
+}
+
+__host__ __device__ __forceinline__ long long ds_off(const DsGeom& g, int kt) {
+  if (kt <= g.kc) return static_cast<long long>(kt) * g.Wc;
+  const long long k = kt, c = g.kc;
+  return c * g.Wc + (k - c) * g.N - (k * (k - 1) - c * (c - 1));
+}
+
 struct Grads {
   const __nv_bfloat16* q;  // head layout, read row by row into TMEM
   const __nv_bfloat16* k;
@@ -275,7 +303,9 @@ struct Grads {
   __nv_bfloat16* dv;
   const float* stats;  // planar [P*hq][2][bsp]
   int bsp;
-  int n_tiles;  // 128-token tiles per rank
+  int n_tiles;         // 128-token tiles per rank
+  __nv_bfloat16* ds;   // stored dS blocks, or null (the dQ pass recomputes S and dP)
+  DsGeom dsg;
 };
 
 // --------------------------------------------------------------- dK / dV
@@ -287,7 +317,8 @@ struct Grads {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
-                const __grid_constant__ CUtensorMap tst, AttnArgs p, Grads g) {
+                const __grid_constant__ CUtensorMap tst, const __grid_constant__ CUtensorMap tds_st, AttnArgs p,
+                Grads g) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -320,10 +351,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     qhi = min(qhi, rq1);
   }
   // statistics slices are fetched by TMA from 16-byte aligned tokens; with the
-  // exchanges fused, 64-token slices must also stay inside one rank's shard
-  qlo &= p.seq_io ? ~(kSL - 1) : ~3;
+  // exchanges fused, 64-token slices must also stay inside one rank's shard.
+  // When dS is stored, whole 128-row query tiles are covered (their extra rows
+  // are masked, so their blocks hold zeros): the dQ pass then finds a block
+  // for every (key tile, query tile) pair it meets.
+  const bool store_ds = g.ds != nullptr;
+  if (store_ds) {
+    qlo &= ~(kBM - 1);
+    qhi = (qhi + kBM - 1) & ~(kBM - 1);
+  } else {
+    qlo &= p.seq_io ? ~(kSL - 1) : ~3;
+  }
   const int n_q = qhi > qlo ? (qhi - qlo + kSL - 1) / kSL : 0;
   const int n_it = n_heads * n_q;
+  // stored dS: this key tile's place in the block numbering of its row
+  const int ds_rowb = u0 / p.S, ds_row0 = ds_rowb * p.S, ds_kt = (u0 - ds_row0) / kBN;
+  const int ds_cnt = store_ds ? ds_count(g.dsg, ds_kt) : 0;
+  const long long ds_off0 = store_ds ? ds_off(g.dsg, ds_kt) : 0;
 
   if (tid == 0) {
     mbar_init(&bars->kv_ready, 8);
@@ -455,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars->kv_ready);
     }
     bool ok = true;
+    int ds_slot = 0;  // dS blocks this warp has staged
     for (int i = 0; i < n_it && ok; ++i) {
       const int s = i % C::NST;
       const uint32_t ph = i & 1;
@@ -497,6 +542,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) x[4 * c4 + e] = pr[4 * c4 + e] * (x[4 * c4 + e] - dv[e]);
       }
+      if (store_ds) {
+        // The warp's [32 key rows][32 query columns] part of dS^T block (head,
+        // row, kt, qs): staged in shared memory in the 64-byte swizzle (16-byte
+        // chunk e of row r at r*64 + (e ^ (r>>1 & 3))*16: every store instruction
+        // is conflict-free) and written by one TMA store of the warp.
+        const int hg = hg0 + i / n_q;
+        const int qs = (qlo - ds_row0) / kSL + i % n_q;
+        const int rel = qs - 2 * ds_kt;
+        if (rel >= 0 && rel < ds_cnt) {
+          const long long blk = (static_cast<long long>(hg) * p.B + ds_rowb) * g.dsg.per_row + ds_off0 + rel;
+          uint8_t* buf = smem + C::A_DS + (warp * 2 + (ds_slot & 1)) * 2048;
+          if (ds_slot >= 2 && lane == 0) bulk_wait_group_read<1>();  // its store from two rounds ago has read it
+          __syncwarp();
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<uint4*>(buf + lane * 64 + ((e ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(pack_bf16x2(x[8 * e], x[8 * e + 1]), pack_bf16x2(x[8 * e + 2], x[8 * e + 3]),
+                           pack_bf16x2(x[8 * e + 4], x[8 * e + 5]), pack_bf16x2(x[8 * e + 6], x[8 * e + 7]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tds_st, buf, grp * 32, (warp & 3) * 32, static_cast<int>(blk));
+            bulk_commit_group();
+          }
+          ++ds_slot;
+        }
+      }
       tmem_st_packed<16>(lb + T_DP + grp * 32, x);
       tc_fence_before();
       __syncwarp();
@@ -513,6 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16* dst = (grp == 0 ? g.dv : g.dk) + row_offset(p, kvh, p.hk, p.Hkv, u, D);
       for (int e = 0; e < D; e += 8) *reinterpret_cast<uint4*>(dst + e) = make_uint4(0, 0, 0, 0);
     }
+    if (ds_slot > 0 && lane == 0) bulk_wait_group_all();  // the dS stores are complete before the CTA ends
   }
 
   tc_fence_before();
@@ -728,6 +801,169 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// --------------------------------------------------------------- dQ from stored dS
+// dQ_t = scale sum_u dS_tu k_u with dS read back from the blocks the dK/dV
+// pass stored: no recomputation of S and dP, one GEMM per key tile.  CTA =
+// (rank, query head, 128 rows).  Per 128-key tile the two 64-query dS blocks
+// (A operand, MN-major: queries contiguous) and the K tile (B operand,
+// MN-major: D contiguous) stream through a shared-memory ring; dQ accumulates
+// in TMEM (128 lanes x D columns).  dS holds the masks already, so no mask is
+// evaluated here.  Warps 0-3: epilogue, warp 4: TMA producer, warp 5: MMA.
+constexpr int kDsThreads = 192;
+
+template <int D>
+struct CfgDs {
+  static constexpr int NCH = D / 64;
+  static constexpr int DSB = 2 * kBN * 128;     // two [128 keys][64 queries] bf16 blocks
+  static constexpr int KT = NCH * kBN * 128;    // K tile [128 keys][D]
+  static constexpr int STAGE = DSB + KT;
+  static constexpr int NST = (D == 128) ? 3 : 4;
+  static constexpr int BAR = NST * STAGE;
+  static constexpr int SMEM = BAR + 1024 + 1024;
+};
+
+struct BarsDs {
+  uint64_t full[4], empty[4];
+  uint64_t fin, mma_done;
+  uint32_t tmem;
+  int abort;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kDsThreads, 1)
+    dq_ds_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tds, AttnArgs p,
+                 Grads g) {
+  using C = CfgDs<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  BarsDs* bars = reinterpret_cast<BarsDs*>(smem + C::BAR);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // late query tiles first (they meet the most key tiles)
+  const int per = p.P * p.hq;
+  const int qt = g.n_tiles - 1 - static_cast<int>(blockIdx.x) / per;
+  const int rem = static_cast<int>(blockIdx.x) % per;
+  const int r = rem / p.hq, j = rem % p.hq;
+  const HeadRef qh = q_head_ref(p, r, j), kvh = kv_head_ref(p, r, j / p.G);
+  const int t0 = qt * kBM;
+
+  const int n_docs = checked_docs(p);
+  if (n_docs == 0) return;
+  int lo, hi;
+  key_range(p, n_docs, t0, min(t0 + kBM, p.BS) - 1, lo, hi);
+  if (p.ring > 1) {  // ring x Ulysses step: one key/value super-chunk
+    int rk0, rk1;
+    ring_key_window(p, t0, rk0, rk1);
+    lo = max(lo, rk0);
+    hi = min(hi, rk1);
+  }
+  const int rowb = t0 / p.S, row0 = rowb * p.S;
+  lo = row0 + ((lo - row0) & ~(kBN - 1));  // blocks belong to aligned key tiles
+  const int n_kv = hi > lo ? (hi - lo + kBN - 1) / kBN : 0;
+  const int kt0 = (lo - row0) / kBN;
+  const int qs0 = (t0 - row0) / kSL;       // the tile's first 64-query slice
+  const long long head_base = (static_cast<long long>(r * p.hq + j) * p.B + rowb) * g.dsg.per_row;
+
+  if (n_kv == 0) {  // no key at this ring step: dQ = 0
+    if (warp < 4) {
+      const int t = t0 + warp * 32 + lane;
+      if (t < p.BS) {
+        uint4* dst = reinterpret_cast<uint4*>(g.dq + row_offset(p, qh, p.hq, p.Hq, t, D));
+        for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    return;
+  }
+
+  if (tid == 0) {
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    mbar_init(&bars->fin, 1);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem, D);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  volatile int* abort = &bars->abort;
+  const uint32_t sbase = smem_u32(smem);
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tds);
+      int issued = 0;
+      for (int n = 0; n < n_kv; ++n) {
+        const int s = n % C::NST;
+        if (n >= C::NST && !mbar_wait(&bars->empty[s], ((n / C::NST) - 1) & 1, abort, p.status)) break;
+        const int kt = kt0 + n, rel = qs0 - 2 * kt;
+        // the dK/dV pass covered whole query tiles, so both blocks exist for
+        // every key tile this query tile meets; anything else is a broken
+        // invariant, recorded instead of read
+        if (rel < 0 || rel + 1 >= ds_count(g.dsg, kt)) {
+          set_status(p.status, USP_ERR_BAD_SEQLENS);
+          *abort = 1;
+          break;
+        }
+        uint8_t* st = smem + s * C::STAGE;
+        mbar_arrive_expect_tx(&bars->full[s], C::STAGE);
+        tma_load_3d(st, &tds, &bars->full[s], 0, 0, static_cast<int>(head_base + ds_off(g.dsg, kt) + rel));
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_rows(st + C::DSB + c * kAtomBytes, &tk, &bars->full[s], p, c, kvh, row0 + kt * kBN);
+        issued = n + 1;
+      }
+      // never leave the CTA with copies still landing in its shared memory
+      for (int n = max(0, issued - C::NST); n < issued; ++n)
+        mbar_wait(&bars->full[n % C::NST], (n / C::NST) & 1, abort, p.status);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kBM, D, true, true);  // [128 queries x D], K = 128 keys
+      bool ok = true;
+      for (int n = 0; n < n_kv && ok; ++n) {
+        const int s = n % C::NST;
+        if (!(ok = mbar_wait(&bars->full[s], (n / C::NST) & 1, abort, p.status))) break;
+        tc_fence_after();
+        const uint32_t a = sbase + s * C::STAGE, b = a + C::DSB;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ss(tmem, mnmajor_desc(a, kBN * 128, kk), mnmajor_desc(b, kAtomBytes, kk), idesc,
+                 (n > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars->empty[s]);
+      }
+      if (ok) mma_commit(&bars->fin);
+      mma_commit(&bars->mma_done);
+      mbar_wait(&bars->mma_done, 0, abort, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int t = t0 + warp * 32 + lane;
+    const bool row_ok = t < p.BS;
+    if (mbar_wait(&bars->fin, 0, abort, p.status)) {
+      tc_fence_after();
+      const uint32_t lb = tmem + ((static_cast<uint32_t>(warp) * 32) << 16);
+      store_row<D>(lb, g.dq + row_offset(p, qh, p.hq, p.Hq, row_ok ? t : 0, D), p.scale, row_ok);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, D);
+  }
+}
+
 }  // namespace bwd
 
 static int stats_row_pitch(int BS) { return (BS + 3) & ~3; }
@@ -736,6 +972,30 @@ size_t attn_bwd_ws_bytes(const usp_attn_params& p) {
   // planar {LSE*log2e, D} per (rank, query head), rows padded to 4 tokens
   size_t n = static_cast<size_t>(p.Hq) * 2 * stats_row_pitch(p.B * p.S);
   return (n * sizeof(float) + 255) / 256 * 256;
+}
+
+// Block numbering of the stored dS (see DsGeom); false when the shape has no
+// stored-dS path (non-causal masks, rows not a multiple of 128 tokens, or more
+// blocks than a tensor-map coordinate holds).
+static bool ds_geom(const usp_attn_params& p, bwd::DsGeom& g, long long& n_blocks) {
+  if (!p.causal || p.S % kBN != 0) return false;
+  g.N = p.S / bwd::kSL;
+  g.Wc = g.N;
+  if (p.window_left >= 0) {
+    const long long wc = 2ll * (1 + (p.window_left + kBN - 1) / kBN);
+    if (wc < g.N) g.Wc = static_cast<int>(wc);
+  }
+  g.kc = (g.N - g.Wc) / 2 + 1;
+  g.per_row = bwd::ds_off(g, p.S / kBN);
+  n_blocks = static_cast<long long>(p.Hq) * p.B * g.per_row;
+  return n_blocks > 0 && n_blocks < (1ll << 31);
+}
+
+size_t attn_bwd_ds_bytes(const usp_attn_params& p) {
+  bwd::DsGeom g;
+  long long n_blocks;
+  if (!ds_geom(p, g, n_blocks)) return 0;
+  return static_cast<size_t>(n_blocks) * kBN * bwd::kSL * 2;
 }
 
 static AttnArgs make_args(const usp_attn_params& prm, int32_t* status) {
@@ -790,24 +1050,41 @@ int launch_attn_bwd_preprocess(const usp_attn_params& prm, const void* o, const 
 
 template <int D>
 static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const void* k, const void* v,
-                         const void* dO, void* dq, void* dk, void* dv, const float* stats, cudaStream_t st) {
+                         const void* dO, void* dq, void* dk, void* dv, const float* stats, void* ds,
+                         const bwd::DsGeom& dsg, long long ds_blocks, cudaStream_t st) {
   using C = bwd::Cfg<D>;
   bwd::Grads g{static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
                static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(dO),
                static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
-               stats, stats_row_pitch(a.BS), (a.BS + kBM - 1) / kBM};
+               stats, stats_row_pitch(a.BS), (a.BS + kBM - 1) / kBM, static_cast<__nv_bfloat16*>(ds), dsg};
   int rc;
+  if (dq_pass && ds != nullptr) {
+    // dQ = dS K from the blocks the dK/dV pass stored
+    using CD = bwd::CfgDs<D>;
+    CUtensorMap tk, tds;
+    if ((rc = make_rows_tmap(&tk, k, a, a.hk, a.Hkv, D, kBN)) != USP_OK) return rc;
+    if ((rc = make_ds_tmap(&tds, ds, ds_blocks)) != USP_OK) return rc;
+    if (cudaFuncSetAttribute(bwd::dq_ds_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, CD::SMEM) !=
+        cudaSuccess)
+      return USP_ERR_CUDA;
+    bwd::dq_ds_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hq, bwd::kDsThreads, CD::SMEM, st>>>(tk, tds, a,
+                                                                                                          g);
+    return check_launch();
+  }
   if (!dq_pass) {
     // 64-query slices of Q, dO and their statistics stream past TMEM-resident K, V
     CUtensorMap tq, tdo, tst;
     if ((rc = make_rows_tmap(&tq, q, a, a.hq, a.Hq, D, bwd::kSL)) != USP_OK) return rc;
     if ((rc = make_rows_tmap(&tdo, dO, a, a.hq, a.Hq, D, bwd::kSL)) != USP_OK) return rc;
     if ((rc = make_stats_tmap(&tst, stats, a.BS, g.bsp, a.P * a.hq, bwd::kSL)) != USP_OK) return rc;
+    CUtensorMap tds_st;
+    memset(&tds_st, 0, sizeof(tds_st));  // unused unless dS is stored
+    if (ds != nullptr && (rc = make_ds_store_tmap(&tds_st, ds, ds_blocks)) != USP_OK) return rc;
     if (cudaFuncSetAttribute(bwd::dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::A_SMEM) !=
         cudaSuccess)
       return USP_ERR_CUDA;
-    bwd::dkdv_kernel<D><<<static_cast<unsigned>(g.n_tiles) * (a.seq_io ? a.Hkv : a.P * a.hk), bwd::kThreads, C::A_SMEM, st>>>(tq, tdo, tst,
-                                                                                                       a, g);
+    const unsigned grid = static_cast<unsigned>(g.n_tiles) * (a.seq_io ? a.Hkv : a.P * a.hk);
+    bwd::dkdv_kernel<D><<<grid, bwd::kThreads, C::A_SMEM, st>>>(tq, tdo, tst, tds_st, a, g);
   } else {
     // 128-key tiles of K and V stream past TMEM-resident Q, dO
     CUtensorMap tk, tv;
@@ -820,33 +1097,50 @@ static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const v
   return check_launch();
 }
 
-// 2. dK, dV
+// The stored-dS region of the workspace (after the statistics), or null when
+// the workspace is too small for it or the shape has no such path.
+static void* ds_region(const usp_attn_params& prm, const void* ws, size_t ws_bytes, bwd::DsGeom& g,
+                       long long& n_blocks) {
+  const size_t need = attn_bwd_ds_bytes(prm);
+  if (need == 0 || ws_bytes < attn_bwd_ws_bytes(prm) + need || !ds_geom(prm, g, n_blocks)) return nullptr;
+  return static_cast<uint8_t*>(const_cast<void*>(ws)) + attn_bwd_ws_bytes(prm);
+}
+
+// 2. dK, dV (and the dS blocks, when the workspace holds them)
 int launch_attn_bwd_dkdv(const usp_attn_params& prm, const void* q, const void* k, const void* v, const float* lse,
-                         const void* dO, void* dk, void* dv, const void* ws, int32_t* status, cudaStream_t st) {
+                         const void* dO, void* dk, void* dv, const void* ws, size_t ws_bytes, int32_t* status,
+                         cudaStream_t st) {
   const AttnArgs a = make_args(prm, status);
   const float* stats = static_cast<const float*>(ws);
   (void)lse;  // read through the preprocess's statistics
-  if (prm.D == 128) return run_grad_pass<128>(false, a, q, k, v, dO, nullptr, dk, dv, stats, st);
-  return run_grad_pass<64>(false, a, q, k, v, dO, nullptr, dk, dv, stats, st);
+  bwd::DsGeom g{};
+  long long nb = 0;
+  void* ds = ds_region(prm, ws, ws_bytes, g, nb);
+  if (prm.D == 128) return run_grad_pass<128>(false, a, q, k, v, dO, nullptr, dk, dv, stats, ds, g, nb, st);
+  return run_grad_pass<64>(false, a, q, k, v, dO, nullptr, dk, dv, stats, ds, g, nb, st);
 }
 
-// 3. dQ
+// 3. dQ (from the stored dS blocks when the workspace holds them, else by
+// recomputing S and dP)
 int launch_attn_bwd_dq(const usp_attn_params& prm, const void* q, const void* k, const void* v, const float* lse,
-                       const void* dO, void* dq, const void* ws, int32_t* status, cudaStream_t st) {
+                       const void* dO, void* dq, const void* ws, size_t ws_bytes, int32_t* status, cudaStream_t st) {
   const AttnArgs a = make_args(prm, status);
   const float* stats = static_cast<const float*>(ws);
   (void)lse;
-  if (prm.D == 128) return run_grad_pass<128>(true, a, q, k, v, dO, dq, nullptr, nullptr, stats, st);
-  return run_grad_pass<64>(true, a, q, k, v, dO, dq, nullptr, nullptr, stats, st);
+  bwd::DsGeom g{};
+  long long nb = 0;
+  void* ds = ds_region(prm, ws, ws_bytes, g, nb);
+  if (prm.D == 128) return run_grad_pass<128>(true, a, q, k, v, dO, dq, nullptr, nullptr, stats, ds, g, nb, st);
+  return run_grad_pass<64>(true, a, q, k, v, dO, dq, nullptr, nullptr, stats, ds, g, nb, st);
 }
 
 int launch_attn_bwd(const usp_attn_params& prm, const void* q, const void* k, const void* v, const void* o,
                     const float* lse, const void* dO, void* dq, void* dk, void* dv, float* dsinks, void* ws,
-                    int32_t* status, cudaStream_t st) {
+                    size_t ws_bytes, int32_t* status, cudaStream_t st) {
   int rc;
   if ((rc = launch_attn_bwd_preprocess(prm, o, lse, dO, dsinks, ws, status, st)) != USP_OK) return rc;
-  if ((rc = launch_attn_bwd_dkdv(prm, q, k, v, lse, dO, dk, dv, ws, status, st)) != USP_OK) return rc;
-  return launch_attn_bwd_dq(prm, q, k, v, lse, dO, dq, ws, status, st);
+  if ((rc = launch_attn_bwd_dkdv(prm, q, k, v, lse, dO, dk, dv, ws, ws_bytes, status, st)) != USP_OK) return rc;
+  return launch_attn_bwd_dq(prm, q, k, v, lse, dO, dq, ws, ws_bytes, status, st);
 }
 
 }  // namespace usp

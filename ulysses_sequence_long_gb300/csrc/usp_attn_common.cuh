@@ -190,6 +190,9 @@ inline int make_rows_tmap(CUtensorMap* m, const void* base, const AttnArgs& a, i
                   : make_head_tmap(m, base, a.P, a.BS, hpr, D, box_rows);
 }
 
+int make_ds_tmap(CUtensorMap* m, const void* base, long long n_blocks);
+int make_ds_store_tmap(CUtensorMap* m, void* base, long long n_blocks);
+
 // Tensor map of the backward's planar statistics, fp32 [P*hq][2][pitch]: dims
 // {BS, 2, P*hq}, box {box_rows, 2, 1} (box_rows tokens of both planes of one
 // head); the token coordinate of a load must be a multiple of 4.

@@ -52,13 +52,15 @@ int launch_attn_fwd(const usp_attn_params& p, const void* q, const void* k, cons
                     int32_t* status, cudaStream_t st);
 int launch_attn_bwd(const usp_attn_params& p, const void* q, const void* k, const void* v, const void* o,
                     const float* lse, const void* dO, void* dq, void* dk, void* dv, float* dsinks, void* ws,
-                    int32_t* status, cudaStream_t st);
+                    size_t ws_bytes, int32_t* status, cudaStream_t st);
 size_t attn_bwd_ws_bytes(const usp_attn_params& p);
+size_t attn_bwd_ds_bytes(const usp_attn_params& p);  // stored-dS blocks (0: no such path for the shape)
 int launch_attn_bwd_preprocess(const usp_attn_params& p, const void* o, const float* lse, const void* dO, float* dsinks,
                                void* ws, int32_t* status, cudaStream_t st);
 int launch_attn_bwd_dkdv(const usp_attn_params& p, const void* q, const void* k, const void* v, const float* lse,
-                         const void* dO, void* dk, void* dv, const void* ws, int32_t* status, cudaStream_t st);
+                         const void* dO, void* dk, void* dv, const void* ws, size_t ws_bytes, int32_t* status,
+                         cudaStream_t st);
 int launch_attn_bwd_dq(const usp_attn_params& p, const void* q, const void* k, const void* v, const float* lse,
-                       const void* dO, void* dq, const void* ws, int32_t* status, cudaStream_t st);
+                       const void* dO, void* dq, const void* ws, size_t ws_bytes, int32_t* status, cudaStream_t st);
 
 }  // namespace usp

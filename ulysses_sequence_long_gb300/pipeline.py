@@ -60,11 +60,30 @@ class Shape:
         return (self.S // self.P) % 128 == 0
 
 
+def backward_workspace(prm: B_.AttnParams, device, stored_ds: Optional[bool] = None):
+    """Workspace of the backward calls and whether it holds the stored dS.
+
+    With the stored dS the dK/dV pass writes dS blocks and the dQ pass reads
+    them instead of recomputing S and dP.  None picks it when the shape has
+    that path and its workspace takes at most half of the free device memory;
+    True insists on it (ValueError if the shape has none)."""
+    fast = B_.usp_attn_bwd_fast_workspace_bytes(prm)
+    if stored_ds is None:
+        free, _ = torch.cuda.mem_get_info(device)
+        stored_ds = 0 < fast <= free // 2
+    if stored_ds and fast == 0:
+        raise ValueError("this shape has no stored-dS backward (it needs a causal mask and S % 128 == 0)")
+    n = fast if stored_ds else B_.usp_attn_bwd_workspace_bytes(prm)
+    return torch.empty((max(n, 256),), dtype=torch.uint8, device=device), bool(stored_ds)
+
+
 class UlyssesAttention:
     """Buffers and calls for one shape on one device."""
 
-    def __init__(self, shape: Shape, device="cuda", with_backward: bool = True, fused: Optional[bool] = None):
+    def __init__(self, shape: Shape, device="cuda", with_backward: bool = True, fused: Optional[bool] = None,
+                 stored_ds: Optional[bool] = None):
         s = self.shape = shape
+        self.stored_ds = stored_ds
         self.fused = shape.can_fuse if fused is None else bool(fused)
         if self.fused and not shape.can_fuse:
             raise ValueError("fused exchanges need S/P to be a multiple of 128")
@@ -108,8 +127,7 @@ class UlyssesAttention:
 
     def _ws(self, prm):
         if self._bwd_ws is None:
-            n = B_.usp_attn_bwd_workspace_bytes(prm)
-            self._bwd_ws = torch.empty((max(n, 256),), dtype=torch.uint8, device=self.lse.device)
+            self._bwd_ws, self.stored_ds = backward_workspace(prm, self.lse.device, self.stored_ds)
         return self._bwd_ws
 
     # -- steps ---------------------------------------------------------------
@@ -209,8 +227,10 @@ class HybridAttention:
     computed once.  Buffers are in the hybrid head layout [U][B][S][H/U][D].
     """
 
-    def __init__(self, shape: Shape, ring: int, device="cuda", with_backward: bool = True):
+    def __init__(self, shape: Shape, ring: int, device="cuda", with_backward: bool = True,
+                 stored_ds: Optional[bool] = None):
         s = self.shape = shape
+        self.stored_ds = stored_ds
         if ring < 1 or s.P % ring != 0:
             raise ValueError("the ring degree must divide the ranks")
         self.ring = R = ring
@@ -296,8 +316,7 @@ class HybridAttention:
         mark = marks or (lambda i: None)
         prm = self.params(sinks, 0)
         if self._bwd_ws is None:
-            n = B_.usp_attn_bwd_workspace_bytes(prm)
-            self._bwd_ws = torch.empty((max(n, 256),), dtype=torch.uint8, device=self.lse.device)
+            self._bwd_ws, self.stored_ds = backward_workspace(prm, self.lse.device, self.stored_ds)
         ws = self._bwd_ws
         mark(0)
         B_.usp_hybrid_relayout_fwd(do_seq, self.do_head, s.B, s.S, s.Hq, s.D, self.ring, self.U, stream)
