@@ -70,3 +70,30 @@ def test_host_checks_without_gpu(lib):
     assert lib.usp_attn_bwd_dkdv(ctypes.byref(prm), p, p, p, p, p, p, p, ws, 1 << 20, None, None) == \
         B.USP_ERR_UNSUPPORTED
     assert lib.usp_attn_bwd_dq(ctypes.byref(prm), p, p, p, p, p, p, ws, 1 << 20, None, None) == B.USP_ERR_UNSUPPORTED
+
+
+def test_fast_workspace_is_stats_plus_stored_ds_blocks(lib):
+    """The stored-dS workspace = the statistics + one 16 KiB block per
+    (query head, batch row, key tile kt, 64-query slice) a causal mask can
+    reach: slices [2kt, 2kt + min(S/64 - 2kt, 2 (1 + ceil(w/128)))).  Counted
+    here by brute force over the slices each key tile meets."""
+    from ulysses_sequence_long_gb300 import binding as B
+
+    def brute(Bb, S, Hq, w):
+        n = 0
+        for kt in range(S // 128):
+            u_last = kt * 128 + 127
+            hi = S if w < 0 else min(S, u_last + w + 1)
+            hi = -(-hi // 128) * 128                      # whole 128-row query tiles
+            n += len(range(2 * kt, min(hi // 64, S // 64)))
+        return n * Hq * Bb * 128 * 64 * 2
+
+    for Bb, S, Hq, Hkv, P, w in [(1, 256, 4, 2, 2, -1), (1, 32768, 32, 8, 8, -1), (1, 16384, 64, 8, 8, 127),
+                                 (2, 640, 4, 2, 2, -1), (1, 1024, 8, 2, 2, 200), (1, 4096, 12, 12, 4, 0)]:
+        prm = B.AttnParams(Bb, S, Hq, Hkv, 64, P, 1, w, 0.0, 16, 16, None)
+        stats = lib.usp_attn_bwd_workspace_bytes(ctypes.byref(prm))
+        assert lib.usp_attn_bwd_fast_workspace_bytes(ctypes.byref(prm)) == stats + brute(Bb, S, Hq, w)
+    # no stored-dS path without a causal mask, or with rows not a multiple of 128
+    for Bb, S, causal in [(1, 512, 0), (1, 320, 1)]:
+        prm = B.AttnParams(Bb, S, 4, 2, 64, 2, causal, -1, 0.0, 16, 16, None)
+        assert lib.usp_attn_bwd_fast_workspace_bytes(ctypes.byref(prm)) == 0
