@@ -489,6 +489,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (key_ok) doc_bounds(p.cu, n_docs, p.BS, u, a, b);
     a = max(a, rq0);  // a ring step: queries of one super-chunk only
     b = min(b, rq1);
+    int vlo, vhi;     // the rows that see this key
+    visible_rows(u, a, b, p.causal, p.window_left, key_ok, vlo, vhi);
     const uint32_t lb = tmem + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
     // K (group 0) or V (group 1) row of this key into TMEM
     {
@@ -510,14 +512,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float x[32];
       tmem_ld_cols<32>(lb + T_S + grp * 32, x);
-      bool full = key_ok && q0 >= a && q0 + 32 <= b && (!p.causal || q0 >= u);
-      if (p.window_left >= 0) full = full && (q0 + 31 - u <= p.window_left) && (p.causal || u - q0 <= p.window_left);
       // only slices that straddle a document, diagonal or window edge pay for
       // the per-element mask (hidden scores become -inf, so exp2 gives 0)
-      if (!full) {
+      const int c_lo = vlo - q0, c_hi = vhi - q0;
+      if (!(c_lo <= 0 && c_hi >= 31)) {
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-          if (!(key_ok && visible_from_key(q0 + c, u, a, b, p.causal, p.window_left))) x[c] = -INFINITY;
+          if (c < c_lo || c > c_hi) x[c] = -INFINITY;
       }
       float pr[32];
 #pragma unroll
@@ -754,6 +755,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     a = max(a, rk0);  // a ring step: one key/value super-chunk only
     b = min(b, rk1);
+    int vlo, vhi;     // the row's visible keys
+    visible_keys(t, a, b, p.causal, p.window_left, row_ok, vlo, vhi);
     const uint32_t s_col = T_S + grp * 64, dp_col = T_DP + grp * 64;
     bool ok = true;
     for (int n = 0; n < n_kv && ok; ++n) {
@@ -763,12 +766,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float x[64];
       tmem_ld_cols<64>(lb + s_col, x);
-      bool full = row_ok && k0 >= a && k0 + 64 <= b && (!p.causal || k0 + 63 <= t);
-      if (p.window_left >= 0) full = full && (t - k0 <= p.window_left) && (p.causal || k0 + 63 - t <= p.window_left);
-      if (!full) {
+      const int c_lo = vlo - k0, c_hi = vhi - k0;
+      if (!(c_lo <= 0 && c_hi >= 63)) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-          if (!(row_ok && visible(t, k0 + c, a, b, p.causal, p.window_left))) x[c] = -INFINITY;
+          if (c < c_lo || c > c_hi) x[c] = -INFINITY;
       }
       float pr[64];
 #pragma unroll

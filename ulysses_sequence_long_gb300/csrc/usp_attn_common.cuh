@@ -130,6 +130,38 @@ __device__ __forceinline__ bool visible_from_key(int t, int u, int a, int b, int
   return v;
 }
 
+// The visibility rule as one interval: the keys row t of document [a, b)
+// sees are exactly [vlo, vhi] (empty when vlo > vhi), so a mask costs two
+// compares per element.
+__device__ __forceinline__ void visible_keys(int t, int a, int b, int causal, int wl, bool ok, int& vlo, int& vhi) {
+  vlo = a;
+  vhi = b - 1;
+  if (causal) vhi = min(vhi, t);
+  if (wl >= 0) {
+    vlo = max(vlo, t - wl);
+    if (!causal) vhi = min(vhi, t + wl);
+  }
+  if (!ok) {
+    vlo = 1;
+    vhi = 0;
+  }
+}
+
+// The rows [vlo, vhi] that see key u, when [a, b) is the key's document.
+__device__ __forceinline__ void visible_rows(int u, int a, int b, int causal, int wl, bool ok, int& vlo, int& vhi) {
+  vlo = a;
+  vhi = b - 1;
+  if (causal) vlo = max(vlo, u);
+  if (wl >= 0) {
+    vhi = min(vhi, u + wl);
+    if (!causal) vlo = max(vlo, u - wl);
+  }
+  if (!ok) {
+    vlo = 1;
+    vhi = 0;
+  }
+}
+
 // First and one-past-last key any of the rows [t_first, t_last] may see.
 __device__ __forceinline__ void key_range(const AttnArgs& p, int n, int t_first, int t_last, int& lo, int& hi) {
   int a0, b0, a1, b1;

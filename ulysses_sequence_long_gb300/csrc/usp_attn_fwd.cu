@@ -290,9 +290,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool full = row_ok && kv0 >= a && kv0 + kBN <= b && (!p.causal || kv0 + kBN - 1 <= t);
       if (p.window_left >= 0) full = full && (t - kv0 <= p.window_left) && (p.causal || kv0 + kBN - 1 - t <= p.window_left);
       if (!full) {
+        int vlo, vhi;  // the row's visible keys, as one interval: two compares per element
+        visible_keys(t, a, b, p.causal, p.window_left, row_ok, vlo, vhi);
+        const int c_lo = vlo - kv0, c_hi = vhi - kv0;
 #pragma unroll
         for (int c = 0; c < kBN; ++c)
-          if (!(row_ok && visible(t, kv0 + c, a, b, p.causal, p.window_left))) s[c] = -INFINITY;
+          if (c < c_lo || c > c_hi) s[c] = -INFINITY;
       }
       // row max as 8 independent chains
       float mx8[8];
