@@ -805,12 +805,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // --------------------------------------------------------------- dQ from stored dS
 // dQ_t = scale sum_u dS_tu k_u with dS read back from the blocks the dK/dV
-// pass stored: no recomputation of S and dP, one GEMM per key tile.  CTA =
-// (rank, query head, 128 rows).  Per 128-key tile the two 64-query dS blocks
-// (A operand, MN-major: queries contiguous) and the K tile (B operand,
-// MN-major: D contiguous) stream through a shared-memory ring; dQ accumulates
-// in TMEM (128 lanes x D columns).  dS holds the masks already, so no mask is
-// evaluated here.  Warps 0-3: epilogue, warp 4: TMA producer, warp 5: MMA.
+// pass stored: no recomputation of S and dP, one GEMM per key tile.  A unit
+// of work = (rank, query head, 128 rows); the kernel is persistent: each CTA
+// walks units blockIdx.x, +gridDim.x, ... (late query tiles first), so the
+// next unit's tiles stream in while the current one finishes.  Per 128-key
+// tile the two 64-query dS blocks (A operand, MN-major: queries contiguous)
+// and the K tile (B operand, MN-major: D contiguous) pass through a
+// shared-memory ring; dQ accumulates in one of two TMEM buffers (128 lanes x
+// D columns each) while the epilogue drains the other.  dS holds the masks
+// already, so no mask is evaluated here.  Warps 0-3: epilogue, warp 4: TMA
+// producer, warp 5: MMA.
 constexpr int kDsThreads = 192;
 
 template <int D>
@@ -826,69 +830,72 @@ struct CfgDs {
 
 struct BarsDs {
   uint64_t full[4], empty[4];
-  uint64_t fin, mma_done;
+  uint64_t fin[2], tfree[2];  // dQ buffer b: accumulated / read out by the epilogue
+  uint64_t mma_done;
   uint32_t tmem;
   int abort;
 };
 
+// One unit's geometry, computed identically by every role.
+struct DsUnit {
+  int t0, r, j, row0, kt0, qs0, n_kv;
+  long long head_base;
+};
+
+__device__ __forceinline__ DsUnit ds_unit(const AttnArgs& p, const Grads& g, int n_docs, int u) {
+  DsUnit w;
+  const int per = p.P * p.hq;
+  const int qt = g.n_tiles - 1 - u / per;
+  const int rem = u % per;
+  w.r = rem / p.hq;
+  w.j = rem % p.hq;
+  w.t0 = qt * kBM;
+  int lo, hi;
+  key_range(p, n_docs, w.t0, min(w.t0 + kBM, p.BS) - 1, lo, hi);
+  if (p.ring > 1) {  // ring x Ulysses step: one key/value super-chunk
+    int rk0, rk1;
+    ring_key_window(p, w.t0, rk0, rk1);
+    lo = max(lo, rk0);
+    hi = min(hi, rk1);
+  }
+  const int rowb = w.t0 / p.S;
+  w.row0 = rowb * p.S;
+  lo = w.row0 + ((lo - w.row0) & ~(kBN - 1));  // blocks belong to aligned key tiles
+  w.n_kv = hi > lo ? (hi - lo + kBN - 1) / kBN : 0;
+  w.kt0 = (lo - w.row0) / kBN;
+  w.qs0 = (w.t0 - w.row0) / kSL;  // the tile's first 64-query slice
+  w.head_base = (static_cast<long long>(w.r * p.hq + w.j) * p.B + rowb) * g.dsg.per_row;
+  return w;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kDsThreads, 1)
     dq_ds_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tds, AttnArgs p,
-                 Grads g) {
+                 Grads g, int n_units) {
   using C = CfgDs<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   BarsDs* bars = reinterpret_cast<BarsDs*>(smem + C::BAR);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // late query tiles first (they meet the most key tiles)
-  const int per = p.P * p.hq;
-  const int qt = g.n_tiles - 1 - static_cast<int>(blockIdx.x) / per;
-  const int rem = static_cast<int>(blockIdx.x) % per;
-  const int r = rem / p.hq, j = rem % p.hq;
-  const HeadRef qh = q_head_ref(p, r, j), kvh = kv_head_ref(p, r, j / p.G);
-  const int t0 = qt * kBM;
-
   const int n_docs = checked_docs(p);
   if (n_docs == 0) return;
-  int lo, hi;
-  key_range(p, n_docs, t0, min(t0 + kBM, p.BS) - 1, lo, hi);
-  if (p.ring > 1) {  // ring x Ulysses step: one key/value super-chunk
-    int rk0, rk1;
-    ring_key_window(p, t0, rk0, rk1);
-    lo = max(lo, rk0);
-    hi = min(hi, rk1);
-  }
-  const int rowb = t0 / p.S, row0 = rowb * p.S;
-  lo = row0 + ((lo - row0) & ~(kBN - 1));  // blocks belong to aligned key tiles
-  const int n_kv = hi > lo ? (hi - lo + kBN - 1) / kBN : 0;
-  const int kt0 = (lo - row0) / kBN;
-  const int qs0 = (t0 - row0) / kSL;       // the tile's first 64-query slice
-  const long long head_base = (static_cast<long long>(r * p.hq + j) * p.B + rowb) * g.dsg.per_row;
-
-  if (n_kv == 0) {  // no key at this ring step: dQ = 0
-    if (warp < 4) {
-      const int t = t0 + warp * 32 + lane;
-      if (t < p.BS) {
-        uint4* dst = reinterpret_cast<uint4*>(g.dq + row_offset(p, qh, p.hq, p.Hq, t, D));
-        for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
-      }
-    }
-    return;
-  }
 
   if (tid == 0) {
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    mbar_init(&bars->fin, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->fin[b], 1);
+      mbar_init(&bars->tfree[b], 4);
+    }
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_barrier_init();
   }
   if (warp == 0) {
-    tmem_alloc(&bars->tmem, D);
+    tmem_alloc(&bars->tmem, 2 * D);
     tmem_relinquish();
     tc_fence_before();
   }
@@ -903,28 +910,34 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&tk);
       prefetch_tmap(&tds);
-      int issued = 0;
-      for (int n = 0; n < n_kv; ++n) {
-        const int s = n % C::NST;
-        if (n >= C::NST && !mbar_wait(&bars->empty[s], ((n / C::NST) - 1) & 1, abort, p.status)) break;
-        const int kt = kt0 + n, rel = qs0 - 2 * kt;
-        // the dK/dV pass covered whole query tiles, so both blocks exist for
-        // every key tile this query tile meets; anything else is a broken
-        // invariant, recorded instead of read
-        if (rel < 0 || rel + 1 >= ds_count(g.dsg, kt)) {
-          set_status(p.status, USP_ERR_BAD_SEQLENS);
-          *abort = 1;
-          break;
+      int gn = 0;  // tiles issued by this CTA over all its units (ring position)
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const DsUnit w = ds_unit(p, g, n_docs, u);
+        const HeadRef kvh = kv_head_ref(p, w.r, w.j / p.G);
+        for (int n = 0; n < w.n_kv; ++n, ++gn) {
+          const int s = gn % C::NST;
+          if (gn >= C::NST && !(ok = mbar_wait(&bars->empty[s], ((gn / C::NST) - 1) & 1, abort, p.status)))
+            break;
+          const int kt = w.kt0 + n, rel = w.qs0 - 2 * kt;
+          // the dK/dV pass covered whole query tiles, so both blocks exist for
+          // every key tile this query tile meets; anything else is a broken
+          // invariant, recorded instead of read
+          if (rel < 0 || rel + 1 >= ds_count(g.dsg, kt)) {
+            set_status(p.status, USP_ERR_BAD_SEQLENS);
+            *abort = 1;
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * C::STAGE;
+          mbar_arrive_expect_tx(&bars->full[s], C::STAGE);
+          tma_load_3d(st, &tds, &bars->full[s], 0, 0, static_cast<int>(w.head_base + ds_off(g.dsg, kt) + rel));
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_rows(st + C::DSB + c * kAtomBytes, &tk, &bars->full[s], p, c, kvh, w.row0 + kt * kBN);
         }
-        uint8_t* st = smem + s * C::STAGE;
-        mbar_arrive_expect_tx(&bars->full[s], C::STAGE);
-        tma_load_3d(st, &tds, &bars->full[s], 0, 0, static_cast<int>(head_base + ds_off(g.dsg, kt) + rel));
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_rows(st + C::DSB + c * kAtomBytes, &tk, &bars->full[s], p, c, kvh, row0 + kt * kBN);
-        issued = n + 1;
       }
       // never leave the CTA with copies still landing in its shared memory
-      for (int n = max(0, issued - C::NST); n < issued; ++n)
+      for (int n = max(0, gn - C::NST); n < gn; ++n)
         mbar_wait(&bars->full[n % C::NST], (n / C::NST) & 1, abort, p.status);
     }
   } else if (warp == 5) {
@@ -932,29 +945,56 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(kBM, D, true, true);  // [128 queries x D], K = 128 keys
       bool ok = true;
-      for (int n = 0; n < n_kv && ok; ++n) {
-        const int s = n % C::NST;
-        if (!(ok = mbar_wait(&bars->full[s], (n / C::NST) & 1, abort, p.status))) break;
+      int gn = 0, ub = 0;  // tiles consumed; units accumulated (buffer ub & 1)
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const DsUnit w = ds_unit(p, g, n_docs, u);
+        if (w.n_kv == 0) continue;
+        const int b = ub & 1;
+        // the epilogue has read this buffer's previous unit out
+        if (ub >= 2 && !(ok = mbar_wait(&bars->tfree[b], ((ub >> 1) - 1) & 1, abort, p.status))) break;
         tc_fence_after();
-        const uint32_t a = sbase + s * C::STAGE, b = a + C::DSB;
+        for (int n = 0; n < w.n_kv && ok; ++n, ++gn) {
+          const int s = gn % C::NST;
+          if (!(ok = mbar_wait(&bars->full[s], (gn / C::NST) & 1, abort, p.status))) break;
+          tc_fence_after();
+          const uint32_t a = sbase + s * C::STAGE, bb = a + C::DSB;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ss(tmem, mnmajor_desc(a, kBN * 128, kk), mnmajor_desc(b, kAtomBytes, kk), idesc,
-                 (n > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars->empty[s]);
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ss(tmem + b * D, mnmajor_desc(a, kBN * 128, kk), mnmajor_desc(bb, kAtomBytes, kk), idesc,
+                   (n > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bars->empty[s]);
+        }
+        if (ok) mma_commit(&bars->fin[b]);
+        ++ub;
       }
-      if (ok) mma_commit(&bars->fin);
       mma_commit(&bars->mma_done);
       mbar_wait(&bars->mma_done, 0, abort, p.status);
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int t = t0 + warp * 32 + lane;
-    const bool row_ok = t < p.BS;
-    if (mbar_wait(&bars->fin, 0, abort, p.status)) {
+    bool ok = true;
+    int ub = 0;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const DsUnit w = ds_unit(p, g, n_docs, u);
+      const HeadRef qh = q_head_ref(p, w.r, w.j);
+      const int t = w.t0 + warp * 32 + lane;
+      const bool row_ok = t < p.BS;
+      if (w.n_kv == 0) {  // no key at this ring step: dQ = 0
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(g.dq + row_offset(p, qh, p.hq, p.Hq, t, D));
+          for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      const int b = ub & 1;
+      if (!(ok = mbar_wait(&bars->fin[b], (ub >> 1) & 1, abort, p.status))) break;
       tc_fence_after();
-      const uint32_t lb = tmem + ((static_cast<uint32_t>(warp) * 32) << 16);
+      const uint32_t lb = tmem + b * D + ((static_cast<uint32_t>(warp) * 32) << 16);
       store_row<D>(lb, g.dq + row_offset(p, qh, p.hq, p.Hq, row_ok ? t : 0, D), p.scale, row_ok);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->tfree[b]);
+      ++ub;
     }
   }
 
@@ -962,7 +1002,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, D);
+    tmem_dealloc(tmem, 2 * D);
   }
 }
 
@@ -1069,8 +1109,9 @@ static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const v
     if (cudaFuncSetAttribute(bwd::dq_ds_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, CD::SMEM) !=
         cudaSuccess)
       return USP_ERR_CUDA;
-    bwd::dq_ds_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hq, bwd::kDsThreads, CD::SMEM, st>>>(tk, tds, a,
-                                                                                                          g);
+    const int n_units = g.n_tiles * a.P * a.hq;
+    const int grid = n_units < device_sm_count() ? n_units : device_sm_count();  // persistent: one CTA per SM
+    bwd::dq_ds_kernel<D><<<grid, bwd::kDsThreads, CD::SMEM, st>>>(tk, tds, a, g, n_units);
     return check_launch();
   }
   if (!dq_pass) {
