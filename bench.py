@@ -184,8 +184,8 @@ class Step:
         self.device = device
         shape = Shape(w.B, w.S, w.Hq, w.Hkv, w.D, w.P, w.causal, w.window_left)
         self.hybrid = w.ring > 1
-        if self.hybrid:   # ring x Ulysses: explicit exchanges inside each ring group
-            self.ua = HybridAttention(shape, w.ring, device=device)
+        if self.hybrid:   # ring x Ulysses: the Ulysses exchange inside each ring group
+            self.ua = HybridAttention(shape, w.ring, device=device, fused=fused)
         else:
             self.ua = UlyssesAttention(shape, device=device, fused=fused)
         if host is None:
@@ -227,9 +227,9 @@ class Step:
     def launches_per_step(self) -> int:
         sink = 1 if self.sinks is not None else 0
         if self.hybrid:
-            # exchanges 1 + 1 + 1 + 3, scan 3, preprocess 1 (+ dsink); per ring
-            # step: forward + merge, dK/dV + 2 sums, dQ + 1 sum
-            return 10 + sink + 7 * self.w.ring
+            # scan 3, preprocess 1 (+ dsink); per ring step: forward + merge,
+            # dK/dV + 2 sums, dQ + 1 sum; explicit exchanges add 1 + 1 + 1 + 3
+            return 4 + sink + 7 * self.w.ring + (0 if self.ua.fused else 6)
         # scan 3, fwd 1, preprocess 1 (+ dsink 1), dK/dV 1, dQ 1; the explicit
         # exchanges add relayout qkv 1, O 1, dO 1, dQ/dK/dV 3
         return 7 + sink + (0 if self.ua.fused else 6)

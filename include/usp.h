@@ -195,10 +195,12 @@ typedef struct {
                                 USP_IO_SEQ (1): the same tensors in seq-layout — the exchanges
                                 are fused into the kernels' loads and stores; needs (S/P) % 128 == 0 */
   int ring;                  /* ring x Ulysses hybrid: ring degree R (0 or 1: no ring).  With R > 1,
-                                P is the Ulysses degree, the tensors are the hybrid head-layout of
-                                usp_hybrid_relayout_fwd, and a call computes one ring step: rows of
+                                P is the Ulysses degree and a call computes one ring step: rows of
                                 super-chunk a (S/R positions each) see only the keys of super-chunk
-                                (a - ring_step) mod R.  Needs (S/R) % 256 == 0 and USP_IO_HEAD. */
+                                (a - ring_step) mod R.  The tensors are the hybrid head-layout of
+                                usp_hybrid_relayout_fwd (USP_IO_HEAD) or the P*R sequence shards
+                                [P*R][B][S/(P*R)][H][D] (USP_IO_SEQ, needs (S/(P*R)) % 128 == 0).
+                                Needs (S/R) % 256 == 0. */
   int ring_step;             /* 0 <= ring_step < R */
 } usp_attn_params;
 
@@ -251,6 +253,9 @@ enum { USP_RING_FIRST = 1, USP_RING_LAST = 2 };
  * o_step (bf16, head layout like o) and lse_step (fp32 [P][B][hq][S], -inf for
  * rows that saw no key) from usp_attn_fwd with params->ring_step = s:
  *   L = ln(e^L_acc + e^L_step),  O = e^(L_acc - L) O_acc + e^(L_step - L) O_step
+ * o_step, o_acc and o share the layout params->io_layout names (the hybrid
+ * head layout, or the sequence shards with USP_IO_SEQ); lse_* are always
+ * [P][B][hq][S].
  * flags USP_RING_FIRST: the running values start as the step's (o_acc/lse_acc
  * are not read).  USP_RING_LAST: the sink logit z = sinks[r*hq + j] (if
  * params->sinks) joins once, L' = ln(e^L + e^z), O' = e^(L - L') O, and the

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import usp_workloads as W
-from gpu_util import assert_close, built_lib, device_inputs, dsink_bound, half_ulp_bf16, shape_of
+from gpu_util import assert_close, built_lib, device_inputs, dsink_bound, half_ulp_bf16, seq_head_values, shape_of
 
 pytestmark = pytest.mark.gpu
 
@@ -24,10 +24,10 @@ def _bits(t):
     return t.contiguous().view(torch.int16).cpu().numpy()
 
 
-def _run(w, backward=True, stored_ds=None):
+def _run(w, backward=True, stored_ds=None, fused=None):
     from ulysses_sequence_long_gb300.pipeline import HybridAttention
     dev, host = device_inputs(w)
-    ha = HybridAttention(shape_of(w), w.ring, with_backward=backward, stored_ds=stored_ds)
+    ha = HybridAttention(shape_of(w), w.ring, with_backward=backward, stored_ds=stored_ds, fused=fused)
     ha.forward(dev["q"], dev["k"], dev["v"], dev["pos"], dev["sinks"])
     if backward:
         ha.backward(dev["do"], dev["sinks"])
@@ -73,14 +73,21 @@ SMALL = [
 ]
 
 
-CASES = [(w, d) for w in SMALL for d in ([True, False] if w.causal else [False])]
+def _can_fuse(w):
+    return (w.S // w.P) % 128 == 0
 
 
-@pytest.mark.parametrize("w,stored_ds", CASES,
-                         ids=[f"{w.name}-{'stored_ds' if d else 'recompute'}" for w, d in CASES])
-def test_hybrid_full_parity_small(w, stored_ds):
-    ha, dev, host = _run(w, stored_ds=stored_ds)
-    assert ha.stored_ds == stored_ds
+# exchanges fused into the kernels' I/O or explicit; dQ from stored dS or recomputed
+CASES = [(w, f, d) for w in SMALL for f in ([True, False] if _can_fuse(w) else [False])
+         for d in ([True, False] if w.causal else [False])]
+
+
+@pytest.mark.parametrize("w,fused,stored_ds", CASES,
+                         ids=[f"{w.name}-{'fused' if f else 'explicit'}-{'stored_ds' if d else 'recompute'}"
+                              for w, f, d in CASES])
+def test_hybrid_full_parity_small(w, fused, stored_ds):
+    ha, dev, host = _run(w, stored_ds=stored_ds, fused=fused)
+    assert ha.stored_ds == stored_ds and ha.fused == fused
     snk = host["sinks"]
     kw = dict(causal=w.causal, window_left=w.window_left, sinks=snk)
     f = oracle.hybrid_fwd(host["q"], host["k"], host["v"], host["pos"], w.ring, **kw)
@@ -114,7 +121,7 @@ def test_hybrid_ring_step_without_keys_gives_empty_block():
     the step's output is O = 0 and LSE = -inf (nothing to merge)."""
     from ulysses_sequence_long_gb300 import binding as B
     w = SMALL[0]
-    ha, dev, host = _run(w, backward=False)
+    ha, dev, host = _run(w, backward=False, fused=False)
     # step 1: super-chunk 0 holds keys of super-chunk 1 (after its rows)
     B.usp_attn_fwd(ha.params(None, 1), ha.q_head, ha.k_head, ha.v_head, ha.o_step, ha.lse_step, ha.status)
     torch.cuda.synchronize()
@@ -127,11 +134,12 @@ def test_hybrid_ring_step_without_keys_gives_empty_block():
 def test_hybrid_refusals():
     from ulysses_sequence_long_gb300 import binding as B
     w = SMALL[0]
-    ha, dev, host = _run(w, backward=False)
+    ha, dev, host = _run(w, backward=False, fused=False)
     bad = [
         (B.attn_params(1, 1024, 8, 2, 64, 2, ha.cu_seqlens, ha.n_docs, ring=2, ring_step=2), B.USP_ERR_INVALID_ARG),
         (B.attn_params(1, 1024, 8, 2, 64, 2, ha.cu_seqlens, ha.n_docs, ring=8, ring_step=0), B.USP_ERR_UNSUPPORTED),
-        (B.attn_params(1, 1024, 8, 2, 64, 2, ha.cu_seqlens, ha.n_docs, ring=2, ring_step=0,
+        # sequence shards of 1024 / (4 * 4) = 64 tokens are too short for fused I/O
+        (B.attn_params(1, 1024, 8, 2, 64, 4, ha.cu_seqlens, ha.n_docs, ring=4, ring_step=0,
                        io_layout=B.USP_IO_SEQ), B.USP_ERR_UNSUPPORTED),
         (B.attn_params(1, 1024, 8, 2, 64, 2, ha.cu_seqlens, ha.n_docs, ring=1, ring_step=1), B.USP_ERR_INVALID_ARG),
         (B.attn_params(1, 1024, 8, 2, 64, 2, ha.cu_seqlens, ha.n_docs, sinks=torch.zeros(8, device="cuda"), ring=2,
@@ -143,11 +151,12 @@ def test_hybrid_refusals():
         assert e.value.code == code
 
 
-def test_hybrid_full_size_sampled():
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "explicit"])
+def test_hybrid_full_size_sampled(fused):
     """Llama-shaped 32K packed workload as ring 2 x ulysses 4: sampled rows
     of O/LSE/dQ and keys of dK/dV against the attention definition."""
     w = W.LLAMA32K_RING2
-    ha, dev, host = _run(w)
+    ha, dev, host = _run(w, fused=fused)
     U = w.P // w.ring
     hq, hk = w.Hq // U, w.Hkv // U
     G = hq // hk
@@ -158,6 +167,12 @@ def test_hybrid_full_size_sampled():
     cu, _, _ = oracle.cu_seqlens_from_position_ids(host["pos"])
     rng = np.random.Generator(np.random.PCG64(23))
     C = w.S // w.ring
+
+    def vals(name, u, h, H_per_u):
+        """float64 [S][D] of local head h of Ulysses rank u for output `name`."""
+        if not fused:
+            return getattr(ha, name + "_head")[u, 0, :, h].double().cpu().numpy()
+        return seq_head_values(getattr(ha, name + "_seq"), u * H_per_u + h)
     for u, j in [(0, 0), (3, 7)]:
         Q, K, V, dO = qh[u, 0], kh[u, 0], vh[u, 0], doh[u, 0]
         # rows on both sides of the super-chunk boundary and at document starts
@@ -165,13 +180,13 @@ def test_hybrid_full_size_sampled():
                                                  cu[1:-1], cu[1:-1] + 1])))
         rows = rows[rows < w.S]
         O, L = oracle.attention_fwd_rows(Q, K, V, cu, rows, j)
-        assert_close(f"O u{u} h{j}", ha.o_head[u, 0, rows, j].double().cpu().numpy(), O)
+        assert_close(f"O u{u} h{j}", vals("o", u, j, hq)[rows], O)
         assert_close(f"LSE u{u} h{j}", ha.lse[u, 0, j, rows].double().cpu().numpy(), L, bf16_out=False)
         inner = rows[~np.isin(rows, np.concatenate([cu[:-1], cu[:-1] + 1]))]
         dq = oracle.attention_bwd_rows(Q, K, V, dO, cu, inner, j)
         dq_steps = [oracle.attention_bwd_rows(Q, K, V, dO, cu, inner, j, key_window=(c * C, (c + 1) * C))
                     for c in range(w.ring)]
-        assert_close(f"dQ u{u} h{j}", ha.dq_head[u, 0, inner, j].double().cpu().numpy(), dq,
+        assert_close(f"dQ u{u} h{j}", vals("dq", u, j, hq)[inner], dq,
                      slack=sum(half_ulp_bf16(x) for x in dq_steps))
         # keys near the end of the last document (few rows see them) and just
         # before the super-chunk boundary (rows of both super-chunks see them)
@@ -180,7 +195,7 @@ def test_hybrid_full_size_sampled():
         dk, dv = oracle.attention_bwd_keys(Q, K, V, dO, cu, keys, kvh)
         parts = [oracle.attention_bwd_keys(Q, K, V, dO, cu, keys, kvh, row_window=(c * C, (c + 1) * C))
                  for c in range(w.ring)]
-        assert_close(f"dK u{u} kv{kvh}", ha.dk_head[u, 0, keys, kvh].double().cpu().numpy(), dk,
+        assert_close(f"dK u{u} kv{kvh}", vals("dk", u, kvh, hk)[keys], dk,
                      slack=sum(half_ulp_bf16(x[0]) for x in parts))
-        assert_close(f"dV u{u} kv{kvh}", ha.dv_head[u, 0, keys, kvh].double().cpu().numpy(), dv,
+        assert_close(f"dV u{u} kv{kvh}", vals("dv", u, kvh, hk)[keys], dv,
                      slack=sum(half_ulp_bf16(x[1]) for x in parts))

@@ -177,17 +177,20 @@ int check_attn_params(const usp_attn_params* p) {
   if (static_cast<int64_t>(p->B) * p->S * p->Hq >= (1ll << 31)) return USP_ERR_UNSUPPORTED;  // 32-bit row counters
   if (p->Hq > 1024) return USP_ERR_UNSUPPORTED;  // the preprocess stages 32 tokens x Hq row sums in shared memory
   if (p->io_layout != USP_IO_HEAD && p->io_layout != USP_IO_SEQ) return USP_ERR_INVALID_ARG;
-  // fused exchanges: tiles of 128 tokens must never straddle a rank's shard
-  if (p->io_layout == USP_IO_SEQ && (p->S / p->P) % 128 != 0) return USP_ERR_UNSUPPORTED;
   // ring x Ulysses step: the kernels' 256-row blocks never straddle a super-chunk
   if (p->ring < 0) return USP_ERR_INVALID_ARG;
-  if (p->ring > 1) {
-    if (p->ring_step < 0 || p->ring_step >= p->ring) return USP_ERR_INVALID_ARG;
-    if (p->S % p->ring != 0 || (p->S / p->ring) % 256 != 0 || p->io_layout != USP_IO_HEAD)
-      return USP_ERR_UNSUPPORTED;
+  const int ring = p->ring > 1 ? p->ring : 1;
+  if (ring > 1) {
+    if (p->ring_step < 0 || p->ring_step >= ring) return USP_ERR_INVALID_ARG;
+    if (p->S % ring != 0 || (p->S / ring) % 256 != 0) return USP_ERR_UNSUPPORTED;
   } else if (p->ring_step != 0) {
     return USP_ERR_INVALID_ARG;
   }
+  // fused exchanges: tiles of 128 tokens must never straddle a sequence shard
+  // (P shards, P*ring for the hybrid)
+  if (p->io_layout == USP_IO_SEQ &&
+      (p->S % (static_cast<int64_t>(p->P) * ring) != 0 || (p->S / (p->P * ring)) % 128 != 0))
+    return USP_ERR_UNSUPPORTED;
   return USP_OK;
 }
 

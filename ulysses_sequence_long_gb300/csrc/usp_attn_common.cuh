@@ -31,8 +31,8 @@ struct AttnArgs {
   const int32_t* n_docs;
   const float* sinks;  // global [Hq] or null
   int32_t* status;
-  int seq_io;  // 1: inputs and outputs in seq-layout [P][B][S/P][H][D] (exchanges fused)
-  int Sl;      // S/P
+  int seq_io;  // 1: inputs and outputs in seq-layout [Ps][B][S/Ps][H][D] (exchanges fused)
+  int Sl;      // shard length S/Ps; Ps = P sequence shards, P*ring for the ring x Ulysses hybrid
   int ring, ring_step, C;  // ring x Ulysses: ring degree (1: none), step, super-chunk length S/ring
 };
 
@@ -218,7 +218,8 @@ int make_seq_tmap(CUtensorMap* m, const void* base, int P, int B, int Sl, int H,
 
 // The map for either layout: head-layout (hpr heads per rank) or seq-layout (H heads).
 inline int make_rows_tmap(CUtensorMap* m, const void* base, const AttnArgs& a, int hpr, int H, int D, int box_rows) {
-  return a.seq_io ? make_seq_tmap(m, base, a.P, a.B, a.Sl, H, D, box_rows)
+  // seq-layout: P*ring shards of Sl tokens (the hybrid's ring groups hold P shards each)
+  return a.seq_io ? make_seq_tmap(m, base, a.P * a.ring, a.B, a.Sl, H, D, box_rows)
                   : make_head_tmap(m, base, a.P, a.BS, hpr, D, box_rows);
 }
 

@@ -428,10 +428,10 @@ int launch_attn_fwd(const usp_attn_params& prm, const void* q, const void* k, co
   a.sinks = prm.sinks;
   a.status = status;
   a.seq_io = prm.io_layout == USP_IO_SEQ ? 1 : 0;
-  a.Sl = prm.S / prm.P;
   a.ring = prm.ring > 1 ? prm.ring : 1;
   a.ring_step = a.ring > 1 ? prm.ring_step : 0;
   a.C = prm.S / a.ring;
+  a.Sl = prm.S / (prm.P * a.ring);  // sequence shard: P Ulysses ranks in each of `ring` groups
   if (prm.D == 128) return run_fwd<128>(prm, a, q, k, v, o, lse, st);
   return run_fwd<64>(prm, a, q, k, v, o, lse, st);
 }

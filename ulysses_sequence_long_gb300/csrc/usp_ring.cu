@@ -44,10 +44,12 @@ __device__ __forceinline__ uint4 pack8(const float f[8]) {
 
 struct MergeGeom {
   int BS, S, B, hq, vpr;  // vpr: 8-element vectors per row (D/8)
-  uint32_t n_vec;         // vectors in the whole head-layout tensor [P][B][S][hq][D]
+  uint32_t n_vec;         // vectors in the whole tensor
+  int seq, Sl, Hq;        // seq-layout [Ps][B][Sl][Hq][D] (shard length Sl) instead of head layout
 };
 
-// Row (rank r, token t, local head j) of the head layout; its LSE sits at
+// Row (rank r, token t, local head j) of the head layout, or (shard, row b,
+// position, global head r*hq + j) of the sequence shards; its LSE sits at
 // [r][b][j][s] of the [P][B][hq][S] statistics.  The lanes of one row are in
 // one warp (vpr divides 32), so the __syncwarp orders every lane's read of
 // the running LSE before the row's first lane overwrites it.
@@ -62,9 +64,22 @@ __global__ void __launch_bounds__(kThreads) fwd_merge_kernel(const uint4* __rest
   for (uint32_t v = blockIdx.x * blockDim.x + threadIdx.x; v < n_pad; v += stride) {
     const bool act = v < g.n_vec;
     const uint32_t row = v / g.vpr, e8 = v - row * g.vpr;
-    const uint32_t j = row % g.hq, rt = row / g.hq;
-    const uint32_t r = rt / g.BS, t = rt - r * g.BS;
-    const uint32_t b = t / g.S, s = t - b * g.S;
+    uint32_t r, j, b, s;
+    if (!g.seq) {  // head layout: row = (r, t, j)
+      j = row % g.hq;
+      const uint32_t rt = row / g.hq;
+      r = rt / g.BS;
+      const uint32_t t = rt - r * g.BS;
+      b = t / g.S;
+      s = t - b * g.S;
+    } else {       // seq layout: row = (shard, b, position in shard, global head)
+      const uint32_t h = row % g.Hq, tok = row / g.Hq;
+      const uint32_t bl = static_cast<uint32_t>(g.B) * g.Sl, rp = tok / bl, rem = tok - rp * bl;
+      b = rem / g.Sl;
+      s = rp * g.Sl + (rem - b * g.Sl);
+      r = h / g.hq;
+      j = h - r * g.hq;
+    }
     const size_t li = ((static_cast<size_t>(r) * g.B + b) * g.hq + j) * g.S + s;
     float la = -INFINITY, ls = -INFINITY, oa[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, os[8];
     if (act) {
@@ -145,6 +160,10 @@ int launch_ring_fwd_merge(const usp_attn_params& p, const void* o_step, const fl
   g.hq = p.Hq / p.P;
   g.vpr = p.D / 8;
   g.n_vec = static_cast<uint32_t>(static_cast<uint64_t>(p.P) * g.BS * g.hq * g.vpr);
+  const int ring = p.ring > 1 ? p.ring : 1;
+  g.seq = p.io_layout == USP_IO_SEQ ? 1 : 0;
+  g.Sl = p.S / (p.P * ring);
+  g.Hq = p.Hq;
   if (g.n_vec == 0) return USP_OK;
   ring::fwd_merge_kernel<<<ring::grid_for(g.n_vec), ring::kThreads, 0, st>>>(
       static_cast<const uint4*>(o_step), lse_step, o_acc, lse_acc, static_cast<uint4*>(o), lse, p.sinks, g, flags);

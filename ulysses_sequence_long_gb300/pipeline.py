@@ -217,68 +217,84 @@ class UlyssesAttention:
 class HybridAttention:
     """Ring x Ulysses (USP) over P = ring * ulysses emulated ranks.
 
-    The Ulysses exchange runs inside each ring group
-    (``usp_hybrid_relayout_*``); then ``ring`` steps each run the attention
-    kernels restricted to the key/value super-chunk a ring rank holds at that
-    step (``params.ring``/``ring_step``).  The forward merges each step's
-    (O, LSE) into the running result (``usp_ring_fwd_merge``, sink folded in
-    at the last step); the backward sums each step's bf16 block gradients in
-    fp32 (``usp_ring_grad_accumulate``) with the final LSE and D statistics
-    computed once.  Buffers are in the hybrid head layout [U][B][S][H/U][D].
+    The Ulysses exchange runs inside each ring group; then ``ring`` steps
+    each run the attention kernels restricted to the key/value super-chunk a
+    ring rank holds at that step (``params.ring``/``ring_step``).  The forward
+    merges each step's (O, LSE) into the running result
+    (``usp_ring_fwd_merge``, sink folded in at the last step); the backward
+    sums each step's bf16 block gradients in fp32
+    (``usp_ring_grad_accumulate``) with the final LSE and D statistics
+    computed once.
+
+    Fused (default when each sequence shard is a multiple of 128 tokens): the
+    kernels read and write the sequence shards directly and every
+    intermediate is in that layout, so no exchange kernel runs.  Explicit:
+    ``usp_hybrid_relayout_*`` move tensors to and from the hybrid head layout
+    [U][B][S][H/U][D].
     """
 
     def __init__(self, shape: Shape, ring: int, device="cuda", with_backward: bool = True,
-                 stored_ds: Optional[bool] = None):
+                 stored_ds: Optional[bool] = None, fused: Optional[bool] = None):
         s = self.shape = shape
         self.stored_ds = stored_ds
         if ring < 1 or s.P % ring != 0:
             raise ValueError("the ring degree must divide the ranks")
         self.ring = R = ring
         self.U = U = s.P // ring
+        can_fuse = (s.S // s.P) % 128 == 0
+        self.fused = can_fuse if fused is None else bool(fused)
+        if self.fused and not can_fuse:
+            raise ValueError("fused exchanges need each sequence shard to be a multiple of 128 tokens")
         dev = torch.device(device)
         bf, f32 = torch.bfloat16, torch.float32
         Bb, S, D = s.B, s.S, s.D
         self.hq = hq = s.Hq // U
         self.hk = hk = s.Hkv // U if s.Hkv >= U else 1
-        head_q, head_kv, stat = (U, Bb, S, hq, D), (U, Bb, S, hk, D), (U, Bb, hq, S)
-        self.q_head = torch.empty(head_q, dtype=bf, device=dev)
-        self.k_head = torch.empty(head_kv, dtype=bf, device=dev)
-        self.v_head = torch.empty(head_kv, dtype=bf, device=dev)
-        self.o_step = torch.empty(head_q, dtype=bf, device=dev)
+        seq_q, seq_kv = (s.P, Bb, S // s.P, s.Hq, D), (s.P, Bb, S // s.P, s.Hkv, D)
+        head_q, head_kv = (U, Bb, S, hq, D), (U, Bb, S, hk, D)
+        lay_q, lay_kv = (seq_q, seq_kv) if self.fused else (head_q, head_kv)
+        stat = (U, Bb, hq, S)
+        if not self.fused:
+            self.q_head = torch.empty(head_q, dtype=bf, device=dev)
+            self.k_head = torch.empty(head_kv, dtype=bf, device=dev)
+            self.v_head = torch.empty(head_kv, dtype=bf, device=dev)
+            self.o_head = torch.empty(head_q, dtype=bf, device=dev)
+        self.o_step = torch.empty(lay_q, dtype=bf, device=dev)
         self.lse_step = torch.empty(stat, dtype=f32, device=dev)
-        self.o_acc = torch.empty(head_q, dtype=f32, device=dev) if R > 1 else None
+        self.o_acc = torch.empty(lay_q, dtype=f32, device=dev) if R > 1 else None
         self.lse_acc = torch.empty(stat, dtype=f32, device=dev) if R > 1 else None
-        self.o_head = torch.empty(head_q, dtype=bf, device=dev)
         self.lse = torch.empty(stat, dtype=f32, device=dev)
-        self.o_seq = torch.empty((s.P, Bb, S // s.P, s.Hq, D), dtype=bf, device=dev)
+        self.o_seq = torch.empty(seq_q, dtype=bf, device=dev)
         self.cu_seqlens = torch.empty((Bb * S + 1,), dtype=torch.int32, device=dev)
         self.n_docs = torch.zeros((1,), dtype=torch.int32, device=dev)
         self.max_len = torch.zeros((1,), dtype=torch.int32, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
         self.scan_ws = torch.empty((B_.usp_cu_seqlens_workspace_bytes(Bb, S),), dtype=torch.uint8, device=dev)
         self.with_backward = with_backward
-        self.fused = False
         if with_backward:
-            self.do_head = torch.empty(head_q, dtype=bf, device=dev)
-            self.dq_step = torch.empty(head_q, dtype=bf, device=dev)
-            self.dk_step = torch.empty(head_kv, dtype=bf, device=dev)
-            self.dv_step = torch.empty(head_kv, dtype=bf, device=dev)
-            self.dq_acc = torch.empty(head_q, dtype=f32, device=dev) if R > 1 else None
-            self.dk_acc = torch.empty(head_kv, dtype=f32, device=dev) if R > 1 else None
-            self.dv_acc = torch.empty(head_kv, dtype=f32, device=dev) if R > 1 else None
-            self.dq_head = torch.empty(head_q, dtype=bf, device=dev)
-            self.dk_head = torch.empty(head_kv, dtype=bf, device=dev)
-            self.dv_head = torch.empty(head_kv, dtype=bf, device=dev)
-            self.dq_seq = torch.empty((s.P, Bb, S // s.P, s.Hq, D), dtype=bf, device=dev)
-            self.dk_seq = torch.empty((s.P, Bb, S // s.P, s.Hkv, D), dtype=bf, device=dev)
-            self.dv_seq = torch.empty((s.P, Bb, S // s.P, s.Hkv, D), dtype=bf, device=dev)
+            if not self.fused:
+                self.do_head = torch.empty(head_q, dtype=bf, device=dev)
+                self.dq_head = torch.empty(head_q, dtype=bf, device=dev)
+                self.dk_head = torch.empty(head_kv, dtype=bf, device=dev)
+                self.dv_head = torch.empty(head_kv, dtype=bf, device=dev)
+            self.dq_step = torch.empty(lay_q, dtype=bf, device=dev)
+            self.dk_step = torch.empty(lay_kv, dtype=bf, device=dev)
+            self.dv_step = torch.empty(lay_kv, dtype=bf, device=dev)
+            self.dq_acc = torch.empty(lay_q, dtype=f32, device=dev) if R > 1 else None
+            self.dk_acc = torch.empty(lay_kv, dtype=f32, device=dev) if R > 1 else None
+            self.dv_acc = torch.empty(lay_kv, dtype=f32, device=dev) if R > 1 else None
+            self.dq_seq = torch.empty(seq_q, dtype=bf, device=dev)
+            self.dk_seq = torch.empty(seq_kv, dtype=bf, device=dev)
+            self.dv_seq = torch.empty(seq_kv, dtype=bf, device=dev)
             self.dsinks = torch.zeros((s.Hq,), dtype=torch.float32, device=dev)
         self._bwd_ws = None
+        self._inputs = None
 
     def params(self, sinks=None, step: int = 0) -> B_.AttnParams:
         s = self.shape
         return B_.attn_params(s.B, s.S, s.Hq, s.Hkv, s.D, self.U, self.cu_seqlens, self.n_docs, s.causal,
-                              s.window_left, s.softmax_scale, sinks, B_.USP_IO_HEAD, self.ring, step)
+                              s.window_left, s.softmax_scale, sinks,
+                              B_.USP_IO_SEQ if self.fused else B_.USP_IO_HEAD, self.ring, step)
 
     def _flags(self, step: int) -> int:
         return (B_.USP_RING_FIRST if step == 0 else 0) | (B_.USP_RING_LAST if step == self.ring - 1 else 0)
@@ -289,19 +305,26 @@ class HybridAttention:
         s = self.shape
         mark = marks or (lambda i: None)
         mark(0)
-        B_.usp_hybrid_relayout_fwd_qkv(q_seq, k_seq, v_seq, self.q_head, self.k_head, self.v_head,
-                                       s.B, s.S, s.Hq, s.Hkv, s.D, self.ring, self.U, stream)
+        if self.fused:
+            self._inputs = (q_seq, k_seq, v_seq)
+            o_out = self.o_seq
+        else:
+            B_.usp_hybrid_relayout_fwd_qkv(q_seq, k_seq, v_seq, self.q_head, self.k_head, self.v_head,
+                                           s.B, s.S, s.Hq, s.Hkv, s.D, self.ring, self.U, stream)
+            self._inputs = (self.q_head, self.k_head, self.v_head)
+            o_out = self.o_head
         mark(1)
         B_.usp_cu_seqlens_from_position_ids(pos_shards, s.B, s.S, s.P, self.cu_seqlens, self.n_docs,
                                             self.max_len, self.scan_ws, self.status, stream)
         mark(2)
+        q, k, v = self._inputs
         for st in range(self.ring):
-            B_.usp_attn_fwd(self.params(None, st), self.q_head, self.k_head, self.v_head, self.o_step,
-                            self.lse_step, self.status, stream)
+            B_.usp_attn_fwd(self.params(None, st), q, k, v, self.o_step, self.lse_step, self.status, stream)
             B_.usp_ring_fwd_merge(self.params(sinks, st), self.o_step, self.lse_step, self.o_acc, self.lse_acc,
-                                  self.o_head, self.lse, self._flags(st), stream)
+                                  o_out, self.lse, self._flags(st), stream)
         mark(3)
-        B_.usp_hybrid_relayout_bwd(self.o_head, self.o_seq, s.B, s.S, s.Hq, s.D, self.ring, self.U, stream)
+        if not self.fused:
+            B_.usp_hybrid_relayout_bwd(self.o_head, self.o_seq, s.B, s.S, s.Hq, s.D, self.ring, self.U, stream)
         mark(4)
         return self.o_seq
 
@@ -318,26 +341,33 @@ class HybridAttention:
         if self._bwd_ws is None:
             self._bwd_ws, self.stored_ds = backward_workspace(prm, self.lse.device, self.stored_ds)
         ws = self._bwd_ws
+        q, k, v = self._inputs
         mark(0)
-        B_.usp_hybrid_relayout_fwd(do_seq, self.do_head, s.B, s.S, s.Hq, s.D, self.ring, self.U, stream)
+        if self.fused:
+            do, o = do_seq, self.o_seq
+            dq_out, dk_out, dv_out = self.dq_seq, self.dk_seq, self.dv_seq
+        else:
+            B_.usp_hybrid_relayout_fwd(do_seq, self.do_head, s.B, s.S, s.Hq, s.D, self.ring, self.U, stream)
+            do, o = self.do_head, self.o_head
+            dq_out, dk_out, dv_out = self.dq_head, self.dk_head, self.dv_head
         mark(1)
-        B_.usp_attn_bwd_preprocess(prm, self.o_head, self.lse, self.do_head,
-                                   self.dsinks if sinks is not None else None, ws, self.status, stream)
+        B_.usp_attn_bwd_preprocess(prm, o, self.lse, do, self.dsinks if sinks is not None else None, ws,
+                                   self.status, stream)
         mark(2)
         for st in range(self.ring):
-            B_.usp_attn_bwd_dkdv(self.params(None, st), self.q_head, self.k_head, self.v_head, self.lse,
-                                 self.do_head, self.dk_step, self.dv_step, ws, self.status, stream)
-            B_.usp_ring_grad_accumulate(self.dk_step, self.dk_acc, self.dk_head, self._flags(st), stream)
-            B_.usp_ring_grad_accumulate(self.dv_step, self.dv_acc, self.dv_head, self._flags(st), stream)
+            B_.usp_attn_bwd_dkdv(self.params(None, st), q, k, v, self.lse, do, self.dk_step, self.dv_step, ws,
+                                 self.status, stream)
+            B_.usp_ring_grad_accumulate(self.dk_step, self.dk_acc, dk_out, self._flags(st), stream)
+            B_.usp_ring_grad_accumulate(self.dv_step, self.dv_acc, dv_out, self._flags(st), stream)
         mark(3)
         for st in range(self.ring):
-            B_.usp_attn_bwd_dq(self.params(None, st), self.q_head, self.k_head, self.v_head, self.lse,
-                               self.do_head, self.dq_step, ws, self.status, stream)
-            B_.usp_ring_grad_accumulate(self.dq_step, self.dq_acc, self.dq_head, self._flags(st), stream)
+            B_.usp_attn_bwd_dq(self.params(None, st), q, k, v, self.lse, do, self.dq_step, ws, self.status, stream)
+            B_.usp_ring_grad_accumulate(self.dq_step, self.dq_acc, dq_out, self._flags(st), stream)
         mark(4)
-        B_.usp_hybrid_relayout_bwd(self.dq_head, self.dq_seq, s.B, s.S, s.Hq, s.D, self.ring, self.U, stream)
-        B_.usp_hybrid_relayout_bwd(self.dk_head, self.dk_seq, s.B, s.S, s.Hkv, s.D, self.ring, self.U, stream)
-        B_.usp_hybrid_relayout_bwd(self.dv_head, self.dv_seq, s.B, s.S, s.Hkv, s.D, self.ring, self.U, stream)
+        if not self.fused:
+            B_.usp_hybrid_relayout_bwd(self.dq_head, self.dq_seq, s.B, s.S, s.Hq, s.D, self.ring, self.U, stream)
+            B_.usp_hybrid_relayout_bwd(self.dk_head, self.dk_seq, s.B, s.S, s.Hkv, s.D, self.ring, self.U, stream)
+            B_.usp_hybrid_relayout_bwd(self.dv_head, self.dv_seq, s.B, s.S, s.Hkv, s.D, self.ring, self.U, stream)
         mark(5)
         return self.dq_seq, self.dk_seq, self.dv_seq
 
