@@ -229,10 +229,11 @@ class Step:
         if self.hybrid:
             # scan 3, preprocess 1 (+ dsink); per ring step: forward + merge,
             # dK/dV + 2 sums, dQ + 1 sum; explicit exchanges add 1 + 1 + 1 + 3
-            return 4 + sink + 7 * self.w.ring + (0 if self.ua.fused else 6)
-        # scan 3, fwd 1, preprocess 1 (+ dsink 1), dK/dV 1, dQ 1; the explicit
-        # exchanges add relayout qkv 1, O 1, dO 1, dQ/dK/dV 3
-        return 7 + sink + (0 if self.ua.fused else 6)
+            return 4 + sink + 7 * self.w.ring + (2 if self.ua.fused else 6)
+        # scan 3, fwd 1, preprocess 1 (+ dsink 1), dK/dV 1, dQ 1; the fused
+        # step adds the k/v exchange for the forward (2), the explicit one
+        # relayout qkv 1, O 1, dO 1, dQ/dK/dV 3
+        return 7 + sink + (2 if self.ua.fused else 6)
 
     # -- end to end: host buffers in and out, through the C ABI
     def make_host_io(self):

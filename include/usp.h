@@ -193,7 +193,12 @@ typedef struct {
   const float* sinks;        /* device fp32 [Hq] (global heads), or NULL */
   int io_layout;             /* USP_IO_HEAD (0): q, k, v, dO, o, dq, dk, dv in head-layout;
                                 USP_IO_SEQ (1): the same tensors in seq-layout — the exchanges
-                                are fused into the kernels' loads and stores; needs (S/P) % 128 == 0 */
+                                are fused into the kernels' loads and stores; needs (S/P) % 128 == 0;
+                                USP_IO_SEQ_KV_HEAD (2, usp_attn_fwd only): q and o in seq-layout,
+                                k and v in head-layout (the forward re-reads every k/v tile many
+                                times, which runs faster from head-layout rows than from rows
+                                strided over all key/value heads; the backward entry points
+                                return USP_ERR_UNSUPPORTED for it) */
   int ring;                  /* ring x Ulysses hybrid: ring degree R (0 or 1: no ring).  With R > 1,
                                 P is the Ulysses degree and a call computes one ring step: rows of
                                 super-chunk a (S/R positions each) see only the keys of super-chunk
@@ -204,7 +209,7 @@ typedef struct {
   int ring_step;             /* 0 <= ring_step < R */
 } usp_attn_params;
 
-enum { USP_IO_HEAD = 0, USP_IO_SEQ = 1 };
+enum { USP_IO_HEAD = 0, USP_IO_SEQ = 1, USP_IO_SEQ_KV_HEAD = 2 };
 
 /* q:   bf16 head-layout [P][B][S][Hq/P][D];  k, v: bf16 [P][B][S][Hkv/P][D]
  *      (with io_layout = USP_IO_SEQ: seq-layout [P][B][S/P][Hq][D] and [P][B][S/P][Hkv][D],

@@ -70,6 +70,10 @@ def test_host_checks_without_gpu(lib):
     assert lib.usp_attn_bwd_dkdv(ctypes.byref(prm), p, p, p, p, p, p, p, ws, 1 << 20, None, None) == \
         B.USP_ERR_UNSUPPORTED
     assert lib.usp_attn_bwd_dq(ctypes.byref(prm), p, p, p, p, p, p, ws, 1 << 20, None, None) == B.USP_ERR_UNSUPPORTED
+    # q/o in shards with k/v in head layout is a forward-only layout
+    prm = B.AttnParams(1, 256, 4, 2, 64, 2, 1, -1, 0.0, 16, 16, None, B.USP_IO_SEQ_KV_HEAD)
+    assert lib.usp_attn_bwd_dkdv(ctypes.byref(prm), p, p, p, p, p, p, p, ws, 1 << 20, None, None) == \
+        B.USP_ERR_UNSUPPORTED
 
 
 def test_fast_workspace_is_stats_plus_stored_ds_blocks(lib):

@@ -62,6 +62,7 @@ class AttnParams(ctypes.Structure):
 
 USP_IO_HEAD = 0
 USP_IO_SEQ = 1
+USP_IO_SEQ_KV_HEAD = 2
 
 
 def lib_path() -> str:

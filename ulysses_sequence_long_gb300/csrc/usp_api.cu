@@ -176,7 +176,8 @@ int check_attn_params(const usp_attn_params* p) {
   if (static_cast<int64_t>(p->P) * p->B * p->S * p->Hq * p->D >= (1ll << 40)) return USP_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(p->B) * p->S * p->Hq >= (1ll << 31)) return USP_ERR_UNSUPPORTED;  // 32-bit row counters
   if (p->Hq > 1024) return USP_ERR_UNSUPPORTED;  // the preprocess stages 32 tokens x Hq row sums in shared memory
-  if (p->io_layout != USP_IO_HEAD && p->io_layout != USP_IO_SEQ) return USP_ERR_INVALID_ARG;
+  if (p->io_layout != USP_IO_HEAD && p->io_layout != USP_IO_SEQ && p->io_layout != USP_IO_SEQ_KV_HEAD)
+    return USP_ERR_INVALID_ARG;
   // ring x Ulysses step: the kernels' 256-row blocks never straddle a super-chunk
   if (p->ring < 0) return USP_ERR_INVALID_ARG;
   const int ring = p->ring > 1 ? p->ring : 1;
@@ -188,7 +189,7 @@ int check_attn_params(const usp_attn_params* p) {
   }
   // fused exchanges: tiles of 128 tokens must never straddle a sequence shard
   // (P shards, P*ring for the hybrid)
-  if (p->io_layout == USP_IO_SEQ &&
+  if (p->io_layout != USP_IO_HEAD &&
       (p->S % (static_cast<int64_t>(p->P) * ring) != 0 || (p->S / (p->P * ring)) % 128 != 0))
     return USP_ERR_UNSUPPORTED;
   return USP_OK;
@@ -321,6 +322,7 @@ int usp_attn_bwd(const usp_attn_params* params, const void* q, const void* k, co
                  size_t ws_bytes, int32_t* dev_status, usp_stream_t stream) {
   int rc = check_attn_params(params);
   if (rc != USP_OK) return rc;
+  if (params->io_layout == USP_IO_SEQ_KV_HEAD) return USP_ERR_UNSUPPORTED;  // a forward-only layout
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr || dO == nullptr ||
       dq == nullptr || dk == nullptr || dv == nullptr)
     return USP_ERR_INVALID_ARG;
@@ -337,6 +339,7 @@ int usp_attn_bwd_preprocess(const usp_attn_params* params, const void* o, const 
                             float* dsinks, void* ws, size_t ws_bytes, int32_t* dev_status, usp_stream_t stream) {
   int rc = check_attn_params(params);
   if (rc != USP_OK) return rc;
+  if (params->io_layout == USP_IO_SEQ_KV_HEAD) return USP_ERR_UNSUPPORTED;  // a forward-only layout
   if (o == nullptr || lse == nullptr || dO == nullptr) return USP_ERR_INVALID_ARG;
   if (!aligned16(o) || !aligned16(lse) || !aligned16(dO)) return USP_ERR_ALIGNMENT;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < attn_bwd_ws_bytes(*params))
@@ -350,6 +353,7 @@ int usp_attn_bwd_dkdv(const usp_attn_params* params, const void* q, const void* 
                       usp_stream_t stream) {
   int rc = check_attn_params(params);
   if (rc != USP_OK) return rc;
+  if (params->io_layout == USP_IO_SEQ_KV_HEAD) return USP_ERR_UNSUPPORTED;  // a forward-only layout
   if (q == nullptr || k == nullptr || v == nullptr || lse == nullptr || dO == nullptr || dk == nullptr ||
       dv == nullptr)
     return USP_ERR_INVALID_ARG;
@@ -367,6 +371,7 @@ int usp_attn_bwd_dq(const usp_attn_params* params, const void* q, const void* k,
                     usp_stream_t stream) {
   int rc = check_attn_params(params);
   if (rc != USP_OK) return rc;
+  if (params->io_layout == USP_IO_SEQ_KV_HEAD) return USP_ERR_UNSUPPORTED;  // a forward-only layout
   if (q == nullptr || k == nullptr || v == nullptr || lse == nullptr || dO == nullptr || dq == nullptr)
     return USP_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(lse) || !aligned16(dO) || !aligned16(dq))

@@ -1060,6 +1060,7 @@ static AttnArgs make_args(const usp_attn_params& prm, int32_t* status) {
   a.sinks = prm.sinks;
   a.status = status;
   a.seq_io = prm.io_layout == USP_IO_SEQ ? 1 : 0;
+  a.kv_seq_io = a.seq_io;
   a.ring = prm.ring > 1 ? prm.ring : 1;
   a.ring_step = a.ring > 1 ? prm.ring_step : 0;
   a.C = prm.S / a.ring;

@@ -31,7 +31,8 @@ struct AttnArgs {
   const int32_t* n_docs;
   const float* sinks;  // global [Hq] or null
   int32_t* status;
-  int seq_io;  // 1: inputs and outputs in seq-layout [Ps][B][S/Ps][H][D] (exchanges fused)
+  int seq_io;     // 1: inputs and outputs in seq-layout [Ps][B][S/Ps][H][D] (exchanges fused)
+  int kv_seq_io;  // k and v in seq-layout too (0 with USP_IO_SEQ_KV_HEAD: k, v in head layout)
   int Sl;      // shard length S/Ps; Ps = P sequence shards, P*ring for the ring x Ulysses hybrid
   int ring, ring_step, C;  // ring x Ulysses: ring degree (1: none), step, super-chunk length S/ring
 };
@@ -84,14 +85,19 @@ __device__ __forceinline__ size_t row_offset(const AttnArgs& p, HeadRef h, int h
 // map.  In seq-layout the rows must lie in one shard of one row of the batch
 // (the kernels align tiles to make sure).
 __device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* m, uint64_t* bar, const AttnArgs& p,
-                                              int c64, HeadRef h, int t) {
-  if (!p.seq_io) {
+                                              int c64, HeadRef h, int t, bool seq) {
+  if (!seq) {
     tma_load_4d(dst, m, bar, c64 * 64, h.j, t, h.r);
   } else {
     const int b = t / p.S, s = t - b * p.S;
     const int rp = s / p.Sl, sp = s - rp * p.Sl;
     tma_load_5d(dst, m, bar, c64 * 64, h.g, sp, b, rp);
   }
+}
+
+__device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* m, uint64_t* bar, const AttnArgs& p,
+                                              int c64, HeadRef h, int t) {
+  tma_load_rows(dst, m, bar, p, c64, h, t, p.seq_io != 0);
 }
 
 // Document index d with cu[d] <= t < cu[d+1] (cu assumed valid, n >= 1).
@@ -217,10 +223,14 @@ int make_head_tmap(CUtensorMap* m, const void* base, int P, int BS, int H, int D
 int make_seq_tmap(CUtensorMap* m, const void* base, int P, int B, int Sl, int H, int D, int box_rows);
 
 // The map for either layout: head-layout (hpr heads per rank) or seq-layout (H heads).
-inline int make_rows_tmap(CUtensorMap* m, const void* base, const AttnArgs& a, int hpr, int H, int D, int box_rows) {
+inline int make_rows_tmap(CUtensorMap* m, const void* base, const AttnArgs& a, int hpr, int H, int D, int box_rows,
+                          bool seq) {
   // seq-layout: P*ring shards of Sl tokens (the hybrid's ring groups hold P shards each)
-  return a.seq_io ? make_seq_tmap(m, base, a.P * a.ring, a.B, a.Sl, H, D, box_rows)
-                  : make_head_tmap(m, base, a.P, a.BS, hpr, D, box_rows);
+  return seq ? make_seq_tmap(m, base, a.P * a.ring, a.B, a.Sl, H, D, box_rows)
+             : make_head_tmap(m, base, a.P, a.BS, hpr, D, box_rows);
+}
+inline int make_rows_tmap(CUtensorMap* m, const void* base, const AttnArgs& a, int hpr, int H, int D, int box_rows) {
+  return make_rows_tmap(m, base, a, hpr, H, D, box_rows, a.seq_io != 0);
 }
 
 int make_ds_tmap(CUtensorMap* m, const void* base, long long n_blocks);

@@ -113,9 +113,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     lo = max(lo, rk0);
     hi = min(hi, rk1);
   }
-  // With the exchanges fused, key tiles are aligned to 128 tokens so that a
-  // tile never straddles a rank's shard (keys before the document are masked).
-  if (p.seq_io) lo &= ~(kBN - 1);
+  // With k/v read from the sequence shards, key tiles are aligned to 128
+  // tokens so that a tile never straddles a shard (keys before the document
+  // are masked).
+  if (p.kv_seq_io) lo &= ~(kBN - 1);
   const int n_kv = hi > lo ? (hi - lo + kBN - 1) / kBN : 0;
   if (n_kv == 0) {
     // no key to see (a ring step whose block lies after these rows): O = 0 and
@@ -179,10 +180,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kv0 = lo + n * kBN;
         mbar_arrive_expect_tx(&bars->k_full[st], C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_rows(smem + C::OFF_K + st * C::TILE + c * kAtomBytes, &tk, &bars->k_full[st], p, c, kvh, kv0);
+          tma_load_rows(smem + C::OFF_K + st * C::TILE + c * kAtomBytes, &tk, &bars->k_full[st], p, c, kvh, kv0,
+                        p.kv_seq_io != 0);
         mbar_arrive_expect_tx(&bars->v_full[st], C::TILE);
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_rows(smem + C::OFF_V + st * C::TILE + c * kAtomBytes, &tv, &bars->v_full[st], p, c, kvh, kv0);
+          tma_load_rows(smem + C::OFF_V + st * C::TILE + c * kAtomBytes, &tv, &bars->v_full[st], p, c, kvh, kv0,
+                        p.kv_seq_io != 0);
         issued = n + 1;
       }
       // Never leave the CTA with copies still landing in its shared memory.
@@ -394,8 +397,8 @@ static int run_fwd(const usp_attn_params& prm, const AttnArgs& a, const void* q,
   CUtensorMap tq, tk, tv;
   int rc;
   if ((rc = make_rows_tmap(&tq, q, a, a.hq, a.Hq, D, kBM)) != USP_OK) return rc;
-  if ((rc = make_rows_tmap(&tk, k, a, a.hk, a.Hkv, D, kBN)) != USP_OK) return rc;
-  if ((rc = make_rows_tmap(&tv, v, a, a.hk, a.Hkv, D, kBN)) != USP_OK) return rc;
+  if ((rc = make_rows_tmap(&tk, k, a, a.hk, a.Hkv, D, kBN, a.kv_seq_io != 0)) != USP_OK) return rc;
+  if ((rc = make_rows_tmap(&tv, v, a, a.hk, a.Hkv, D, kBN, a.kv_seq_io != 0)) != USP_OK) return rc;
   fwd::Out out{static_cast<__nv_bfloat16*>(o), lse, (a.BS + 2 * kBM - 1) / (2 * kBM)};
   const int smem = fwd::Cfg<D>::SMEM;
   if (cudaFuncSetAttribute(fwd::attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
@@ -427,7 +430,8 @@ int launch_attn_fwd(const usp_attn_params& prm, const void* q, const void* k, co
   a.n_docs = prm.n_docs;
   a.sinks = prm.sinks;
   a.status = status;
-  a.seq_io = prm.io_layout == USP_IO_SEQ ? 1 : 0;
+  a.seq_io = prm.io_layout != USP_IO_HEAD ? 1 : 0;
+  a.kv_seq_io = prm.io_layout == USP_IO_SEQ ? 1 : 0;
   a.ring = prm.ring > 1 ? prm.ring : 1;
   a.ring_step = a.ring > 1 ? prm.ring_step : 0;
   a.C = prm.S / a.ring;

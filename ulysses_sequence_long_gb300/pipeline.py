@@ -9,9 +9,11 @@ sequence, and the output exchange back; the backward swaps the exchanges.
 Two ways to run the exchanges:
 
 * fused (default when S/P is a multiple of 128): the attention kernels read
-  q/k/v/dO straight from the sequence shards and write O/dQ/dK/dV straight
-  back (``io_layout = USP_IO_SEQ``); the permutation happens in their TMA
-  loads and stores, so no exchange kernel runs;
+  q/dO (and, in the backward, k/v) straight from the sequence shards and
+  write O/dQ/dK/dV straight back (``io_layout = USP_IO_SEQ``); the
+  permutation happens in their TMA loads and stores.  Only k and v are
+  exchanged explicitly for the forward (``USP_IO_SEQ_KV_HEAD``), which
+  re-reads every k/v tile many times and runs faster from head-layout rows;
 * explicit: ``usp_relayout_*`` kernels move the tensors between the shard
   layout and the head layout around head-layout attention.
 
@@ -92,10 +94,10 @@ class UlyssesAttention:
         P, Bb, S, D = s.P, s.B, s.S, s.D
         seq_q = (P, Bb, S // P, s.Hq, D)
         seq_kv = (P, Bb, S // P, s.Hkv, D)
+        self.k_head = torch.empty((P, Bb, S, s.hk, D), dtype=bf, device=dev)
+        self.v_head = torch.empty((P, Bb, S, s.hk, D), dtype=bf, device=dev)
         if not self.fused:
             self.q_head = torch.empty((P, Bb, S, s.hq, D), dtype=bf, device=dev)
-            self.k_head = torch.empty((P, Bb, S, s.hk, D), dtype=bf, device=dev)
-            self.v_head = torch.empty((P, Bb, S, s.hk, D), dtype=bf, device=dev)
             self.o_head = torch.empty((P, Bb, S, s.hq, D), dtype=bf, device=dev)
         self.lse = torch.empty((P, Bb, s.hq, S), dtype=torch.float32, device=dev)
         self.o_seq = torch.empty(seq_q, dtype=bf, device=dev)
@@ -119,11 +121,12 @@ class UlyssesAttention:
         self._bwd_ws = None
         self._inputs = None  # the forward's q/k/v as the attention kernels read them
 
-    def params(self, sinks: Optional[torch.Tensor]) -> B_.AttnParams:
+    def params(self, sinks: Optional[torch.Tensor], io: Optional[int] = None) -> B_.AttnParams:
         s = self.shape
+        if io is None:
+            io = B_.USP_IO_SEQ if self.fused else B_.USP_IO_HEAD
         return B_.attn_params(s.B, s.S, s.Hq, s.Hkv, s.D, s.P, self.cu_seqlens, self.n_docs, s.causal,
-                              s.window_left, s.softmax_scale, sinks,
-                              B_.USP_IO_SEQ if self.fused else B_.USP_IO_HEAD)
+                              s.window_left, s.softmax_scale, sinks, io)
 
     def _ws(self, prm):
         if self._bwd_ws is None:
@@ -134,6 +137,9 @@ class UlyssesAttention:
     def exchange_qkv(self, q_seq, k_seq, v_seq, stream=None):
         s = self.shape
         if self.fused:
+            # q stays in its shards; k and v go to head layout for the forward
+            B_.usp_relayout_fwd(k_seq, self.k_head, s.B, s.S, s.Hkv, s.D, s.P, stream)
+            B_.usp_relayout_fwd(v_seq, self.v_head, s.B, s.S, s.Hkv, s.D, s.P, stream)
             self._inputs = (q_seq, k_seq, v_seq)
             return
         B_.usp_relayout_fwd_qkv(q_seq, k_seq, v_seq, self.q_head, self.k_head, self.v_head,
@@ -147,8 +153,11 @@ class UlyssesAttention:
 
     def attention(self, sinks=None, stream=None):
         q, k, v = self._inputs
-        out = self.o_seq if self.fused else self.o_head
-        B_.usp_attn_fwd(self.params(sinks), q, k, v, out, self.lse, self.status, stream)
+        if self.fused:
+            B_.usp_attn_fwd(self.params(sinks, B_.USP_IO_SEQ_KV_HEAD), q, self.k_head, self.v_head, self.o_seq,
+                            self.lse, self.status, stream)
+        else:
+            B_.usp_attn_fwd(self.params(sinks), q, k, v, self.o_head, self.lse, self.status, stream)
 
     def exchange_out(self, stream=None):
         s = self.shape
@@ -254,10 +263,10 @@ class HybridAttention:
         head_q, head_kv = (U, Bb, S, hq, D), (U, Bb, S, hk, D)
         lay_q, lay_kv = (seq_q, seq_kv) if self.fused else (head_q, head_kv)
         stat = (U, Bb, hq, S)
+        self.k_head = torch.empty(head_kv, dtype=bf, device=dev)
+        self.v_head = torch.empty(head_kv, dtype=bf, device=dev)
         if not self.fused:
             self.q_head = torch.empty(head_q, dtype=bf, device=dev)
-            self.k_head = torch.empty(head_kv, dtype=bf, device=dev)
-            self.v_head = torch.empty(head_kv, dtype=bf, device=dev)
             self.o_head = torch.empty(head_q, dtype=bf, device=dev)
         self.o_step = torch.empty(lay_q, dtype=bf, device=dev)
         self.lse_step = torch.empty(stat, dtype=f32, device=dev)
@@ -290,11 +299,12 @@ class HybridAttention:
         self._bwd_ws = None
         self._inputs = None
 
-    def params(self, sinks=None, step: int = 0) -> B_.AttnParams:
+    def params(self, sinks=None, step: int = 0, io: Optional[int] = None) -> B_.AttnParams:
         s = self.shape
+        if io is None:
+            io = B_.USP_IO_SEQ if self.fused else B_.USP_IO_HEAD
         return B_.attn_params(s.B, s.S, s.Hq, s.Hkv, s.D, self.U, self.cu_seqlens, self.n_docs, s.causal,
-                              s.window_left, s.softmax_scale, sinks,
-                              B_.USP_IO_SEQ if self.fused else B_.USP_IO_HEAD, self.ring, step)
+                              s.window_left, s.softmax_scale, sinks, io, self.ring, step)
 
     def _flags(self, step: int) -> int:
         return (B_.USP_RING_FIRST if step == 0 else 0) | (B_.USP_RING_LAST if step == self.ring - 1 else 0)
@@ -306,6 +316,9 @@ class HybridAttention:
         mark = marks or (lambda i: None)
         mark(0)
         if self.fused:
+            # q stays in its shards; k and v go to the hybrid head layout for the forward
+            B_.usp_hybrid_relayout_fwd(k_seq, self.k_head, s.B, s.S, s.Hkv, s.D, self.ring, self.U, stream)
+            B_.usp_hybrid_relayout_fwd(v_seq, self.v_head, s.B, s.S, s.Hkv, s.D, self.ring, self.U, stream)
             self._inputs = (q_seq, k_seq, v_seq)
             o_out = self.o_seq
         else:
@@ -318,8 +331,10 @@ class HybridAttention:
                                             self.max_len, self.scan_ws, self.status, stream)
         mark(2)
         q, k, v = self._inputs
+        io_fwd = B_.USP_IO_SEQ_KV_HEAD if self.fused else B_.USP_IO_HEAD
         for st in range(self.ring):
-            B_.usp_attn_fwd(self.params(None, st), q, k, v, self.o_step, self.lse_step, self.status, stream)
+            B_.usp_attn_fwd(self.params(None, st, io_fwd), q, self.k_head, self.v_head, self.o_step, self.lse_step,
+                            self.status, stream)
             B_.usp_ring_fwd_merge(self.params(sinks, st), self.o_step, self.lse_step, self.o_acc, self.lse_acc,
                                   o_out, self.lse, self._flags(st), stream)
         mark(3)
