@@ -177,6 +177,17 @@ __device__ __forceinline__ void tmem_st_packed(uint32_t taddr, const float* x) {
   tmem_wait_st();
 }
 
+// 16 packed columns into TMEM columns [taddr, taddr + 16) (this warp's lanes).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&pk)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7]), "r"(pk[8]),
+      "r"(pk[9]), "r"(pk[10]), "r"(pk[11]), "r"(pk[12]), "r"(pk[13]), "r"(pk[14]), "r"(pk[15])
+      : "memory");
+  tmem_wait_st();
+}
+
 // One bf16 row of D elements (global, 16-byte aligned) into TMEM as D/2 packed
 // columns: the A-operand layout (lane = row, column = pair of K elements).
 template <int D>
@@ -543,6 +554,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) x[4 * c4 + e] = pr[4 * c4 + e] * (x[4 * c4 + e] - dv[e]);
       }
+      // dS^T packed once: into TMEM for the dK MMA (first: the MMA thread
+      // waits on it), then, if dS is stored, into the staging buffer
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+      tmem_st16(lb + T_DP + grp * 32, pk);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->ds_full);
       if (store_ds) {
         // The warp's [32 key rows][32 query columns] part of dS^T block (head,
         // row, kt, qs): staged in shared memory in the 64-byte swizzle (16-byte
@@ -559,8 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             *reinterpret_cast<uint4*>(buf + lane * 64 + ((e ^ ((lane >> 1) & 3)) << 4)) =
-                make_uint4(pack_bf16x2(x[8 * e], x[8 * e + 1]), pack_bf16x2(x[8 * e + 2], x[8 * e + 3]),
-                           pack_bf16x2(x[8 * e + 4], x[8 * e + 5]), pack_bf16x2(x[8 * e + 6], x[8 * e + 7]));
+                make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -570,10 +589,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++ds_slot;
         }
       }
-      tmem_st_packed<16>(lb + T_DP + grp * 32, x);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->ds_full);
     }
     if (ok && n_it > 0 && (ok = mbar_wait(&bars->fin, 0, abort, p.status))) {
       tc_fence_after();
