@@ -200,15 +200,21 @@ class Step:
         self.stream = torch.cuda.current_stream(device)
         self.n_events = 0
 
-    def run(self, events=None):
+    def run(self, events=None, group_events=None):
         """One whole step; optional CUDA events recorded between the calls
         (event i+1 closes CALLS[i]; exchanges that the fused mode folds into
-        the attention kernels take ~0 ms)."""
+        the attention kernels take ~0 ms).  When the backward runs in
+        key/value head groups, group_events[g][0] / [1] close group g's dK/dV
+        and dQ passes."""
         ua, d, s = self.ua, self.dev, self.stream
 
         def mark(i):
             if events is not None:
                 events[i].record(s)
+
+        def gmark(g, i):
+            if group_events is not None:
+                group_events[g][i].record(s)
 
         if self.hybrid:
             ua.forward_phases(d["q"], d["k"], d["v"], self.pos, self.sinks, s, marks=mark)
@@ -222,18 +228,19 @@ class Step:
         ua.attention(self.sinks, s)
         mark(3)
         ua.exchange_out(s)
-        ua.backward_phases(d["do"], self.sinks, s, marks=lambda i: mark(4 + i))
+        ua.backward_phases(d["do"], self.sinks, s, marks=lambda i: mark(4 + i), group_marks=gmark)
 
     def launches_per_step(self) -> int:
         sink = 1 if self.sinks is not None else 0
+        extra = 2 * (len(self.ua.ds_groups) - 1)   # dK/dV + dQ of each further key/value head group
         if self.hybrid:
             # scan 3, preprocess 1 (+ dsink); per ring step: forward + merge,
             # dK/dV + 2 sums, dQ + 1 sum; explicit exchanges add 1 + 1 + 1 + 3
-            return 4 + sink + 7 * self.w.ring + (2 if self.ua.fused else 6)
+            return 4 + sink + (7 + extra) * self.w.ring + (2 if self.ua.fused else 6)
         # scan 3, fwd 1, preprocess 1 (+ dsink 1), dK/dV 1, dQ 1; the fused
         # step adds the k/v exchange for the forward (2), the explicit one
         # relayout qkv 1, O 1, dO 1, dQ/dK/dV 3
-        return 7 + sink + (2 if self.ua.fused else 6)
+        return 7 + sink + extra + (2 if self.ua.fused else 6)
 
     # -- end to end: host buffers in and out, through the C ABI
     def make_host_io(self):
@@ -428,13 +435,16 @@ def main():
 
     # ---- timed region: K whole steps, events between the calls
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(args.steps)]
+    n_groups = len(step.ua.ds_groups)
+    gev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_groups)]
+           for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         barrier()
         torch.cuda.synchronize()
         start.record()
         for k in range(args.steps):
-            step.run(ev[k])
+            step.run(ev[k], gev[k] if n_groups > 1 else None)
         stop.record()
         torch.cuda.synchronize()
         barrier()
@@ -443,6 +453,18 @@ def main():
     per_call = {}
     for i, name in enumerate(CALLS):
         per_call[name] = statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps))
+    if n_groups > 1 and not step.hybrid:   # the passes alternate group by group
+        dkdv_i = CALLS.index("attn_bwd_dkdv")
+        t_dkdv, t_dq = [], []
+        for k in range(args.steps):
+            prev, a, b = ev[k][dkdv_i], 0.0, 0.0
+            for g in range(n_groups):
+                a += prev.elapsed_time(gev[k][g][0])
+                b += gev[k][g][0].elapsed_time(gev[k][g][1])
+                prev = gev[k][g][1]
+            t_dkdv.append(a)
+            t_dq.append(b)
+        per_call["attn_bwd_dkdv"], per_call["attn_bwd_dq"] = statistics.mean(t_dkdv), statistics.mean(t_dq)
 
     value = fl["total"] * world / (ms * 1e-3) / 1e12
     peaks = measured_peaks()
@@ -478,7 +500,9 @@ def main():
                        "documents": len(W.document_lengths(w)[0]), "visible_pairs_per_head": fl["pairs"],
                        "fwd_bwd_flop": fl["total"], "parallelism": f"emulated ulysses P={w.P}, replicas={world}",
                        "exchanges": "fused" if step.ua.fused else "explicit", "ring": w.ring,
-                       "dq_pass": "stored dS" if step.ua.stored_ds else "recomputed S and dP",
+                       "dq_pass": ("recomputed S and dP" if not step.ua.stored_ds else
+                                   "stored dS" if len(step.ua.ds_groups) == 1 else
+                                   f"stored dS, {len(step.ua.ds_groups)} key/value head groups"),
                        "l2": "inputs larger than L2 (no flush)"},
             "relayout_gbs": relayout_gbs, "relayout_frac_hbm": relayout_gbs / peaks["hbm_gbs"],
             "relayout_measured": relayout_note,

@@ -207,6 +207,11 @@ typedef struct {
                                 [P*R][B][S/(P*R)][H][D] (USP_IO_SEQ, needs (S/(P*R)) % 128 == 0).
                                 Needs (S/R) % 256 == 0. */
   int ring_step;             /* 0 <= ring_step < R */
+  int head_first, head_count; /* usp_attn_bwd_dkdv / usp_attn_bwd_dq with USP_IO_SEQ only: process the
+                                key/value heads [head_first, head_first + head_count) and their query
+                                heads (0, 0: all), so that the stored dS of a long sequence can be
+                                produced and consumed a group of heads at a time; every other entry
+                                point needs 0, 0 */
 } usp_attn_params;
 
 enum { USP_IO_HEAD = 0, USP_IO_SEQ = 1, USP_IO_SEQ_KV_HEAD = 2 };
@@ -292,6 +297,9 @@ int usp_ring_grad_accumulate(const void* g_step, float* g_acc, void* g_out, size
  * dK/dV and dQ calls of one backward must get the same ws and ws_bytes, with
  * the dK/dV call first. */
 size_t usp_attn_bwd_fast_workspace_bytes(const usp_attn_params* params);
+/* (With params->head_count > 0 the blocks are those of that head group, and
+ * the dK/dV and dQ calls of the group use that workspace; the statistics
+ * part still covers every head, as the preprocess writes it for all.) */
 
 /* Bytes of workspace usp_attn_bwd needs: the fp32 row statistic
  * D_t = sum_d dO_td O_td for every query row and head, 256-byte aligned. */

@@ -18,10 +18,11 @@ def _lib():
     built_lib()
 
 
-def _fwd_bwd(w, fused=False, stored_ds=None):
+def _fwd_bwd(w, fused=False, stored_ds=None, ds_group_size=None):
     from ulysses_sequence_long_gb300.pipeline import UlyssesAttention
     dev, host = device_inputs(w)
-    ua = UlyssesAttention(shape_of(w), with_backward=True, fused=fused, stored_ds=stored_ds)
+    ua = UlyssesAttention(shape_of(w), with_backward=True, fused=fused, stored_ds=stored_ds,
+                          ds_group_size=ds_group_size)
     ua.forward(dev["q"], dev["k"], dev["v"], dev["pos"], dev["sinks"])
     ua.backward(dev["do"], dev["sinks"])
     torch.cuda.synchronize()
@@ -123,6 +124,21 @@ def test_backward_full_size_whole_groups(w, groups, fused, stored_ds):
             do_r = doh.reshape(1, w.B, w.S, hq, w.D)
             bound = dsink_bound(lse_r, snk, o_r, do_r, hq)[heads]
             assert np.all(np.abs(got - ds[heads]) <= bound), (np.abs(got - ds[heads]), bound)
+
+
+@pytest.mark.parametrize("w,group", [(SMALL[2], 1), (SMALL[3], 3), (SMALL[6], 1), (W.MHA4K, 5)],
+                         ids=lambda x: x.name if hasattr(x, "name") else str(x))
+def test_backward_stored_ds_in_head_groups(w, group):
+    """The stored-dS passes run a group of key/value heads at a time over one
+    workspace (how a long sequence fits): same gradients as the oracle."""
+    ua, dev, host = _fwd_bwd(w, True, None, group)
+    assert ua.stored_ds and len(ua.ds_groups) == -(-w.Hkv // group)
+    snk = host["sinks"]
+    f = oracle.ulysses_fwd(host["q"], host["k"], host["v"], host["pos"], w.causal, w.window_left, None, snk)
+    g = oracle.ulysses_bwd(f, host["do"], w.causal, w.window_left, None, snk)
+    assert_close("dq", ua.dq_seq.float().cpu().numpy(), g["dq_seq"])
+    assert_close("dk", ua.dk_seq.float().cpu().numpy(), g["dk_seq"])
+    assert_close("dv", ua.dv_seq.float().cpu().numpy(), g["dv_seq"])
 
 
 @pytest.mark.parametrize("fused", [True, False], ids=["fused", "explicit"])

@@ -74,6 +74,21 @@ def test_host_checks_without_gpu(lib):
     prm = B.AttnParams(1, 256, 4, 2, 64, 2, 1, -1, 0.0, 16, 16, None, B.USP_IO_SEQ_KV_HEAD)
     assert lib.usp_attn_bwd_dkdv(ctypes.byref(prm), p, p, p, p, p, p, p, ws, 1 << 20, None, None) == \
         B.USP_ERR_UNSUPPORTED
+    # head groups: sequence-shard I/O only, inside [0, Hkv), backward passes only
+    def grp(io, h0, hc, S=256, Hq=4, Hkv=2, P=2, w=-1):
+        return B.AttnParams(1, S, Hq, Hkv, 64, P, 1, w, 0.0, 16, 16, None, io, 1, 0, h0, hc)
+    dkdv = lambda prm: lib.usp_attn_bwd_dkdv(ctypes.byref(prm), p, p, p, p, p, p, p, ws, 1 << 20, None, None)
+    assert dkdv(grp(B.USP_IO_HEAD, 0, 1)) == B.USP_ERR_UNSUPPORTED
+    seq = B.USP_IO_SEQ
+    assert dkdv(grp(seq, 1, 2)) == \
+        B.USP_ERR_INVALID_ARG
+    assert dkdv(grp(seq, 1, 0)) == \
+        B.USP_ERR_INVALID_ARG
+    assert dkdv(grp(seq, -1, 1)) == \
+        B.USP_ERR_INVALID_ARG
+    prm = grp(seq, 1, 1)
+    assert lib.usp_attn_fwd(ctypes.byref(prm), p, p, p, p, p, None, None) == B.USP_ERR_INVALID_ARG
+    assert lib.usp_attn_bwd_preprocess(ctypes.byref(prm), p, p, p, None, ws, 1 << 20, None, None) == B.USP_ERR_INVALID_ARG
 
 
 def test_fast_workspace_is_stats_plus_stored_ds_blocks(lib):
@@ -97,6 +112,14 @@ def test_fast_workspace_is_stats_plus_stored_ds_blocks(lib):
         prm = B.AttnParams(Bb, S, Hq, Hkv, 64, P, 1, w, 0.0, 16, 16, None)
         stats = lib.usp_attn_bwd_workspace_bytes(ctypes.byref(prm))
         assert lib.usp_attn_bwd_fast_workspace_bytes(ctypes.byref(prm)) == stats + brute(Bb, S, Hq, w)
+    # a head group stores the blocks of its own query heads only; the statistics stay whole
+    for Bb, S, Hq, Hkv, P, w, h0, hc in [(1, 32768, 32, 8, 8, -1, 2, 3), (1, 16384, 64, 8, 8, 127, 7, 1),
+                                         (1, 4096, 12, 12, 4, -1, 0, 5)]:
+        prm = B.AttnParams(Bb, S, Hq, Hkv, 64, P, 1, w, 0.0, 16, 16, None, B.USP_IO_SEQ, 1, 0, h0, hc)
+        whole = B.AttnParams(Bb, S, Hq, Hkv, 64, P, 1, w, 0.0, 16, 16, None, B.USP_IO_SEQ)
+        stats = lib.usp_attn_bwd_workspace_bytes(ctypes.byref(whole))
+        assert lib.usp_attn_bwd_workspace_bytes(ctypes.byref(prm)) == stats
+        assert lib.usp_attn_bwd_fast_workspace_bytes(ctypes.byref(prm)) == stats + brute(Bb, S, hc * Hq // Hkv, w)
     # no stored-dS path without a causal mask, or with rows not a multiple of 128
     for Bb, S, causal in [(1, 512, 0), (1, 320, 1)]:
         prm = B.AttnParams(Bb, S, 4, 2, 64, 2, causal, -1, 0.0, 16, 16, None)

@@ -57,6 +57,7 @@ class AttnParams(ctypes.Structure):
         ("window_left", ctypes.c_int), ("softmax_scale", ctypes.c_float),
         ("cu_seqlens", ctypes.c_void_p), ("n_docs", ctypes.c_void_p), ("sinks", ctypes.c_void_p),
         ("io_layout", ctypes.c_int), ("ring", ctypes.c_int), ("ring_step", ctypes.c_int),
+        ("head_first", ctypes.c_int), ("head_count", ctypes.c_int),
     ]
 
 
@@ -183,10 +184,11 @@ def usp_cu_seqlens_from_position_ids_noalloc(pos, B, S, P, cu_seqlens, n_docs, m
 
 
 def attn_params(B, S, Hq, Hkv, D, P, cu_seqlens, n_docs, causal=True, window_left=-1, softmax_scale=0.0,
-                sinks=None, io_layout=USP_IO_HEAD, ring=1, ring_step=0) -> AttnParams:
+                sinks=None, io_layout=USP_IO_HEAD, ring=1, ring_step=0, head_first=0, head_count=0) -> AttnParams:
     return AttnParams(B, S, Hq, Hkv, D, P, 1 if causal else 0, window_left, softmax_scale,
                       _dev(cu_seqlens, "cu_seqlens", torch.int32), _dev(n_docs, "n_docs", torch.int32),
-                      _dev(sinks, "sinks", torch.float32), int(io_layout), int(ring), int(ring_step))
+                      _dev(sinks, "sinks", torch.float32), int(io_layout), int(ring), int(ring_step),
+                      int(head_first), int(head_count))
 
 
 def usp_attn_fwd(params: AttnParams, q, k, v, o, lse, dev_status=None, stream=None):

@@ -187,6 +187,13 @@ int check_attn_params(const usp_attn_params* p) {
   } else if (p->ring_step != 0) {
     return USP_ERR_INVALID_ARG;
   }
+  // a head group of the backward passes (fused layout only)
+  if (p->head_count < 0 || p->head_first < 0) return USP_ERR_INVALID_ARG;
+  if (p->head_count == 0 && p->head_first != 0) return USP_ERR_INVALID_ARG;
+  if (p->head_count > 0) {
+    if (p->io_layout != USP_IO_SEQ) return USP_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(p->head_first) + p->head_count > p->Hkv) return USP_ERR_INVALID_ARG;
+  }
   // fused exchanges: tiles of 128 tokens must never straddle a sequence shard
   // (P shards, P*ring for the hybrid)
   if (p->io_layout != USP_IO_HEAD &&
@@ -298,6 +305,7 @@ int usp_attn_fwd(const usp_attn_params* params, const void* q, const void* k, co
                  int32_t* dev_status, usp_stream_t stream) {
   int rc = check_attn_params(params);
   if (rc != USP_OK) return rc;
+  if (params->head_count != 0) return USP_ERR_INVALID_ARG;  // head groups are for the dK/dV and dQ passes
   // a ring step leaves the sink out; usp_ring_fwd_merge adds it once at the last step
   if (params->ring > 1 && params->sinks != nullptr) return USP_ERR_INVALID_ARG;
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr) return USP_ERR_INVALID_ARG;
@@ -322,6 +330,7 @@ int usp_attn_bwd(const usp_attn_params* params, const void* q, const void* k, co
                  size_t ws_bytes, int32_t* dev_status, usp_stream_t stream) {
   int rc = check_attn_params(params);
   if (rc != USP_OK) return rc;
+  if (params->head_count != 0) return USP_ERR_INVALID_ARG;  // head groups are for the dK/dV and dQ passes
   if (params->io_layout == USP_IO_SEQ_KV_HEAD) return USP_ERR_UNSUPPORTED;  // a forward-only layout
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr || dO == nullptr ||
       dq == nullptr || dk == nullptr || dv == nullptr)
@@ -339,6 +348,7 @@ int usp_attn_bwd_preprocess(const usp_attn_params* params, const void* o, const 
                             float* dsinks, void* ws, size_t ws_bytes, int32_t* dev_status, usp_stream_t stream) {
   int rc = check_attn_params(params);
   if (rc != USP_OK) return rc;
+  if (params->head_count != 0) return USP_ERR_INVALID_ARG;  // head groups are for the dK/dV and dQ passes
   if (params->io_layout == USP_IO_SEQ_KV_HEAD) return USP_ERR_UNSUPPORTED;  // a forward-only layout
   if (o == nullptr || lse == nullptr || dO == nullptr) return USP_ERR_INVALID_ARG;
   if (!aligned16(o) || !aligned16(lse) || !aligned16(dO)) return USP_ERR_ALIGNMENT;
@@ -386,6 +396,7 @@ int usp_ring_fwd_merge(const usp_attn_params* params, const void* o_step, const 
                        float* lse_acc, void* o, float* lse, int flags, usp_stream_t stream) {
   int rc = check_attn_params(params);
   if (rc != USP_OK) return rc;
+  if (params->head_count != 0) return USP_ERR_INVALID_ARG;  // head groups are for the dK/dV and dQ passes
   if (flags & ~(USP_RING_FIRST | USP_RING_LAST)) return USP_ERR_INVALID_ARG;
   const bool first = flags & USP_RING_FIRST, last = flags & USP_RING_LAST;
   if (o_step == nullptr || lse_step == nullptr) return USP_ERR_INVALID_ARG;

@@ -341,12 +341,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (its gradient sums that rank's G query heads; replicas of a head are
   // summed by the exchange back), in seq-layout the global head, whose
   // gradient sums the whole group of Hq/Hkv query heads over the ranks.
-  const int per = p.seq_io ? p.Hkv : p.P * p.hk;
+  const int per = p.seq_io ? p.n_kvh : p.P * p.hk;
   const int kt = static_cast<int>(blockIdx.x) / per;
   const int unit = static_cast<int>(blockIdx.x) % per;
-  const HeadRef kvh = p.seq_io ? HeadRef{0, 0, unit} : kv_head_ref(p, unit / p.hk, unit % p.hk);
+  const HeadRef kvh = p.seq_io ? HeadRef{0, 0, p.kvh0 + unit} : kv_head_ref(p, unit / p.hk, unit % p.hk);
   const int n_heads = p.seq_io ? p.Hq / p.Hkv : p.G;
-  const int hg0 = p.seq_io ? unit * n_heads : kvh.r * p.hq + kvh.j * p.G;  // global index of the first query head
+  const int hg0 = p.seq_io ? (p.kvh0 + unit) * n_heads : kvh.r * p.hq + kvh.j * p.G;  // first query head (global)
   const int u0 = kt * kBN;
 
   const int n_docs = checked_docs(p);
@@ -572,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qs = (qlo - ds_row0) / kSL + i % n_q;
         const int rel = qs - 2 * ds_kt;
         if (rel >= 0 && rel < ds_cnt) {
-          const long long blk = (static_cast<long long>(hg) * p.B + ds_rowb) * g.dsg.per_row + ds_off0 + rel;
+          const long long blk = (static_cast<long long>(hg - p.hq0) * p.B + ds_rowb) * g.dsg.per_row + ds_off0 + rel;
           uint8_t* buf = smem + C::A_DS + (warp * 2 + (ds_slot & 1)) * 2048;
           if (ds_slot >= 2 && lane == 0) bulk_wait_group_read<1>();  // its store from two rounds ago has read it
           __syncwarp();
@@ -630,10 +630,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // late query tiles first (they see the most keys)
-  const int per = p.P * p.hq;
+  const int per = p.n_qh;  // the query heads of this pass's head group
   const int qt = g.n_tiles - 1 - static_cast<int>(blockIdx.x) / per;
-  const int rem = static_cast<int>(blockIdx.x) % per;
-  const int r = rem / p.hq, j = rem % p.hq;
+  const int hg = p.hq0 + static_cast<int>(blockIdx.x) % per;
+  const int r = hg / p.hq, j = hg % p.hq;
   const HeadRef qh = q_head_ref(p, r, j), kvh = kv_head_ref(p, r, j / p.G);
   const int t0 = qt * kBM;
 
@@ -859,11 +859,11 @@ struct DsUnit {
 
 __device__ __forceinline__ DsUnit ds_unit(const AttnArgs& p, const Grads& g, int n_docs, int u) {
   DsUnit w;
-  const int per = p.P * p.hq;
+  const int per = p.n_qh;  // the query heads of this pass's head group
   const int qt = g.n_tiles - 1 - u / per;
-  const int rem = u % per;
-  w.r = rem / p.hq;
-  w.j = rem % p.hq;
+  const int rem = u % per, hg = p.hq0 + rem;
+  w.r = hg / p.hq;
+  w.j = hg % p.hq;
   w.t0 = qt * kBM;
   int lo, hi;
   key_range(p, n_docs, w.t0, min(w.t0 + kBM, p.BS) - 1, lo, hi);
@@ -879,7 +879,7 @@ __device__ __forceinline__ DsUnit ds_unit(const AttnArgs& p, const Grads& g, int
   w.n_kv = hi > lo ? (hi - lo + kBN - 1) / kBN : 0;
   w.kt0 = (lo - w.row0) / kBN;
   w.qs0 = (w.t0 - w.row0) / kSL;  // the tile's first 64-query slice
-  w.head_base = (static_cast<long long>(w.r * p.hq + w.j) * p.B + rowb) * g.dsg.per_row;
+  w.head_base = (static_cast<long long>(rem) * p.B + rowb) * g.dsg.per_row;
   return w;
 }
 
@@ -1044,7 +1044,8 @@ static bool ds_geom(const usp_attn_params& p, bwd::DsGeom& g, long long& n_block
   }
   g.kc = (g.N - g.Wc) / 2 + 1;
   g.per_row = bwd::ds_off(g, p.S / kBN);
-  n_blocks = static_cast<long long>(p.Hq) * p.B * g.per_row;
+  const long long heads = p.head_count > 0 ? static_cast<long long>(p.head_count) * (p.Hq / p.Hkv) : p.Hq;
+  n_blocks = heads * p.B * g.per_row;
   return n_blocks > 0 && n_blocks < (1ll << 31);
 }
 
@@ -1080,6 +1081,11 @@ static AttnArgs make_args(const usp_attn_params& prm, int32_t* status) {
   a.ring_step = a.ring > 1 ? prm.ring_step : 0;
   a.C = prm.S / a.ring;
   a.Sl = prm.S / (prm.P * a.ring);  // sequence shard: P Ulysses ranks in each of `ring` groups
+  const int gf = prm.Hq / prm.Hkv;
+  a.kvh0 = prm.head_count > 0 ? prm.head_first : 0;
+  a.n_kvh = prm.head_count > 0 ? prm.head_count : prm.Hkv;
+  a.hq0 = a.kvh0 * gf;
+  a.n_qh = a.n_kvh * gf;
   return a;
 }
 
@@ -1125,7 +1131,7 @@ static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const v
     if (cudaFuncSetAttribute(bwd::dq_ds_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, CD::SMEM) !=
         cudaSuccess)
       return USP_ERR_CUDA;
-    const int n_units = g.n_tiles * a.P * a.hq;
+    const int n_units = g.n_tiles * a.n_qh;
     const int grid = n_units < device_sm_count() ? n_units : device_sm_count();  // persistent: one CTA per SM
     bwd::dq_ds_kernel<D><<<grid, bwd::kDsThreads, CD::SMEM, st>>>(tk, tds, a, g, n_units);
     return check_launch();
@@ -1142,7 +1148,7 @@ static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const v
     if (cudaFuncSetAttribute(bwd::dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::A_SMEM) !=
         cudaSuccess)
       return USP_ERR_CUDA;
-    const unsigned grid = static_cast<unsigned>(g.n_tiles) * (a.seq_io ? a.Hkv : a.P * a.hk);
+    const unsigned grid = static_cast<unsigned>(g.n_tiles) * (a.seq_io ? a.n_kvh : a.P * a.hk);
     bwd::dkdv_kernel<D><<<grid, bwd::kThreads, C::A_SMEM, st>>>(tq, tdo, tst, tds_st, a, g);
   } else {
     // 128-key tiles of K and V stream past TMEM-resident Q, dO
@@ -1151,7 +1157,7 @@ static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const v
     if ((rc = make_rows_tmap(&tv, v, a, a.hk, a.Hkv, D, kBN)) != USP_OK) return rc;
     if (cudaFuncSetAttribute(bwd::dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::B_SMEM) != cudaSuccess)
       return USP_ERR_CUDA;
-    bwd::dq_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.P * a.hq, bwd::kThreads, C::B_SMEM, st>>>(tk, tv, a, g);
+    bwd::dq_kernel<D><<<static_cast<unsigned>(g.n_tiles) * a.n_qh, bwd::kThreads, C::B_SMEM, st>>>(tk, tv, a, g);
   }
   return check_launch();
 }

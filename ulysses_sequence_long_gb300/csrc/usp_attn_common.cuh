@@ -35,6 +35,9 @@ struct AttnArgs {
   int kv_seq_io;  // k and v in seq-layout too (0 with USP_IO_SEQ_KV_HEAD: k, v in head layout)
   int Sl;      // shard length S/Ps; Ps = P sequence shards, P*ring for the ring x Ulysses hybrid
   int ring, ring_step, C;  // ring x Ulysses: ring degree (1: none), step, super-chunk length S/ring
+  // backward head group: key/value heads [kvh0, kvh0 + n_kvh) and their query
+  // heads [hq0, hq0 + n_qh) (all heads unless a group was asked for)
+  int kvh0, n_kvh, hq0, n_qh;
 };
 
 // Ring x Ulysses: at ring step `ring_step` the rows of super-chunk a (of

@@ -436,6 +436,10 @@ int launch_attn_fwd(const usp_attn_params& prm, const void* q, const void* k, co
   a.ring_step = a.ring > 1 ? prm.ring_step : 0;
   a.C = prm.S / a.ring;
   a.Sl = prm.S / (prm.P * a.ring);  // sequence shard: P Ulysses ranks in each of `ring` groups
+  a.kvh0 = 0;
+  a.n_kvh = prm.Hkv;
+  a.hq0 = 0;
+  a.n_qh = prm.Hq;
   if (prm.D == 128) return run_fwd<128>(prm, a, q, k, v, o, lse, st);
   return run_fwd<64>(prm, a, q, k, v, o, lse, st);
 }

@@ -62,30 +62,53 @@ class Shape:
         return (self.S // self.P) % 128 == 0
 
 
-def backward_workspace(prm: B_.AttnParams, device, stored_ds: Optional[bool] = None):
-    """Workspace of the backward calls and whether it holds the stored dS.
+def backward_workspace(prm: B_.AttnParams, device, stored_ds: Optional[bool] = None, Hkv: int = 0,
+                       groups_ok: bool = False, group_size: Optional[int] = None):
+    """Workspace of the backward calls, whether it holds stored dS, and the
+    key/value head groups the dK/dV and dQ passes run in.
 
-    With the stored dS the dK/dV pass writes dS blocks and the dQ pass reads
-    them instead of recomputing S and dP.  None picks it when the shape has
-    that path and its workspace takes at most half of the free device memory;
-    True insists on it (ValueError if the shape has none)."""
+    With stored dS the dK/dV pass writes dS blocks and the dQ pass reads them
+    instead of recomputing S and dP.  None picks it when its workspace takes
+    at most half of the free device memory, for all heads at once or, when
+    ``groups_ok`` (fused layout), for the largest group of key/value heads
+    that fits (the passes then run group by group over the same workspace);
+    True insists on it (ValueError if the shape has none).  ``group_size``
+    forces groups of that many key/value heads."""
     fast = B_.usp_attn_bwd_fast_workspace_bytes(prm)
-    if stored_ds is None:
+    groups = [(0, 0)]
+    if group_size is not None:
+        if not groups_ok or stored_ds is False:
+            raise ValueError("head groups need the fused layout and the stored-dS backward")
+        prm_c = B_.AttnParams(*[getattr(prm, f) for f, _ in prm._fields_])
+        prm_c.head_first, prm_c.head_count = 0, group_size
+        fast, stored_ds = B_.usp_attn_bwd_fast_workspace_bytes(prm_c), True
+        groups = [(h, min(group_size, Hkv - h)) for h in range(0, Hkv, group_size)]
+    elif stored_ds is None:
         free, _ = torch.cuda.mem_get_info(device)
         stored_ds = 0 < fast <= free // 2
+        if not stored_ds and fast > 0 and groups_ok:
+            for c in range(Hkv - 1, 0, -1):
+                prm_c = B_.AttnParams(*[getattr(prm, f) for f, _ in prm._fields_])
+                prm_c.head_first, prm_c.head_count = 0, c
+                need = B_.usp_attn_bwd_fast_workspace_bytes(prm_c)
+                if 0 < need <= free // 2:
+                    fast, stored_ds = need, True
+                    groups = [(h, min(c, Hkv - h)) for h in range(0, Hkv, c)]
+                    break
     if stored_ds and fast == 0:
         raise ValueError("this shape has no stored-dS backward (it needs a causal mask and S % 128 == 0)")
     n = fast if stored_ds else B_.usp_attn_bwd_workspace_bytes(prm)
-    return torch.empty((max(n, 256),), dtype=torch.uint8, device=device), bool(stored_ds)
+    return torch.empty((max(n, 256),), dtype=torch.uint8, device=device), bool(stored_ds), groups
 
 
 class UlyssesAttention:
     """Buffers and calls for one shape on one device."""
 
     def __init__(self, shape: Shape, device="cuda", with_backward: bool = True, fused: Optional[bool] = None,
-                 stored_ds: Optional[bool] = None):
+                 stored_ds: Optional[bool] = None, ds_group_size: Optional[int] = None):
         s = self.shape = shape
         self.stored_ds = stored_ds
+        self.ds_group_size = ds_group_size
         self.fused = shape.can_fuse if fused is None else bool(fused)
         if self.fused and not shape.can_fuse:
             raise ValueError("fused exchanges need S/P to be a multiple of 128")
@@ -119,18 +142,21 @@ class UlyssesAttention:
             self.dv_seq = torch.empty(seq_kv, dtype=bf, device=dev)
             self.dsinks = torch.zeros((s.Hq,), dtype=torch.float32, device=dev)
         self._bwd_ws = None
+        self.ds_groups = [(0, 0)]
         self._inputs = None  # the forward's q/k/v as the attention kernels read them
 
-    def params(self, sinks: Optional[torch.Tensor], io: Optional[int] = None) -> B_.AttnParams:
+    def params(self, sinks: Optional[torch.Tensor], io: Optional[int] = None, group=(0, 0)) -> B_.AttnParams:
         s = self.shape
         if io is None:
             io = B_.USP_IO_SEQ if self.fused else B_.USP_IO_HEAD
         return B_.attn_params(s.B, s.S, s.Hq, s.Hkv, s.D, s.P, self.cu_seqlens, self.n_docs, s.causal,
-                              s.window_left, s.softmax_scale, sinks, io)
+                              s.window_left, s.softmax_scale, sinks, io, head_first=group[0], head_count=group[1])
 
     def _ws(self, prm):
         if self._bwd_ws is None:
-            self._bwd_ws, self.stored_ds = backward_workspace(prm, self.lse.device, self.stored_ds)
+            self._bwd_ws, self.stored_ds, self.ds_groups = backward_workspace(
+                prm, self.lse.device, self.stored_ds, self.shape.Hkv, groups_ok=self.fused,
+                group_size=self.ds_group_size)
         return self._bwd_ws
 
     # -- steps ---------------------------------------------------------------
@@ -172,10 +198,13 @@ class UlyssesAttention:
         self.exchange_out(stream)
         return self.o_seq
 
-    def backward_phases(self, do_seq, sinks=None, stream=None, marks=None):
+    def backward_phases(self, do_seq, sinks=None, stream=None, marks=None, group_marks=None):
         """The backward as its separate library calls; `marks(i)` is called
         between them (for timing): 0 before, 1 after the dO exchange, 2 after
-        the preprocess, 3 after dK/dV, 4 after dQ, 5 after the output exchanges."""
+        the preprocess, 3 after dK/dV, 4 after dQ, 5 after the output exchanges.
+        When the passes run in key/value head groups, marks 3 and 4 both come
+        after the last group and `group_marks(g, 0)` / `group_marks(g, 1)`
+        after group g's dK/dV and dQ passes."""
         s = self.shape
         prm = self.params(sinks)
         ws = self._ws(prm)
@@ -191,9 +220,19 @@ class UlyssesAttention:
         B_.usp_attn_bwd_preprocess(prm, o, self.lse, do, self.dsinks if sinks is not None else None, ws,
                                    self.status, stream)
         mark(2)
-        B_.usp_attn_bwd_dkdv(prm, q, k, v, self.lse, do, dk, dv, ws, self.status, stream)
-        mark(3)
-        B_.usp_attn_bwd_dq(prm, q, k, v, self.lse, do, dq, ws, self.status, stream)
+        if len(self.ds_groups) == 1:
+            B_.usp_attn_bwd_dkdv(prm, q, k, v, self.lse, do, dk, dv, ws, self.status, stream)
+            mark(3)
+            B_.usp_attn_bwd_dq(prm, q, k, v, self.lse, do, dq, ws, self.status, stream)
+        else:  # stored dS a key/value head group at a time (both passes per group)
+            gmark = group_marks or (lambda g, i: None)
+            for gi, grp in enumerate(self.ds_groups):
+                prm_g = self.params(None, group=grp)
+                B_.usp_attn_bwd_dkdv(prm_g, q, k, v, self.lse, do, dk, dv, ws, self.status, stream)
+                gmark(gi, 0)
+                B_.usp_attn_bwd_dq(prm_g, q, k, v, self.lse, do, dq, ws, self.status, stream)
+                gmark(gi, 1)
+            mark(3)
         mark(4)
         if not self.fused:
             B_.usp_relayout_bwd(self.dq_head, self.dq_seq, s.B, s.S, s.Hq, s.D, s.P, stream)
@@ -243,9 +282,10 @@ class HybridAttention:
     """
 
     def __init__(self, shape: Shape, ring: int, device="cuda", with_backward: bool = True,
-                 stored_ds: Optional[bool] = None, fused: Optional[bool] = None):
+                 stored_ds: Optional[bool] = None, fused: Optional[bool] = None, ds_group_size: Optional[int] = None):
         s = self.shape = shape
         self.stored_ds = stored_ds
+        self.ds_group_size = ds_group_size
         if ring < 1 or s.P % ring != 0:
             raise ValueError("the ring degree must divide the ranks")
         self.ring = R = ring
@@ -297,14 +337,15 @@ class HybridAttention:
             self.dv_seq = torch.empty(seq_kv, dtype=bf, device=dev)
             self.dsinks = torch.zeros((s.Hq,), dtype=torch.float32, device=dev)
         self._bwd_ws = None
+        self.ds_groups = [(0, 0)]
         self._inputs = None
 
-    def params(self, sinks=None, step: int = 0, io: Optional[int] = None) -> B_.AttnParams:
+    def params(self, sinks=None, step: int = 0, io: Optional[int] = None, group=(0, 0)) -> B_.AttnParams:
         s = self.shape
         if io is None:
             io = B_.USP_IO_SEQ if self.fused else B_.USP_IO_HEAD
         return B_.attn_params(s.B, s.S, s.Hq, s.Hkv, s.D, self.U, self.cu_seqlens, self.n_docs, s.causal,
-                              s.window_left, s.softmax_scale, sinks, io, self.ring, step)
+                              s.window_left, s.softmax_scale, sinks, io, self.ring, step, group[0], group[1])
 
     def _flags(self, step: int) -> int:
         return (B_.USP_RING_FIRST if step == 0 else 0) | (B_.USP_RING_LAST if step == self.ring - 1 else 0)
@@ -354,7 +395,8 @@ class HybridAttention:
         mark = marks or (lambda i: None)
         prm = self.params(sinks, 0)
         if self._bwd_ws is None:
-            self._bwd_ws, self.stored_ds = backward_workspace(prm, self.lse.device, self.stored_ds)
+            self._bwd_ws, self.stored_ds, self.ds_groups = backward_workspace(
+                prm, self.lse.device, self.stored_ds, s.Hkv, groups_ok=self.fused, group_size=self.ds_group_size)
         ws = self._bwd_ws
         q, k, v = self._inputs
         mark(0)
@@ -369,15 +411,28 @@ class HybridAttention:
         B_.usp_attn_bwd_preprocess(prm, o, self.lse, do, self.dsinks if sinks is not None else None, ws,
                                    self.status, stream)
         mark(2)
-        for st in range(self.ring):
-            B_.usp_attn_bwd_dkdv(self.params(None, st), q, k, v, self.lse, do, self.dk_step, self.dv_step, ws,
-                                 self.status, stream)
-            B_.usp_ring_grad_accumulate(self.dk_step, self.dk_acc, dk_out, self._flags(st), stream)
-            B_.usp_ring_grad_accumulate(self.dv_step, self.dv_acc, dv_out, self._flags(st), stream)
-        mark(3)
-        for st in range(self.ring):
-            B_.usp_attn_bwd_dq(self.params(None, st), q, k, v, self.lse, do, self.dq_step, ws, self.status, stream)
-            B_.usp_ring_grad_accumulate(self.dq_step, self.dq_acc, dq_out, self._flags(st), stream)
+        if len(self.ds_groups) == 1:
+            for st in range(self.ring):
+                B_.usp_attn_bwd_dkdv(self.params(None, st), q, k, v, self.lse, do, self.dk_step, self.dv_step, ws,
+                                     self.status, stream)
+                B_.usp_ring_grad_accumulate(self.dk_step, self.dk_acc, dk_out, self._flags(st), stream)
+                B_.usp_ring_grad_accumulate(self.dv_step, self.dv_acc, dv_out, self._flags(st), stream)
+            mark(3)
+            for st in range(self.ring):
+                B_.usp_attn_bwd_dq(self.params(None, st), q, k, v, self.lse, do, self.dq_step, ws, self.status,
+                                   stream)
+                B_.usp_ring_grad_accumulate(self.dq_step, self.dq_acc, dq_out, self._flags(st), stream)
+        else:  # stored dS a key/value head group at a time (both passes per group)
+            for st in range(self.ring):
+                for grp in self.ds_groups:
+                    prm_g = self.params(None, st, group=grp)
+                    B_.usp_attn_bwd_dkdv(prm_g, q, k, v, self.lse, do, self.dk_step, self.dv_step, ws, self.status,
+                                         stream)
+                    B_.usp_attn_bwd_dq(prm_g, q, k, v, self.lse, do, self.dq_step, ws, self.status, stream)
+                B_.usp_ring_grad_accumulate(self.dk_step, self.dk_acc, dk_out, self._flags(st), stream)
+                B_.usp_ring_grad_accumulate(self.dv_step, self.dv_acc, dv_out, self._flags(st), stream)
+                B_.usp_ring_grad_accumulate(self.dq_step, self.dq_acc, dq_out, self._flags(st), stream)
+            mark(3)
         mark(4)
         if not self.fused:
             B_.usp_hybrid_relayout_bwd(self.dq_head, self.dq_seq, s.B, s.S, s.Hq, s.D, self.ring, self.U, stream)
