@@ -10,7 +10,7 @@
 // rank those are its own heads (contiguous head blocks keep groups local).
 //
 // Launches (each phase has its own entry point):
-//   preprocess  D_t and LSE_t*log2(e) for every (rank, query head, token), in a
+//   preprocess  D_t and -LSE_t*log2(e) for every (rank, query head, token), in a
 //               planar fp32 workspace [P*hq][2][B*S padded to 4]; then the sink
 //               gradients (one block per head, fixed-order tree reduction).
 //   dK/dV       CTA = (rank, kv head, 128 keys).  K and V live in TMEM for the
@@ -53,8 +53,9 @@ __device__ __forceinline__ size_t stat_index(const AttnArgs& p, int r, int j, in
   return (static_cast<size_t>(r * p.B + b) * p.hq + j) * p.S + s;
 }
 
-// Planar statistics: plane 0 = LSE*log2(e), plane 1 = D, rows of `bsp`
-// (B*S rounded up to a multiple of 4, so every plane starts 16-byte aligned).
+// Planar statistics: plane 0 = -LSE*log2(e) (negated, so that the packed FMA
+// adds it), plane 1 = D, rows of `bsp` (B*S rounded up to a multiple of 4, so
+// every plane starts 16-byte aligned).
 __device__ __forceinline__ size_t plane_index(int bsp, int hq, int r, int j, int plane, int t) {
   return ((static_cast<size_t>(r) * hq + j) * 2 + plane) * bsp + t;
 }
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
       const int h = idx / kPreTok, k = idx - h * kPreTok;
       if (k < ntok) {
         const int r = p.seq_io ? h / p.hq : r0, j = p.seq_io ? h - r * p.hq : h, t = t0 + k;
-        stats[plane_index(bsp, p.hq, r, j, 0, t)] = __ldg(lse + stat_index(p, r, j, t)) * kLog2e;
+        stats[plane_index(bsp, p.hq, r, j, 0, t)] = __ldg(lse + stat_index(p, r, j, t)) * -kLog2e;
         stats[plane_index(bsp, p.hq, r, j, 1, t)] = dsum[idx];
       }
     }
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(256) dsink_kernel(const float* __restrict__ st
   const float* l2 = stats + plane_index(bsp, p.hq, r, j, 0, 0);
   const float* dd = stats + plane_index(bsp, p.hq, r, j, 1, 0);
   float acc = 0.f;
-  for (int t = threadIdx.x; t < p.BS; t += blockDim.x) acc -= ex2(z2 - __ldg(l2 + t)) * __ldg(dd + t);
+  for (int t = threadIdx.x; t < p.BS; t += blockDim.x) acc -= ex2(z2 + __ldg(l2 + t)) * __ldg(dd + t);
   red[threadIdx.x] = acc;
   __syncthreads();
   for (int s = 128; s > 0; s >>= 1) {
@@ -241,7 +242,7 @@ template <int D>
 struct Cfg {
   static constexpr int NCH = D / 64;
   static constexpr int SLICE = NCH * kSliceBytes;  // 64-row bf16 tile
-  static constexpr int STAT = 2 * kSL * 4;        // [2][64] fp32: LSE*log2e, D
+  static constexpr int STAT = 2 * kSL * 4;        // [2][64] fp32: -LSE*log2e, D
   static constexpr int NST = (D == 128) ? 5 : 8;  // stages of the streamed slices
   // dK/dV: ring of (Q, dO, stats) 64-query slices, then two 2 KB dS staging
   // buffers per compute warp (its [32 keys][32 queries] part of a dS block)
@@ -532,13 +533,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c < c_lo || c > c_hi) x[c] = -INFINITY;
       }
       float pr[32];
+      const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(st + 4 * c4);
-        pr[4 * c4] = ex2(fmaf(x[4 * c4], p.scale_log2, -l4.x));
-        pr[4 * c4 + 1] = ex2(fmaf(x[4 * c4 + 1], p.scale_log2, -l4.y));
-        pr[4 * c4 + 2] = ex2(fmaf(x[4 * c4 + 2], p.scale_log2, -l4.z));
-        pr[4 * c4 + 3] = ex2(fmaf(x[4 * c4 + 3], p.scale_log2, -l4.w));
+        const float4 l4 = *reinterpret_cast<const float4*>(st + 4 * c4);  // -LSE*log2(e)
+        const float2 e0 = f2_unpack(f2_fma(f2_pack(x[4 * c4], x[4 * c4 + 1]), sc2, f2_pack(l4.x, l4.y)));
+        const float2 e1 = f2_unpack(f2_fma(f2_pack(x[4 * c4 + 2], x[4 * c4 + 3]), sc2, f2_pack(l4.z, l4.w)));
+        pr[4 * c4] = ex2(e0.x);
+        pr[4 * c4 + 1] = ex2(e0.y);
+        pr[4 * c4 + 2] = ex2(e1.x);
+        pr[4 * c4 + 3] = ex2(e1.y);
       }
       tmem_st_packed<16>(lb + T_S + grp * 32, pr);
       tc_fence_before();
@@ -550,9 +554,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
         const float4 d4 = *reinterpret_cast<const float4*>(st + kSL + 4 * c4);
-        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[4 * c4 + e] = pr[4 * c4 + e] * (x[4 * c4 + e] - dv[e]);
+        const float2 g0 = f2_unpack(f2_mul(f2_pack(pr[4 * c4], pr[4 * c4 + 1]),
+                                           f2_sub(f2_pack(x[4 * c4], x[4 * c4 + 1]), f2_pack(d4.x, d4.y))));
+        const float2 g1 = f2_unpack(f2_mul(f2_pack(pr[4 * c4 + 2], pr[4 * c4 + 3]),
+                                           f2_sub(f2_pack(x[4 * c4 + 2], x[4 * c4 + 3]), f2_pack(d4.z, d4.w))));
+        x[4 * c4] = g0.x;
+        x[4 * c4 + 1] = g0.y;
+        x[4 * c4 + 2] = g1.x;
+        x[4 * c4 + 3] = g1.y;
       }
       // dS^T packed once: into TMEM for the dK MMA (first: the MMA thread
       // waits on it), then, if dS is stored, into the staging buffer
@@ -762,10 +771,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars->qd_ready);
     }
     int a = 0, b = 0;
-    float lse2 = INFINITY, dvt = 0.f;
+    float nlse2 = -INFINITY, dvt = 0.f;  // -LSE*log2(e) of the row
     if (row_ok) {
       doc_bounds(p.cu, n_docs, p.BS, t, a, b);
-      lse2 = __ldg(g.stats + plane_index(g.bsp, p.hq, r, j, 0, t));
+      nlse2 = __ldg(g.stats + plane_index(g.bsp, p.hq, r, j, 0, t));
       dvt = __ldg(g.stats + plane_index(g.bsp, p.hq, r, j, 1, t));
     }
     a = max(a, rk0);  // a ring step: one key/value super-chunk only
@@ -788,13 +797,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c < c_lo || c > c_hi) x[c] = -INFINITY;
       }
       float pr[64];
+      {
+        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nl2 = f2_pack(nlse2, nlse2);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) pr[c] = ex2(fmaf(x[c], p.scale_log2, -lse2));
+        for (int c = 0; c < 64; c += 2) {
+          const float2 e = f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), sc2, nl2));
+          pr[c] = ex2(e.x);
+          pr[c + 1] = ex2(e.y);
+        }
+      }
       if (!(ok = mbar_wait(&bars->dp_full, ph, abort, p.status))) break;
       tc_fence_after();
       tmem_ld_cols<64>(lb + dp_col, x);
+      {
+        const uint64_t d2 = f2_pack(dvt, dvt);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) x[c] = pr[c] * (x[c] - dvt);
+        for (int c = 0; c < 64; c += 2) {
+          const float2 g2 = f2_unpack(f2_mul(f2_pack(pr[c], pr[c + 1]), f2_sub(f2_pack(x[c], x[c + 1]), d2)));
+          x[c] = g2.x;
+          x[c + 1] = g2.y;
+        }
+      }
       tmem_st_packed<32>(lb + s_col, x);
       tc_fence_before();
       __syncwarp();
@@ -1026,7 +1049,7 @@ __global__ void __launch_bounds__(kDsThreads, 1)
 static int stats_row_pitch(int BS) { return (BS + 3) & ~3; }
 
 size_t attn_bwd_ws_bytes(const usp_attn_params& p) {
-  // planar {LSE*log2e, D} per (rank, query head), rows padded to 4 tokens
+  // planar {-LSE*log2e, D} per (rank, query head), rows padded to 4 tokens
   size_t n = static_cast<size_t>(p.Hq) * 2 * stats_row_pitch(p.B * p.S);
   return (n * sizeof(float) + 255) / 256 * 256;
 }
@@ -1089,7 +1112,7 @@ static AttnArgs make_args(const usp_attn_params& prm, int32_t* status) {
   return a;
 }
 
-// 1. D = rowsum(dO * O) and LSE*log2e into the workspace, then the sink gradients.
+// 1. D = rowsum(dO * O) and -LSE*log2e into the workspace, then the sink gradients.
 int launch_attn_bwd_preprocess(const usp_attn_params& prm, const void* o, const float* lse, const void* dO,
                                float* dsinks, void* ws, int32_t* status, cudaStream_t st) {
   const AttnArgs a = make_args(prm, status);

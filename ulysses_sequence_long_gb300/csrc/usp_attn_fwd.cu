@@ -320,20 +320,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = m_new;
       }
       const float m_use = (m == -INFINITY) ? 0.f : m;
-      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
+      uint64_t rs2[4] = {0, 0, 0, 0};  // 8 independent partial sums, two per register
+      const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(-m_use, -m_use);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {  // each 64-column half is packed and stored as soon as it is done
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          const float p0 = ex2(fmaf(s[64 * h + 2 * c], p.scale_log2, -m_use));
-          const float p1 = ex2(fmaf(s[64 * h + 2 * c + 1], p.scale_log2, -m_use));
-          rs8[c & 7] += p0 + p1;
+          const float2 e = f2_unpack(f2_fma(f2_pack(s[64 * h + 2 * c], s[64 * h + 2 * c + 1]), sc2, nm2));
+          const float p0 = ex2(e.x), p1 = ex2(e.y);
+          rs2[c & 3] = f2_add(rs2[c & 3], f2_pack(p0, p1));
           pk[c] = pack_bf16x2(p0, p1);
         }
         tmem_st32(s_tm + 32 * h, pk);
       }
-      l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      const float2 r01 = f2_unpack(f2_add(rs2[0], rs2[1])), r23 = f2_unpack(f2_add(rs2[2], rs2[3]));
+      l += (r01.x + r01.y) + (r23.x + r23.y);
       // The running max moved for some row of this warp: rescale the O rows.
       // PV of the previous tile has finished (S of this tile was committed
       // after it), and PV of this tile waits for this warp's arrival below.
