@@ -437,10 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(kBN, kSL, false, false);  // [128 keys x 64 queries], K = D
       constexpr uint32_t id_g = idesc_bf16(kBN, D, false, true);      // [128 keys x D], K = 64 queries
-      auto issue_st = [&](int i) -> bool {  // S^T_i = K Q_i^T
+      // S^T_i = K Q_i^T.  Slot i has landed: the compute warps wait for it
+      // before handing in P of iteration i-1 (each barrier wait of this
+      // thread stalls the tensor core, so it keeps only the hand-offs).
+      auto issue_st = [&](int i) -> bool {
         const int s = i % C::NST;
-        if (!mbar_wait(&bars->qdo_full[s], (i / C::NST) & 1, abort, p.status)) return false;
-        tc_fence_after();
         const uint32_t qa = sbase + C::A_Q + s * C::SLICE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -458,9 +459,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A operand columns of a packed 64-query slice: the two halves sit at +0 and +32
       auto acol = [](int kk) -> uint32_t { return kk < 2 ? kk * 8 : 32 + (kk - 2) * 8; };
       bool ok = mbar_wait(&bars->kv_ready, 0, abort, p.status);
-      if (ok && n_it > 0) {
-        ok = issue_st(0);
-        if (ok) issue_dpt(0);
+      if (ok && n_it > 0 && (ok = mbar_wait(&bars->qdo_full[0], 0, abort, p.status))) {
+        tc_fence_after();
+        issue_st(0);
+        issue_dpt(0);
       }
       for (int i = 0; i < n_it && ok; ++i) {
         const int s = i % C::NST;
@@ -512,13 +514,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->kv_ready);
     }
-    bool ok = true;
+    bool ok = n_it == 0 || mbar_wait(&bars->qdo_full[0], 0, abort, p.status);
     int ds_slot = 0;  // dS blocks this warp has staged
     for (int i = 0; i < n_it && ok; ++i) {
       const int s = i % C::NST;
       const uint32_t ph = i & 1;
       const int q0 = qlo + (i % n_q) * kSL + grp * 32;  // first query column of this group
-      if (!(ok = mbar_wait(&bars->qdo_full[s], (i / C::NST) & 1, abort, p.status))) break;
+      // the next slot lands before P of this iteration is handed in: the MMA
+      // thread issues S^T of the next iteration on that hand-off alone
+      if (i + 1 < n_it &&
+          !(ok = mbar_wait(&bars->qdo_full[(i + 1) % C::NST], ((i + 1) / C::NST) & 1, abort, p.status)))
+        break;
       const float* st = reinterpret_cast<const float*>(smem + C::A_STAT + s * C::STAT) + grp * 32;
       if (!(ok = mbar_wait(&bars->st_full, ph, abort, p.status))) break;
       tc_fence_after();
