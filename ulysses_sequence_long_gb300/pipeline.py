@@ -62,43 +62,55 @@ class Shape:
         return (self.S // self.P) % 128 == 0
 
 
-def backward_workspace(prm: B_.AttnParams, device, stored_ds: Optional[bool] = None, Hkv: int = 0,
-                       groups_ok: bool = False, group_size: Optional[int] = None):
-    """Workspace of the backward calls, whether it holds stored dS, and the
-    key/value head groups the dK/dV and dQ passes run in.
+def plan_backward(prm: B_.AttnParams, free_bytes: int, stored_ds: Optional[bool] = None, Hkv: int = 0,
+                  groups_ok: bool = False, group_size: Optional[int] = None):
+    """(workspace bytes, stored dS?, key/value head groups) of the backward
+    calls for ``free_bytes`` of free device memory (host arithmetic only).
 
     With stored dS the dK/dV pass writes dS blocks and the dQ pass reads them
     instead of recomputing S and dP.  None picks it when its workspace takes
-    at most half of the free device memory, for all heads at once or, when
+    at most half of the free memory, for all heads at once or, when
     ``groups_ok`` (fused layout), for the largest group of key/value heads
     that fits (the passes then run group by group over the same workspace);
     True insists on it (ValueError if the shape has none).  ``group_size``
-    forces groups of that many key/value heads."""
+    forces groups of that many key/value heads.  A group is (first key/value
+    head, count); [(0, 0)] means all heads in one pass."""
+    def with_group(c):
+        prm_c = B_.AttnParams(*[getattr(prm, f) for f, _ in prm._fields_])
+        prm_c.head_first, prm_c.head_count = 0, c
+        return B_.usp_attn_bwd_fast_workspace_bytes(prm_c)
+
     fast = B_.usp_attn_bwd_fast_workspace_bytes(prm)
     groups = [(0, 0)]
     if group_size is not None:
         if not groups_ok or stored_ds is False:
             raise ValueError("head groups need the fused layout and the stored-dS backward")
-        prm_c = B_.AttnParams(*[getattr(prm, f) for f, _ in prm._fields_])
-        prm_c.head_first, prm_c.head_count = 0, group_size
-        fast, stored_ds = B_.usp_attn_bwd_fast_workspace_bytes(prm_c), True
+        if not 0 < group_size <= Hkv:
+            raise ValueError(f"group_size must be in [1, {Hkv}]")
+        fast, stored_ds = with_group(group_size), True
         groups = [(h, min(group_size, Hkv - h)) for h in range(0, Hkv, group_size)]
     elif stored_ds is None:
-        free, _ = torch.cuda.mem_get_info(device)
-        stored_ds = 0 < fast <= free // 2
+        stored_ds = 0 < fast <= free_bytes // 2
         if not stored_ds and fast > 0 and groups_ok:
             for c in range(Hkv - 1, 0, -1):
-                prm_c = B_.AttnParams(*[getattr(prm, f) for f, _ in prm._fields_])
-                prm_c.head_first, prm_c.head_count = 0, c
-                need = B_.usp_attn_bwd_fast_workspace_bytes(prm_c)
-                if 0 < need <= free // 2:
+                need = with_group(c)
+                if 0 < need <= free_bytes // 2:
                     fast, stored_ds = need, True
                     groups = [(h, min(c, Hkv - h)) for h in range(0, Hkv, c)]
                     break
     if stored_ds and fast == 0:
         raise ValueError("this shape has no stored-dS backward (it needs a causal mask and S % 128 == 0)")
     n = fast if stored_ds else B_.usp_attn_bwd_workspace_bytes(prm)
-    return torch.empty((max(n, 256),), dtype=torch.uint8, device=device), bool(stored_ds), groups
+    return n, bool(stored_ds), groups
+
+
+def backward_workspace(prm: B_.AttnParams, device, stored_ds: Optional[bool] = None, Hkv: int = 0,
+                       groups_ok: bool = False, group_size: Optional[int] = None):
+    """The workspace tensor of the backward calls on ``device``, with the
+    choices of ``plan_backward`` for the device's free memory."""
+    free = torch.cuda.mem_get_info(device)[0] if stored_ds is None and group_size is None else 0
+    n, stored_ds, groups = plan_backward(prm, free, stored_ds, Hkv, groups_ok, group_size)
+    return torch.empty((max(n, 256),), dtype=torch.uint8, device=device), stored_ds, groups
 
 
 class UlyssesAttention:
