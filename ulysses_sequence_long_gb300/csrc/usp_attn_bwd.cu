@@ -15,7 +15,7 @@
 //               gradients (one block per head, fixed-order tree reduction).
 //   dK/dV       CTA = (rank, kv head, 128 keys).  K and V live in TMEM for the
 //               whole CTA and serve as the A operands of S^T = K Q^T and
-//               dP^T = V dO^T; 64-query slices of Q, dO and their statistics
+//               dP^T = V dO^T; query slices (64 at D=128, 128 at D=64) of Q, dO and their statistics
 //               stream through shared memory; P^T and dS^T (bf16) are written
 //               over S^T / dP^T and feed dV += P^T dO, dK += dS^T Q.
 //   dQ          CTA = (rank, query head, 128 rows).  Q and dO live in TMEM as
@@ -42,8 +42,7 @@ namespace usp {
 namespace bwd {
 
 constexpr int kThreads = 320;
-constexpr int kSL = 64;                      // slice width (queries in dK/dV, keys in dQ)
-constexpr int kSliceBytes = kSL * 128;       // 64-row, 128-byte-wide swizzle column
+constexpr int kSL = 64;                      // queries of a stored dS block
 constexpr int kAtomBytes = kBN * 128;        // 128-row, 128-byte-wide swizzle column
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -241,11 +240,15 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int atom_bytes, 
 template <int D>
 struct Cfg {
   static constexpr int NCH = D / 64;
-  static constexpr int SLICE = NCH * kSliceBytes;  // 64-row bf16 tile
-  static constexpr int STAT = 2 * kSL * 4;        // [2][64] fp32: -LSE*log2e, D
-  static constexpr int NST = (D == 128) ? 5 : 8;  // stages of the streamed slices
-  // dK/dV: ring of (Q, dO, stats) 64-query slices, then two 2 KB dS staging
-  // buffers per compute warp (its [32 keys][32 queries] part of a dS block)
+  // dK/dV query slice: 64 queries at D=128 (TMEM holds S^T, dP^T, dV, dK, K,
+  // V in its 512 columns only so), 128 at D=64 (twice the work per hand-off)
+  static constexpr int SL = (D == 64) ? 128 : 64;
+  static constexpr int SLB = SL * 128;            // one 64-column swizzle atom of a slice
+  static constexpr int SLICE = NCH * SLB;         // SL-row bf16 tile
+  static constexpr int STAT = 2 * SL * 4;         // [2][SL] fp32: -LSE*log2e, D
+  static constexpr int NST = 5;                   // stages of the streamed slices
+  // dK/dV: ring of (Q, dO, stats) slices, then two 2 KB dS staging buffers
+  // per compute warp (a [32 keys][32 queries] part of a dS block)
   static constexpr int A_Q = 0;
   static constexpr int A_DO = A_Q + NST * SLICE;
   static constexpr int A_STAT = A_DO + NST * SLICE;
@@ -372,9 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     qlo &= ~(kBM - 1);
     qhi = (qhi + kBM - 1) & ~(kBM - 1);
   } else {
-    qlo &= p.seq_io ? ~(kSL - 1) : ~3;
+    qlo &= p.seq_io ? ~(C::SL - 1) : ~3;
   }
-  const int n_q = qhi > qlo ? (qhi - qlo + kSL - 1) / kSL : 0;
+  const int n_q = qhi > qlo ? (qhi - qlo + C::SL - 1) / C::SL : 0;
   const int n_it = n_heads * n_q;
   // stored dS: this key tile's place in the block numbering of its row
   const int ds_rowb = u0 / p.S, ds_row0 = ds_rowb * p.S, ds_kt = (u0 - ds_row0) / kBN;
@@ -406,7 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem;
   volatile int* abort = &bars->abort;
   const uint32_t sbase = smem_u32(smem);
-  constexpr uint32_t T_S = 0, T_DP = 64, T_DV = 128, T_DK = 128 + D, T_K = 128 + 2 * D, T_V = T_K + D / 2;
+  // TMEM: S^T [0,SL) dP^T [SL,2SL) dV, dK (D each) K, V (D/2 packed each): 512 columns at D=128, 448 at D=64
+  constexpr uint32_t T_S = 0, T_DP = C::SL, T_DV = 2 * C::SL, T_DK = T_DV + D, T_K = T_DK + D, T_V = T_K + D / 2;
+  static_assert(T_V + D / 2 <= 512, "TMEM columns");
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
@@ -420,11 +425,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i >= C::NST && !mbar_wait(&bars->qdo_empty[s], ((i / C::NST) - 1) & 1, abort, p.status)) break;
         const int hg = hg0 + i / n_q;
         const HeadRef qh{hg / p.hq, hg % p.hq, hg};
-        const int q0 = qlo + (i % n_q) * kSL;
+        const int q0 = qlo + (i % n_q) * C::SL;
         mbar_arrive_expect_tx(&bars->qdo_full[s], 2 * C::SLICE + C::STAT);
         for (int c = 0; c < C::NCH; ++c) {
-          tma_load_rows(smem + C::A_Q + s * C::SLICE + c * kSliceBytes, &tq, &bars->qdo_full[s], p, c, qh, q0);
-          tma_load_rows(smem + C::A_DO + s * C::SLICE + c * kSliceBytes, &tdo, &bars->qdo_full[s], p, c, qh, q0);
+          tma_load_rows(smem + C::A_Q + s * C::SLICE + c * C::SLB, &tq, &bars->qdo_full[s], p, c, qh, q0);
+          tma_load_rows(smem + C::A_DO + s * C::SLICE + c * C::SLB, &tdo, &bars->qdo_full[s], p, c, qh, q0);
         }
         tma_load_3d(smem + C::A_STAT + s * C::STAT, &tst, &bars->qdo_full[s], q0, 0, hg);
         issued = i + 1;
@@ -435,8 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(kBN, kSL, false, false);  // [128 keys x 64 queries], K = D
-      constexpr uint32_t id_g = idesc_bf16(kBN, D, false, true);      // [128 keys x D], K = 64 queries
+      constexpr uint32_t id_s = idesc_bf16(kBN, C::SL, false, false);  // [128 keys x SL queries], K = D
+      constexpr uint32_t id_g = idesc_bf16(kBN, D, false, true);       // [128 keys x D], K = SL queries
       // S^T_i = K Q_i^T.  Slot i has landed: the compute warps wait for it
       // before handing in P of iteration i-1 (each barrier wait of this
       // thread stalls the tensor core, so it keeps only the hand-offs).
@@ -445,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t qa = sbase + C::A_Q + s * C::SLICE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts(tmem + T_S, tmem + T_K + kk * 8, kmajor_desc(qa, kSliceBytes, kk), id_s, kk > 0);
+          mma_ts(tmem + T_S, tmem + T_K + kk * 8, kmajor_desc(qa, C::SLB, kk), id_s, kk > 0);
         mma_commit(&bars->st_full);
         return true;
       };
@@ -453,11 +458,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t da = sbase + C::A_DO + (i % C::NST) * C::SLICE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts(tmem + T_DP, tmem + T_V + kk * 8, kmajor_desc(da, kSliceBytes, kk), id_s, kk > 0);
+          mma_ts(tmem + T_DP, tmem + T_V + kk * 8, kmajor_desc(da, C::SLB, kk), id_s, kk > 0);
         mma_commit(&bars->dpt_full);
       };
-      // A operand columns of a packed 64-query slice: the two halves sit at +0 and +32
-      auto acol = [](int kk) -> uint32_t { return kk < 2 ? kk * 8 : 32 + (kk - 2) * 8; };
+      // A operand columns of a packed slice: compute group g packs its SL/2
+      // queries into the SL/4 columns at g*SL/2 (K step kk: 16 queries, 8 columns)
+      auto acol = [](int kk) -> uint32_t {
+        constexpr int per = C::SL / 32;  // K steps per group
+        return static_cast<uint32_t>((kk / per) * (C::SL / 2) + (kk % per) * 8);
+      };
       bool ok = mbar_wait(&bars->kv_ready, 0, abort, p.status);
       if (ok && n_it > 0 && (ok = mbar_wait(&bars->qdo_full[0], 0, abort, p.status))) {
         tc_fence_after();
@@ -472,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(&bars->p_full, ph, abort, p.status))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kSL / 16; ++kk)
-          mma_ts(tmem + T_DV, tmem + T_S + acol(kk), mnmajor_desc(da, kSliceBytes, kk), id_g,
+        for (int kk = 0; kk < C::SL / 16; ++kk)
+          mma_ts(tmem + T_DV, tmem + T_S + acol(kk), mnmajor_desc(da, C::SLB, kk), id_g,
                  (i > 0 || kk > 0) ? 1u : 0u);
         const bool more = i + 1 < n_it;
         if (more && !(ok = issue_st(i + 1))) break;  // S^T region is free once dV has read P^T
@@ -481,8 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(&bars->ds_full, ph, abort, p.status))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kSL / 16; ++kk)
-          mma_ts(tmem + T_DK, tmem + T_DP + acol(kk), mnmajor_desc(qa, kSliceBytes, kk), id_g,
+        for (int kk = 0; kk < C::SL / 16; ++kk)
+          mma_ts(tmem + T_DK, tmem + T_DP + acol(kk), mnmajor_desc(qa, C::SLB, kk), id_g,
                  (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->qdo_empty[s]);
         if (more)
@@ -495,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ compute
-    const int grp = warp >> 2;                      // query columns [32*grp, 32*grp + 32) of each slice
+    const int grp = warp >> 2;                      // query columns [grp*SL/2, (grp+1)*SL/2) of each slice
     const int krow = (warp & 3) * 32 + lane;        // TMEM lane = key row
     const int u = u0 + krow;
     const bool key_ok = u < p.BS;
@@ -514,79 +523,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->kv_ready);
     }
+    // The group's SL/2 query columns of a slice, in 32-column chunks.  Packed
+    // P^T (dS^T) of chunk c goes to the group's columns gc + 16c, over fp32
+    // columns the group has already read.
+    constexpr int NCK = C::SL / 64;
+    const int gc = grp * (C::SL / 2);
     bool ok = n_it == 0 || mbar_wait(&bars->qdo_full[0], 0, abort, p.status);
     int ds_slot = 0;  // dS blocks this warp has staged
     for (int i = 0; i < n_it && ok; ++i) {
       const int s = i % C::NST;
       const uint32_t ph = i & 1;
-      const int q0 = qlo + (i % n_q) * kSL + grp * 32;  // first query column of this group
+      const int q0 = qlo + (i % n_q) * C::SL + gc;  // first query column of this group
       // the next slot lands before P of this iteration is handed in: the MMA
       // thread issues S^T of the next iteration on that hand-off alone
       if (i + 1 < n_it &&
           !(ok = mbar_wait(&bars->qdo_full[(i + 1) % C::NST], ((i + 1) / C::NST) & 1, abort, p.status)))
         break;
-      const float* st = reinterpret_cast<const float*>(smem + C::A_STAT + s * C::STAT) + grp * 32;
+      const float* st = reinterpret_cast<const float*>(smem + C::A_STAT + s * C::STAT) + gc;
       if (!(ok = mbar_wait(&bars->st_full, ph, abort, p.status))) break;
       tc_fence_after();
-      float x[32];
-      tmem_ld_cols<32>(lb + T_S + grp * 32, x);
-      // only slices that straddle a document, diagonal or window edge pay for
-      // the per-element mask (hidden scores become -inf, so exp2 gives 0)
-      const int c_lo = vlo - q0, c_hi = vhi - q0;
-      if (!(c_lo <= 0 && c_hi >= 31)) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (c < c_lo || c > c_hi) x[c] = -INFINITY;
-      }
-      float pr[32];
       const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+      float pr[NCK][32];
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(st + 4 * c4);  // -LSE*log2(e)
-        const float2 e0 = f2_unpack(f2_fma(f2_pack(x[4 * c4], x[4 * c4 + 1]), sc2, f2_pack(l4.x, l4.y)));
-        const float2 e1 = f2_unpack(f2_fma(f2_pack(x[4 * c4 + 2], x[4 * c4 + 3]), sc2, f2_pack(l4.z, l4.w)));
-        pr[4 * c4] = ex2(e0.x);
-        pr[4 * c4 + 1] = ex2(e0.y);
-        pr[4 * c4 + 2] = ex2(e1.x);
-        pr[4 * c4 + 3] = ex2(e1.y);
+      for (int c = 0; c < NCK; ++c) {
+        float x[32];
+        tmem_ld_cols<32>(lb + T_S + gc + 32 * c, x);
+        // only chunks that straddle a document, diagonal or window edge pay
+        // for the per-element mask (hidden scores become -inf, so exp2 gives 0)
+        const int c_lo = vlo - (q0 + 32 * c), c_hi = vhi - (q0 + 32 * c);
+        if (!(c_lo <= 0 && c_hi >= 31)) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (e < c_lo || e > c_hi) x[e] = -INFINITY;
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(st + 32 * c + 4 * c4);  // -LSE*log2(e)
+          const float2 e0 = f2_unpack(f2_fma(f2_pack(x[4 * c4], x[4 * c4 + 1]), sc2, f2_pack(l4.x, l4.y)));
+          const float2 e1 = f2_unpack(f2_fma(f2_pack(x[4 * c4 + 2], x[4 * c4 + 3]), sc2, f2_pack(l4.z, l4.w)));
+          pr[c][4 * c4] = ex2(e0.x);
+          pr[c][4 * c4 + 1] = ex2(e0.y);
+          pr[c][4 * c4 + 2] = ex2(e1.x);
+          pr[c][4 * c4 + 3] = ex2(e1.y);
+        }
+        tmem_st_packed<16>(lb + T_S + gc + 16 * c, pr[c]);
       }
-      tmem_st_packed<16>(lb + T_S + grp * 32, pr);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->p_full);
       if (!(ok = mbar_wait(&bars->dpt_full, ph, abort, p.status))) break;
       tc_fence_after();
-      tmem_ld_cols<32>(lb + T_DP + grp * 32, x);
-#pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 d4 = *reinterpret_cast<const float4*>(st + kSL + 4 * c4);
-        const float2 g0 = f2_unpack(f2_mul(f2_pack(pr[4 * c4], pr[4 * c4 + 1]),
-                                           f2_sub(f2_pack(x[4 * c4], x[4 * c4 + 1]), f2_pack(d4.x, d4.y))));
-        const float2 g1 = f2_unpack(f2_mul(f2_pack(pr[4 * c4 + 2], pr[4 * c4 + 3]),
-                                           f2_sub(f2_pack(x[4 * c4 + 2], x[4 * c4 + 3]), f2_pack(d4.z, d4.w))));
-        x[4 * c4] = g0.x;
-        x[4 * c4 + 1] = g0.y;
-        x[4 * c4 + 2] = g1.x;
-        x[4 * c4 + 3] = g1.y;
-      }
       // dS^T packed once: into TMEM for the dK MMA (first: the MMA thread
-      // waits on it), then, if dS is stored, into the staging buffer
-      uint32_t pk[16];
+      // waits on it), then, if dS is stored, into the staging buffers
+      uint32_t pk[NCK][16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
-      tmem_st16(lb + T_DP + grp * 32, pk);
+      for (int c = 0; c < NCK; ++c) {
+        float x[32];
+        tmem_ld_cols<32>(lb + T_DP + gc + 32 * c, x);
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(st + C::SL + 32 * c + 4 * c4);
+          const float2 g0 = f2_unpack(f2_mul(f2_pack(pr[c][4 * c4], pr[c][4 * c4 + 1]),
+                                             f2_sub(f2_pack(x[4 * c4], x[4 * c4 + 1]), f2_pack(d4.x, d4.y))));
+          const float2 g1 = f2_unpack(f2_mul(f2_pack(pr[c][4 * c4 + 2], pr[c][4 * c4 + 3]),
+                                             f2_sub(f2_pack(x[4 * c4 + 2], x[4 * c4 + 3]), f2_pack(d4.z, d4.w))));
+          x[4 * c4] = g0.x;
+          x[4 * c4 + 1] = g0.y;
+          x[4 * c4 + 2] = g1.x;
+          x[4 * c4 + 3] = g1.y;
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[c][e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+        tmem_st16(lb + T_DP + gc + 16 * c, pk[c]);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->ds_full);
       if (store_ds) {
-        // The warp's [32 key rows][32 query columns] part of dS^T block (head,
-        // row, kt, qs): staged in shared memory in the 64-byte swizzle (16-byte
-        // chunk e of row r at r*64 + (e ^ (r>>1 & 3))*16: every store instruction
-        // is conflict-free) and written by one TMA store of the warp.
+        // The warp's [32 key rows][32 query columns] parts of the dS^T blocks
+        // (head, row, kt, qs) of 64 queries: staged in shared memory in the
+        // 64-byte swizzle (16-byte chunk e of row r at r*64 + (e ^ (r>>1 & 3))*16:
+        // every store instruction is conflict-free), each written by one TMA
+        // store of the warp.
         const int hg = hg0 + i / n_q;
-        const int qs = (qlo - ds_row0) / kSL + i % n_q;
-        const int rel = qs - 2 * ds_kt;
-        if (rel >= 0 && rel < ds_cnt) {
+#pragma unroll
+        for (int c = 0; c < NCK; ++c) {
+          const int qcol = gc + 32 * c;  // column of this chunk in the slice
+          const int qs = (qlo - ds_row0) / kSL + (i % n_q) * (C::SL / kSL) + qcol / kSL;
+          const int rel = qs - 2 * ds_kt;
+          if (rel < 0 || rel >= ds_cnt) continue;
           const long long blk = (static_cast<long long>(hg - p.hq0) * p.B + ds_rowb) * g.dsg.per_row + ds_off0 + rel;
           uint8_t* buf = smem + C::A_DS + (warp * 2 + (ds_slot & 1)) * 2048;
           if (ds_slot >= 2 && lane == 0) bulk_wait_group_read<1>();  // its store from two rounds ago has read it
@@ -594,11 +619,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             *reinterpret_cast<uint4*>(buf + lane * 64 + ((e ^ ((lane >> 1) & 3)) << 4)) =
-                make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                make_uint4(pk[c][4 * e], pk[c][4 * e + 1], pk[c][4 * e + 2], pk[c][4 * e + 3]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d(&tds_st, buf, grp * 32, (warp & 3) * 32, static_cast<int>(blk));
+            tma_store_3d(&tds_st, buf, qcol % kSL, (warp & 3) * 32, static_cast<int>(blk));
             bulk_commit_group();
           }
           ++ds_slot;
@@ -1166,11 +1191,11 @@ static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const v
     return check_launch();
   }
   if (!dq_pass) {
-    // 64-query slices of Q, dO and their statistics stream past TMEM-resident K, V
+    // query slices of Q, dO and their statistics stream past TMEM-resident K, V
     CUtensorMap tq, tdo, tst;
-    if ((rc = make_rows_tmap(&tq, q, a, a.hq, a.Hq, D, bwd::kSL)) != USP_OK) return rc;
-    if ((rc = make_rows_tmap(&tdo, dO, a, a.hq, a.Hq, D, bwd::kSL)) != USP_OK) return rc;
-    if ((rc = make_stats_tmap(&tst, stats, a.BS, g.bsp, a.P * a.hq, bwd::kSL)) != USP_OK) return rc;
+    if ((rc = make_rows_tmap(&tq, q, a, a.hq, a.Hq, D, C::SL)) != USP_OK) return rc;
+    if ((rc = make_rows_tmap(&tdo, dO, a, a.hq, a.Hq, D, C::SL)) != USP_OK) return rc;
+    if ((rc = make_stats_tmap(&tst, stats, a.BS, g.bsp, a.P * a.hq, C::SL)) != USP_OK) return rc;
     CUtensorMap tds_st;
     memset(&tds_st, 0, sizeof(tds_st));  // unused unless dS is stored
     if (ds != nullptr && (rc = make_ds_store_tmap(&tds_st, ds, ds_blocks)) != USP_OK) return rc;
