@@ -355,6 +355,31 @@ def oracle_sample(w: W.Workload, budget_s: float = 20.0):
                       f"fp64 numpy forward+backward, {dt:.2f} s"}
 
 
+def rank_sync(world: int, device):
+    """barrier() and max_over_ranks(x) over the job's ranks (no-ops for one
+    rank): every rank runs the whole emulated layer, the job's time is the
+    slowest rank's."""
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    return barrier, max_over_ranks
+
+
+def job_tflops(flop_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes its own copy of the step."""
+    return flop_per_rank_step * world / (ms_per_step * 1e-3) / 1e12
+
+
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -404,19 +429,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    barrier, max_over_ranks = rank_sync(world, device)
 
     from ulysses_sequence_long_gb300 import _build
     if rank == 0 or world == 1:
@@ -466,7 +479,7 @@ def main():
             t_dq.append(b)
         per_call["attn_bwd_dkdv"], per_call["attn_bwd_dq"] = statistics.mean(t_dkdv), statistics.mean(t_dq)
 
-    value = fl["total"] * world / (ms * 1e-3) / 1e12
+    value = job_tflops(fl["total"], world, ms)
     peaks = measured_peaks()
     attn_ms = per_call["attn_fwd"] + per_call["attn_bwd_pre"] + per_call["attn_bwd_dkdv"] + per_call["attn_bwd_dq"]
     if step.ua.fused:
@@ -523,7 +536,7 @@ def main():
         ems = run_e2e(slots, pin, outs, args.steps) / args.steps
         barrier()
         ems = max_over_ranks(ems)
-        line["e2e"] = {"value": fl["total"] * world / (ems * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ems,
+        line["e2e"] = {"value": job_tflops(fl["total"], world, ems), "unit": "TFLOP/s", "ms_per_step": ems,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(w)
