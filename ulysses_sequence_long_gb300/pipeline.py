@@ -22,6 +22,11 @@ head is replicated on P/Hkv ranks; the exchange back of dK/dV sums the
 replicas (explicit mode), or the dK/dV kernel sums the whole query group
 directly (fused mode).
 
+The backward stores dS for the dQ pass when the workspace fits in half the
+free memory; for long sequences whose whole dS does not, the dK/dV and dQ
+passes run one group of key/value heads at a time over one workspace
+(``plan_backward``).
+
 torch only allocates the buffers and supplies the stream; every step runs in
 the library's kernels.
 """
