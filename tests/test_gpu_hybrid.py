@@ -24,10 +24,11 @@ def _bits(t):
     return t.contiguous().view(torch.int16).cpu().numpy()
 
 
-def _run(w, backward=True, stored_ds=None, fused=None):
+def _run(w, backward=True, stored_ds=None, fused=None, ds_group_size=None):
     from ulysses_sequence_long_gb300.pipeline import HybridAttention
     dev, host = device_inputs(w)
-    ha = HybridAttention(shape_of(w), w.ring, with_backward=backward, stored_ds=stored_ds, fused=fused)
+    ha = HybridAttention(shape_of(w), w.ring, with_backward=backward, stored_ds=stored_ds, fused=fused,
+                         ds_group_size=ds_group_size)
     ha.forward(dev["q"], dev["k"], dev["v"], dev["pos"], dev["sinks"])
     if backward:
         ha.backward(dev["do"], dev["sinks"])
@@ -88,6 +89,19 @@ CASES = [(w, f, d) for w in SMALL for f in ([True, False] if _can_fuse(w) else [
 def test_hybrid_full_parity_small(w, fused, stored_ds):
     ha, dev, host = _run(w, stored_ds=stored_ds, fused=fused)
     assert ha.stored_ds == stored_ds and ha.fused == fused
+    _check_parity(ha, w, host)
+
+
+@pytest.mark.parametrize("w", [SMALL[0], SMALL[3]], ids=lambda w: w.name)
+def test_hybrid_stored_ds_in_head_groups(w):
+    """Every ring step's dK/dV and dQ passes run one key/value head at a
+    time over one stored-dS workspace: same gradients as the oracle."""
+    ha, dev, host = _run(w, fused=True, ds_group_size=1)
+    assert ha.stored_ds and len(ha.ds_groups) == w.Hkv
+    _check_parity(ha, w, host)
+
+
+def _check_parity(ha, w, host):
     snk = host["sinks"]
     kw = dict(causal=w.causal, window_left=w.window_left, sinks=snk)
     f = oracle.hybrid_fwd(host["q"], host["k"], host["v"], host["pos"], w.ring, **kw)
