@@ -123,6 +123,50 @@ int usp_relayout_fwd_qkv(const void* q_seq, const void* k_seq, const void* v_seq
                          usp_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * One real rank's side of the exchanges, for P processes (one per GPU) that
+ * run the all-to-all themselves (NCCL all_to_all_single, or any transport
+ * that sends chunk p of a buffer to rank p and lays the received chunks out
+ * in source-rank order).  accelerate PR #4209, the comment on the four
+ * _SeqAllToAll.apply call sites: each rank sends every other rank that rank's
+ * heads of its own sequence chunk and receives its own heads of every chunk;
+ * the way back swaps scatter and gather.
+ *
+ * Shapes (Sl = S/P positions per rank, hpr = H/P heads per rank, or 1 with
+ * H < P where each head is replicated on P/H ranks, rank p holding head
+ * p / (P/H)):
+ *   x_local [B][Sl][H][D]     the rank's sequence chunk, all heads
+ *   x_head  [B][P*Sl][hpr][D] the whole sequence, the rank's heads (what
+ *                             usp_attn_fwd/_bwd take with P = 1 and Hq/Hkv set
+ *                             to the rank's head counts)
+ *   send, recv [P][B][Sl][hpr][D]  chunk p goes to / came from rank p
+ *
+ *   usp_a2a_pack_seq_to_head:   send[p][b][s][j][d] = x_local[b][s][p*hpr + j][d]
+ *                               (H < P: x_local[b][s][p / (P/H)][d])
+ *   usp_a2a_unpack_seq_to_head: x_head[b][p*Sl + s][j][d] = recv[p][b][s][j][d]
+ *   usp_a2a_pack_head_to_seq:   send[p][b][s][j][d] = x_head[b][p*Sl + s][j][d]
+ *   usp_a2a_unpack_head_to_seq: x_local[b][s][p*hpr + j][d] = recv[p][b][s][j][d]
+ *                               (H < P: x_local[b][s][h][d] = sum over the P/H ranks p
+ *                               with p / (P/H) == h of recv[p][b][s][0][d], in fp32 in
+ *                               rank order, rounded once; bf16 only)
+ * With B == 1 the unpack after the seq->head exchange and the pack before the
+ * head->seq exchange are plain copies (recv already is x_head, x_head already
+ * is send), and a caller may skip them.  H is always the global head count.
+ * Apart from the replica sum every result is a bit-exact copy.  Buffers must
+ * not overlap; pointers and each contiguous run of hpr*D*elem_bytes bytes must
+ * be 16-byte aligned.
+ * Errors: USP_ERR_INVALID_ARG, USP_ERR_INDIVISIBLE (H and P), USP_ERR_ALIGNMENT,
+ * USP_ERR_UNSUPPORTED, USP_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+int usp_a2a_pack_seq_to_head(const void* x_local, void* send, int B, int S_local, int H, int D, int P,
+                             int elem_bytes, usp_stream_t stream);
+int usp_a2a_unpack_seq_to_head(const void* recv, void* x_head, int B, int S_local, int H, int D, int P,
+                               int elem_bytes, usp_stream_t stream);
+int usp_a2a_pack_head_to_seq(const void* x_head, void* send, int B, int S_local, int H, int D, int P,
+                             int elem_bytes, usp_stream_t stream);
+int usp_a2a_unpack_head_to_seq(const void* recv, void* x_local, int B, int S_local, int H, int D, int P,
+                               int elem_bytes, usp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Document boundaries from the gathered position_ids.  accelerate PR #4209:
  * position_ids are all-gathered once per forward in the model's pre-hook and
  * every layer reads them; the per-shard cu_seq_lens_q/k and max_length_q/k a
@@ -158,8 +202,9 @@ int usp_cu_seqlens_from_position_ids(const int32_t* pos, int B, int S, int P,
  * library, which every GPU that loads the library holds until the process
  * exits.  The pages have no counterpart of this call.
  *   - B*S may be at most 2^24 tokens; larger sizes return USP_ERR_UNSUPPORTED.
- *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     (the first lookup on a device may load the library's device code
+ *     there); make the first call on a device before any stream capture.
  *   - Every call shares the one array: calls whose kernels may overlap on the
  *     GPU (other streams, other host threads) race and must be ordered by the
  *     caller.  Leftover contents from an earlier call never matter.

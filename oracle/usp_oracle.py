@@ -72,6 +72,8 @@ __all__ = [
     "visible_pairs",
     "hybrid_relayout_fwd", "hybrid_relayout_bwd", "ring_block_fwd", "ring_merge",
     "hybrid_fwd", "hybrid_bwd",
+    "a2a_pack_seq_to_head", "a2a_unpack_seq_to_head", "a2a_pack_head_to_seq", "a2a_unpack_head_to_seq",
+    "all_to_all",
 ]
 
 
@@ -161,6 +163,70 @@ def relayout_bwd(x_head: np.ndarray, P: int, heads: Optional[int] = None) -> np.
     y = x_head.reshape(P, B, P, Sl, Hp, D)      # [r][b][r'][s'][j][d]
     y = y.transpose(2, 1, 3, 0, 4, 5)           # [r'][b][s'][r][j][d]
     return np.ascontiguousarray(y).reshape(P, B, Sl, P * Hp, D)
+
+
+# ---------------------------------------------------------------------------
+# one real rank's side of the same exchanges: what it sends to every other
+# rank and how it lays out what it receives (the all-to-all of the comment on
+# the four _SeqAllToAll.apply call sites, seen from rank r)
+# ---------------------------------------------------------------------------
+
+def a2a_pack_seq_to_head(x_local: np.ndarray, P: int, replicate: bool = False) -> np.ndarray:
+    """Rank r's send buffer of the seq->head exchange: chunk p holds rank p's
+    heads of r's sequence chunk.  ``x_local`` is ``[B][Sl][H][D]``; the result
+    is ``[P][B][Sl][H/P][D]`` with ``send[p][b][s][j][d] = x_local[b][s][p*H/P + j][d]``,
+    or, with ``replicate`` and H < P, ``send[p][b][s][0][d] = x_local[b][s][p // (P/H)][d]``."""
+    B, Sl, H, D = x_local.shape
+    _check_divisible(Sl * P, H, P, replicate)
+    if H < P:
+        owner = np.arange(P) // (P // H)
+        y = x_local[:, :, owner, :]                  # [b][s][p][d]
+        return np.ascontiguousarray(y.transpose(2, 0, 1, 3)).reshape(P, B, Sl, 1, D)
+    y = x_local.reshape(B, Sl, P, H // P, D)         # [b][s][p][j][d]
+    return np.ascontiguousarray(y.transpose(2, 0, 1, 3, 4))
+
+
+def a2a_unpack_seq_to_head(recv: np.ndarray) -> np.ndarray:
+    """The received chunks ``[P][B][Sl][hpr][D]`` (chunk p = rank p's positions)
+    as the whole sequence of the rank's heads, ``[B][P*Sl][hpr][D]``:
+    ``x_head[b][p*Sl + s] = recv[p][b][s]``."""
+    P, B, Sl, hpr, D = recv.shape
+    return np.ascontiguousarray(recv.transpose(1, 0, 2, 3, 4)).reshape(B, P * Sl, hpr, D)
+
+
+def a2a_pack_head_to_seq(x_head: np.ndarray, P: int) -> np.ndarray:
+    """Rank r's send buffer of the head->seq exchange: chunk p holds rank p's
+    positions of r's heads, ``send[p][b][s] = x_head[b][p*Sl + s]``."""
+    B, S, hpr, D = x_head.shape
+    if S % P != 0:
+        raise OracleError(f"sp size {P} does not divide sequence length {S}")
+    y = x_head.reshape(B, P, S // P, hpr, D)
+    return np.ascontiguousarray(y.transpose(1, 0, 2, 3, 4))
+
+
+def a2a_unpack_head_to_seq(recv: np.ndarray, heads: Optional[int] = None) -> np.ndarray:
+    """The received chunks ``[P][B][Sl][hpr][D]`` (chunk p = rank p's heads) as
+    the rank's sequence chunk with all heads ``[B][Sl][H][D]``:
+    ``x_local[b][s][p*hpr + j] = recv[p][b][s][j]``.  With ``heads`` = H < P
+    (replicated heads) the replicas' values are summed, the adjoint of the
+    replication: ``x_local[b][s][h] = sum over p with p // (P/H) == h of recv[p][b][s][0]``."""
+    P, B, Sl, hpr, D = recv.shape
+    H = hpr * P if heads is None else heads
+    if H < P:
+        if hpr != 1 or P % H != 0:
+            raise OracleError("replicated heads hold one head per rank")
+        y = recv.reshape(H, P // H, B, Sl, D).sum(axis=1)     # [h][b][s][d]
+        return np.ascontiguousarray(y.transpose(1, 2, 0, 3))
+    if H != hpr * P:
+        raise OracleError("head count does not match the received chunks")
+    return np.ascontiguousarray(recv.transpose(1, 2, 0, 3, 4)).reshape(B, Sl, H, D)
+
+
+def all_to_all(sends):
+    """The collective itself for P ranks at once: rank r receives chunk r of
+    every rank's send buffer, in source-rank order (``recv_r[p] = send_p[r]``)."""
+    P = len(sends)
+    return [np.stack([sends[p][r] for p in range(P)]) for r in range(P)]
 
 
 # ---------------------------------------------------------------------------

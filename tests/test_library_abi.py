@@ -49,6 +49,14 @@ def test_host_checks_without_gpu(lib):
     assert lib.usp_relayout_fwd(p, ctypes.c_void_p(1 << 20), 1, 8, 2, 3, 2, 2, None) == B.USP_ERR_ALIGNMENT
     assert lib.usp_relayout_fwd(p, ctypes.c_void_p(32), 1, 8, 2, 8, 2, 2, None) == B.USP_ERR_INVALID_ARG  # overlap
     assert lib.usp_cu_seqlens_workspace_bytes(1, 4096) >= 16
+    # one real rank's exchange buffers: the same refusals as the emulated exchange
+    q = ctypes.c_void_p(1 << 20)
+    assert lib.usp_a2a_pack_seq_to_head(None, q, 1, 8, 4, 8, 2, 2, None) == B.USP_ERR_INVALID_ARG
+    assert lib.usp_a2a_pack_seq_to_head(p, q, 1, 8, 6, 8, 4, 2, None) == B.USP_ERR_INDIVISIBLE
+    assert lib.usp_a2a_unpack_seq_to_head(p, q, 1, 8, 6, 8, 4, 2, None) == B.USP_ERR_INDIVISIBLE
+    assert lib.usp_a2a_pack_head_to_seq(p, q, 1, 8, 3, 8, 2, 2, None) == B.USP_ERR_INDIVISIBLE
+    assert lib.usp_a2a_unpack_head_to_seq(p, q, 1, 8, 2, 3, 2, 2, None) == B.USP_ERR_ALIGNMENT
+    assert lib.usp_a2a_unpack_head_to_seq(p, q, 1, 8, 2, 8, 4, 4, None) == B.USP_ERR_UNSUPPORTED  # fp32 replica sum
     prm = B.AttnParams(1, 256, 4, 2, 96, 2, 1, -1, 0.0, 16, 16, None)
     assert lib.usp_attn_fwd(ctypes.byref(prm), p, p, p, p, p, None, None) == B.USP_ERR_UNSUPPORTED
     prm = B.AttnParams(1, 256, 4, 2, 64, 8, 1, -1, 0.0, 16, 16, None)   # 8 ranks, 4 query heads

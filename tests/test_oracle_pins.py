@@ -127,6 +127,75 @@ def test_relayout_replicated_bwd_is_the_adjoint_of_fwd(P, H):
 
 
 # ---------------------------------------------------------------------------
+# one real rank's side of the exchanges (send buffers, received chunks)
+# ---------------------------------------------------------------------------
+
+def _ranks_seq_to_head(x, P, replicate=False):
+    """Every rank packs its shard, the collective delivers, every rank unpacks."""
+    sends = [oracle.a2a_pack_seq_to_head(x[r], P, replicate) for r in range(P)]
+    return [oracle.a2a_unpack_seq_to_head(rv) for rv in oracle.all_to_all(sends)]
+
+
+@pytest.mark.parametrize("P,B,S,H,D", [(2, 1, 8, 4, 3), (4, 2, 8, 8, 2), (1, 1, 4, 3, 2), (3, 2, 6, 6, 1)])
+def test_rank_exchange_seq_to_head_gives_whole_sequence_of_own_heads(P, B, S, H, D):
+    x = _encoded_seq_tensor(P, B, S, H, D)
+    Sl, Hp = S // P, H // P
+    for r in range(P):
+        send = oracle.a2a_pack_seq_to_head(x[r], P)
+        assert send.shape == (P, B, Sl, Hp, D)
+        # chunk p of rank r's send buffer: rank p's heads of r's positions
+        for p in range(P):
+            for b in range(B):
+                for s in range(Sl):
+                    for j in range(Hp):
+                        assert _decode(int(send[p, b, s, j, 0]), S, H, D) == (b, r * Sl + s, p * Hp + j, 0)
+    heads = _ranks_seq_to_head(x, P)
+    for r in range(P):
+        assert heads[r].shape == (B, S, Hp, D)
+        for b in range(B):
+            for pos in range(S):
+                for j in range(Hp):
+                    for d in range(D):
+                        assert _decode(int(heads[r][b, pos, j, d]), S, H, D) == (b, pos, r * Hp + j, d)
+        # the same as the emulated exchange's rank r
+        assert np.array_equal(heads[r], oracle.relayout_fwd(x, P)[r])
+
+
+@pytest.mark.parametrize("P,B,S,H,D", [(4, 1, 8, 2, 3), (4, 2, 8, 1, 2), (8, 1, 16, 2, 1)])
+def test_rank_exchange_replicated_heads(P, B, S, H, D):
+    x = _encoded_seq_tensor(P, B, S, H, D)
+    heads = _ranks_seq_to_head(x, P, replicate=True)
+    rep = P // H
+    for r in range(P):
+        for b in range(B):
+            for pos in range(S):
+                assert _decode(int(heads[r][b, pos, 0, 1 % D]), S, H, D) == (b, pos, r // rep, 1 % D)
+        assert np.array_equal(heads[r], oracle.relayout_fwd(x, P, replicate=True)[r])
+    # the way back sums the replicas: the adjoint of the replicating exchange
+    y = _rng(24).standard_normal((P, B, S, 1, D))
+    sends = [oracle.a2a_pack_head_to_seq(y[r], P) for r in range(P)]
+    back = [oracle.a2a_unpack_head_to_seq(rv, H) for rv in oracle.all_to_all(sends)]
+    xs = _rng(25).standard_normal((P, B, S // P, H, D))
+    lhs = float(np.sum(oracle.relayout_fwd(xs, P, replicate=True) * y))
+    rhs = float(sum(np.sum(xs[r] * back[r]) for r in range(P)))
+    assert abs(lhs - rhs) <= 1e-12 * max(1.0, abs(lhs))
+
+
+@pytest.mark.parametrize("P,B,S,H,D", [(2, 1, 8, 4, 3), (4, 2, 8, 8, 2), (3, 1, 6, 6, 2)])
+def test_rank_exchange_head_to_seq_inverts_seq_to_head(P, B, S, H, D):
+    x = _encoded_seq_tensor(P, B, S, H, D)
+    heads = _ranks_seq_to_head(x, P)
+    sends = [oracle.a2a_pack_head_to_seq(heads[r], P) for r in range(P)]
+    for r in range(P):
+        # chunk p of rank r's send buffer: rank p's positions of r's heads
+        for p in range(P):
+            assert _decode(int(sends[r][p, 0, 0, 0, 0]), S, H, D) == (0, p * (S // P), r * (H // P), 0)
+    back = [oracle.a2a_unpack_head_to_seq(rv) for rv in oracle.all_to_all(sends)]
+    for r in range(P):
+        assert np.array_equal(back[r], x[r])
+
+
+# ---------------------------------------------------------------------------
 # cu_seqlens
 # ---------------------------------------------------------------------------
 

@@ -37,6 +37,8 @@ EXPORTED = [
     "usp_attn_bwd_preprocess", "usp_attn_bwd_dkdv", "usp_attn_bwd_dq",
     "usp_hybrid_relayout_fwd", "usp_hybrid_relayout_bwd", "usp_hybrid_relayout_fwd_qkv",
     "usp_ring_fwd_merge", "usp_ring_grad_accumulate", "usp_attn_bwd_fast_workspace_bytes",
+    "usp_a2a_pack_seq_to_head", "usp_a2a_unpack_seq_to_head", "usp_a2a_pack_head_to_seq",
+    "usp_a2a_unpack_head_to_seq",
 ]
 
 USP_RING_FIRST = 1
@@ -103,12 +105,16 @@ def load() -> ctypes.CDLL:
     L.usp_hybrid_relayout_fwd_qkv.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp]
     L.usp_ring_fwd_merge.argtypes = [ctypes.POINTER(AttnParams), vp, vp, vp, vp, vp, vp, i32, vp]
     L.usp_ring_grad_accumulate.argtypes = [vp, vp, vp, sz, i32, vp]
+    for name in ("usp_a2a_pack_seq_to_head", "usp_a2a_unpack_seq_to_head", "usp_a2a_pack_head_to_seq",
+                 "usp_a2a_unpack_head_to_seq"):
+        getattr(L, name).argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp]
     for name in ("usp_relayout_fwd", "usp_relayout_bwd", "usp_relayout_fwd_qkv",
                  "usp_cu_seqlens_from_position_ids", "usp_cu_seqlens_from_position_ids_noalloc",
                  "usp_attn_fwd", "usp_attn_bwd",
                  "usp_attn_bwd_preprocess", "usp_attn_bwd_dkdv", "usp_attn_bwd_dq",
                  "usp_hybrid_relayout_fwd", "usp_hybrid_relayout_bwd", "usp_hybrid_relayout_fwd_qkv",
-                 "usp_ring_fwd_merge", "usp_ring_grad_accumulate"):
+                 "usp_ring_fwd_merge", "usp_ring_grad_accumulate", "usp_a2a_pack_seq_to_head",
+                 "usp_a2a_unpack_seq_to_head", "usp_a2a_pack_head_to_seq", "usp_a2a_unpack_head_to_seq"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -272,3 +278,24 @@ def usp_ring_grad_accumulate(g_step, g_acc, g_out, flags, stream=None):
         _dev(g_step, "g_step", torch.bfloat16), _dev(g_acc, "g_acc", torch.float32),
         _dev(g_out, "g_out", torch.bfloat16), g_step.numel(), int(flags), _stream(stream)),
         "usp_ring_grad_accumulate")
+
+
+def _a2a(name, src, dst, B, S_local, H, D, P, stream):
+    _check(getattr(load(), name)(_dev(src, "src"), _dev(dst, "dst"), B, S_local, H, D, P, src.element_size(),
+                                 _stream(stream)), name)
+
+
+def usp_a2a_pack_seq_to_head(x_local, send, B, S_local, H, D, P, stream=None):
+    _a2a("usp_a2a_pack_seq_to_head", x_local, send, B, S_local, H, D, P, stream)
+
+
+def usp_a2a_unpack_seq_to_head(recv, x_head, B, S_local, H, D, P, stream=None):
+    _a2a("usp_a2a_unpack_seq_to_head", recv, x_head, B, S_local, H, D, P, stream)
+
+
+def usp_a2a_pack_head_to_seq(x_head, send, B, S_local, H, D, P, stream=None):
+    _a2a("usp_a2a_pack_head_to_seq", x_head, send, B, S_local, H, D, P, stream)
+
+
+def usp_a2a_unpack_head_to_seq(recv, x_local, B, S_local, H, D, P, stream=None):
+    _a2a("usp_a2a_unpack_head_to_seq", recv, x_local, B, S_local, H, D, P, stream)

@@ -283,6 +283,49 @@ int usp_hybrid_relayout_fwd_qkv(const void* q_seq, const void* k_seq, const void
   return relayout_qkv(q_seq, k_seq, v_seq, q_head, k_head, v_head, B, S, Hq, Hkv, D, ps, ulysses, eb, stream);
 }
 
+// ---- one real rank's side of the exchanges: send buffers for an all-to-all
+// between processes and the receive buffers back into the rank's layouts.
+// All four are the relayout kernel with one side of the permutation trivial:
+// Ps = 1 sequence shard and Ph = P head blocks (the rank's own shard split by
+// destination), or Ps = P shards (one per source rank) and Ph = 1 block.
+static int a2a_heads_per_rank(int H, int P) { return H >= P ? H / P : 1; }
+
+int usp_a2a_pack_seq_to_head(const void* x_local, void* send, int B, int S_local, int H, int D, int P, int eb,
+                             usp_stream_t stream) {
+  int rc = check_relayout_args(x_local, send, B, S_local, H, D, 1, P, eb, true);
+  if (rc != USP_OK) return rc;
+  return launch_relayout(x_local, send, B, S_local, H, D, 1, P, eb, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_a2a_unpack_seq_to_head(const void* recv, void* x_head, int B, int S_local, int H, int D, int P, int eb,
+                               usp_stream_t stream) {
+  if (H <= 0 || P <= 0 || S_local <= 0) return USP_ERR_INVALID_ARG;
+  if (H >= P ? H % P != 0 : P % H != 0) return USP_ERR_INDIVISIBLE;
+  if (static_cast<int64_t>(S_local) * P >= (1ll << 31)) return USP_ERR_UNSUPPORTED;
+  const int hpr = a2a_heads_per_rank(H, P), S = S_local * P;
+  int rc = check_relayout_args(recv, x_head, B, S, hpr, D, P, 1, eb, true);
+  if (rc != USP_OK) return rc;
+  return launch_relayout(recv, x_head, B, S, hpr, D, P, 1, eb, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_a2a_pack_head_to_seq(const void* x_head, void* send, int B, int S_local, int H, int D, int P, int eb,
+                             usp_stream_t stream) {
+  if (H <= 0 || P <= 0 || S_local <= 0) return USP_ERR_INVALID_ARG;
+  if (H >= P ? H % P != 0 : P % H != 0) return USP_ERR_INDIVISIBLE;
+  if (static_cast<int64_t>(S_local) * P >= (1ll << 31)) return USP_ERR_UNSUPPORTED;
+  const int hpr = a2a_heads_per_rank(H, P), S = S_local * P;
+  int rc = check_relayout_args(x_head, send, B, S, hpr, D, P, 1, eb, false);
+  if (rc != USP_OK) return rc;
+  return launch_relayout(x_head, send, B, S, hpr, D, P, 1, eb, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int usp_a2a_unpack_head_to_seq(const void* recv, void* x_local, int B, int S_local, int H, int D, int P, int eb,
+                               usp_stream_t stream) {
+  int rc = check_relayout_args(recv, x_local, B, S_local, H, D, 1, P, eb, false);
+  if (rc != USP_OK) return rc;
+  return launch_relayout(recv, x_local, B, S_local, H, D, 1, P, eb, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t usp_cu_seqlens_workspace_bytes(int B, int S) {
   if (B <= 0 || S <= 0) return 0;
   return cu_seqlens_ws_bytes(B, S);
