@@ -133,14 +133,20 @@ def test_relayout_refusals():
 
 # ------------------------------------------------------------------ cu_seqlens
 
-def _run_scan(pos_shards, B, S, P):
+def _run_scan(pos_shards, B, S, P, offset=0, ws=None):
+    """The scan on the device; `offset` int32 elements of padding in front of
+    the positions (offset 1: a buffer that is not 16-byte aligned)."""
     from ulysses_sequence_long_gb300 import binding as Bd
-    pos = torch.from_numpy(np.ascontiguousarray(pos_shards, dtype=np.int32)).cuda()
+    flat = torch.from_numpy(np.ascontiguousarray(pos_shards, dtype=np.int32).reshape(-1))
+    buf = torch.zeros((offset + flat.numel(),), dtype=torch.int32, device="cuda")
+    buf[offset:] = flat.cuda()
+    pos = buf[offset:]
     cu = torch.full((B * S + 1,), -7, dtype=torch.int32, device="cuda")
     n = torch.zeros(1, dtype=torch.int32, device="cuda")
     mx = torch.zeros(1, dtype=torch.int32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    ws = torch.empty((Bd.usp_cu_seqlens_workspace_bytes(B, S),), dtype=torch.uint8, device="cuda")
+    if ws is None:
+        ws = torch.empty((Bd.usp_cu_seqlens_workspace_bytes(B, S),), dtype=torch.uint8, device="cuda")
     Bd.usp_cu_seqlens_from_position_ids(pos, B, S, P, cu, n, mx, ws, st)
     torch.cuda.synchronize()
     nn = int(n.item())
@@ -158,13 +164,38 @@ def test_cu_seqlens_bit_exact(w):
 
 
 @pytest.mark.parametrize("B,S,P,mean", [(2, 4096, 4, 300), (1, 1 << 20, 8, 37), (3, 12288, 3, 5000),
-                                        (1, 4096 * 3 + 64, 2, 1), (2, 256, 1, 100000)])
+                                        (1, 4096 * 3 + 64, 2, 1), (2, 256, 1, 100000), (2, 4104, 3, 200),
+                                        (3, 1000, 5, 7), (1, 4096 * 40 + 24, 4, 4096 * 9)])
 def test_cu_seqlens_many_blocks_and_rows(B, S, P, mean):
     w = W.Workload("scan", B=B, S=S, Hq=P, Hkv=P, D=64, P=P, doc_mode="geometric", doc_mean=mean, seed=B + S)
     pos = W.position_ids_shards(w)
     cu, n, mx, st = _run_scan(pos, B, S, P)
     rcu, rn, rmx = oracle.cu_seqlens_from_position_ids(pos)
     assert st == 0 and n == rn and mx == rmx and np.array_equal(cu, rcu)
+
+
+@pytest.mark.parametrize("B,S,P,mean", [(1, 1 << 16, 4, 300), (2, 8192, 2, 50)])
+def test_cu_seqlens_unaligned_positions(B, S, P, mean):
+    # positions that do not start on a 16-byte boundary take the scalar loads
+    w = W.Workload("scan_unaligned", B=B, S=S, Hq=P, Hkv=P, D=64, P=P, doc_mode="geometric", doc_mean=mean, seed=3)
+    pos = W.position_ids_shards(w)
+    rcu, rn, rmx = oracle.cu_seqlens_from_position_ids(pos)
+    for offset in (1, 2, 3):
+        cu, n, mx, st = _run_scan(pos, B, S, P, offset=offset)
+        assert st == 0 and n == rn and mx == rmx and np.array_equal(cu, rcu)
+
+
+def test_cu_seqlens_workspace_reused_across_calls():
+    # the block states left by one call must never leak into the next
+    from ulysses_sequence_long_gb300 import binding as Bd
+    ws = torch.empty((Bd.usp_cu_seqlens_workspace_bytes(1, 1 << 20),), dtype=torch.uint8, device="cuda")
+    for seed, mean in ((1, 500), (2, 20000), (3, 3), (4, 1 << 21)):
+        w = W.Workload("scan_reuse", B=1, S=1 << 20, Hq=8, Hkv=8, D=64, P=8, doc_mode="geometric", doc_mean=mean,
+                       seed=seed)
+        pos = W.position_ids_shards(w)
+        cu, n, mx, st = _run_scan(pos, 1, 1 << 20, 8, ws=ws)
+        rcu, rn, rmx = oracle.cu_seqlens_from_position_ids(pos)
+        assert st == 0 and n == rn and mx == rmx and np.array_equal(cu, rcu)
 
 
 def test_cu_seqlens_flags_negative_positions():

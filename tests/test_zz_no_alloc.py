@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import usp_workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -44,9 +45,13 @@ def test_noalloc_matches_workspace_form_on_consecutive_calls():
     cases = [
         W.Workload("many_docs", B=1, S=1 << 20, Hq=8, Hkv=8, D=64, P=8, doc_mode="geometric", doc_mean=37, seed=9),
         W.Workload("two_rows", B=2, S=12288, Hq=4, Hkv=4, D=64, P=4, doc_mode="geometric", doc_mean=900, seed=2),
+        # the largest size the fixed array takes: B*S = 2^24 positions
+        W.Workload("at_the_limit", B=1, S=1 << 24, Hq=8, Hkv=8, D=64, P=8, doc_mode="geometric", doc_mean=5000,
+                   seed=4),
     ]
-    for w in cases:   # two calls in a row, the second over different data
-        pos = torch.from_numpy(W.position_ids_shards(w)).cuda()
+    for w in cases:   # calls in a row, each over different data
+        pos_np = W.position_ids_shards(w)
+        pos = torch.from_numpy(pos_np).cuda()
         a = _with_workspace(pos, w.B, w.S, w.P)
         b = _without_workspace(pos, w.B, w.S, w.P)
         torch.cuda.synchronize()
@@ -54,6 +59,10 @@ def test_noalloc_matches_workspace_form_on_consecutive_calls():
         assert int(b[1].item()) == n and int(b[2].item()) == int(a[2].item())
         assert int(a[3].item()) == 0 and int(b[3].item()) == 0
         assert np.array_equal(a[0][: n + 1].cpu().numpy(), b[0][: n + 1].cpu().numpy())
+        # and straight against the oracle's sequential scan
+        rcu, rn, rmx = oracle.cu_seqlens_from_position_ids(pos_np)
+        assert int(b[1].item()) == rn and int(b[2].item()) == rmx
+        assert np.array_equal(b[0][: rn + 1].cpu().numpy(), rcu)
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch():

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "usp_internal.h"
 #include "usp_ptx.cuh"
 
@@ -206,13 +208,52 @@ int launch_relayout_qkv(const void* const src[3], void* const dst[3], const int 
 //
 // Gathered index g = b*S + s (s = r*Sl + s') reads pos[r][b][s'].  A document
 // starts at g when s == 0 or the position there is 0.
+//
+// One pass over the positions (single-pass scan with decoupled look-back,
+// Merrill & Garland, "Single-pass Parallel Prefix Scan with Decoupled
+// Look-back", NVIDIA tech report NVR-2016-002): every block takes kScanChunk
+// positions in the order blocks start (a ticket, so that every block a block
+// looks back at is already running), counts its document starts and notes
+// its last one, publishes that aggregate, then looks back over its
+// predecessors' published states for the exclusive prefix (number of starts
+// before it, latest start before it), publishes its inclusive state and
+// scatters its starts into cu_seqlens.  A document's length is taken where it
+// ends: at the next start (in the same block or, for a block's first start,
+// after the latest start before the block), and after the last start by the
+// last block.  A small kernel before it resets the block states.
 constexpr int kScanThreads = 256;
-constexpr int kScanItems = 16;                      // consecutive items per thread
-constexpr int kScanChunk = kScanThreads * kScanItems;  // items per block
-constexpr int kBig = 0x7FFFFFFF;
+constexpr int kScanItems = kScanChunk / kScanThreads;  // 16 consecutive positions per thread
+static_assert(kScanItems == 16, "a thread's positions are four 16-byte vectors");
 
 struct ScanGeom {
-  int B, S, P, Sl, total;
+  int B, S, P, Sl, total, nblk;
+  int vec;  // 1: each thread's 16 positions are one aligned, contiguous run
+};
+
+// Per-block state, one 64-bit word: flag (2 bits: 0 nothing yet, 1 the
+// block's own aggregate, 2 its inclusive prefix), starts counted (31 bits)
+// and latest start + 1 (31 bits, 0 = none).  B*S < 2^31 - 1 keeps both in range.
+__device__ __forceinline__ uint64_t scan_state(uint32_t flag, uint32_t count, int last) {
+  return (static_cast<uint64_t>(flag) << 62) | (static_cast<uint64_t>(count & 0x7FFFFFFFu) << 31) |
+         static_cast<uint64_t>(static_cast<uint32_t>(last + 1) & 0x7FFFFFFFu);
+}
+__device__ __forceinline__ uint32_t state_flag(uint64_t s) { return static_cast<uint32_t>(s >> 62); }
+__device__ __forceinline__ uint32_t state_count(uint64_t s) { return static_cast<uint32_t>(s >> 31) & 0x7FFFFFFFu; }
+__device__ __forceinline__ int state_last(uint64_t s) { return static_cast<int>(s & 0x7FFFFFFFu) - 1; }
+
+__device__ __forceinline__ void st_release(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Workspace: [0] ticket counter, then (from byte 256) one state per block.
+struct ScanWs {
+  uint32_t* ticket;
+  uint64_t* state;
 };
 
 __device__ __forceinline__ int load_pos(const int32_t* __restrict__ pos, const ScanGeom& g, int gi) {
@@ -222,177 +263,189 @@ __device__ __forceinline__ int load_pos(const int32_t* __restrict__ pos, const S
   return __ldg(pos + (static_cast<size_t>(r) * g.B + b) * g.Sl + sp);
 }
 
-// Flags of this thread's kScanItems consecutive items (bit i), and whether any position was negative.
+// This thread's kScanItems positions starting at gathered index `first`:
+// start flags (bit i) and whether any position was negative.
 __device__ __forceinline__ uint32_t thread_flags(const int32_t* __restrict__ pos, const ScanGeom& g, int first,
                                                  bool& negative) {
+  int v[kScanItems];
+  if (g.vec && first + kScanItems <= g.total) {
+    // sixteen consecutive positions of one shard row: four 16-byte loads
+    size_t at = static_cast<size_t>(first);
+    if (g.P != 1 && g.B != 1) {
+      const int b = first / g.S, s = first - b * g.S, r = s / g.Sl;
+      at = (static_cast<size_t>(r) * g.B + b) * g.Sl + (s - r * g.Sl);
+    }
+    const int4* p4 = reinterpret_cast<const int4*>(pos + at);
+#pragma unroll
+    for (int k = 0; k < kScanItems / 4; ++k) {
+      const int4 x = __ldg(p4 + k);
+      v[4 * k] = x.x;
+      v[4 * k + 1] = x.y;
+      v[4 * k + 2] = x.z;
+      v[4 * k + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kScanItems; ++i) v[i] = first + i < g.total ? load_pos(pos, g, first + i) : 1;
+  }
+  // row starts inside [first, first + kScanItems): one division per thread
+  const int rem = first % g.S;
+  long long next_row = rem == 0 ? first : static_cast<long long>(first) + (g.S - rem);
   uint32_t f = 0;
   negative = false;
 #pragma unroll
   for (int i = 0; i < kScanItems; ++i) {
-    int gi = first + i;
-    if (gi < g.total) {
-      int p = load_pos(pos, g, gi);
-      negative |= p < 0;
-      int s = gi % g.S;
-      if (p == 0 || s == 0) f |= 1u << i;
-    }
+    const int gi = first + i;
+    const bool in = gi < g.total;
+    negative |= in && v[i] < 0;
+    const bool row = gi == next_row;
+    if (row) next_row += g.S;
+    if (in && (v[i] == 0 || row)) f |= 1u << i;
   }
   return f;
 }
 
-// Block-wide exclusive sum (returned) and total (in *total) of one int per thread.
-__device__ __forceinline__ int block_excl_sum(int x, int* total, int* sh) {
-  int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int incl = x;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) sh[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    int v = lane < kScanThreads / 32 ? sh[lane] : 0;
-    int vi = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, vi, o);
-      if (lane >= o) vi += y;
-    }
-    if (lane < kScanThreads / 32) sh[32 + lane] = vi - v;
-    if (lane == kScanThreads / 32 - 1) sh[64] = vi;
-  }
-  __syncthreads();
-  int r = sh[32 + w] + incl - x;
-  *total = sh[64];
-  __syncthreads();
-  return r;
-}
-
-// Pass 1: per block, the number of document starts and the first start index.
-__global__ void __launch_bounds__(kScanThreads) scan_count_kernel(const int32_t* __restrict__ pos, ScanGeom g,
-                                                                  int32_t* __restrict__ counts,
-                                                                  int32_t* __restrict__ firsts, int32_t* status) {
-  __shared__ int sh[72];
-  __shared__ int first_sh;
-  int first = blockIdx.x * kScanChunk + threadIdx.x * kScanItems;
-  bool neg;
-  uint32_t f = thread_flags(pos, g, first, neg);
-  if (neg) set_status(status, USP_ERR_BAD_POSITIONS);
-  if (threadIdx.x == 0) first_sh = kBig;
-  __syncthreads();
-  if (f) atomicMin(&first_sh, first + __ffs(f) - 1);
-  int total;
-  block_excl_sum(__popc(f), &total, sh);
-  if (threadIdx.x == 0) {
-    counts[blockIdx.x] = total;
-    firsts[blockIdx.x] = first_sh;
-  }
-}
-
-// Pass 2 (one block): exclusive offsets of the blocks, the first start after
-// each block, n_docs, cu[n_docs] = B*S, and max_len reset.
-__global__ void __launch_bounds__(1024) scan_blocks_kernel(int nblk, const int32_t* __restrict__ counts,
-                                                           const int32_t* __restrict__ firsts,
-                                                           int32_t* __restrict__ offsets,
-                                                           int32_t* __restrict__ next_after, int total_items,
-                                                           int32_t* cu, int32_t* n_docs, int32_t* max_len) {
-  __shared__ int sh_sum[1024];
-  __shared__ int sh_min[1024];
-  int per = (nblk + blockDim.x - 1) / blockDim.x;
-  int b0 = threadIdx.x * per, b1 = min(nblk, b0 + per);
-  int s = 0, mn = kBig;
-  for (int b = b0; b < b1; ++b) s += counts[b];
-  for (int b = b0; b < b1; ++b) mn = min(mn, firsts[b]);
-  sh_sum[threadIdx.x] = s;
-  sh_min[threadIdx.x] = mn;
-  __syncthreads();
-  // Hillis-Steele scans over 1024 thread partials: prefix sums, suffix minima.
-  for (int o = 1; o < 1024; o <<= 1) {
-    int a = threadIdx.x >= o ? sh_sum[threadIdx.x - o] : 0;
-    int m = threadIdx.x + o < 1024 ? sh_min[threadIdx.x + o] : kBig;
-    __syncthreads();
-    sh_sum[threadIdx.x] += a;
-    sh_min[threadIdx.x] = min(sh_min[threadIdx.x], m);
-    __syncthreads();
-  }
-  int run = sh_sum[threadIdx.x] - s;                                  // exclusive
-  int after = threadIdx.x + 1 < 1024 ? sh_min[threadIdx.x + 1] : kBig;  // first start beyond my blocks
-  for (int b = b0; b < b1; ++b) {
-    offsets[b] = run;
-    run += counts[b];
-  }
-  for (int b = b1 - 1; b >= b0; --b) {
-    next_after[b] = after == kBig ? total_items : after;
-    after = min(after, firsts[b]);
-  }
-  if (threadIdx.x == 1023) {
-    int n = sh_sum[1023];
-    *n_docs = n;
-    cu[n] = total_items;
+__global__ void scan_init_kernel(ScanWs ws, int nblk, int32_t* max_len) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nblk; i += gridDim.x * blockDim.x) ws.state[i] = 0;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *ws.ticket = 0;
     *max_len = 0;
   }
 }
 
-// Pass 3: scatter every document start to its slot; max document length.
-__global__ void __launch_bounds__(kScanThreads) scan_scatter_kernel(const int32_t* __restrict__ pos, ScanGeom g,
-                                                                    const int32_t* __restrict__ offsets,
-                                                                    const int32_t* __restrict__ next_after,
-                                                                    int32_t* __restrict__ cu, int32_t* max_len) {
-  __shared__ int sh[72];
-  __shared__ int nxt[kScanThreads];
-  __shared__ int bmax;
-  int first = blockIdx.x * kScanChunk + threadIdx.x * kScanItems;
-  bool neg;
-  uint32_t f = thread_flags(pos, g, first, neg);
-  int total;
-  int off = block_excl_sum(__popc(f), &total, sh) + offsets[blockIdx.x];
-  // first start owned by each thread, then the first start after each thread
-  nxt[threadIdx.x] = f ? first + __ffs(f) - 1 : kBig;
-  if (threadIdx.x == 0) bmax = 0;
-  __syncthreads();
-  for (int o = 1; o < kScanThreads; o <<= 1) {
-    int m = threadIdx.x + o < kScanThreads ? nxt[threadIdx.x + o] : kBig;
-    __syncthreads();
-    nxt[threadIdx.x] = min(nxt[threadIdx.x], m);
-    __syncthreads();
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(const int32_t* __restrict__ pos, ScanGeom g, ScanWs ws,
+                                                            int32_t* __restrict__ cu, int32_t* n_docs,
+                                                            int32_t* max_len, int32_t* status) {
+  __shared__ int sh_cnt[kScanThreads / 32], sh_last[kScanThreads / 32];
+  __shared__ int sh_bid, sh_pre_cnt, sh_pre_last, sh_max;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    sh_bid = static_cast<int>(atomicAdd(ws.ticket, 1u));
+    sh_max = 0;
   }
-  int after = threadIdx.x + 1 < kScanThreads ? nxt[threadIdx.x + 1] : kBig;
-  if (after == kBig) after = next_after[blockIdx.x];
+  __syncthreads();
+  const int bid = sh_bid;
+  const int first = bid * kScanChunk + tid * kScanItems;
+  bool neg;
+  const uint32_t f = thread_flags(pos, g, first, neg);
+  if (neg) set_status(status, USP_ERR_BAD_POSITIONS);
+
+  // block scan of (starts, latest start) over the threads: warp shuffles,
+  // then the warps' totals
+  const int cnt = __popc(f);
+  const int last = f ? first + 31 - __clz(f) : -1;
+  int inc_cnt = cnt, inc_last = last;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int c = __shfl_up_sync(0xffffffffu, inc_cnt, o);
+    const int l = __shfl_up_sync(0xffffffffu, inc_last, o);
+    if (lane >= o) {
+      inc_cnt += c;
+      inc_last = max(inc_last, l);
+    }
+  }
+  if (lane == 31) {
+    sh_cnt[warp] = inc_cnt;
+    sh_last[warp] = inc_last;
+  }
+  __syncthreads();
+  int w_cnt = 0, w_last = -1, b_cnt = 0, b_last = -1;  // before this warp; the whole block
+#pragma unroll
+  for (int w = 0; w < kScanThreads / 32; ++w) {
+    if (w < warp) {
+      w_cnt += sh_cnt[w];
+      w_last = max(w_last, sh_last[w]);
+    }
+    b_cnt += sh_cnt[w];
+    b_last = max(b_last, sh_last[w]);
+  }
+  const int ex_cnt = w_cnt + inc_cnt - cnt;                                         // starts before this thread
+  const int up_last = __shfl_up_sync(0xffffffffu, inc_last, 1);
+  const int ex_last = max(w_last, lane > 0 ? up_last : -1);                          // latest start before it
+
+  // look back over the predecessors (warp 0)
+  if (warp == 0) {
+    int pre_cnt = 0, pre_last = -1;
+    if (bid == 0) {
+      if (lane == 0) st_release(ws.state, scan_state(2, b_cnt, b_last));
+    } else {
+      if (lane == 0) st_release(ws.state + bid, scan_state(1, b_cnt, b_last));
+      int base = bid - 1;
+      const uint64_t t0 = global_ns();
+      while (true) {
+        const int j = base - lane;
+        const uint64_t s = j >= 0 ? ld_acquire(ws.state + j) : scan_state(2, 0, -1);
+        const uint32_t fl = state_flag(s);
+        const uint32_t incl = __ballot_sync(0xffffffffu, fl == 2);
+        const uint32_t none = __ballot_sync(0xffffffffu, fl == 0);
+        // lanes up to the nearest inclusive state (all 32 if there is none here)
+        const uint32_t upto = incl ? ((incl & (0u - incl)) << 1) - 1u : 0xffffffffu;
+        if ((none & upto) == 0) {
+          int c = (upto >> lane) & 1u ? static_cast<int>(state_count(s)) : 0;
+          int l = (upto >> lane) & 1u ? state_last(s) : -1;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            c += __shfl_xor_sync(0xffffffffu, c, o);
+            l = max(l, __shfl_xor_sync(0xffffffffu, l, o));
+          }
+          pre_cnt += c;
+          pre_last = max(pre_last, l);
+          if (incl) break;
+          base -= 32;
+        } else if (global_ns() - t0 > 2000000000ull) {  // every block looked at is running: never expected
+          if (lane == 0) set_status(status, USP_ERR_TIMEOUT);
+          break;
+        }
+      }
+      if (lane == 0) st_release(ws.state + bid, scan_state(2, pre_cnt + b_cnt, max(pre_last, b_last)));
+    }
+    if (lane == 0) {
+      sh_pre_cnt = pre_cnt;
+      sh_pre_last = pre_last;
+    }
+  }
+  __syncthreads();
+
+  // scatter the starts; each document's length where it ends
+  int off = sh_pre_cnt + ex_cnt;
+  int prev = max(sh_pre_last, ex_last);
   int local_max = 0;
-  int prev = -1;
+#pragma unroll
   for (int i = 0; i < kScanItems; ++i) {
     if (f & (1u << i)) {
-      int gi = first + i;
+      const int gi = first + i;
       cu[off++] = gi;
       if (prev >= 0) local_max = max(local_max, gi - prev);
       prev = gi;
     }
   }
-  if (prev >= 0) local_max = max(local_max, after - prev);
-  if (local_max) atomicMax(&bmax, local_max);
+  if (bid == g.nblk - 1 && tid == kScanThreads - 1) {
+    // the last document ends at B*S
+    const int n = sh_pre_cnt + b_cnt;
+    *n_docs = n;
+    cu[n] = g.total;
+    local_max = max(local_max, g.total - max(sh_pre_last, b_last));
+  }
+  if (local_max) atomicMax(&sh_max, local_max);
   __syncthreads();
-  if (threadIdx.x == 0 && bmax) atomicMax(max_len, bmax);
+  if (tid == 0 && sh_max) atomicMax(max_len, sh_max);
 }
 
 size_t cu_seqlens_ws_bytes(int B, int S) {
-  size_t total = static_cast<size_t>(B) * S;
-  size_t nblk = (total + kScanChunk - 1) / kScanChunk;
-  if (nblk < 1) nblk = 1;
-  return ((4 * nblk * sizeof(int32_t)) + 255) / 256 * 256;
+  return cu_seqlens_ws_bytes_for(static_cast<long long>(B) * S);
 }
 
 int launch_cu_seqlens(const int32_t* pos, int B, int S, int P, int32_t* cu, int32_t* n_docs, int32_t* max_len,
                       int32_t* ws, int32_t* status, cudaStream_t st) {
-  ScanGeom g{B, S, P, S / P, B * S};
-  int nblk = (g.total + kScanChunk - 1) / kScanChunk;
-  int32_t* counts = ws;
-  int32_t* firsts = ws + nblk;
-  int32_t* offsets = ws + 2 * nblk;
-  int32_t* next_after = ws + 3 * nblk;
-  scan_count_kernel<<<nblk, kScanThreads, 0, st>>>(pos, g, counts, firsts, status);
-  scan_blocks_kernel<<<1, 1024, 0, st>>>(nblk, counts, firsts, offsets, next_after, g.total, cu, n_docs, max_len);
-  scan_scatter_kernel<<<nblk, kScanThreads, 0, st>>>(pos, g, offsets, next_after, cu, max_len);
+  ScanGeom g{B, S, P, S / P, B * S, 0, 0};
+  g.nblk = (g.total + kScanChunk - 1) / kScanChunk;
+  g.vec = (reinterpret_cast<uintptr_t>(pos) & 15u) == 0 &&
+          (P == 1 || B == 1 || (g.Sl % kScanItems == 0 && S % kScanItems == 0));
+  ScanWs w{reinterpret_cast<uint32_t*>(ws),
+           reinterpret_cast<uint64_t*>(reinterpret_cast<char*>(ws) + kScanHeaderBytes)};
+  const int init_grid = std::min(std::max(1, (g.nblk + 255) / 256), 4 * device_sm_count());
+  scan_init_kernel<<<init_grid, 256, 0, st>>>(w, g.nblk, max_len);
+  scan_kernel<<<g.nblk, kScanThreads, 0, st>>>(pos, g, w, cu, n_docs, max_len, status);
   return check_launch();
 }
 

@@ -44,6 +44,14 @@ int launch_relayout_qkv(const void* const src[3], void* const dst[3], const int 
 int launch_ring_fwd_merge(const usp_attn_params& p, const void* o_step, const float* lse_step, float* o_acc,
                           float* lse_acc, void* o, float* lse, int flags, cudaStream_t st);
 int launch_ring_grad_accumulate(const void* g_step, float* g_acc, void* g_out, size_t n, int flags, cudaStream_t st);
+// Document-boundary scan: positions per block, and its workspace (a 256-byte
+// header holding the block ticket, then one 64-bit state per block).
+constexpr int kScanChunk = 4096;
+constexpr size_t kScanHeaderBytes = 256;
+constexpr size_t cu_seqlens_ws_bytes_for(long long tokens) {
+  return kScanHeaderBytes +
+         (8 * static_cast<size_t>(tokens > kScanChunk ? (tokens + kScanChunk - 1) / kScanChunk : 1) + 255) / 256 * 256;
+}
 int launch_cu_seqlens(const int32_t* pos, int B, int S, int P, int32_t* cu, int32_t* n_docs, int32_t* max_len,
                       int32_t* ws, int32_t* status, cudaStream_t st);
 size_t cu_seqlens_ws_bytes(int B, int S);

@@ -2,7 +2,7 @@
 // workspace.
 //
 // usp_cu_seqlens_from_position_ids needs a small device workspace for its
-// per-block partial counts.  Some callers cannot provide one: code that may
+// per-block scan states.  Some callers cannot provide one: code that may
 // not call cudaMalloc (or any allocator) on its path — for example a runtime
 // whose device memory is entirely pre-reserved by another allocator, or a
 // plugin interface that hands the library only its input and output pointers.
@@ -14,38 +14,30 @@
 // the process exits.  All calls share it: two calls whose kernels overlap on
 // the GPU (different streams, or different host threads) race on it, so
 // callers must order such calls.  Nothing in it needs to start at zero: the
-// first of the three kernels writes every partial the later ones read, so
-// whatever a previous call left there is overwritten before it is used.
+// first of the scan's two kernels resets every block state and the counter
+// the second one uses, so whatever a previous call left there never matters.
 #include <cuda_runtime.h>
 #include <stdint.h>
-
-#include <mutex>
 
 #include "usp_internal.h"
 
 namespace {
 
 constexpr int kMaxTokens = 1 << 24;
-constexpr int kScanChunk = 4096;                          // tokens per scan block
-constexpr int kScratchInts = 4 * (kMaxTokens / kScanChunk);  // four int32 partials per block
+constexpr int kScratchInts = 16384;  // 64 KiB
+static_assert(usp::cu_seqlens_ws_bytes_for(kMaxTokens) <= sizeof(int32_t) * kScratchInts,
+              "the fixed scratch must hold the scan's workspace for kMaxTokens positions");
 
 static __device__ __align__(256) int32_t g_scan_scratch[kScratchInts];
 
 // Device address of g_scan_scratch on the current device.  In host code the
 // name g_scan_scratch is only a host-side stand-in, not a device address, so
-// it is looked up once per device with that device current and cached.
+// it is looked up with the device current, on every call: a cached address
+// would go stale if the caller reset the device between calls.
 int scratch_for_current_device(int32_t** out) {
-  static std::mutex mu;
-  static int32_t* cache[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return USP_ERR_CUDA;
-  std::lock_guard<std::mutex> g(mu);
-  if (cache[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_scan_scratch) != cudaSuccess || p == nullptr) return USP_ERR_CUDA;
-    cache[dev] = static_cast<int32_t*>(p);
-  }
-  *out = cache[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_scan_scratch) != cudaSuccess || p == nullptr) return USP_ERR_CUDA;
+  *out = static_cast<int32_t*>(p);
   return USP_OK;
 }
 
