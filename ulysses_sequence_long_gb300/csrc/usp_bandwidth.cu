@@ -209,30 +209,41 @@ int launch_relayout_qkv(const void* const src[3], void* const dst[3], const int 
 // Gathered index g = b*S + s (s = r*Sl + s') reads pos[r][b][s'].  A document
 // starts at g when s == 0 or the position there is 0.
 //
-// One pass over the positions (single-pass scan with decoupled look-back,
-// Merrill & Garland, "Single-pass Parallel Prefix Scan with Decoupled
-// Look-back", NVIDIA tech report NVR-2016-002): every block takes kScanChunk
-// positions in the order blocks start (a ticket, so that every block a block
-// looks back at is already running), counts its document starts and notes
-// its last one, publishes that aggregate, then looks back over its
-// predecessors' published states for the exclusive prefix (number of starts
-// before it, latest start before it), publishes its inclusive state and
-// scatters its starts into cu_seqlens.  A document's length is taken where it
-// ends: at the next start (in the same block or, for a block's first start,
-// after the latest start before the block), and after the last start by the
-// last block.  A small kernel before it resets the block states.
-constexpr int kScanThreads = 256;
-constexpr int kScanItems = kScanChunk / kScanThreads;  // 16 consecutive positions per thread
-static_assert(kScanItems == 16, "a thread's positions are four 16-byte vectors");
+// One pass over the positions.  The grid is persistent-sized (at most one
+// 1024-thread block per SM); block k, in the order blocks start (a ticket,
+// so that every block a block waits for is already running), owns the k-th
+// contiguous range of the gathered sequence:
+//   1. it streams its range (1024 consecutive positions per warp and step,
+//      coalesced 16-byte loads), keeps the start flags as bits in shared
+//      memory, and publishes its aggregate: number of starts and latest start;
+//   2. it sums the aggregates of all blocks before it (32 at a time, one
+//      warp) for its prefix: starts before it and the latest start before it.
+//      Every aggregate is published after one pass over one range, so no
+//      block waits on a chain of other blocks' prefixes;
+//   3. every thread takes a contiguous run of the flag words, a block-wide
+//      scan gives each its first output slot and the start before its run,
+//      and it writes its starts into cu_seqlens.  A document's length is
+//      taken where it ends (the next start, or B*S after the last start).
+// Flags beyond the shared-memory budget (ranges longer than kScanSmemWords *
+// 32 positions) are recomputed from the positions in step 3.  With several
+// blocks a small kernel before it resets the block states; a sequence of at
+// most one block's range (every workload here) takes the one launch alone.
+constexpr int kScanThreads = 1024;
+constexpr int kScanItems = 32;                                 // positions per thread and step: one flag word
+constexpr int kScanStep = kScanThreads * kScanItems;           // positions per block and step
+constexpr int kScanSmemWords = 56 * 1024;                      // 224 KB of flag words
+static_assert(kScanChunk % kScanStep == 0, "ranges are whole steps");
 
 struct ScanGeom {
-  int B, S, P, Sl, total, nblk;
-  int vec;  // 1: each thread's 16 positions are one aligned, contiguous run
+  int B, S, P, Sl, total;
+  int nblk;   // blocks in the grid (1: no ticket, no block states, no reset kernel)
+  int range;  // positions per block (a multiple of kScanStep)
+  int vec;    // 1: each thread's 32 positions are one aligned, contiguous run
 };
 
 // Per-block state, one 64-bit word: flag (2 bits: 0 nothing yet, 1 the
-// block's own aggregate, 2 its inclusive prefix), starts counted (31 bits)
-// and latest start + 1 (31 bits, 0 = none).  B*S < 2^31 - 1 keeps both in range.
+// block's aggregate), starts counted (31 bits) and latest start + 1 (31 bits,
+// 0 = none).  B*S < 2^31 - 1 keeps both in range.
 __device__ __forceinline__ uint64_t scan_state(uint32_t flag, uint32_t count, int last) {
   return (static_cast<uint64_t>(flag) << 62) | (static_cast<uint64_t>(count & 0x7FFFFFFFu) << 31) |
          static_cast<uint64_t>(static_cast<uint32_t>(last + 1) & 0x7FFFFFFFu);
@@ -241,12 +252,14 @@ __device__ __forceinline__ uint32_t state_flag(uint64_t s) { return static_cast<
 __device__ __forceinline__ uint32_t state_count(uint64_t s) { return static_cast<uint32_t>(s >> 31) & 0x7FFFFFFFu; }
 __device__ __forceinline__ int state_last(uint64_t s) { return static_cast<int>(s & 0x7FFFFFFFu) - 1; }
 
-__device__ __forceinline__ void st_release(uint64_t* p, uint64_t v) {
-  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+// A state word carries everything a reader needs (no other data is published
+// with it), so relaxed gpu-scope accesses suffice.
+__device__ __forceinline__ void st_state(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p) {
+__device__ __forceinline__ uint64_t ld_state(const uint64_t* p) {
   uint64_t v;
-  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -269,7 +282,7 @@ __device__ __forceinline__ uint32_t thread_flags(const int32_t* __restrict__ pos
                                                  bool& negative) {
   int v[kScanItems];
   if (g.vec && first + kScanItems <= g.total) {
-    // sixteen consecutive positions of one shard row: four 16-byte loads
+    // 32 consecutive positions of one shard row: eight 16-byte loads
     size_t at = static_cast<size_t>(first);
     if (g.P != 1 && g.B != 1) {
       const int b = first / g.S, s = first - b * g.S, r = s / g.Sl;
@@ -305,6 +318,74 @@ __device__ __forceinline__ uint32_t thread_flags(const int32_t* __restrict__ pos
   return f;
 }
 
+// Flags of the 1024 positions [base, base + 1024) for one warp, loaded
+// coalesced: at step k every lane reads the four positions base + 128k + 4L
+// (one 16-byte vector per lane when `vec`, else four scalar loads).  The
+// 32-position flag word w = 4k + L/8 is assembled from eight lanes' nibbles
+// by a segmented OR over shuffles; lane L ends up holding word (L % 8) * 4 +
+// L / 8 (returned, with that word's index in *wi).
+__device__ __forceinline__ uint32_t warp_flags(const int32_t* __restrict__ pos, const ScanGeom& g, int base,
+                                               bool vec, int& wi, bool& negative) {
+  const int lane = threadIdx.x & 31;
+  int v[8][4];
+  if (vec) {
+    size_t at = static_cast<size_t>(base);
+    if (g.P != 1 && g.B != 1) {
+      const int b = base / g.S, s = base - b * g.S, r = s / g.Sl;
+      at = (static_cast<size_t>(r) * g.B + b) * g.Sl + (s - r * g.Sl);
+    }
+    const int4* p4 = reinterpret_cast<const int4*>(pos + at) + lane;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int4 x = __ldg(p4 + 32 * k);
+      v[k][0] = x.x;
+      v[k][1] = x.y;
+      v[k][2] = x.z;
+      v[k][3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int gi = base + 128 * k + 4 * lane + e;
+        v[k][e] = gi < g.total ? load_pos(pos, g, gi) : 1;
+      }
+  }
+  uint32_t mine = 0;
+  negative = false;
+  int rem = (base + 4 * lane) % g.S;  // g0 mod S, carried from step to step when S > 128
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int g0 = base + 128 * k + 4 * lane;
+    if (k > 0) {
+      if (g.S > 128) {
+        rem += 128;
+        if (rem >= g.S) rem -= g.S;
+      } else {
+        rem = g0 % g.S;
+      }
+    }
+    // the next row start at or after g0 is g0 + (S - rem) % S
+    const int to_row = rem == 0 ? 0 : g.S - rem;
+    uint32_t nib = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const bool in = g0 + e < g.total;
+      negative |= in && v[k][e] < 0;
+      const bool row = (e >= to_row) && ((e - to_row) % g.S == 0);
+      if (in && (v[k][e] == 0 || row)) nib |= 1u << e;
+    }
+    uint32_t w = nib << (4 * (lane & 7));
+    w |= __shfl_xor_sync(0xffffffffu, w, 1);
+    w |= __shfl_xor_sync(0xffffffffu, w, 2);
+    w |= __shfl_xor_sync(0xffffffffu, w, 4);
+    if ((lane & 7) == k) mine = w;
+  }
+  wi = (lane & 7) * 4 + (lane >> 3);
+  return mine;
+}
+
 __global__ void scan_init_kernel(ScanWs ws, int nblk, int32_t* max_len) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nblk; i += gridDim.x * blockDim.x) ws.state[i] = 0;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -313,91 +394,127 @@ __global__ void scan_init_kernel(ScanWs ws, int nblk, int32_t* max_len) {
   }
 }
 
-__global__ void __launch_bounds__(kScanThreads) scan_kernel(const int32_t* __restrict__ pos, ScanGeom g, ScanWs ws,
-                                                            int32_t* __restrict__ cu, int32_t* n_docs,
-                                                            int32_t* max_len, int32_t* status) {
-  __shared__ int sh_cnt[kScanThreads / 32], sh_last[kScanThreads / 32];
-  __shared__ int sh_bid, sh_pre_cnt, sh_pre_last, sh_max;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    sh_bid = static_cast<int>(atomicAdd(ws.ticket, 1u));
-    sh_max = 0;
-  }
-  __syncthreads();
-  const int bid = sh_bid;
-  const int first = bid * kScanChunk + tid * kScanItems;
-  bool neg;
-  const uint32_t f = thread_flags(pos, g, first, neg);
-  if (neg) set_status(status, USP_ERR_BAD_POSITIONS);
-
-  // block scan of (starts, latest start) over the threads: warp shuffles,
-  // then the warps' totals
-  const int cnt = __popc(f);
-  const int last = f ? first + 31 - __clz(f) : -1;
-  int inc_cnt = cnt, inc_last = last;
+// Block-wide exclusive sum and max (-1 for none) of one value per thread;
+// `tot_*` receive the block's totals.  sh: 2 * 32 ints.
+__device__ __forceinline__ void block_scan2(int c, int l, int& ex_c, int& ex_l, int& tot_c, int& tot_l, int* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int ic = c, il = l;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int c = __shfl_up_sync(0xffffffffu, inc_cnt, o);
-    const int l = __shfl_up_sync(0xffffffffu, inc_last, o);
+    const int yc = __shfl_up_sync(0xffffffffu, ic, o);
+    const int yl = __shfl_up_sync(0xffffffffu, il, o);
     if (lane >= o) {
-      inc_cnt += c;
-      inc_last = max(inc_last, l);
+      ic += yc;
+      il = max(il, yl);
     }
   }
   if (lane == 31) {
-    sh_cnt[warp] = inc_cnt;
-    sh_last[warp] = inc_last;
+    sh[warp] = ic;
+    sh[32 + warp] = il;
   }
   __syncthreads();
-  int w_cnt = 0, w_last = -1, b_cnt = 0, b_last = -1;  // before this warp; the whole block
-#pragma unroll
-  for (int w = 0; w < kScanThreads / 32; ++w) {
-    if (w < warp) {
-      w_cnt += sh_cnt[w];
-      w_last = max(w_last, sh_last[w]);
-    }
-    b_cnt += sh_cnt[w];
-    b_last = max(b_last, sh_last[w]);
-  }
-  const int ex_cnt = w_cnt + inc_cnt - cnt;                                         // starts before this thread
-  const int up_last = __shfl_up_sync(0xffffffffu, inc_last, 1);
-  const int ex_last = max(w_last, lane > 0 ? up_last : -1);                          // latest start before it
-
-  // look back over the predecessors (warp 0)
   if (warp == 0) {
-    int pre_cnt = 0, pre_last = -1;
-    if (bid == 0) {
-      if (lane == 0) st_release(ws.state, scan_state(2, b_cnt, b_last));
-    } else {
-      if (lane == 0) st_release(ws.state + bid, scan_state(1, b_cnt, b_last));
-      int base = bid - 1;
-      const uint64_t t0 = global_ns();
-      while (true) {
-        const int j = base - lane;
-        const uint64_t s = j >= 0 ? ld_acquire(ws.state + j) : scan_state(2, 0, -1);
-        const uint32_t fl = state_flag(s);
-        const uint32_t incl = __ballot_sync(0xffffffffu, fl == 2);
-        const uint32_t none = __ballot_sync(0xffffffffu, fl == 0);
-        // lanes up to the nearest inclusive state (all 32 if there is none here)
-        const uint32_t upto = incl ? ((incl & (0u - incl)) << 1) - 1u : 0xffffffffu;
-        if ((none & upto) == 0) {
-          int c = (upto >> lane) & 1u ? static_cast<int>(state_count(s)) : 0;
-          int l = (upto >> lane) & 1u ? state_last(s) : -1;
+    const int wc = sh[lane], wl = sh[32 + lane];
+    int jc = wc, jl = wl;
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            c += __shfl_xor_sync(0xffffffffu, c, o);
-            l = max(l, __shfl_xor_sync(0xffffffffu, l, o));
-          }
-          pre_cnt += c;
-          pre_last = max(pre_last, l);
-          if (incl) break;
-          base -= 32;
-        } else if (global_ns() - t0 > 2000000000ull) {  // every block looked at is running: never expected
-          if (lane == 0) set_status(status, USP_ERR_TIMEOUT);
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yc = __shfl_up_sync(0xffffffffu, jc, o);
+      const int yl = __shfl_up_sync(0xffffffffu, jl, o);
+      if (lane >= o) {
+        jc += yc;
+        jl = max(jl, yl);
+      }
+    }
+    sh[lane] = jc - wc;                                             // exclusive over warps
+    sh[32 + lane] = __shfl_up_sync(0xffffffffu, jl, 1) * (lane > 0) + (lane == 0 ? -1 : 0);
+    if (lane == 31) {
+      sh[64] = jc;
+      sh[65] = jl;
+    }
+  }
+  __syncthreads();
+  const int up_l = __shfl_up_sync(0xffffffffu, il, 1);
+  ex_c = sh[warp] + ic - c;
+  ex_l = max(sh[32 + warp], lane > 0 ? up_l : -1);
+  tot_c = sh[64];
+  tot_l = sh[65];
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const int32_t* __restrict__ pos, ScanGeom g, ScanWs ws,
+                                                               int32_t* __restrict__ cu, int32_t* n_docs,
+                                                               int32_t* max_len, int32_t* status) {
+  extern __shared__ uint32_t flag_words[];  // min(range/32, kScanSmemWords)
+  __shared__ int sh[72];
+  __shared__ int sh_bid, sh_pre_cnt, sh_pre_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool single = g.nblk == 1;
+  if (tid == 0) {
+    sh_bid = single ? 0 : static_cast<int>(atomicAdd(ws.ticket, 1u));
+    if (single) *max_len = 0;  // (the reset kernel does this when there are several blocks)
+  }
+  __syncthreads();
+  const int bid = sh_bid;
+  const int lo = bid * g.range;                                  // first position of this block's range
+  const int hi = min(g.total, lo + g.range);
+  const int n_steps = hi > lo ? (hi - lo + kScanStep - 1) / kScanStep : 0;
+  const int n_words = n_steps * kScanThreads;
+
+  // 1. flags of the range (kept as bits), count and latest start: each warp
+  // takes 1024 consecutive positions per step
+  int cnt = 0, last = -1;
+  bool neg = false;
+  for (int k = 0; k < n_steps; ++k) {
+    const int base = lo + k * kScanStep + warp * (32 * kScanItems);
+    if (base >= hi) {  // past the end of the sequence: these words hold no start
+      const int w = k * kScanThreads + warp * 32 + lane;
+      if (w < kScanSmemWords) flag_words[w] = 0u;
+      continue;
+    }
+    int wl;
+    bool n_ = false;
+    // whole 1024-position chunks of one shard row take 16-byte loads
+    const bool vec = g.vec && base + 32 * kScanItems <= hi;
+    const uint32_t b = warp_flags(pos, g, base, vec, wl, n_);
+    neg |= n_;
+    const int w = k * kScanThreads + warp * 32 + wl;  // word index in the range
+    if (w < kScanSmemWords) flag_words[w] = b;
+    cnt += __popc(b);
+    if (b) last = max(last, lo + w * kScanItems + 31 - __clz(b));
+  }
+  if (neg) set_status(status, USP_ERR_BAD_POSITIONS);
+  int ex_c, ex_l, b_cnt, b_last;
+  block_scan2(cnt, last, ex_c, ex_l, b_cnt, b_last, sh);
+  if (tid == 0 && !single) st_state(ws.state + bid, scan_state(1, b_cnt, b_last));
+
+  // 2. prefix: the aggregates of every block before this one
+  if (warp == 0 && single) {
+    if (lane == 0) {
+      sh_pre_cnt = 0;
+      sh_pre_last = -1;
+    }
+  } else if (warp == 0) {
+    int pre_cnt = 0, pre_last = -1;
+    const uint64_t t0 = global_ns();
+    for (int j0 = 0; j0 < bid; j0 += 32) {
+      const int j = j0 + lane;
+      uint64_t s = j < bid ? ld_state(ws.state + j) : scan_state(1, 0, -1);
+      while (state_flag(s) == 0) {  // that block is still on its range (it has started: it took a ticket first)
+        if (global_ns() - t0 > 2000000000ull) {
+          set_status(status, USP_ERR_TIMEOUT);
+          s = scan_state(1, 0, -1);
           break;
         }
+        __nanosleep(128);
+        s = ld_state(ws.state + j);
       }
-      if (lane == 0) st_release(ws.state + bid, scan_state(2, pre_cnt + b_cnt, max(pre_last, b_last)));
+      pre_cnt += static_cast<int>(state_count(s));
+      pre_last = max(pre_last, state_last(s));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      pre_cnt += __shfl_xor_sync(0xffffffffu, pre_cnt, o);
+      pre_last = max(pre_last, __shfl_xor_sync(0xffffffffu, pre_last, o));
     }
     if (lane == 0) {
       sh_pre_cnt = pre_cnt;
@@ -406,29 +523,46 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const int32_t* __res
   }
   __syncthreads();
 
-  // scatter the starts; each document's length where it ends
-  int off = sh_pre_cnt + ex_cnt;
-  int prev = max(sh_pre_last, ex_last);
+  // 3. every thread a contiguous run of flag words: slots and the start before it
+  const int per = (n_words + kScanThreads - 1) / kScanThreads;
+  const int wa = min(n_words, tid * per), wb = min(n_words, wa + per);
+  auto word = [&](int wi) -> uint32_t {
+    if (wi < kScanSmemWords) return flag_words[wi];
+    const int f = lo + wi * kScanItems;  // beyond the shared-memory budget: recompute
+    bool n_ = false;
+    return f < hi ? thread_flags(pos, g, f, n_) : 0u;
+  };
+  int rc = 0, rl = -1;
+  for (int wi = wa; wi < wb; ++wi) {
+    const uint32_t w = word(wi);
+    rc += __popc(w);
+    if (w) rl = max(rl, lo + wi * kScanItems + 31 - __clz(w));
+  }
+  int off, prev, tc, tl;
+  block_scan2(rc, rl, off, prev, tc, tl, sh);
+  off += sh_pre_cnt;
+  prev = max(prev, sh_pre_last);
   int local_max = 0;
-#pragma unroll
-  for (int i = 0; i < kScanItems; ++i) {
-    if (f & (1u << i)) {
-      const int gi = first + i;
+  for (int wi = wa; wi < wb; ++wi) {
+    uint32_t w = word(wi);
+    while (w) {
+      const int gi = lo + wi * kScanItems + __ffs(w) - 1;
+      w &= w - 1;
       cu[off++] = gi;
       if (prev >= 0) local_max = max(local_max, gi - prev);
       prev = gi;
     }
   }
-  if (bid == g.nblk - 1 && tid == kScanThreads - 1) {
+  if (bid == g.nblk - 1 && tid == 0) {
     // the last document ends at B*S
     const int n = sh_pre_cnt + b_cnt;
     *n_docs = n;
     cu[n] = g.total;
     local_max = max(local_max, g.total - max(sh_pre_last, b_last));
   }
-  if (local_max) atomicMax(&sh_max, local_max);
-  __syncthreads();
-  if (tid == 0 && sh_max) atomicMax(max_len, sh_max);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) local_max = max(local_max, __shfl_xor_sync(0xffffffffu, local_max, o));
+  if (lane == 0 && local_max) atomicMax(max_len, local_max);
 }
 
 size_t cu_seqlens_ws_bytes(int B, int S) {
@@ -437,15 +571,29 @@ size_t cu_seqlens_ws_bytes(int B, int S) {
 
 int launch_cu_seqlens(const int32_t* pos, int B, int S, int P, int32_t* cu, int32_t* n_docs, int32_t* max_len,
                       int32_t* ws, int32_t* status, cudaStream_t st) {
-  ScanGeom g{B, S, P, S / P, B * S, 0, 0};
-  g.nblk = (g.total + kScanChunk - 1) / kScanChunk;
+  ScanGeom g{B, S, P, S / P, B * S, 0, 0, 0};
+  // as many blocks as SMs (at most one per kScanChunk positions, the
+  // workspace's state count); each block's range a whole number of steps
+  const long long chunks = (static_cast<long long>(g.total) + kScanChunk - 1) / kScanChunk;
+  const int want = static_cast<int>(std::min<long long>(std::max<long long>(chunks, 1), device_sm_count()));
+  const long long steps = (static_cast<long long>(g.total) + kScanStep - 1) / kScanStep;
+  g.range = static_cast<int>((steps + want - 1) / want) * kScanStep;
+  g.nblk = static_cast<int>((static_cast<long long>(g.total) + g.range - 1) / g.range);
+  if (g.nblk < 1) g.nblk = 1;
+  // 16-byte loads: an aligned buffer whose 32-position runs (one thread, when
+  // recomputing) and 1024-position runs (one warp) never cross a shard row
   g.vec = (reinterpret_cast<uintptr_t>(pos) & 15u) == 0 &&
-          (P == 1 || B == 1 || (g.Sl % kScanItems == 0 && S % kScanItems == 0));
+          (P == 1 || B == 1 || (g.Sl % (32 * kScanItems) == 0 && S % (32 * kScanItems) == 0));
   ScanWs w{reinterpret_cast<uint32_t*>(ws),
            reinterpret_cast<uint64_t*>(reinterpret_cast<char*>(ws) + kScanHeaderBytes)};
-  const int init_grid = std::min(std::max(1, (g.nblk + 255) / 256), 4 * device_sm_count());
-  scan_init_kernel<<<init_grid, 256, 0, st>>>(w, g.nblk, max_len);
-  scan_kernel<<<g.nblk, kScanThreads, 0, st>>>(pos, g, w, cu, n_docs, max_len, status);
+  const size_t smem = sizeof(uint32_t) * std::min<size_t>(g.range / kScanItems, kScanSmemWords);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+          cudaSuccess)
+    return USP_ERR_CUDA;
+  // (one block needs no ticket and no block states: no reset kernel)
+  if (g.nblk > 1) scan_init_kernel<<<1, 256, 0, st>>>(w, g.nblk, max_len);
+  scan_kernel<<<g.nblk, kScanThreads, smem, st>>>(pos, g, w, cu, n_docs, max_len, status);
   return check_launch();
 }
 

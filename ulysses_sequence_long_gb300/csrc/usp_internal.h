@@ -44,9 +44,10 @@ int launch_relayout_qkv(const void* const src[3], void* const dst[3], const int 
 int launch_ring_fwd_merge(const usp_attn_params& p, const void* o_step, const float* lse_step, float* o_acc,
                           float* lse_acc, void* o, float* lse, int flags, cudaStream_t st);
 int launch_ring_grad_accumulate(const void* g_step, float* g_acc, void* g_out, size_t n, int flags, cudaStream_t st);
-// Document-boundary scan: positions per block, and its workspace (a 256-byte
-// header holding the block ticket, then one 64-bit state per block).
-constexpr int kScanChunk = 4096;
+// Document-boundary scan: at most one block per kScanChunk positions, and its
+// workspace (a 256-byte header holding the block ticket, then one 64-bit state
+// per block).
+constexpr int kScanChunk = 32768;
 constexpr size_t kScanHeaderBytes = 256;
 constexpr size_t cu_seqlens_ws_bytes_for(long long tokens) {
   return kScanHeaderBytes +
