@@ -9,16 +9,18 @@
 //     LSE_t = ln( sum_{u visible} exp(scale q_t.k_u) + exp(z_{r*hq+j}) )
 //     O_t   = sum_{u visible} exp(scale q_t.k_u - LSE_t) v_u
 //
-// CTA = one (rank, query head, block of 256 query rows) = two 128-row Q tiles
-// that share every K/V tile.  Warp roles (320 threads):
+// CTA = one (rank, query head, block of 128*NQT query rows) = NQT 128-row Q
+// tiles that share every K/V tile.  Warp roles (NQT = 2: 320 threads):
 //   warps 0-3   softmax for Q tile 0 (thread = query row = TMEM lane)
-//   warps 4-7   softmax for Q tile 1
-//   warp  8     TMA producer: Q tiles once, then a ring of K/V stages
-//   warp  9     MMA issuer (one thread): S_q = Q_q K^T into TMEM, then
+//   warps 4-7   softmax for Q tile 1 (NQT = 2)
+//   warp  4NQT  TMA producer: Q tiles once, then a ring of K/V stages
+//   warp  4NQT+1 MMA issuer (one thread): S_q = Q_q K^T into TMEM, then
 //               O_q += P_q V with P_q read from TMEM (bf16, written over S_q)
-// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
-// The MMA thread alternates the two tiles (PV_0, S_0 next, PV_1, S_1 next), so
-// the tensor core works on one tile while the other tile's softmax runs.
+// TMEM: S_q [128q, 128q+128), O_q [128NQT + qD, 128NQT + (q+1)D) (512 columns
+// for NQT = 2).  With two tiles the MMA thread alternates them (PV_0, S_0
+// next, PV_1, S_1 next), so the tensor core works on one tile while the other
+// tile's softmax runs; with one tile (short windows at D = 64) two CTAs share
+// an SM and overlap instead.
 //
 // Online softmax in the log2 domain with a lazy rescale: the running max only
 // moves when a row's new max exceeds it by more than 8 (a factor 256), and the
@@ -37,19 +39,27 @@ namespace usp {
 
 namespace fwd {
 
-constexpr int kThreads = 320;
 constexpr int kAtomBytes = kBM * 128;  // one 64-column (128-byte) swizzle column of a 128-row tile
 
-template <int D>
+// NQT Q tiles per CTA: 2 (two softmax warpgroups that alternate on the tensor
+// core, 512 TMEM columns, one CTA per SM) or 1 (one softmax warpgroup; at
+// D = 64 its 192 TMEM columns and 82 KB of shared memory let two CTAs share
+// an SM, which then overlap each other's latencies).
+template <int D, int NQT>
 struct Cfg {
+  static constexpr int THREADS = 128 * NQT + 64;      // softmax warpgroups, producer warp, MMA warp
+  static constexpr int WP = 4 * NQT;                  // producer warp (the MMA warp is WP + 1)
+  static constexpr int CTAS = (NQT == 1 && D == 64) ? 2 : 1;  // CTAs per SM
+  static constexpr uint32_t TCOLS = NQT == 2 ? 512 : 256;     // TMEM columns allocated
   static constexpr int NCH = D / 64;                  // 64-wide column atoms per row
-  static constexpr int ST = (D == 128) ? 2 : 4;       // K/V pipeline stages
+  static constexpr int ST = (D == 128 || NQT == 1) ? 2 : 4;  // K/V pipeline stages
   static constexpr int TILE = NCH * kAtomBytes;       // bytes of one 128-row tile
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + 2 * TILE;
+  static constexpr int OFF_K = OFF_Q + NQT * TILE;
   static constexpr int OFF_V = OFF_K + ST * TILE;
   static constexpr int OFF_BAR = OFF_V + ST * TILE;
   static constexpr int SMEM = OFF_BAR + 1024 + 1024;  // barriers + alignment slack
+  static constexpr uint32_t T_O = 128 * NQT;          // first O column (S_q at 128q)
 };
 
 struct Bars {
@@ -68,14 +78,14 @@ struct Bars {
 struct Out {
   __nv_bfloat16* o;
   float* lse;
-  int nqb;  // 256-row query blocks per (rank, head)
+  int nqb;  // query blocks (NQT tiles of 128 rows) per (rank, head)
 };
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int NQT>
+__global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, AttnArgs p, Out out) {
-  using C = Cfg<D>;
+  using C = Cfg<D, NQT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
@@ -88,14 +98,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rem = static_cast<int>(blockIdx.x) % per_blk;
   const int r = rem / p.hq, j = rem % p.hq;
   const HeadRef qh = q_head_ref(p, r, j), kvh = kv_head_ref(p, r, j / p.G);
-  const int t0 = qb * 2 * kBM;
+  const int t0 = qb * NQT * kBM;
 
   const int n_docs = checked_docs(p);
   if (n_docs == 0) return;
 
-  bool tile_ok[2];
+  bool tile_ok[NQT];
   int lo = 0x7FFFFFFF, hi = 0;
-  for (int q = 0; q < 2; ++q) {
+  for (int q = 0; q < NQT; ++q) {
     int first = t0 + q * kBM;
     tile_ok[q] = first < p.BS;
     if (tile_ok[q]) {
@@ -106,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   // Ring x Ulysses step: only the key/value super-chunk held at this step (the
-  // CTA's 256 rows lie in one super-chunk).
+  // CTA's rows lie in one super-chunk).
   int rk0 = 0, rk1 = 0x7FFFFFFF;
   if (p.ring > 1) {
     ring_key_window(p, t0, rk0, rk1);
@@ -121,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (n_kv == 0) {
     // no key to see (a ring step whose block lies after these rows): O = 0 and
     // LSE = the sink logit alone, or -inf
-    if (warp < 8) {
+    if (warp < C::WP) {
       const int q = warp >> 2, t = t0 + q * kBM + (tid & 127);
       if (tile_ok[q] && t < p.BS) {
         uint4* dst = reinterpret_cast<uint4*>(out.o + row_offset(p, qh, p.hq, p.Hq, t, D));
@@ -135,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (tid == 0) {
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < NQT; ++q) {
       mbar_init(&bars->q_full[q], 1);
       mbar_init(&bars->s_full[q], 1);
       mbar_init(&bars->p_full[q], 4);
@@ -151,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == 0) {
-    tmem_alloc(&bars->tmem, 512);
+    tmem_alloc(&bars->tmem, C::TCOLS);
     tmem_relinquish();
     tc_fence_before();
   }
@@ -161,13 +171,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = &bars->abort;
   const uint32_t sbase = smem_u32(smem);
 
-  if (warp == 8) {
+  if (warp == C::WP) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
-      for (int q = 0; q < 2; ++q) {
+      for (int q = 0; q < NQT; ++q) {
         if (!tile_ok[q]) continue;
         mbar_arrive_expect_tx(&bars->q_full[q], C::TILE);
         for (int c = 0; c < C::NCH; ++c)
@@ -193,16 +203,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&bars->k_full[n % C::ST], (n / C::ST) & 1, abort, p.status);
         mbar_wait(&bars->v_full[n % C::ST], (n / C::ST) & 1, abort, p.status);
       }
-      for (int q = 0; q < 2; ++q)
+      for (int q = 0; q < NQT; ++q)
         if (tile_ok[q]) mbar_wait(&bars->q_full[q], 0, abort, p.status);
     }
-  } else if (warp == 9) {
+  } else if (warp == C::WP + 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(kBM, kBN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(kBM, D, false, true);
       bool ok = true;
-      for (int q = 0; q < 2 && ok; ++q)
+      for (int q = 0; q < NQT && ok; ++q)
         if (tile_ok[q]) ok = mbar_wait(&bars->q_full[q], 0, abort, p.status);
       // descriptors are built once per tile and moved by a constant per MMA step
       auto issue_s = [&](int q, int st) {
@@ -218,13 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t vd = sdesc_sw128(sbase + C::OFF_V + st * C::TILE, kAtomBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + 256 + q * D, tmem + q * kBN + kk * 8, sdesc_add(vd, kk * 16 * 128), idesc_o,
+          mma_ts(tmem + C::T_O + q * D, tmem + q * kBN + kk * 8, sdesc_add(vd, kk * 16 * 128), idesc_o,
                  (acc || kk > 0) ? 1u : 0u);
       };
       if (ok) ok = mbar_wait(&bars->k_full[0], 0, abort, p.status);
       if (ok) {
         tc_fence_after();
-        for (int q = 0; q < 2; ++q)
+        for (int q = 0; q < NQT; ++q)
           if (tile_ok[q]) {
             issue_s(q, 0);
             mma_commit(&bars->s_full[q]);
@@ -234,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = n % C::ST;
         if (!(ok = mbar_wait(&bars->v_full[st], (n / C::ST) & 1, abort, p.status))) break;
         bool next_k_ready = false;
-        for (int q = 0; q < 2 && ok; ++q) {
+        for (int q = 0; q < NQT && ok; ++q) {
           if (!tile_ok[q]) continue;
           if (!(ok = mbar_wait(&bars->p_full[q], n & 1, abort, p.status))) break;
           tc_fence_after();
@@ -266,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_ok = t < p.BS;
     const uint32_t lane_base = tmem + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
     const uint32_t s_tm = lane_base + q * kBN;
-    const uint32_t o_tm = lane_base + 256 + q * D;
+    const uint32_t o_tm = lane_base + C::T_O + q * D;
     int a = 0, b = 0;
     if (row_ok) doc_bounds(p.cu, n_docs, p.BS, t, a, b);
     a = max(a, rk0);  // a ring step sees one key/value super-chunk
@@ -387,29 +397,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::TCOLS);
   }
 }
 
 }  // namespace fwd
 
+template <int D, int NQT>
+static int run_fwd(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o,
+                   float* lse, cudaStream_t st) {
+  using C = fwd::Cfg<D, NQT>;
+  fwd::Out out{static_cast<__nv_bfloat16*>(o), lse, (a.BS + NQT * kBM - 1) / (NQT * kBM)};
+  if (cudaFuncSetAttribute(fwd::attn_fwd_kernel<D, NQT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+      cudaSuccess)
+    return USP_ERR_CUDA;
+  const unsigned grid = static_cast<unsigned>(out.nqb) * a.P * a.hq;
+  fwd::attn_fwd_kernel<D, NQT><<<grid, C::THREADS, C::SMEM, st>>>(tq, tk, tv, a, out);
+  return check_launch();
+}
+
 template <int D>
-static int run_fwd(const usp_attn_params& prm, const AttnArgs& a, const void* q, const void* k, const void* v,
-                   void* o, float* lse, cudaStream_t st) {
+static int run_fwd(const AttnArgs& a, const void* q, const void* k, const void* v, void* o, float* lse,
+                   cudaStream_t st) {
   CUtensorMap tq, tk, tv;
   int rc;
   if ((rc = make_rows_tmap(&tq, q, a, a.hq, a.Hq, D, kBM)) != USP_OK) return rc;
   if ((rc = make_rows_tmap(&tk, k, a, a.hk, a.Hkv, D, kBN, a.kv_seq_io != 0)) != USP_OK) return rc;
   if ((rc = make_rows_tmap(&tv, v, a, a.hk, a.Hkv, D, kBN, a.kv_seq_io != 0)) != USP_OK) return rc;
-  fwd::Out out{static_cast<__nv_bfloat16*>(o), lse, (a.BS + 2 * kBM - 1) / (2 * kBM)};
-  const int smem = fwd::Cfg<D>::SMEM;
-  if (cudaFuncSetAttribute(fwd::attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-      cudaSuccess)
-    return USP_ERR_CUDA;
-  const unsigned grid = static_cast<unsigned>(out.nqb) * a.P * a.hq;
-  fwd::attn_fwd_kernel<D><<<grid, fwd::kThreads, smem, st>>>(tq, tk, tv, a, out);
-  (void)prm;
-  return check_launch();
+  // One Q tile per CTA when each row sees few key tiles (a short window at
+  // D = 64: the two tiles of a CTA would share little, and two small CTAs
+  // per SM overlap each other's set-up and latencies instead).
+  const bool one = D == 64 && a.window_left >= 0 && a.window_left < 4 * kBN;
+  return one ? run_fwd<D, 1>(a, tq, tk, tv, o, lse, st) : run_fwd<D, 2>(a, tq, tk, tv, o, lse, st);
 }
 
 int launch_attn_fwd(const usp_attn_params& prm, const void* q, const void* k, const void* v, void* o, float* lse,
@@ -442,8 +461,8 @@ int launch_attn_fwd(const usp_attn_params& prm, const void* q, const void* k, co
   a.n_kvh = prm.Hkv;
   a.hq0 = 0;
   a.n_qh = prm.Hq;
-  if (prm.D == 128) return run_fwd<128>(prm, a, q, k, v, o, lse, st);
-  return run_fwd<64>(prm, a, q, k, v, o, lse, st);
+  if (prm.D == 128) return run_fwd<128>(a, q, k, v, o, lse, st);
+  return run_fwd<64>(a, q, k, v, o, lse, st);
 }
 
 }  // namespace usp
