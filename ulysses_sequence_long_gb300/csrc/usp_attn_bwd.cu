@@ -72,6 +72,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
                                                          const float* __restrict__ lse, float* __restrict__ stats,
                                                          AttnArgs p, int bsp, int n_chunks) {
   constexpr int LPR = D / 8;           // 16-byte lanes per row
+  // passes whose loads are issued before any of them is reduced, so that
+  // enough bytes are in flight (D = 64 rows are short; D = 128 keeps one)
+  constexpr int kPreUnroll = D == 64 ? 4 : 1;
   constexpr int RPP = 256 / LPR;       // rows per pass of the block
   extern __shared__ float dsum[];      // [Hb][kPreTok]
   const int Hb = p.seq_io ? p.P * p.hq : p.hq;
@@ -96,20 +99,29 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
       base = (static_cast<size_t>(r0) * p.BS + t0) * Hb * D;
     }
     const int nrows = ntok * Hb;
-    for (int i0 = 0; i0 < nrows; i0 += RPP) {
-      const int i = i0 + tid / LPR;
-      float acc = 0.f;
-      if (i < nrows) {
-        const size_t e = (base + static_cast<size_t>(i) * D) / 8 + lane_row;
-        const uint4 a = __ldg(o + e);
-        const uint4 bq = __ldg(dO + e);
-        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {bq.x, bq.y, bq.z, bq.w};
+    for (int i0 = 0; i0 < nrows; i0 += kPreUnroll * RPP) {
+      uint4 a[kPreUnroll], bq[kPreUnroll];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) acc += bf16lo(av[k]) * bf16lo(bv[k]) + bf16hi(av[k]) * bf16hi(bv[k]);
+      for (int u = 0; u < kPreUnroll; ++u) {
+        const int i = i0 + u * RPP + tid / LPR;
+        a[u] = bq[u] = make_uint4(0, 0, 0, 0);
+        if (i < nrows) {
+          const size_t e = (base + static_cast<size_t>(i) * D) / 8 + lane_row;
+          a[u] = __ldg(o + e);
+          bq[u] = __ldg(dO + e);
+        }
       }
 #pragma unroll
-      for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (i < nrows && lane_row == 0) dsum[(i % Hb) * kPreTok + i / Hb] = acc;
+      for (int u = 0; u < kPreUnroll; ++u) {
+        const int i = i0 + u * RPP + tid / LPR;
+        const uint32_t av[4] = {a[u].x, a[u].y, a[u].z, a[u].w}, bv[4] = {bq[u].x, bq[u].y, bq[u].z, bq[u].w};
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc += bf16lo(av[k]) * bf16lo(bv[k]) + bf16hi(av[k]) * bf16hi(bv[k]);
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (i < nrows && lane_row == 0) dsum[(i % Hb) * kPreTok + i / Hb] = acc;
+      }
     }
     __syncthreads();
     for (int idx = tid; idx < Hb * kPreTok; idx += 256) {
