@@ -204,6 +204,52 @@ def relayout_bandwidth(w: W.Workload, device, t, steps: int):
     return touched / (ms * 1e-3) / 1e9, ms, how
 
 
+def scan_positions(n: int, mean: int = 4096, seed: int = 11, device="cuda"):
+    """position_ids of n tokens packed with documents of geometric lengths
+    (mean `mean`, seeded), built on the device: positions count from 0 in
+    each document.  Returns (positions int32 [n], number of documents)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lens, tot = [], 0
+    while tot < n:
+        L = min(int(rng.geometric(1.0 / mean)), n - tot)
+        lens.append(L)
+        tot += L
+    lens_t = torch.tensor(lens, dtype=torch.int64, device=device)
+    starts = torch.cumsum(lens_t, 0) - lens_t
+    pos = torch.arange(n, dtype=torch.int64, device=device) - torch.repeat_interleave(starts, lens_t)
+    return pos.to(torch.int32), len(lens)
+
+
+def scan_bandwidth(device, reps: int = 10, n: int = 1 << 28):
+    """GB/s of the document-boundary scan alone over n positions (1 GiB at
+    2^28), L2 flushed before every call: 4n bytes read plus 4(docs+1)
+    written per call, median of per-call CUDA events."""
+    from ulysses_sequence_long_gb300 import binding as B
+    pos, docs = scan_positions(n, device=device)
+    cu = torch.empty((n + 1,), dtype=torch.int32, device=device)
+    nd = torch.zeros(1, dtype=torch.int32, device=device)
+    mx, st = torch.zeros_like(nd), torch.zeros_like(nd)
+    ws = torch.empty((B.usp_cu_seqlens_workspace_bytes(1, n),), dtype=torch.uint8, device=device)
+    scrub = torch.empty((256 * 1024 * 1024,), dtype=torch.uint8, device=device)
+    times = []
+    for r in range(reps + 3):
+        scrub.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        B.usp_cu_seqlens_from_position_ids(pos, 1, n, 8, cu, nd, mx, ws, st)
+        b.record()
+        torch.cuda.synchronize()
+        if r >= 3:
+            times.append(a.elapsed_time(b))
+    assert int(st.item()) == 0 and int(nd.item()) == docs, "scan sweep: wrong document count"
+    ms = statistics.median(times)
+    byts = 4 * n + 4 * (docs + 1)
+    del pos, cu, ws, scrub
+    torch.cuda.empty_cache()
+    return {"tokens": n, "documents": docs, "ms": ms, "gbs": byts / (ms * 1e-3) / 1e9,
+            "how": "one call over 2^28 positions, L2 flushed before each, median of CUDA events"}
+
+
 class Step:
     def __init__(self, w: W.Workload, device, host=None, fused=None):
         from ulysses_sequence_long_gb300.pipeline import HybridAttention, Shape, UlyssesAttention
@@ -616,6 +662,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--bandwidth", default=None, choices=["relayout", "scan"],
+                    help="time only the explicit exchange of --workload (L2 flushed) or the scan over 2^28 positions")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the other workloads' figures (per_config)")
     ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)   # internal: one oracle sample
@@ -650,6 +698,17 @@ def main():
     fused = {"auto": None, "fused": True, "explicit": False}[args.exchange]
     peaks = measured_peaks()
     rb = relayout_bytes(w)
+    if args.bandwidth is not None:   # one bandwidth kernel alone (for profiler captures)
+        if args.bandwidth == "scan":
+            r = scan_bandwidth(device, args.steps)
+        else:
+            t = {n: x.to(device) for n, x in W.qkv_do_shards(w, names=("q", "k", "v")).items()}
+            g, ms, how = relayout_bandwidth(w, device, t, args.steps)
+            r = {"workload": w.name, "ms": ms, "gbs": g, "how": how}
+        r["frac_hbm"] = r["gbs"] / peaks["hbm_gbs"]
+        if rank == 0:
+            print(json.dumps({"bandwidth": args.bandwidth, **r}))
+        return 0
 
     # ---- timed region of the headline workload: K whole steps, events between the calls
     step, m = measure(w, device, args.steps, args.warmup, fused, world, barrier, max_over_ranks, local)
@@ -737,6 +796,10 @@ def main():
             torch.cuda.empty_cache()
             per[ow.name] = om
         line["per_config"] = per
+    if not args.no_per_config:   # the scan's bandwidth at scale (every workload's scan is <= 512 KB)
+        sw = scan_bandwidth(device)
+        sw["frac_hbm"] = sw["gbs"] / peaks["hbm_gbs"]
+        line["scan_2e28"] = sw
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
