@@ -306,14 +306,17 @@ class Step:
     def launches_per_step(self) -> int:
         sink = 1 if self.sinks is not None else 0
         extra = 2 * (len(self.ua.ds_groups) - 1)   # dK/dV + dQ of each further key/value head group
+        # the scan is one launch up to 32768 positions (one block), else a
+        # state reset and the scan
+        scan = 1 if self.w.B * self.w.S <= 32768 else 2
         if self.hybrid:
-            # scan 2, preprocess 1 (+ dsink); per ring step: forward + merge,
+            # scan, preprocess 1 (+ dsink); per ring step: forward + merge,
             # dK/dV + 2 sums, dQ + 1 sum; explicit exchanges add 1 + 1 + 1 + 3
-            return 3 + sink + (7 + extra) * self.w.ring + (2 if self.ua.fused else 6)
-        # scan 2 (state reset + one pass), fwd 1, preprocess 1 (+ dsink 1),
-        # dK/dV 1, dQ 1; the fused step adds the k/v exchange for the forward
-        # (2), the explicit one relayout qkv 1, O 1, dO 1, dQ/dK/dV 3
-        return 6 + sink + extra + (2 if self.ua.fused else 6)
+            return scan + 1 + sink + (7 + extra) * self.w.ring + (2 if self.ua.fused else 6)
+        # scan, fwd 1, preprocess 1 (+ dsink 1), dK/dV 1, dQ 1; the fused
+        # step adds the k/v exchange for the forward (2), the explicit one
+        # relayout qkv 1, O 1, dO 1, dQ/dK/dV 3
+        return scan + 4 + sink + extra + (2 if self.ua.fused else 6)
 
     # -- end to end: host buffers in and out, through the C ABI
     def make_host_io(self):
