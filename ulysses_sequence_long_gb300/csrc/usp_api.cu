@@ -105,17 +105,17 @@ int make_ds_tmap(CUtensorMap* m, const void* base, long long n_blocks) {
   return rc == CUDA_SUCCESS ? USP_OK : USP_ERR_CUDA;
 }
 
-// The same blocks as store targets of one compute warp: box {32, 32, 1} (32
-// query columns of 32 key rows, 64-byte rows), 64-byte swizzle.
+// The same blocks as store targets of one compute warp: box {64, 32, 1} (the
+// 64 query columns of 32 key rows, 128-byte rows), 128-byte swizzle.
 int make_ds_store_tmap(CUtensorMap* m, void* base, long long n_blocks) {
   auto fn = encode_fn();
   if (fn == nullptr) return USP_ERR_CUDA;
   cuuint64_t dims[3] = {64, 128, static_cast<cuuint64_t>(n_blocks)};
   cuuint64_t strides[2] = {128, 128 * 128};
-  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t box[3] = {64, 32, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult rc = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return rc == CUDA_SUCCESS ? USP_OK : USP_ERR_CUDA;
 }

@@ -13,18 +13,22 @@
 //   preprocess  D_t and -LSE_t*log2(e) for every (rank, query head, token), in a
 //               planar fp32 workspace [P*hq][2][B*S padded to 4]; then the sink
 //               gradients (one block per head, fixed-order tree reduction).
-//   dK/dV       CTA = (rank, kv head, 128 keys).  K and V live in TMEM for the
-//               whole CTA and serve as the A operands of S^T = K Q^T and
-//               dP^T = V dO^T; query slices (64 at D=128, 128 at D=64) of Q, dO and their statistics
-//               stream through shared memory; P^T and dS^T (bf16) are written
-//               over S^T / dP^T and feed dV += P^T dO, dK += dS^T Q.
+//   dK/dV       CTA = (rank, kv head, 128 keys).  K and V stay resident for
+//               the whole CTA (TMEM at D=64, shared memory at D=128) as the A
+//               operands of S^T = K Q^T and dP^T = V dO^T; 128-query slices of
+//               Q, dO and their statistics stream through shared memory; P^T
+//               and dS^T (bf16) are written over S^T / dP^T and feed
+//               dV += P^T dO, dK += dS^T Q.
 //   dQ          CTA = (rank, query head, 128 rows).  Q and dO live in TMEM as
 //               the A operands of S = Q K^T and dP = dO V^T; 128-key tiles of
 //               K and V stream through shared memory; dS (bf16 over S) feeds
 //               dQ += dS K.
-// Every MMA takes its A operand from TMEM and only its B operand from shared
-// memory: that keeps the tensor core's shared-memory reads well under the
-// SM's bandwidth, which smem x smem MMAs at these tile widths exceed.
+// The products with P^T and dS^T take their A operand from TMEM.  The dK/dV
+// scores read K (or V) from TMEM at D=64 and from shared memory at D=128,
+// where TMEM holds only the four accumulators: with N = 128 such an SS MMA
+// reads 8 KB per 128x128x16 step, about the shared-memory bandwidth of the SM
+// over the step's duration (at N = 64 the step would take as long for half the
+// work).
 // Warp roles (320 threads): warps 0-7 compute (warp w owns TMEM lanes
 // 32*(w%4)..+31), warp 8 feeds shared memory (TMA), warp 9 issues the MMAs
 // from one thread.
@@ -45,6 +49,7 @@ constexpr int kThreads = 320;
 constexpr int kSL = 64;                      // queries of a stored dS block
 constexpr int kAtomBytes = kBN * 128;        // 128-row, 128-byte-wide swizzle column
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxDynSmem = 227 * 1024;      // opt-in dynamic shared memory per CTA
 
 // index of (rank r, local head j, rank-local token t) in a [P][B][hq][S] array
 __device__ __forceinline__ size_t stat_index(const AttnArgs& p, int r, int j, int t) {
@@ -252,21 +257,26 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int atom_bytes, 
 template <int D>
 struct Cfg {
   static constexpr int NCH = D / 64;
-  // dK/dV query slice: 64 queries at D=128 (TMEM holds S^T, dP^T, dV, dK, K,
-  // V in its 512 columns only so), 128 at D=64 (twice the work per hand-off)
-  static constexpr int SL = (D == 64) ? 128 : 64;
+  // dK/dV: 128-query slices.  At D=128 TMEM holds only the four 128-column
+  // accumulators S^T, dP^T, dV, dK, so K and V sit in shared memory as the A
+  // operands of S^T and dP^T; at D=64 they fit into TMEM beside them.
+  static constexpr bool KV_SMEM = D == 128;
+  static constexpr int SL = 128;
   static constexpr int SLB = SL * 128;            // one 64-column swizzle atom of a slice
   static constexpr int SLICE = NCH * SLB;         // SL-row bf16 tile
   static constexpr int STAT = 2 * SL * 4;         // [2][SL] fp32: -LSE*log2e, D
-  static constexpr int NST = 5;                   // stages of the streamed slices
-  // dK/dV: ring of (Q, dO, stats) slices, then two 2 KB dS staging buffers
-  // per compute warp (a [32 keys][32 queries] part of a dS block)
-  static constexpr int A_Q = 0;
+  static constexpr int NST = KV_SMEM ? 2 : 5;     // stages of the streamed slices
+  static constexpr int STG = 32 * (SL / 2) * 2;   // a compute warp's [32 keys][64 queries] dS part
+  // dK/dV: K and V tiles (KV_SMEM), rings of Q and dO slices and statistics,
+  // one dS staging buffer per compute warp
+  static constexpr int A_KV = 0;
+  static constexpr int A_Q = KV_SMEM ? 2 * NCH * kBN * 128 : 0;
   static constexpr int A_DO = A_Q + NST * SLICE;
   static constexpr int A_STAT = A_DO + NST * SLICE;
   static constexpr int A_DS = (A_STAT + NST * STAT + 1023) / 1024 * 1024;
-  static constexpr int A_BAR = A_DS + 8 * 2 * 2048;
-  static constexpr int A_SMEM = A_BAR + 1024 + 1024;
+  static constexpr int A_BAR = A_DS + 8 * STG;
+  static constexpr int A_NEED = A_BAR + 256;      // bytes used past the 1024-aligned base
+  static constexpr int A_SMEM = A_NEED + 1024 < kMaxDynSmem ? A_NEED + 1024 : kMaxDynSmem;
   // dQ: ring of (K, V) 128-key tiles
   static constexpr int TILE = NCH * kBN * 128;       // 128-row bf16 tile
   static constexpr int KST = (D == 128) ? 3 : 6;
@@ -277,14 +287,15 @@ struct Cfg {
 };
 
 struct BarsA {
-  uint64_t kv_ready;  // K, V rows stored into TMEM by the compute warps
-  uint64_t qdo_full[8];
-  uint64_t qdo_empty[8];
+  uint64_t kv_ready;  // K, V in place (TMEM rows from the compute warps, or the TMA tiles)
+  uint64_t q_full[5], q_empty[5], do_full[5], do_empty[5];
   uint64_t st_full, dpt_full, p_full, ds_full;
   uint64_t fin, mma_done;
   uint32_t tmem;
   int abort;
 };
+static_assert(sizeof(BarsA) <= 256, "dK/dV barrier block");
+static_assert(Cfg<128>::A_NEED <= kMaxDynSmem && Cfg<64>::A_NEED + 1024 <= kMaxDynSmem, "dK/dV shared memory");
 
 struct BarsB {
   uint64_t qd_ready;  // Q, dO rows stored into TMEM by the compute warps
@@ -336,21 +347,33 @@ struct Grads {
 };
 
 // --------------------------------------------------------------- dK / dV
-// TMEM: S^T [0,64)  dP^T [64,128)  dV [128,128+D)  dK [128+D,128+2D)
-//       K [128+2D, 128+2D+D/2)  V [128+2D+D/2, 128+3D)        (D=128: 512 columns)
+// TMEM: S^T [0,128)  dP^T [128,256)  dV [256,256+D)  dK [256+D,256+2D), and at
+//       D=64 K [384,416)  V [416,448) as packed A operands (D=128: K and V are
+//       128-key tiles in shared memory, the A operands of SS MMAs).
 // Compute warps w: TMEM lanes 32*(w%4).. = key rows; group g = w/4 takes query
-// columns [32g, 32g+32) of every slice and writes its 16 packed columns of
-// P^T / dS^T at column offset 32g (columns it has read itself).
+// columns [64g, 64g+64) of every slice (one stored 64-query dS block) and
+// writes its 32 packed columns of P^T / dS^T at column 64g (columns it has
+// read itself).
+// Q and dO slices stream through separate rings: dO_i is free once dV_i has
+// read it, Q_i (with its statistics) once dK_i has.  The MMA thread issues, per
+// slice i:  [P^T_i] dV_i, S^T_{i+1}  [dS^T_i] dK_i, dP^T_{i+1}  (brackets: the
+// compute warps' hand-offs), so the tensor core works on the next slice's
+// scores while the compute warps turn the current one into P^T and dS^T.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
-                const __grid_constant__ CUtensorMap tst, const __grid_constant__ CUtensorMap tds_st, AttnArgs p,
+                const __grid_constant__ CUtensorMap tst, const __grid_constant__ CUtensorMap tds_st,
+                const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, AttnArgs p,
                 Grads g) {
   using C = Cfg<D>;
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  BarsA* bars = reinterpret_cast<BarsA*>(smem + C::A_BAR);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (static_cast<int>(smem - smem_raw) > C::A_SMEM - C::A_NEED) {  // the launch's bytes cannot hold the layout
+    if (tid == 0) set_status(p.status, USP_ERR_CUDA);
+    return;
+  }
+  BarsA* bars = reinterpret_cast<BarsA*>(smem + C::A_BAR);
 
   // key tiles in order (early keys of a causal document see the most queries).
   // A CTA owns one key/value head: in head-layout the local head kl of rank r
@@ -378,10 +401,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     qhi = min(qhi, rq1);
   }
   // statistics slices are fetched by TMA from 16-byte aligned tokens; with the
-  // exchanges fused, 64-token slices must also stay inside one rank's shard.
-  // When dS is stored, whole 128-row query tiles are covered (their extra rows
-  // are masked, so their blocks hold zeros): the dQ pass then finds a block
-  // for every (key tile, query tile) pair it meets.
+  // exchanges fused, slices must also stay inside one rank's shard.  When dS
+  // is stored, whole 128-row query tiles are covered (their extra rows are
+  // masked, so their blocks hold zeros): the dQ pass then finds a block for
+  // every (key tile, query tile) pair it meets.
   const bool store_ds = g.ds != nullptr;
   if (store_ds) {
     qlo &= ~(kBM - 1);
@@ -397,10 +420,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long ds_off0 = store_ds ? ds_off(g.dsg, ds_kt) : 0;
 
   if (tid == 0) {
-    mbar_init(&bars->kv_ready, 8);
+    mbar_init(&bars->kv_ready, C::KV_SMEM ? 1 : 8);
     for (int s = 0; s < C::NST; ++s) {
-      mbar_init(&bars->qdo_full[s], 1);
-      mbar_init(&bars->qdo_empty[s], 1);
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1);
+      mbar_init(&bars->do_full[s], 1);
+      mbar_init(&bars->do_empty[s], 1);
     }
     mbar_init(&bars->st_full, 1);
     mbar_init(&bars->dpt_full, 1);
@@ -421,9 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem;
   volatile int* abort = &bars->abort;
   const uint32_t sbase = smem_u32(smem);
-  // TMEM: S^T [0,SL) dP^T [SL,2SL) dV, dK (D each) K, V (D/2 packed each): 512 columns at D=128, 448 at D=64
   constexpr uint32_t T_S = 0, T_DP = C::SL, T_DV = 2 * C::SL, T_DK = T_DV + D, T_K = T_DK + D, T_V = T_K + D / 2;
-  static_assert(T_V + D / 2 <= 512, "TMEM columns");
+  static_assert(C::KV_SMEM ? T_K <= 512 : T_V + D / 2 <= 512, "TMEM columns");
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
@@ -431,85 +455,106 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tq);
       prefetch_tmap(&tdo);
       prefetch_tmap(&tst);
+      if (C::KV_SMEM && n_it > 0) {
+        mbar_arrive_expect_tx(&bars->kv_ready, 2 * C::NCH * kAtomBytes);
+        for (int c = 0; c < C::NCH; ++c) {
+          tma_load_rows(smem + C::A_KV + c * kAtomBytes, &tk, &bars->kv_ready, p, c, kvh, u0);
+          tma_load_rows(smem + C::A_KV + (C::NCH + c) * kAtomBytes, &tv, &bars->kv_ready, p, c, kvh, u0);
+        }
+      }
       int issued = 0;
       for (int i = 0; i < n_it; ++i) {
         const int s = i % C::NST;
-        if (i >= C::NST && !mbar_wait(&bars->qdo_empty[s], ((i / C::NST) - 1) & 1, abort, p.status)) break;
+        const uint32_t pe = ((i / C::NST) - 1) & 1;
+        if (i >= C::NST && (!mbar_wait(&bars->q_empty[s], pe, abort, p.status) ||
+                            !mbar_wait(&bars->do_empty[s], pe, abort, p.status)))
+          break;
         const int hg = hg0 + i / n_q;
         const HeadRef qh{hg / p.hq, hg % p.hq, hg};
         const int q0 = qlo + (i % n_q) * C::SL;
-        mbar_arrive_expect_tx(&bars->qdo_full[s], 2 * C::SLICE + C::STAT);
-        for (int c = 0; c < C::NCH; ++c) {
-          tma_load_rows(smem + C::A_Q + s * C::SLICE + c * C::SLB, &tq, &bars->qdo_full[s], p, c, qh, q0);
-          tma_load_rows(smem + C::A_DO + s * C::SLICE + c * C::SLB, &tdo, &bars->qdo_full[s], p, c, qh, q0);
-        }
-        tma_load_3d(smem + C::A_STAT + s * C::STAT, &tst, &bars->qdo_full[s], q0, 0, hg);
+        mbar_arrive_expect_tx(&bars->q_full[s], C::SLICE + C::STAT);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_rows(smem + C::A_Q + s * C::SLICE + c * C::SLB, &tq, &bars->q_full[s], p, c, qh, q0);
+        tma_load_3d(smem + C::A_STAT + s * C::STAT, &tst, &bars->q_full[s], q0, 0, hg);
+        mbar_arrive_expect_tx(&bars->do_full[s], C::SLICE);
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_rows(smem + C::A_DO + s * C::SLICE + c * C::SLB, &tdo, &bars->do_full[s], p, c, qh, q0);
         issued = i + 1;
       }
-      for (int i = max(0, issued - C::NST); i < issued; ++i)
-        mbar_wait(&bars->qdo_full[i % C::NST], (i / C::NST) & 1, abort, p.status);
+      // never leave the CTA with copies still landing in its shared memory
+      if (C::KV_SMEM && n_it > 0) mbar_wait(&bars->kv_ready, 0, abort, p.status);
+      for (int i = max(0, issued - C::NST); i < issued; ++i) {
+        mbar_wait(&bars->q_full[i % C::NST], (i / C::NST) & 1, abort, p.status);
+        mbar_wait(&bars->do_full[i % C::NST], (i / C::NST) & 1, abort, p.status);
+      }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(kBN, C::SL, false, false);  // [128 keys x SL queries], K = D
       constexpr uint32_t id_g = idesc_bf16(kBN, D, false, true);       // [128 keys x D], K = SL queries
-      // S^T_i = K Q_i^T.  Slot i has landed: the compute warps wait for it
-      // before handing in P of iteration i-1 (each barrier wait of this
-      // thread stalls the tensor core, so it keeps only the hand-offs).
-      auto issue_st = [&](int i) -> bool {
-        const int s = i % C::NST;
-        const uint32_t qa = sbase + C::A_Q + s * C::SLICE;
+      // S^T_i = K Q_i^T and dP^T_i = V dO_i^T (their slices have landed)
+      auto issue_scores = [&](uint32_t t_out, uint32_t kv_t, uint32_t kv_s, uint32_t slice, uint64_t* done) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts(tmem + T_S, tmem + T_K + kk * 8, kmajor_desc(qa, C::SLB, kk), id_s, kk > 0);
-        mma_commit(&bars->st_full);
-        return true;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          if constexpr (C::KV_SMEM)
+            mma_ss(tmem + t_out, kmajor_desc(kv_s, kAtomBytes, kk), kmajor_desc(slice, C::SLB, kk), id_s, kk > 0);
+          else
+            mma_ts(tmem + t_out, tmem + kv_t + kk * 8, kmajor_desc(slice, C::SLB, kk), id_s, kk > 0);
+        }
+        mma_commit(done);
       };
-      auto issue_dpt = [&](int i) {  // dP^T_i = V dO_i^T (its slice has landed: issue_st waited)
-        const uint32_t da = sbase + C::A_DO + (i % C::NST) * C::SLICE;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts(tmem + T_DP, tmem + T_V + kk * 8, kmajor_desc(da, C::SLB, kk), id_s, kk > 0);
-        mma_commit(&bars->dpt_full);
-      };
+      const uint32_t k_s = sbase + C::A_KV, v_s = k_s + C::NCH * kAtomBytes;
+      auto q_slot = [&](int i) { return sbase + C::A_Q + (i % C::NST) * C::SLICE; };
+      auto do_slot = [&](int i) { return sbase + C::A_DO + (i % C::NST) * C::SLICE; };
       // A operand columns of a packed slice: compute group g packs its SL/2
       // queries into the SL/4 columns at g*SL/2 (K step kk: 16 queries, 8 columns)
       auto acol = [](int kk) -> uint32_t {
         constexpr int per = C::SL / 32;  // K steps per group
         return static_cast<uint32_t>((kk / per) * (C::SL / 2) + (kk % per) * 8);
       };
-      bool ok = mbar_wait(&bars->kv_ready, 0, abort, p.status);
-      if (ok && n_it > 0 && (ok = mbar_wait(&bars->qdo_full[0], 0, abort, p.status))) {
+      bool ok = n_it == 0 || mbar_wait(&bars->kv_ready, 0, abort, p.status);
+      if (ok && n_it > 0 && (ok = mbar_wait(&bars->q_full[0], 0, abort, p.status))) {
         tc_fence_after();
-        issue_st(0);
-        issue_dpt(0);
+        issue_scores(T_S, T_K, k_s, q_slot(0), &bars->st_full);
+        if ((ok = mbar_wait(&bars->do_full[0], 0, abort, p.status))) {
+          tc_fence_after();
+          issue_scores(T_DP, T_V, v_s, do_slot(0), &bars->dpt_full);
+        }
       }
       for (int i = 0; i < n_it && ok; ++i) {
         const int s = i % C::NST;
-        const uint32_t ph = i & 1;
-        const uint32_t da = sbase + C::A_DO + s * C::SLICE, qa = sbase + C::A_Q + s * C::SLICE;
-        // dV += P^T_i dO_i
+        const uint32_t ph = i & 1, pn = ((i + 1) / C::NST) & 1;
+        const bool more = i + 1 < n_it;
+        // dV += P^T_i dO_i; then dO_i's slot is free
         if (!(ok = mbar_wait(&bars->p_full, ph, abort, p.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::SL / 16; ++kk)
-          mma_ts(tmem + T_DV, tmem + T_S + acol(kk), mnmajor_desc(da, C::SLB, kk), id_g,
+          mma_ts(tmem + T_DV, tmem + T_S + acol(kk), mnmajor_desc(do_slot(i), C::SLB, kk), id_g,
                  (i > 0 || kk > 0) ? 1u : 0u);
-        const bool more = i + 1 < n_it;
-        if (more && !(ok = issue_st(i + 1))) break;  // S^T region is free once dV has read P^T
-        // dK += dS^T_i Q_i
+        mma_commit(&bars->do_empty[s]);
+        // S^T_{i+1}: the S^T columns are free once dV_i has read P^T_i (in order)
+        if (more) {
+          if (!(ok = mbar_wait(&bars->q_full[(i + 1) % C::NST], pn, abort, p.status))) break;
+          tc_fence_after();
+          issue_scores(T_S, T_K, k_s, q_slot(i + 1), &bars->st_full);
+        }
+        // dK += dS^T_i Q_i; then Q_i's slot (and its statistics) is free
         if (!(ok = mbar_wait(&bars->ds_full, ph, abort, p.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::SL / 16; ++kk)
-          mma_ts(tmem + T_DK, tmem + T_DP + acol(kk), mnmajor_desc(qa, C::SLB, kk), id_g,
+          mma_ts(tmem + T_DK, tmem + T_DP + acol(kk), mnmajor_desc(q_slot(i), C::SLB, kk), id_g,
                  (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars->qdo_empty[s]);
-        if (more)
-          issue_dpt(i + 1);
-        else
+        mma_commit(&bars->q_empty[s]);
+        if (more) {
+          if (!(ok = mbar_wait(&bars->do_full[(i + 1) % C::NST], pn, abort, p.status))) break;
+          tc_fence_after();
+          issue_scores(T_DP, T_V, v_s, do_slot(i + 1), &bars->dpt_full);
+        } else {
           mma_commit(&bars->fin);
+        }
       }
       mma_commit(&bars->mma_done);
       mbar_wait(&bars->mma_done, 0, abort, p.status);
@@ -527,8 +572,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int vlo, vhi;     // the rows that see this key
     visible_rows(u, a, b, p.causal, p.window_left, key_ok, vlo, vhi);
     const uint32_t lb = tmem + ((static_cast<uint32_t>(warp & 3) * 32) << 16);
-    // K (group 0) or V (group 1) row of this key into TMEM
-    {
+    if constexpr (!C::KV_SMEM) {
+      // K (group 0) or V (group 1) row of this key into TMEM
       const size_t off = row_offset(p, kvh, p.hk, p.Hkv, key_ok ? u : 0, D);
       row_to_tmem<D>(lb + (grp == 0 ? T_K : T_V), (grp == 0 ? g.k : g.v) + off, key_ok);
       tc_fence_before();
@@ -540,17 +585,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // columns the group has already read.
     constexpr int NCK = C::SL / 64;
     const int gc = grp * (C::SL / 2);
-    bool ok = n_it == 0 || mbar_wait(&bars->qdo_full[0], 0, abort, p.status);
-    int ds_slot = 0;  // dS blocks this warp has staged
+    uint8_t* stg = smem + C::A_DS + warp * C::STG;  // this warp's dS staging buffer
+    bool ok = true, staged = false;
     for (int i = 0; i < n_it && ok; ++i) {
       const int s = i % C::NST;
       const uint32_t ph = i & 1;
       const int q0 = qlo + (i % n_q) * C::SL + gc;  // first query column of this group
-      // the next slot lands before P of this iteration is handed in: the MMA
-      // thread issues S^T of the next iteration on that hand-off alone
-      if (i + 1 < n_it &&
-          !(ok = mbar_wait(&bars->qdo_full[(i + 1) % C::NST], ((i + 1) / C::NST) & 1, abort, p.status)))
-        break;
+      // the statistics came with Q_i: observing its barrier makes them visible
+      if (!(ok = mbar_wait(&bars->q_full[s], (i / C::NST) & 1, abort, p.status))) break;
       const float* st = reinterpret_cast<const float*>(smem + C::A_STAT + s * C::STAT) + gc;
       if (!(ok = mbar_wait(&bars->st_full, ph, abort, p.status))) break;
       tc_fence_after();
@@ -586,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait(&bars->dpt_full, ph, abort, p.status))) break;
       tc_fence_after();
       // dS^T packed once: into TMEM for the dK MMA (first: the MMA thread
-      // waits on it), then, if dS is stored, into the staging buffers
+      // waits on it), then, if dS is stored, into the staging buffer
       uint32_t pk[NCK][16];
 #pragma unroll
       for (int c = 0; c < NCK; ++c) {
@@ -612,33 +654,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->ds_full);
       if (store_ds) {
-        // The warp's [32 key rows][32 query columns] parts of the dS^T blocks
-        // (head, row, kt, qs) of 64 queries: staged in shared memory in the
-        // 64-byte swizzle (16-byte chunk e of row r at r*64 + (e ^ (r>>1 & 3))*16:
-        // every store instruction is conflict-free), each written by one TMA
-        // store of the warp.
+        // The warp's [32 key rows][64 query columns] part of the dS^T block
+        // (head, row, kt, qs): staged in shared memory in the 128-byte swizzle
+        // (16-byte chunk e of row r at r*128 + (e ^ r%8)*16: every store
+        // instruction is conflict-free) and written by one TMA store.
         const int hg = hg0 + i / n_q;
-#pragma unroll
-        for (int c = 0; c < NCK; ++c) {
-          const int qcol = gc + 32 * c;  // column of this chunk in the slice
-          const int qs = (qlo - ds_row0) / kSL + (i % n_q) * (C::SL / kSL) + qcol / kSL;
-          const int rel = qs - 2 * ds_kt;
-          if (rel < 0 || rel >= ds_cnt) continue;
+        const int qs = (qlo - ds_row0) / kSL + (i % n_q) * (C::SL / kSL) + grp;
+        const int rel = qs - 2 * ds_kt;
+        if (rel >= 0 && rel < ds_cnt) {
           const long long blk = (static_cast<long long>(hg - p.hq0) * p.B + ds_rowb) * g.dsg.per_row + ds_off0 + rel;
-          uint8_t* buf = smem + C::A_DS + (warp * 2 + (ds_slot & 1)) * 2048;
-          if (ds_slot >= 2 && lane == 0) bulk_wait_group_read<1>();  // its store from two rounds ago has read it
+          if (staged && lane == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
           __syncwarp();
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            *reinterpret_cast<uint4*>(buf + lane * 64 + ((e ^ ((lane >> 1) & 3)) << 4)) =
-                make_uint4(pk[c][4 * e], pk[c][4 * e + 1], pk[c][4 * e + 2], pk[c][4 * e + 3]);
+          for (int e = 0; e < 8; ++e)
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((e ^ (lane & 7)) << 4)) =
+                make_uint4(pk[e / 4][4 * (e % 4)], pk[e / 4][4 * (e % 4) + 1], pk[e / 4][4 * (e % 4) + 2],
+                           pk[e / 4][4 * (e % 4) + 3]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d(&tds_st, buf, qcol % kSL, (warp & 3) * 32, static_cast<int>(blk));
+            tma_store_3d(&tds_st, stg, 0, (warp & 3) * 32, static_cast<int>(blk));
             bulk_commit_group();
           }
-          ++ds_slot;
+          staged = true;
         }
       }
     }
@@ -653,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16* dst = (grp == 0 ? g.dv : g.dk) + row_offset(p, kvh, p.hk, p.Hkv, u, D);
       for (int e = 0; e < D; e += 8) *reinterpret_cast<uint4*>(dst + e) = make_uint4(0, 0, 0, 0);
     }
-    if (ds_slot > 0 && lane == 0) bulk_wait_group_all();  // the dS stores are complete before the CTA ends
+    if (staged && lane == 0) bulk_wait_group_all();  // the dS stores are complete before the CTA ends
   }
 
   tc_fence_before();
@@ -1208,14 +1246,20 @@ static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const v
     if ((rc = make_rows_tmap(&tq, q, a, a.hq, a.Hq, D, C::SL)) != USP_OK) return rc;
     if ((rc = make_rows_tmap(&tdo, dO, a, a.hq, a.Hq, D, C::SL)) != USP_OK) return rc;
     if ((rc = make_stats_tmap(&tst, stats, a.BS, g.bsp, a.P * a.hq, C::SL)) != USP_OK) return rc;
-    CUtensorMap tds_st;
+    CUtensorMap tds_st, tk, tv;
     memset(&tds_st, 0, sizeof(tds_st));  // unused unless dS is stored
+    memset(&tk, 0, sizeof(tk));          // unused unless K, V are shared-memory tiles
+    memset(&tv, 0, sizeof(tv));
     if (ds != nullptr && (rc = make_ds_store_tmap(&tds_st, ds, ds_blocks)) != USP_OK) return rc;
+    if (C::KV_SMEM) {
+      if ((rc = make_rows_tmap(&tk, k, a, a.hk, a.Hkv, D, kBN)) != USP_OK) return rc;
+      if ((rc = make_rows_tmap(&tv, v, a, a.hk, a.Hkv, D, kBN)) != USP_OK) return rc;
+    }
     if (cudaFuncSetAttribute(bwd::dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::A_SMEM) !=
         cudaSuccess)
       return USP_ERR_CUDA;
     const unsigned grid = static_cast<unsigned>(g.n_tiles) * (a.seq_io ? a.n_kvh : a.P * a.hk);
-    bwd::dkdv_kernel<D><<<grid, bwd::kThreads, C::A_SMEM, st>>>(tq, tdo, tst, tds_st, a, g);
+    bwd::dkdv_kernel<D><<<grid, bwd::kThreads, C::A_SMEM, st>>>(tq, tdo, tst, tds_st, tk, tv, a, g);
   } else {
     // 128-key tiles of K and V stream past TMEM-resident Q, dO
     CUtensorMap tk, tv;
