@@ -61,6 +61,15 @@ SMALL = [
     W.Workload("kv_rep_d64", B=1, S=512, Hq=8, Hkv=2, D=64, P=4, doc_mode="explicit", doc_lens=(200, 180, 132)),
     W.Workload("mqa_rep_win_sink_d128", B=1, S=1024, Hq=8, Hkv=1, D=128, P=8, window_left=150, sinks=True,
                doc_mode="explicit", doc_lens=(300, 1, 400, 323)),
+    # short causal windows at D=64 (the persistent schedule over a group's heads):
+    # an odd group size, a replicated key/value head at window 128, window 0 with
+    # a ragged batch of rows that are not a multiple of 128 tokens
+    W.Workload("win_d64_odd_group", B=1, S=1024, Hq=12, Hkv=4, D=64, P=4, window_left=100, sinks=True,
+               doc_mode="geometric", doc_mean=300, seed=7),
+    W.Workload("win_d64_rep_w128", B=2, S=512, Hq=8, Hkv=2, D=64, P=4, window_left=128,
+               doc_mode="geometric", doc_mean=150, seed=9),
+    W.Workload("win_d64_w0_ragged", B=3, S=200, Hq=4, Hkv=2, D=64, P=2, window_left=0, sinks=True,
+               doc_mode="geometric", doc_mean=60, seed=13),
 ]
 
 

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libusp.so")
-SOURCES = ["usp_api.cu", "usp_bandwidth.cu", "usp_attn_fwd.cu", "usp_attn_bwd.cu", "usp_noalloc.cu", "usp_ring.cu"]
+SOURCES = ["usp_api.cu", "usp_bandwidth.cu", "usp_attn_fwd.cu", "usp_attn_fwd_window.cu", "usp_attn_bwd.cu", "usp_noalloc.cu", "usp_ring.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]

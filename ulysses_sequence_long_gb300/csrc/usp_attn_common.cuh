@@ -103,6 +103,20 @@ __device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* m, u
   tma_load_rows(dst, m, bar, p, c64, h, t, p.seq_io != 0);
 }
 
+// TMA store of a tile staged in shared memory (fenced by the caller) to the
+// rows starting at rank-local token t of head h, same addressing as the loads;
+// rows past the tensor's end are dropped by the copy.
+__device__ __forceinline__ void tma_store_rows(const CUtensorMap* m, const void* src, const AttnArgs& p, int c64,
+                                               HeadRef h, int t) {
+  if (!p.seq_io) {
+    tma_store_4d(m, src, c64 * 64, h.j, t, h.r);
+  } else {
+    const int b = t / p.S, s = t - b * p.S;
+    const int rp = s / p.Sl, sp = s - rp * p.Sl;
+    tma_store_5d(m, src, c64 * 64, h.g, sp, b, rp);
+  }
+}
+
 // Document index d with cu[d] <= t < cu[d+1] (cu assumed valid, n >= 1).
 __device__ __forceinline__ int find_doc(const int32_t* __restrict__ cu, int n, int t) {
   int lo = 0, hi = n;  // invariant: cu[lo] <= t < cu[hi]
@@ -235,6 +249,12 @@ inline int make_rows_tmap(CUtensorMap* m, const void* base, const AttnArgs& a, i
 inline int make_rows_tmap(CUtensorMap* m, const void* base, const AttnArgs& a, int hpr, int H, int D, int box_rows) {
   return make_rows_tmap(m, base, a, hpr, H, D, box_rows, a.seq_io != 0);
 }
+
+// Forward for short causal windows at D = 64 (usp_attn_fwd_window.cu): whether
+// the shape qualifies, and the launch with the general forward's tensor maps.
+bool fwd_window_fits(const AttnArgs& a, int D);
+int run_fwd_window(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, void* o,
+                   float* lse, cudaStream_t st);
 
 int make_ds_tmap(CUtensorMap* m, const void* base, long long n_blocks);
 int make_ds_store_tmap(CUtensorMap* m, void* base, long long n_blocks);

@@ -424,9 +424,11 @@ static int run_fwd(const AttnArgs& a, const void* q, const void* k, const void* 
   if ((rc = make_rows_tmap(&tq, q, a, a.hq, a.Hq, D, kBM)) != USP_OK) return rc;
   if ((rc = make_rows_tmap(&tk, k, a, a.hk, a.Hkv, D, kBN, a.kv_seq_io != 0)) != USP_OK) return rc;
   if ((rc = make_rows_tmap(&tv, v, a, a.hk, a.Hkv, D, kBN, a.kv_seq_io != 0)) != USP_OK) return rc;
-  // One Q tile per CTA when each row sees few key tiles (a short window at
-  // D = 64: the two tiles of a CTA would share little, and two small CTAs
-  // per SM overlap each other's set-up and latencies instead).
+  // Short causal windows at D = 64: the persistent schedule over the heads of
+  // a key/value group.  Other short windows at D = 64: one Q tile per CTA (the
+  // two tiles of a CTA would share little, and two small CTAs per SM overlap
+  // each other's set-up and latencies instead).
+  if (fwd_window_fits(a, D)) return run_fwd_window(a, tq, tk, tv, o, lse, st);
   const bool one = D == 64 && a.window_left >= 0 && a.window_left < 4 * kBN;
   return one ? run_fwd<D, 1>(a, tq, tk, tv, o, lse, st) : run_fwd<D, 2>(a, tq, tk, tv, o, lse, st);
 }
