@@ -597,9 +597,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait(&bars->st_full, ph, abort, p.status))) break;
       tc_fence_after();
       const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+      // bit c: some key row of this warp sees a query of chunk c; the other
+      // chunks have P = dS = 0 and skip their loads and exponentials
+      uint32_t vis = 0;
+#pragma unroll
+      for (int c = 0; c < NCK; ++c) {
+        const int c_lo = vlo - (q0 + 32 * c), c_hi = vhi - (q0 + 32 * c);
+        vis |= (__any_sync(0xffffffffu, c_lo <= c_hi && c_hi >= 0 && c_lo <= 31) ? 1u : 0u) << c;
+      }
       float pr[NCK][32];
 #pragma unroll
       for (int c = 0; c < NCK; ++c) {
+        if (!(vis >> c & 1u)) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pr[c][e] = 0.f;
+          tmem_st_packed<16>(lb + T_S + gc + 16 * c, pr[c]);
+          continue;
+        }
         float x[32];
         tmem_ld_cols<32>(lb + T_S + gc + 32 * c, x);
         // only chunks that straddle a document, diagonal or window edge pay
@@ -632,6 +646,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pk[NCK][16];
 #pragma unroll
       for (int c = 0; c < NCK; ++c) {
+        if (!(vis >> c & 1u)) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk[c][e] = 0u;
+          tmem_st16(lb + T_DP + gc + 16 * c, pk[c]);
+          continue;
+        }
         float x[32];
         tmem_ld_cols<32>(lb + T_DP + gc + 32 * c, x);
 #pragma unroll

@@ -70,7 +70,7 @@ struct Bars {
   uint64_t mma_done;
   uint64_t k_full[4];
   uint64_t v_full[4];
-  uint64_t kv_empty[4];
+  uint64_t k_empty[4], v_empty[4];  // K stage free once its S MMAs are done, V once its PV MMAs are
   uint32_t tmem;
   int abort;
 };
@@ -155,7 +155,8 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
     for (int s = 0; s < C::ST; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     bars->abort = 0;
     fence_barrier_init();
@@ -183,26 +184,31 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
         for (int c = 0; c < C::NCH; ++c)
           tma_load_rows(smem + C::OFF_Q + q * C::TILE + c * kAtomBytes, &tq, &bars->q_full[q], p, c, qh, t0 + q * kBM);
       }
-      int issued = 0;
+      int issued = 0, k_issued = 0;  // tiles whose V (and K) loads were issued
+      bool kv_ok = true;
       for (int n = 0; n < n_kv; ++n) {
         const int st = n % C::ST;
-        if (n >= C::ST && !mbar_wait(&bars->kv_empty[st], ((n / C::ST) - 1) & 1, abort, p.status)) break;
         const int kv0 = lo + n * kBN;
-        mbar_arrive_expect_tx(&bars->k_full[st], C::TILE);
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_rows(smem + C::OFF_K + st * C::TILE + c * kAtomBytes, &tk, &bars->k_full[st], p, c, kvh, kv0,
-                        p.kv_seq_io != 0);
-        mbar_arrive_expect_tx(&bars->v_full[st], C::TILE);
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_rows(smem + C::OFF_V + st * C::TILE + c * kAtomBytes, &tv, &bars->v_full[st], p, c, kvh, kv0,
-                        p.kv_seq_io != 0);
+        // K_n, then V_n, each as soon as its stage has been released (K one
+        // step before V: S of a tile is issued a step before its PV)
+        for (int kv = 0; kv < 2; ++kv) {
+          uint64_t* full = kv == 0 ? &bars->k_full[st] : &bars->v_full[st];
+          uint64_t* empty = kv == 0 ? &bars->k_empty[st] : &bars->v_empty[st];
+          uint8_t* dst = smem + (kv == 0 ? C::OFF_K : C::OFF_V) + st * C::TILE;
+          const CUtensorMap* m = kv == 0 ? &tk : &tv;
+          if (n >= C::ST && !(kv_ok = mbar_wait(empty, ((n / C::ST) - 1) & 1, abort, p.status))) break;
+          mbar_arrive_expect_tx(full, C::TILE);
+          for (int c = 0; c < C::NCH; ++c) tma_load_rows(dst + c * kAtomBytes, m, full, p, c, kvh, kv0, p.kv_seq_io != 0);
+          if (kv == 0) k_issued = n + 1;
+        }
+        if (!kv_ok) break;
         issued = n + 1;
       }
       // Never leave the CTA with copies still landing in its shared memory.
-      for (int n = max(0, issued - C::ST); n < issued; ++n) {
+      for (int n = max(0, k_issued - C::ST); n < k_issued; ++n)
         mbar_wait(&bars->k_full[n % C::ST], (n / C::ST) & 1, abort, p.status);
+      for (int n = max(0, issued - C::ST); n < issued; ++n)
         mbar_wait(&bars->v_full[n % C::ST], (n / C::ST) & 1, abort, p.status);
-      }
       for (int q = 0; q < NQT; ++q)
         if (tile_ok[q]) mbar_wait(&bars->q_full[q], 0, abort, p.status);
     }
@@ -224,6 +230,11 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
           mma_ss(tmem + q * kBN, sdesc_add(qd, off), sdesc_add(kd, off), idesc_s, kk > 0);
         }
       };
+      // A stage is released once the MMAs issued so far are done; only
+      // stages that will be refilled need it.
+      auto release = [&](uint64_t* empty, bool refilled) {
+        if (refilled) mma_commit(empty);
+      };
       auto issue_pv = [&](int q, int st, bool acc) {
         const uint64_t vd = sdesc_sw128(sbase + C::OFF_V + st * C::TILE, kAtomBytes, 1024);
 #pragma unroll
@@ -239,6 +250,7 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
             issue_s(q, 0);
             mma_commit(&bars->s_full[q]);
           }
+        release(&bars->k_empty[0], C::ST < n_kv);
       }
       for (int n = 0; n < n_kv && ok; ++n) {
         const int st = n % C::ST;
@@ -262,7 +274,8 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
             mma_commit(&bars->o_final[q]);
           }
         }
-        mma_commit(&bars->kv_empty[st]);
+        if (ok && n + 1 < n_kv) release(&bars->k_empty[(n + 1) % C::ST], n + 1 + C::ST < n_kv);
+        release(&bars->v_empty[st], n + C::ST < n_kv);
       }
       // Every MMA issued above has finished before TMEM can be released.
       mma_commit(&bars->mma_done);
