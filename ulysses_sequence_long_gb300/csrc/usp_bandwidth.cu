@@ -366,14 +366,16 @@ __device__ __forceinline__ uint32_t warp_flags(const int32_t* __restrict__ pos, 
         rem = g0 % g.S;
       }
     }
-    // the next row start at or after g0 is g0 + (S - rem) % S
+    // the next row start at or after g0 is g0 + (S - rem) % S; with rows of
+    // 4 or more positions it is the only one among these four
     const int to_row = rem == 0 ? 0 : g.S - rem;
+    const bool long_rows = g.S >= 4;
     uint32_t nib = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const bool in = g0 + e < g.total;
       negative |= in && v[k][e] < 0;
-      const bool row = (e >= to_row) && ((e - to_row) % g.S == 0);
+      const bool row = long_rows ? e == to_row : (e >= to_row) && ((e - to_row) % g.S == 0);
       if (in && (v[k][e] == 0 || row)) nib |= 1u << e;
     }
     uint32_t w = nib << (4 * (lane & 7));
