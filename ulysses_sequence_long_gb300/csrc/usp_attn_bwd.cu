@@ -65,42 +65,43 @@ __device__ __forceinline__ size_t plane_index(int bsp, int hq, int r, int j, int
 }
 
 // --------------------------------------------------------------- preprocess
-// A block takes a chunk of kPreTok consecutive tokens with every head stored
-// next to them (seq-layout: all H heads of the shard; head-layout: the hq
-// heads of one rank), so its O/dO reads are one contiguous run.  Row sums go
-// to shared memory, then each head's kPreTok statistics are written (and its
-// LSE read) as one contiguous 128-byte run.
-constexpr int kPreTok = 32;
+// A block takes a chunk of `tok` consecutive tokens (32; 16 or 8 when a short
+// sequence would leave SMs without a chunk) with every head stored next to
+// them (seq-layout: all H heads of the shard; head-layout: the hq heads of one
+// rank), so its O/dO reads are one contiguous run.  Row sums go to shared
+// memory, then each head's `tok` statistics are written (and its LSE read) as
+// one contiguous run.
+constexpr int kPreTok = 32;  // the most tokens of a chunk
 
 template <int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
                                                          const float* __restrict__ lse, float* __restrict__ stats,
-                                                         AttnArgs p, int bsp, int n_chunks) {
+                                                         AttnArgs p, int bsp, int n_chunks, int tok) {
   constexpr int LPR = D / 8;           // 16-byte lanes per row
   // passes whose loads are issued before any of them is reduced, so that
   // enough bytes are in flight (D = 64 rows are short; D = 128 keeps one)
   constexpr int kPreUnroll = D == 64 ? 4 : 1;
   constexpr int RPP = 256 / LPR;       // rows per pass of the block
-  extern __shared__ float dsum[];      // [Hb][kPreTok]
+  extern __shared__ float dsum[];      // [Hb][tok]
   const int Hb = p.seq_io ? p.P * p.hq : p.hq;
   const int tid = threadIdx.x, lane_row = tid % LPR;
-  const int nct = (p.BS + kPreTok - 1) / kPreTok;  // head-layout chunks per rank
+  const int nct = (p.BS + tok - 1) / tok;  // head-layout chunks per rank
   for (int c = blockIdx.x; c < n_chunks; c += gridDim.x) {
     // chunk -> first token t0 (rank-local, b*S + s), its rank (head-layout) and
     // the element offset of its first row
     int r0 = 0, t0, ntok;
     size_t base;
     if (p.seq_io) {
-      const int g0 = c * kPreTok;                    // token index in memory order (shard, row, position)
+      const int g0 = c * tok;                        // token index in memory order (shard, row, position)
       const int rp = g0 / (p.B * p.Sl), rem = g0 - rp * p.B * p.Sl;
       const int b = rem / p.Sl, sp = rem - b * p.Sl;
       t0 = b * p.S + rp * p.Sl + sp;
-      ntok = kPreTok;                                // S/P is a multiple of 128
+      ntok = tok;                                    // S/P is a multiple of 128
       base = static_cast<size_t>(g0) * Hb * D;
     } else {
       r0 = c / nct;
-      t0 = (c - r0 * nct) * kPreTok;
-      ntok = min(kPreTok, p.BS - t0);
+      t0 = (c - r0 * nct) * tok;
+      ntok = min(tok, p.BS - t0);
       base = (static_cast<size_t>(r0) * p.BS + t0) * Hb * D;
     }
     const int nrows = ntok * Hb;
@@ -125,12 +126,12 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict
         for (int k = 0; k < 4; ++k) acc += bf16lo(av[k]) * bf16lo(bv[k]) + bf16hi(av[k]) * bf16hi(bv[k]);
 #pragma unroll
         for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (i < nrows && lane_row == 0) dsum[(i % Hb) * kPreTok + i / Hb] = acc;
+        if (i < nrows && lane_row == 0) dsum[(i % Hb) * tok + i / Hb] = acc;
       }
     }
     __syncthreads();
-    for (int idx = tid; idx < Hb * kPreTok; idx += 256) {
-      const int h = idx / kPreTok, k = idx - h * kPreTok;
+    for (int idx = tid; idx < Hb * tok; idx += 256) {
+      const int h = idx / tok, k = idx - h * tok;
       if (k < ntok) {
         const int r = p.seq_io ? h / p.hq : r0, j = p.seq_io ? h - r * p.hq : h, t = t0 + k;
         stats[plane_index(bsp, p.hq, r, j, 0, t)] = __ldg(lse + stat_index(p, r, j, t)) * -kLog2e;
@@ -1220,14 +1221,18 @@ int launch_attn_bwd_preprocess(const usp_attn_params& prm, const void* o, const 
   float* stats = static_cast<float*>(ws);
   const int bsp = stats_row_pitch(a.BS);
   const int Hb = a.seq_io ? a.P * a.hq : a.hq;
-  const int n_chunks = a.seq_io ? a.BS / bwd::kPreTok : a.P * ((a.BS + bwd::kPreTok - 1) / bwd::kPreTok);
-  const int smem = Hb * bwd::kPreTok * static_cast<int>(sizeof(float));
+  // tokens per chunk: halved (down to 8) while there are fewer than two chunks per SM
+  auto chunks_of = [&](int tok) { return a.seq_io ? a.BS / tok : a.P * ((a.BS + tok - 1) / tok); };
+  int tok = bwd::kPreTok;
+  while (tok > 8 && chunks_of(tok) < device_sm_count() * 2) tok /= 2;
+  const int n_chunks = chunks_of(tok);
+  const int smem = Hb * tok * static_cast<int>(sizeof(float));
   int grid = n_chunks < device_sm_count() * 8 ? n_chunks : device_sm_count() * 8;
   auto kern = prm.D == 128 ? bwd::preprocess_kernel<128> : bwd::preprocess_kernel<64>;
   if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return USP_ERR_CUDA;
   kern<<<grid, 256, smem, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dO), lse, stats, a, bsp,
-                                n_chunks);
+                                n_chunks, tok);
   if (check_launch() != USP_OK) return USP_ERR_CUDA;
   if (dsinks != nullptr && a.sinks != nullptr) {
     bwd::dsink_kernel<<<a.P * a.hq, 256, 0, st>>>(stats, dsinks, a, bsp);
