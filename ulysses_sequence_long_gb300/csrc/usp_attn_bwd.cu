@@ -964,13 +964,18 @@ struct CfgDs {
   static constexpr int KT = NCH * kBN * 128;    // K tile [128 keys][D]
   static constexpr int STAGE = DSB + KT;
   static constexpr int NST = (D == 128) ? 3 : 4;
-  static constexpr int BAR = NST * STAGE;
+  static constexpr int STG = NCH * kBM * 128;   // the unit's dQ tile, staged for its TMA store
+  static constexpr int OFF_STG = NST * STAGE;
+  static constexpr int BAR = OFF_STG + STG;
   static constexpr int SMEM = BAR + 1024 + 1024;
 };
+static_assert(CfgDs<128>::SMEM <= 227 * 1024 && CfgDs<64>::SMEM <= 227 * 1024, "dQ shared memory");
 
 struct BarsDs {
   uint64_t full[4], empty[4];
   uint64_t fin[2], tfree[2];  // dQ buffer b: accumulated / read out by the epilogue
+  uint64_t stg_full;          // the 4 epilogue warps have staged the unit's dQ tile
+  uint64_t stg_free;          // its TMA store has read the staging tile
   uint64_t mma_done;
   uint32_t tmem;
   int abort;
@@ -1010,8 +1015,8 @@ __device__ __forceinline__ DsUnit ds_unit(const AttnArgs& p, const Grads& g, int
 
 template <int D>
 __global__ void __launch_bounds__(kDsThreads, 1)
-    dq_ds_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tds, AttnArgs p,
-                 Grads g, int n_units) {
+    dq_ds_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tds,
+                 const __grid_constant__ CUtensorMap tdq, AttnArgs p, Grads g, int n_units) {
   using C = CfgDs<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1030,6 +1035,8 @@ __global__ void __launch_bounds__(kDsThreads, 1)
       mbar_init(&bars->fin[b], 1);
       mbar_init(&bars->tfree[b], 4);
     }
+    mbar_init(&bars->stg_full, 4);
+    mbar_init(&bars->stg_free, 1);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_barrier_init();
@@ -1112,8 +1119,14 @@ __global__ void __launch_bounds__(kDsThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    bool ok = true;
+    // dQ rows leave through a staging tile in the 128-byte swizzle of the
+    // tensor map (16-byte chunk e of row r of a 64-column atom at
+    // r*128 + (e ^ r%8)*16, conflict-free) and one TMA store per atom, issued
+    // by thread 0 once the four warps have staged the tile: per-thread row
+    // stores would touch 32 lines per store instruction.
+    bool ok = true, stored = false;
     int ub = 0;
+    uint8_t* stg = smem + C::OFF_STG;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const DsUnit w = ds_unit(p, g, n_docs, u);
       const HeadRef qh = q_head_ref(p, w.r, w.j);
@@ -1130,12 +1143,46 @@ __global__ void __launch_bounds__(kDsThreads, 1)
       if (!(ok = mbar_wait(&bars->fin[b], (ub >> 1) & 1, abort, p.status))) break;
       tc_fence_after();
       const uint32_t lb = tmem + b * D + ((static_cast<uint32_t>(warp) * 32) << 16);
-      store_row<D>(lb, g.dq + row_offset(p, qh, p.hq, p.Hq, row_ok ? t : 0, D), p.scale, row_ok);
+      // the previous unit's store has read the staging tile
+      if (ub > 0 && !(ok = mbar_wait(&bars->stg_free, (ub - 1) & 1, abort, p.status))) break;
+      const int row = warp * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(lb + c * 32, v);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * p.scale, __uint_as_float(v[2 * e + 1]) * p.scale);
+        uint8_t* atom = stg + (c >> 1) * (kBM * 128);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4)
+          *reinterpret_cast<uint4*>(atom + row * 128 + ((((c & 1) * 4 + k4) ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
+      }
       tc_fence_before();
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->tfree[b]);
+      if (lane == 0) {
+        mbar_arrive(&bars->tfree[b]);
+        mbar_arrive(&bars->stg_full);
+      }
+      if (warp == 0 && lane == 0 && mbar_wait(&bars->stg_full, ub & 1, abort, p.status)) {
+        for (int c = 0; c < C::NCH; ++c) tma_store_rows(&tdq, stg + c * (kBM * 128), p, c, qh, w.t0);
+        bulk_commit_group();
+        stored = true;
+        bulk_wait_group_read<0>();
+        mbar_arrive(&bars->stg_free);
+      }
+      __syncwarp();
+      if (*abort) {  // a wait gave up (the whole warp leaves together)
+        ok = false;
+        break;
+      }
       ++ub;
     }
+    if (stored) bulk_wait_group_all();  // the dQ stores are complete before the CTA ends
   }
 
   tc_fence_before();
@@ -1254,15 +1301,16 @@ static int run_grad_pass(bool dq_pass, const AttnArgs& a, const void* q, const v
   if (dq_pass && ds != nullptr) {
     // dQ = dS K from the blocks the dK/dV pass stored
     using CD = bwd::CfgDs<D>;
-    CUtensorMap tk, tds;
+    CUtensorMap tk, tds, tdq;
     if ((rc = make_rows_tmap(&tk, k, a, a.hk, a.Hkv, D, kBN)) != USP_OK) return rc;
     if ((rc = make_ds_tmap(&tds, ds, ds_blocks)) != USP_OK) return rc;
+    if ((rc = make_rows_tmap(&tdq, dq, a, a.hq, a.Hq, D, kBM)) != USP_OK) return rc;
     if (cudaFuncSetAttribute(bwd::dq_ds_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, CD::SMEM) !=
         cudaSuccess)
       return USP_ERR_CUDA;
     const int n_units = g.n_tiles * a.n_qh;
     const int grid = n_units < device_sm_count() ? n_units : device_sm_count();  // persistent: one CTA per SM
-    bwd::dq_ds_kernel<D><<<grid, bwd::kDsThreads, CD::SMEM, st>>>(tk, tds, a, g, n_units);
+    bwd::dq_ds_kernel<D><<<grid, bwd::kDsThreads, CD::SMEM, st>>>(tk, tds, tdq, a, g, n_units);
     return check_launch();
   }
   if (!dq_pass) {
