@@ -71,6 +71,10 @@ SMALL = [
                doc_lens=(600, 424)),
     W.Workload("usp_r2u2_two_rows_d128", B=2, S=512, Hq=4, Hkv=2, D=128, P=4, ring=2, doc_mode="geometric",
                doc_mean=150, seed=7),
+    # a short causal window at D=64 (the persistent window forward): ring steps
+    # whose units see no key at all
+    W.Workload("usp_r2u2_win_sink_d64", B=1, S=1024, Hq=8, Hkv=2, D=64, P=4, ring=2, window_left=100,
+               sinks=True, doc_mode="explicit", doc_lens=(400, 1, 623)),
 ]
 
 
