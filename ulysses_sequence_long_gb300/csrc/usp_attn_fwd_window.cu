@@ -15,10 +15,12 @@
 //     heads of the key/value head; K/V stages are double-buffered across units
 //     so the next unit's tiles land while the current one computes;
 //   * two softmax warpgroups take the query heads in pairs (head 2i to group 0,
-//     2i+1 to group 1) and alternate on the tensor core, and each writes its
-//     own O rows while the other group's scores are computed;
+//     2i+1 to group 1) and share the tensor core;
 //   * 32-column chunks that every row of a warp has masked skip the
-//     exponentials (about half of the two tiles' columns at window 127).
+//     exponentials (about half of the two tiles' columns at window 127), and
+//     only chunks a row cuts pay for the per-element mask;
+//   * O leaves through the head's Q tile (its S MMAs are done) with one TMA
+//     store instead of per-thread row stores.
 // Warp roles (320 threads): warps 0-3 softmax group 0, 4-7 group 1 (thread =
 // query row = TMEM lane), warp 8 TMA producer, warp 9 MMA issuer (one thread).
 // TMEM: S_q [128q, 128q+128), O_q [256 + 64q, 256 + 64q + 64).
@@ -65,7 +67,7 @@ struct Unit {
   int rk0, rk1;   // ring step key window
 };
 
-__device__ __forceinline__ Unit unit_at(const AttnArgs& p, int n_docs, int n_tiles, int u) {
+__device__ __forceinline__ Unit unit_at(const AttnArgs& p, int n_docs, int u) {
   Unit w;
   const int per = p.P * p.hk;
   const int qt = u / per, rem = u - qt * per;
@@ -84,14 +86,13 @@ __device__ __forceinline__ Unit unit_at(const AttnArgs& p, int n_docs, int n_til
   if (p.kv_seq_io) lo &= ~(kBN - 1);  // tiles never straddle a sequence shard
   w.lo = lo;
   w.n_kv = hi > lo ? (hi - lo + kBN - 1) / kBN : 0;
-  (void)n_tiles;
   return w;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_window_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                            const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
-                           AttnArgs p, __nv_bfloat16* o_out, float* lse_out, int n_units, int n_tiles) {
+                           AttnArgs p, __nv_bfloat16* o_out, float* lse_out, int n_units) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + OFF_BAR);
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int gk = 0, it = 0;  // key tiles and head pairs issued (ring positions)
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const Unit w = unit_at(p, n_docs, n_tiles, u);
+        const Unit w = unit_at(p, n_docs, u);
         if (w.n_kv == 0 || w.n_kv > kMaxKV) continue;
         const HeadRef kvh = kv_head_ref(p, w.r, w.kl);
         for (int n = 0; n < w.n_kv; ++n, ++gk) {
@@ -191,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int gk = 0, it = 0, pc[2] = {0, 0};  // key tiles, head pairs, p_full phases per group
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const Unit w = unit_at(p, n_docs, n_tiles, u);
+        const Unit w = unit_at(p, n_docs, u);
         if (w.n_kv == 0) continue;
         if (w.n_kv > kMaxKV) {  // outside what this schedule holds: the host never sends such a shape
           set_status(p.status, USP_ERR_UNSUPPORTED);
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool stored = false; // this thread has issued O stores
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit w = unit_at(p, n_docs, n_tiles, u);
+      const Unit w = unit_at(p, n_docs, u);
       if (w.n_kv > kMaxKV) continue;
       const int t = w.t0 + row;
       const bool row_ok = t < p.BS;
@@ -449,7 +450,7 @@ int run_fwd_window(const AttnArgs& a, const CUtensorMap& tq, const CUtensorMap& 
   const int sms = device_sm_count();
   const int grid = n_units < sms ? n_units : sms;  // persistent: one CTA per SM
   fwdw::attn_fwd_window_kernel<<<grid, fwdw::kThreads, fwdw::SMEM, st>>>(
-      tq, tk, tv, to, a, static_cast<__nv_bfloat16*>(o), lse, n_units, n_tiles);
+      tq, tk, tv, to, a, static_cast<__nv_bfloat16*>(o), lse, n_units);
   return check_launch();
 }
 
