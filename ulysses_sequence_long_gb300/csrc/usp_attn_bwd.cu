@@ -289,7 +289,7 @@ struct Cfg {
 
 struct BarsA {
   uint64_t kv_ready;  // K, V in place (TMEM rows from the compute warps, or the TMA tiles)
-  uint64_t q_full[5], q_empty[5], do_full[5], do_empty[5];
+  uint64_t q_full[5], q_empty[5], do_full[5];  // q_empty: the slice pair (Q and dO) is free
   uint64_t st_full, dpt_full, p_full, ds_full;
   uint64_t fin, mma_done;
   uint32_t tmem;
@@ -355,8 +355,9 @@ struct Grads {
 // columns [64g, 64g+64) of every slice (one stored 64-query dS block) and
 // writes its 32 packed columns of P^T / dS^T at column 64g (columns it has
 // read itself).
-// Q and dO slices stream through separate rings: dO_i is free once dV_i has
-// read it, Q_i (with its statistics) once dK_i has.  The MMA thread issues, per
+// Q and dO slices (with the statistics) stream through a ring whose slot is
+// freed by one commit after dK_i (dV_i, which read dO_i, is done by then); the
+// MMA thread waits for the next Q slice itself.  The MMA thread issues, per
 // slice i:  [P^T_i] dV_i, S^T_{i+1}  [dS^T_i] dK_i, dP^T_{i+1}  (brackets: the
 // compute warps' hand-offs), so the tensor core works on the next slice's
 // scores while the compute warps turn the current one into P^T and dS^T.
@@ -426,7 +427,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->q_full[s], 1);
       mbar_init(&bars->q_empty[s], 1);
       mbar_init(&bars->do_full[s], 1);
-      mbar_init(&bars->do_empty[s], 1);
     }
     mbar_init(&bars->st_full, 1);
     mbar_init(&bars->dpt_full, 1);
@@ -466,10 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int i = 0; i < n_it; ++i) {
         const int s = i % C::NST;
-        const uint32_t pe = ((i / C::NST) - 1) & 1;
-        if (i >= C::NST && (!mbar_wait(&bars->q_empty[s], pe, abort, p.status) ||
-                            !mbar_wait(&bars->do_empty[s], pe, abort, p.status)))
-          break;
+        // dK_i done means dV_i is done too (in order): both slices are free
+        if (i >= C::NST && !mbar_wait(&bars->q_empty[s], ((i / C::NST) - 1) & 1, abort, p.status)) break;
         const int hg = hg0 + i / n_q;
         const HeadRef qh{hg / p.hq, hg % p.hq, hg};
         const int q0 = qlo + (i % n_q) * C::SL;
@@ -527,21 +525,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = i % C::NST;
         const uint32_t ph = i & 1, pn = ((i + 1) / C::NST) & 1;
         const bool more = i + 1 < n_it;
-        // dV += P^T_i dO_i; then dO_i's slot is free
+        // dV += P^T_i dO_i
         if (!(ok = mbar_wait(&bars->p_full, ph, abort, p.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::SL / 16; ++kk)
           mma_ts(tmem + T_DV, tmem + T_S + acol(kk), mnmajor_desc(do_slot(i), C::SLB, kk), id_g,
                  (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars->do_empty[s]);
         // S^T_{i+1}: the S^T columns are free once dV_i has read P^T_i (in order)
         if (more) {
           if (!(ok = mbar_wait(&bars->q_full[(i + 1) % C::NST], pn, abort, p.status))) break;
           tc_fence_after();
           issue_scores(T_S, T_K, k_s, q_slot(i + 1), &bars->st_full);
         }
-        // dK += dS^T_i Q_i; then Q_i's slot (and its statistics) is free
+        // dK += dS^T_i Q_i; then the slices of iteration i (Q, dO, statistics) are free
         if (!(ok = mbar_wait(&bars->ds_full, ph, abort, p.status))) break;
         tc_fence_after();
 #pragma unroll
