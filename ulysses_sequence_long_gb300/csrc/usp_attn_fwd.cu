@@ -40,6 +40,10 @@ namespace usp {
 namespace fwd {
 
 constexpr int kAtomBytes = kBM * 128;  // one 64-column (128-byte) swizzle column of a 128-row tile
+// Stage-release barriers in flight: more than the K/V stages, so that the
+// producer's waits (at most ST - 1 releases behind the MMA thread) never see
+// a barrier two phases ahead.
+constexpr int kRel = 8;
 
 // NQT Q tiles per CTA: 2 (two softmax warpgroups that alternate on the tensor
 // core, 512 TMEM columns, one CTA per SM) or 1 (one softmax warpgroup; at
@@ -70,7 +74,9 @@ struct Bars {
   uint64_t mma_done;
   uint64_t k_full[4];
   uint64_t v_full[4];
-  uint64_t k_empty[4], v_empty[4];  // K stage free once its S MMAs are done, V once its PV MMAs are
+  // rel[j % kRel] completes once the MMAs issued up to S_j are done: K_j's
+  // stage and V_{j-1}'s (its PV was issued before S_j) are free
+  uint64_t rel[8];
   uint32_t tmem;
   int abort;
 };
@@ -152,11 +158,11 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
       mbar_init(&bars->o_final[q], 1);
     }
     mbar_init(&bars->mma_done, 1);
+    for (int j = 0; j < kRel; ++j) mbar_init(&bars->rel[j], 1);
     for (int s = 0; s < C::ST; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
+
     }
     bars->abort = 0;
     fence_barrier_init();
@@ -189,14 +195,15 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
       for (int n = 0; n < n_kv; ++n) {
         const int st = n % C::ST;
         const int kv0 = lo + n * kBN;
-        // K_n, then V_n, each as soon as its stage has been released (K one
-        // step before V: S of a tile is issued a step before its PV)
+        // K_n, then V_n, each as soon as its stage has been released: K_n
+        // replaces K_{n-ST} (free after S_{n-ST}, release n-ST), V_n replaces
+        // V_{n-ST} (free after its PV, release n-ST+1) — K one step earlier
         for (int kv = 0; kv < 2; ++kv) {
           uint64_t* full = kv == 0 ? &bars->k_full[st] : &bars->v_full[st];
-          uint64_t* empty = kv == 0 ? &bars->k_empty[st] : &bars->v_empty[st];
+          const int j = n - C::ST + kv;  // the release this load waits for
           uint8_t* dst = smem + (kv == 0 ? C::OFF_K : C::OFF_V) + st * C::TILE;
           const CUtensorMap* m = kv == 0 ? &tk : &tv;
-          if (n >= C::ST && !(kv_ok = mbar_wait(empty, ((n / C::ST) - 1) & 1, abort, p.status))) break;
+          if (n >= C::ST && !(kv_ok = mbar_wait(&bars->rel[j % kRel], (j / kRel) & 1, abort, p.status))) break;
           mbar_arrive_expect_tx(full, C::TILE);
           for (int c = 0; c < C::NCH; ++c) tma_load_rows(dst + c * kAtomBytes, m, full, p, c, kvh, kv0, p.kv_seq_io != 0);
           if (kv == 0) k_issued = n + 1;
@@ -230,10 +237,10 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
           mma_ss(tmem + q * kBN, sdesc_add(qd, off), sdesc_add(kd, off), idesc_s, kk > 0);
         }
       };
-      // A stage is released once the MMAs issued so far are done; only
-      // stages that will be refilled need it.
-      auto release = [&](uint64_t* empty, bool refilled) {
-        if (refilled) mma_commit(empty);
+      // Release j (after S_j): one commit frees K_j and V_{j-1}; only the
+      // releases a later load waits for are committed (j - 1 + ST < n_kv).
+      auto release = [&](int j) {
+        if (j - 1 + C::ST < n_kv) mma_commit(&bars->rel[j % kRel]);
       };
       auto issue_pv = [&](int q, int st, bool acc) {
         const uint64_t vd = sdesc_sw128(sbase + C::OFF_V + st * C::TILE, kAtomBytes, 1024);
@@ -250,7 +257,7 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
             issue_s(q, 0);
             mma_commit(&bars->s_full[q]);
           }
-        release(&bars->k_empty[0], C::ST < n_kv);
+        release(0);
       }
       for (int n = 0; n < n_kv && ok; ++n) {
         const int st = n % C::ST;
@@ -274,8 +281,7 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
             mma_commit(&bars->o_final[q]);
           }
         }
-        if (ok && n + 1 < n_kv) release(&bars->k_empty[(n + 1) % C::ST], n + 1 + C::ST < n_kv);
-        release(&bars->v_empty[st], n + C::ST < n_kv);
+        if (ok && n + 1 < n_kv) release(n + 1);
       }
       // Every MMA issued above has finished before TMEM can be released.
       mma_commit(&bars->mma_done);
