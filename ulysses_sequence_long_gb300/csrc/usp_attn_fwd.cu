@@ -57,6 +57,7 @@ struct Cfg {
   static constexpr uint32_t TCOLS = NQT == 2 ? 512 : 256;     // TMEM columns allocated
   static constexpr int NCH = D / 64;                  // 64-wide column atoms per row
   static constexpr int ST = (D == 128 || NQT == 1) ? 2 : 4;  // K/V pipeline stages
+  static constexpr bool KV_ONE = ST >= 4;             // one barrier for a stage's K and V
   static constexpr int TILE = NCH * kAtomBytes;       // bytes of one 128-row tile
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQT * TILE;
@@ -72,8 +73,10 @@ struct Bars {
   uint64_t p_full[2];
   uint64_t o_final[2];
   uint64_t mma_done;
-  uint64_t k_full[4];
-  uint64_t v_full[4];
+  // kv_full: K of a stage landed, and V too when the ring has four stages (V
+  // then has time to land before S, and PV needs no wait of its own); with
+  // two stages V signals v_full, waited just before its PV
+  uint64_t kv_full[4], v_full[4];
   // rel[j % kRel] completes once the MMAs issued up to S_j are done: K_j's
   // stage and V_{j-1}'s (its PV was issued before S_j) are free
   uint64_t rel[8];
@@ -160,7 +163,7 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
     mbar_init(&bars->mma_done, 1);
     for (int j = 0; j < kRel; ++j) mbar_init(&bars->rel[j], 1);
     for (int s = 0; s < C::ST; ++s) {
-      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
 
     }
@@ -190,7 +193,7 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
         for (int c = 0; c < C::NCH; ++c)
           tma_load_rows(smem + C::OFF_Q + q * C::TILE + c * kAtomBytes, &tq, &bars->q_full[q], p, c, qh, t0 + q * kBM);
       }
-      int issued = 0, k_issued = 0;  // tiles whose V (and K) loads were issued
+      int k_issued = 0, v_issued = 0;  // tiles whose K, V loads were issued
       bool kv_ok = true;
       for (int n = 0; n < n_kv; ++n) {
         const int st = n % C::ST;
@@ -199,23 +202,23 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
         // replaces K_{n-ST} (free after S_{n-ST}, release n-ST), V_n replaces
         // V_{n-ST} (free after its PV, release n-ST+1) — K one step earlier
         for (int kv = 0; kv < 2; ++kv) {
-          uint64_t* full = kv == 0 ? &bars->k_full[st] : &bars->v_full[st];
+          uint64_t* full = (kv == 0 || C::KV_ONE) ? &bars->kv_full[st] : &bars->v_full[st];
           const int j = n - C::ST + kv;  // the release this load waits for
           uint8_t* dst = smem + (kv == 0 ? C::OFF_K : C::OFF_V) + st * C::TILE;
           const CUtensorMap* m = kv == 0 ? &tk : &tv;
           if (n >= C::ST && !(kv_ok = mbar_wait(&bars->rel[j % kRel], (j / kRel) & 1, abort, p.status))) break;
-          mbar_arrive_expect_tx(full, C::TILE);
+          if (kv == 0 || !C::KV_ONE) mbar_arrive_expect_tx(full, (C::KV_ONE ? 2 : 1) * C::TILE);
           for (int c = 0; c < C::NCH; ++c) tma_load_rows(dst + c * kAtomBytes, m, full, p, c, kvh, kv0, p.kv_seq_io != 0);
-          if (kv == 0) k_issued = n + 1;
+          if (kv == 0) k_issued = n + 1; else v_issued = n + 1;
         }
         if (!kv_ok) break;
-        issued = n + 1;
       }
       // Never leave the CTA with copies still landing in its shared memory.
       for (int n = max(0, k_issued - C::ST); n < k_issued; ++n)
-        mbar_wait(&bars->k_full[n % C::ST], (n / C::ST) & 1, abort, p.status);
-      for (int n = max(0, issued - C::ST); n < issued; ++n)
-        mbar_wait(&bars->v_full[n % C::ST], (n / C::ST) & 1, abort, p.status);
+        mbar_wait(&bars->kv_full[n % C::ST], (n / C::ST) & 1, abort, p.status);
+      if (!C::KV_ONE)
+        for (int n = max(0, v_issued - C::ST); n < v_issued; ++n)
+          mbar_wait(&bars->v_full[n % C::ST], (n / C::ST) & 1, abort, p.status);
       for (int q = 0; q < NQT; ++q)
         if (tile_ok[q]) mbar_wait(&bars->q_full[q], 0, abort, p.status);
     }
@@ -249,7 +252,7 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
           mma_ts(tmem + C::T_O + q * D, tmem + q * kBN + kk * 8, sdesc_add(vd, kk * 16 * 128), idesc_o,
                  (acc || kk > 0) ? 1u : 0u);
       };
-      if (ok) ok = mbar_wait(&bars->k_full[0], 0, abort, p.status);
+      if (ok) ok = mbar_wait(&bars->kv_full[0], 0, abort, p.status);
       if (ok) {
         tc_fence_after();
         for (int q = 0; q < NQT; ++q)
@@ -261,8 +264,8 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
       }
       for (int n = 0; n < n_kv && ok; ++n) {
         const int st = n % C::ST;
-        if (!(ok = mbar_wait(&bars->v_full[st], (n / C::ST) & 1, abort, p.status))) break;
-        bool next_k_ready = false;
+        if (!C::KV_ONE && !(ok = mbar_wait(&bars->v_full[st], (n / C::ST) & 1, abort, p.status))) break;
+        bool next_k_ready = false;  // (with KV_ONE, V_n landed with K_n, waited before S_n)
         for (int q = 0; q < NQT && ok; ++q) {
           if (!tile_ok[q]) continue;
           if (!(ok = mbar_wait(&bars->p_full[q], n & 1, abort, p.status))) break;
@@ -271,7 +274,7 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
           if (n + 1 < n_kv) {
             if (!next_k_ready) {
               const int st1 = (n + 1) % C::ST;
-              if (!(ok = mbar_wait(&bars->k_full[st1], ((n + 1) / C::ST) & 1, abort, p.status))) break;
+              if (!(ok = mbar_wait(&bars->kv_full[st1], ((n + 1) / C::ST) & 1, abort, p.status))) break;
               tc_fence_after();
               next_k_ready = true;
             }
