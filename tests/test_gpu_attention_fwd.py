@@ -70,6 +70,9 @@ SMALL = [
                doc_mode="geometric", doc_mean=150, seed=9),
     W.Workload("win_d64_w0_ragged", B=3, S=200, Hq=4, Hkv=2, D=64, P=2, window_left=0, sinks=True,
                doc_mode="geometric", doc_mean=60, seed=13),
+    # ... and a group of one query head (MHA): the second softmax group has no head
+    W.Workload("win_d64_mha", B=1, S=512, Hq=4, Hkv=4, D=64, P=2, window_left=64,
+               doc_mode="explicit", doc_lens=(130, 382)),
 ]
 
 
