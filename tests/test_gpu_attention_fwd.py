@@ -73,6 +73,9 @@ SMALL = [
     # ... and a group of one query head (MHA): the second softmax group has no head
     W.Workload("win_d64_mha", B=1, S=512, Hq=4, Hkv=4, D=64, P=2, window_left=64,
                doc_mode="explicit", doc_lens=(130, 382)),
+    # a wider window at D=64 (one Q tile per CTA, two K/V stages)
+    W.Workload("win_d64_wide", B=1, S=1024, Hq=8, Hkv=2, D=64, P=2, window_left=300, sinks=True,
+               doc_mode="explicit", doc_lens=(700, 324)),
 ]
 
 

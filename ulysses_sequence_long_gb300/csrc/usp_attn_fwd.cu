@@ -73,10 +73,12 @@ struct Bars {
   uint64_t p_full[2];
   uint64_t o_final[2];
   uint64_t mma_done;
-  // kv_full: K of a stage landed, and V too when the ring has four stages (V
-  // then has time to land before S, and PV needs no wait of its own); with
-  // two stages V signals v_full, waited just before its PV
-  uint64_t kv_full[4], v_full[4];
+  // Four stages (KV_ONE): kv_full[s] = K and V of the tile in stage s
+  // landed (V has time to land before S, so PV needs no wait of its own).
+  // Two stages: K_0 signals k_first, and kv_full[m % 2] = V_m and K_{m+1}
+  // landed (both are loaded once release m-1 completes, and one wait before
+  // PV_m covers them).
+  uint64_t kv_full[4], k_first;
   // rel[j % kRel] completes once the MMAs issued up to S_j are done: K_j's
   // stage and V_{j-1}'s (its PV was issued before S_j) are free
   uint64_t rel[8];
@@ -162,9 +164,9 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
     }
     mbar_init(&bars->mma_done, 1);
     for (int j = 0; j < kRel; ++j) mbar_init(&bars->rel[j], 1);
+    mbar_init(&bars->k_first, 1);
     for (int s = 0; s < C::ST; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->v_full[s], 1);
 
     }
     bars->abort = 0;
@@ -193,32 +195,49 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
         for (int c = 0; c < C::NCH; ++c)
           tma_load_rows(smem + C::OFF_Q + q * C::TILE + c * kAtomBytes, &tq, &bars->q_full[q], p, c, qh, t0 + q * kBM);
       }
-      int k_issued = 0, v_issued = 0;  // tiles whose K, V loads were issued
-      bool kv_ok = true;
-      for (int n = 0; n < n_kv; ++n) {
-        const int st = n % C::ST;
-        const int kv0 = lo + n * kBN;
-        // K_n, then V_n, each as soon as its stage has been released: K_n
-        // replaces K_{n-ST} (free after S_{n-ST}, release n-ST), V_n replaces
-        // V_{n-ST} (free after its PV, release n-ST+1) — K one step earlier
-        for (int kv = 0; kv < 2; ++kv) {
-          uint64_t* full = (kv == 0 || C::KV_ONE) ? &bars->kv_full[st] : &bars->v_full[st];
-          const int j = n - C::ST + kv;  // the release this load waits for
-          uint8_t* dst = smem + (kv == 0 ? C::OFF_K : C::OFF_V) + st * C::TILE;
-          const CUtensorMap* m = kv == 0 ? &tk : &tv;
-          if (n >= C::ST && !(kv_ok = mbar_wait(&bars->rel[j % kRel], (j / kRel) & 1, abort, p.status))) break;
-          if (kv == 0 || !C::KV_ONE) mbar_arrive_expect_tx(full, (C::KV_ONE ? 2 : 1) * C::TILE);
-          for (int c = 0; c < C::NCH; ++c) tma_load_rows(dst + c * kAtomBytes, m, full, p, c, kvh, kv0, p.kv_seq_io != 0);
-          if (kv == 0) k_issued = n + 1; else v_issued = n + 1;
+      auto load = [&](int kv, int n, uint64_t* full) {  // K (kv 0) or V tile n into its stage
+        uint8_t* dst = smem + (kv == 0 ? C::OFF_K : C::OFF_V) + (n % C::ST) * C::TILE;
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_rows(dst + c * kAtomBytes, kv == 0 ? &tk : &tv, full, p, c, kvh, lo + n * kBN, p.kv_seq_io != 0);
+      };
+      int issued = 0;  // KV_ONE: tiles whose K and V loads were issued; else V_m (with K_{m+1}) groups
+      if constexpr (C::KV_ONE) {
+        // K_n and V_n once their stage is free: K_n replaces K_{n-ST} (free
+        // after release n-ST), V_n replaces V_{n-ST} (release n-ST+1)
+        for (int n = 0; n < n_kv; ++n) {
+          const int st = n % C::ST;
+          bool ok_n = true;
+          for (int kv = 0; kv < 2 && ok_n; ++kv) {
+            const int j = n - C::ST + kv;  // the release this load waits for
+            if (n >= C::ST && !(ok_n = mbar_wait(&bars->rel[j % kRel], (j / kRel) & 1, abort, p.status))) break;
+            if (kv == 0) mbar_arrive_expect_tx(&bars->kv_full[st], 2 * C::TILE);
+            load(kv, n, &bars->kv_full[st]);
+          }
+          if (!ok_n) break;
+          issued = n + 1;
         }
-        if (!kv_ok) break;
+        for (int n = max(0, issued - C::ST); n < issued; ++n)
+          mbar_wait(&bars->kv_full[n % C::ST], (n / C::ST) & 1, abort, p.status);
+      } else {
+        // K_0 alone; then V_m with K_{m+1}: V_m replaces V_{m-2} (free after
+        // PV_{m-2}), K_{m+1} replaces K_{m-1} (free after S_{m-1}), both by
+        // release m-1
+        mbar_arrive_expect_tx(&bars->k_first, C::TILE);
+        load(0, 0, &bars->k_first);
+        for (int m = 0; m < n_kv; ++m) {
+          if (m >= 1 && !mbar_wait(&bars->rel[(m - 1) % kRel], ((m - 1) / kRel) & 1, abort, p.status)) break;
+          const bool k_next = m + 1 < n_kv;
+          uint64_t* full = &bars->kv_full[m & 1];
+          mbar_arrive_expect_tx(full, (k_next ? 2 : 1) * C::TILE);
+          load(1, m, full);
+          if (k_next) load(0, m + 1, full);
+          issued = m + 1;
+        }
+        mbar_wait(&bars->k_first, 0, abort, p.status);
+        for (int m = max(0, issued - 2); m < issued; ++m)
+          mbar_wait(&bars->kv_full[m & 1], (m >> 1) & 1, abort, p.status);
       }
-      // Never leave the CTA with copies still landing in its shared memory.
-      for (int n = max(0, k_issued - C::ST); n < k_issued; ++n)
-        mbar_wait(&bars->kv_full[n % C::ST], (n / C::ST) & 1, abort, p.status);
-      if (!C::KV_ONE)
-        for (int n = max(0, v_issued - C::ST); n < v_issued; ++n)
-          mbar_wait(&bars->v_full[n % C::ST], (n / C::ST) & 1, abort, p.status);
+      // Never leave the CTA with copies still landing in its shared memory (above).
       for (int q = 0; q < NQT; ++q)
         if (tile_ok[q]) mbar_wait(&bars->q_full[q], 0, abort, p.status);
     }
@@ -252,7 +271,8 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
           mma_ts(tmem + C::T_O + q * D, tmem + q * kBN + kk * 8, sdesc_add(vd, kk * 16 * 128), idesc_o,
                  (acc || kk > 0) ? 1u : 0u);
       };
-      if (ok) ok = mbar_wait(&bars->kv_full[0], 0, abort, p.status);
+      if (ok) ok = C::KV_ONE ? mbar_wait(&bars->kv_full[0], 0, abort, p.status)
+                             : mbar_wait(&bars->k_first, 0, abort, p.status);
       if (ok) {
         tc_fence_after();
         for (int q = 0; q < NQT; ++q)
@@ -264,8 +284,9 @@ __global__ void __launch_bounds__(Cfg<D, NQT>::THREADS, Cfg<D, NQT>::CTAS)
       }
       for (int n = 0; n < n_kv && ok; ++n) {
         const int st = n % C::ST;
-        if (!C::KV_ONE && !(ok = mbar_wait(&bars->v_full[st], (n / C::ST) & 1, abort, p.status))) break;
-        bool next_k_ready = false;  // (with KV_ONE, V_n landed with K_n, waited before S_n)
+        // two stages: V_n and K_{n+1} in one wait; KV_ONE: V_n landed with K_n
+        if (!C::KV_ONE && !(ok = mbar_wait(&bars->kv_full[n & 1], (n >> 1) & 1, abort, p.status))) break;
+        bool next_k_ready = !C::KV_ONE;
         for (int q = 0; q < NQT && ok; ++q) {
           if (!tile_ok[q]) continue;
           if (!(ok = mbar_wait(&bars->p_full[q], n & 1, abort, p.status))) break;
