@@ -89,6 +89,16 @@ __device__ __forceinline__ Unit unit_at(const AttnArgs& p, int n_docs, int u) {
   return w;
 }
 
+// 16 packed columns into TMEM (this warp's lanes).
+__device__ __forceinline__ void tmem_st16_cols(uint32_t taddr, const uint32_t (&pk)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7]), "r"(pk[8]),
+      "r"(pk[9]), "r"(pk[10]), "r"(pk[11]), "r"(pk[12]), "r"(pk[13]), "r"(pk[14]), "r"(pk[15])
+      : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_window_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                            const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
@@ -335,26 +345,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t nm2 = f2_pack(-m_use, -m_use);
           uint64_t rs2[2] = {0, 0};
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t pk[32];
+          // P of chunk c, packed, to the 16 columns at 16c (S is all in registers)
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-              const int c = 2 * h + c2;
-              if (vis >> c & 1u) {
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t pk[16];
+            if (vis >> c & 1u) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                  const int col = 32 * c + 2 * e;
-                  const float2 x = f2_unpack(f2_fma(f2_pack(s[col], s[col + 1]), sc2, nm2));
-                  const float p0 = ex2(x.x), p1 = ex2(x.y);
-                  rs2[e & 1] = f2_add(rs2[e & 1], f2_pack(p0, p1));
-                  pk[16 * c2 + e] = pack_bf16x2(p0, p1);
-                }
-              } else {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) pk[16 * c2 + e] = 0u;
+              for (int e = 0; e < 16; ++e) {
+                const int col = 32 * c + 2 * e;
+                const float2 x = f2_unpack(f2_fma(f2_pack(s[col], s[col + 1]), sc2, nm2));
+                const float p0 = ex2(x.x), p1 = ex2(x.y);
+                rs2[e & 1] = f2_add(rs2[e & 1], f2_pack(p0, p1));
+                pk[e] = pack_bf16x2(p0, p1);
               }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) pk[e] = 0u;
             }
-            tmem_st32(s_tm + 32 * h, pk);
+            tmem_st16_cols(s_tm + 16 * c, pk);
           }
           const float2 r01 = f2_unpack(f2_add(rs2[0], rs2[1]));
           l += r01.x + r01.y;
