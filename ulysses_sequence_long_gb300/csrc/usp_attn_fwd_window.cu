@@ -258,12 +258,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w.n_kv > kMaxKV) continue;
       const int t = w.t0 + row;
       const bool row_ok = t < p.BS;
-      const int bb = row_ok ? t / p.S : 0, ss = row_ok ? t - bb * p.S : 0;
       if (w.n_kv == 0) {
         // no key to see (a ring step whose block lies after these rows): O = 0
         // and LSE = the sink logit alone, or -inf
         for (int g = q; g < G && row_ok; g += 2) {
           const int j = w.kl * G + g;
+          const int bb = t / p.S, ss = t - bb * p.S;
           uint4* dst = reinterpret_cast<uint4*>(o_out + row_offset(p, q_head_ref(p, w.r, j), p.hq, p.Hq, t, D));
           for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
           lse_out[(static_cast<size_t>(w.r * p.B + bb) * p.hq + j) * p.S + ss] =
@@ -413,15 +413,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->o_staged[q]);
-        if (row == 0) {
-          if (!(ok = mbar_wait(&bars->o_staged[q], (oc - 1) & 1, abort, p.status))) break;
+        if (row == 0 && mbar_wait(&bars->o_staged[q], (oc - 1) & 1, abort, p.status)) {
           tma_store_rows(&to, stg, p, 0, q_head_ref(p, w.r, j), w.t0);
           bulk_commit_group();
           bulk_wait_group_read<0>();  // the tile has been read: the Q set may be reloaded
           mbar_arrive(&bars->q_empty[set]);
           stored = true;
         }
+        __syncwarp();
+        if (*abort) {  // a wait gave up: the whole warp leaves (the others see it at their next wait)
+          ok = false;
+          break;
+        }
         if (row_ok) {
+          const int bb = t / p.S, ss = t - bb * p.S;
           lse_out[(static_cast<size_t>(w.r * p.B + bb) * p.hq + j) * p.S + ss] =
               l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
         }
